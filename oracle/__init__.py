@@ -1,0 +1,285 @@
+"""Plain CPU oracle of the sparse-attention indexer (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``. The product library never imports
+it and shares no code with it. The arithmetic lives in ``indexer_oracle.c``
+(plain C, fp64 except the fp32 steps that decide the fp8 codes of q); this
+module only builds it with gcc, loads it with ctypes and marshals numpy arrays.
+
+Every function states the passage of the pages it restates; see the header of
+``indexer_oracle.c`` for the readings taken where the pages are silent.
+Parity pins: every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle.py`` (library routines, closed forms, worked examples from
+the pages, brute force, invariants).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "indexer_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PAGE_TOKENS = 64
+DIM = 128
+PAGE_BYTES = PAGE_TOKENS * (DIM + 4)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``indexer_oracle.c`` into ``liboracle.so`` next to it (gcc)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-pthread",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = C.CDLL(_LIB_PATH)
+        P = C.c_void_p
+        i32, i64, u8 = C.c_int32, C.c_int64, C.c_uint8
+        lib.ora_e4m3_decode.restype = C.c_double
+        lib.ora_e4m3_decode.argtypes = [u8]
+        lib.ora_e4m3_encode.restype = u8
+        lib.ora_e4m3_encode.argtypes = [C.c_float]
+        lib.ora_quantize_q.restype = None
+        lib.ora_quantize_q.argtypes = [P, P, i64, i32, i32, P, P, P]
+        lib.ora_expand_rows.restype = i64
+        lib.ora_expand_rows.argtypes = [P, P, i32, i32, i32, P, i64, i32, P, P, i64, i64]
+        lib.ora_row_logits.restype = C.c_int
+        lib.ora_row_logits.argtypes = [P, P, i32, i32, P, i64, P, i64, P, P, P]
+        lib.ora_topk_row.restype = None
+        lib.ora_topk_row.argtypes = [P, i64, i32, P]
+        lib.ora_score_select_rows.restype = C.c_int
+        lib.ora_score_select_rows.argtypes = [P, P, i32, i32, P, i64, P, i64, P, P, P, i64,
+                                              i32, P, P, P, P, P, i32]
+        lib.ora_num_threads.restype = C.c_int
+        lib.ora_num_threads.argtypes = []
+        lib.ora_plan_prefill_chunks.restype = i64
+        lib.ora_plan_prefill_chunks.argtypes = [P, P, i32, i64, i64, P, i64]
+        lib.ora_prefill_rows.restype = None
+        lib.ora_prefill_rows.argtypes = [P, P, i32, P, P]
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return C.c_void_p(a.ctypes.data)
+
+
+def num_threads() -> int:
+    return int(_load().ora_num_threads())
+
+
+# --------------------------------------------------------------------------
+# fp8 e4m3fn codec (closed-form definition; no infinities, max 448)
+# --------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.ora_e4m3_decode(int(x)) for x in c], dtype=np.float64).reshape(
+        np.shape(codes))
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round-to-nearest-even onto the e4m3fn grid, saturating at +-448."""
+    lib = _load()
+    v = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.ora_e4m3_encode(float(f)) for f in v], dtype=np.uint8).reshape(
+        np.shape(x))
+
+
+# --------------------------------------------------------------------------
+# q quantisation (per token row and head)
+# --------------------------------------------------------------------------
+
+def quantize_q(q_bf16_bits: np.ndarray, w: np.ndarray):
+    """q_bf16_bits: uint16 [rows, H, D] raw bf16; w: float32 [rows, H].
+
+    Returns (q8 uint8 [rows, H, D], sq float64 [rows, H], wprime float64 [rows, H])
+    with amax = max|q|, inv = 448/amax (fp32), q8 = e4m3(q*inv) (fp32 product),
+    sq = amax/448, wprime = w*sq.
+    """
+    q = np.ascontiguousarray(q_bf16_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, H, D = q.shape
+    q8 = np.empty((rows, H, D), np.uint8)
+    sq = np.empty((rows, H), np.float64)
+    wp = np.empty((rows, H), np.float64)
+    _load().ora_quantize_q(_p(q), _p(w), rows, H, D, _p(q8), _p(sq), _p(wp))
+    return q8, sq, wp
+
+
+# --------------------------------------------------------------------------
+# decode row expansion
+# --------------------------------------------------------------------------
+
+def expand_rows(seq_lens, decode_lens, next_n: int, mode: int = 0, block_table=None,
+                num_out_rows: int | None = None):
+    """mode 0: padded [R, next_n] grid; mode 1: flatten (sum d_b rows, zero tail).
+
+    Returns (row_lens int32, row_block_table int32 or None, token_rows).
+    """
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    dl = np.ascontiguousarray(decode_lens, dtype=np.int32)
+    R = sl.shape[0]
+    if num_out_rows is None:
+        num_out_rows = R * next_n
+    row_lens = np.zeros(num_out_rows, np.int32)
+    row_bt = None
+    W, stride, bt = 0, 0, None
+    if block_table is not None:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        W = bt.shape[1]
+        stride = W
+        row_bt = np.full((num_out_rows, W), -7, np.int32)
+    n = _load().ora_expand_rows(_p(sl), _p(dl), R, next_n, mode, _p(bt), stride, W,
+                                _p(row_lens), _p(row_bt), W, num_out_rows)
+    if n < 0:
+        raise ValueError("token rows do not fit in num_out_rows")
+    return row_lens, row_bt, int(n)
+
+
+# --------------------------------------------------------------------------
+# scoring and selection
+# --------------------------------------------------------------------------
+
+def row_logits(q8_row, wprime_row, cache, bt_row, length: int):
+    """Logits and tolerance magnitudes (A, B) of one token row, fp64."""
+    q8_row = np.ascontiguousarray(q8_row, dtype=np.uint8)
+    wp = np.ascontiguousarray(wprime_row, dtype=np.float64)
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    bt_row = np.ascontiguousarray(bt_row, dtype=np.int32)
+    H, D = q8_row.shape
+    lg = np.empty(max(length, 1), np.float64)
+    ta = np.empty_like(lg)
+    tb = np.empty_like(lg)
+    rc = _load().ora_row_logits(_p(q8_row), _p(wp), H, D, _p(cache), cache.shape[0], _p(bt_row),
+                                length, _p(lg), _p(ta), _p(tb))
+    if rc != 0:
+        raise ValueError(f"oracle: bad page id in block table (rc={rc})")
+    return lg[:length], ta[:length], tb[:length]
+
+
+def topk_row(logits, length: int, k: int) -> np.ndarray:
+    lg = np.ascontiguousarray(logits, dtype=np.float64)
+    out = np.empty(k, np.int32)
+    _load().ora_topk_row(_p(lg), length, k, _p(out))
+    return out
+
+
+def score_select_rows(q8, wprime, cache, block_table, qrows, bt_rows, lens, k: int | None,
+                      want_logits: bool = False, threads: int = 0):
+    """Scores (and selects top-k of) token rows in parallel.
+
+    q8 [rows, H, D], wprime [rows, H]; qrows[i] picks the q row, bt_rows[i] the
+    block-table row and lens[i] the key count of output row i. Returns
+    (out_idx [n, k] or None, logits list or None, tol_a list, tol_b list).
+    """
+    q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+    wp = np.ascontiguousarray(wprime, dtype=np.float64)
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    qrows = np.ascontiguousarray(qrows, dtype=np.int64)
+    bt_rows = np.ascontiguousarray(bt_rows, dtype=np.int64)
+    lens = np.ascontiguousarray(lens, dtype=np.int64)
+    n = lens.shape[0]
+    H, D = q8.shape[1], q8.shape[2]
+    out = np.empty((n, k), np.int32) if k is not None else None
+    off = lg = ta = tb = None
+    if want_logits:
+        off = np.zeros(n, np.int64)
+        if n > 1:
+            off[1:] = np.cumsum(lens[:-1])
+        total = int(lens.sum())
+        lg = np.zeros(max(total, 1), np.float64)
+        ta = np.zeros_like(lg)
+        tb = np.zeros_like(lg)
+    rc = _load().ora_score_select_rows(
+        _p(q8), _p(wp), H, D, _p(cache), cache.shape[0], _p(bt), bt.shape[1], _p(qrows),
+        _p(bt_rows), _p(lens), n, k if k is not None else 0, _p(out), _p(off), _p(lg), _p(ta),
+        _p(tb), threads)
+    if rc != 0:
+        raise ValueError(f"oracle: bad page id in block table (rc={rc})")
+    if not want_logits:
+        return out, None, None, None
+    split = lambda a: [a[o:o + l] for o, l in zip(off, lens)]
+    return out, split(lg), split(ta), split(tb)
+
+
+def decode_topk(q_bf16_bits, w, cache, block_table, row_lens, next_n: int, k: int,
+                rows=None, want_logits: bool = False, threads: int = 0):
+    """The decode indexer for token rows laid out as a [R, next_n] grid (row
+    b*next_n + j uses block-table row b). ``rows`` restricts the work to a
+    sample of token rows. Returns (out_idx [n, k], logits, tol_a, tol_b, rows)."""
+    q8, _, wp = quantize_q(q_bf16_bits, w)
+    row_lens = np.asarray(row_lens, dtype=np.int64)
+    if rows is None:
+        rows = np.arange(row_lens.shape[0], dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    out, lg, ta, tb = score_select_rows(q8, wp, cache, block_table, rows, rows // next_n,
+                                        row_lens[rows], k, want_logits, threads)
+    return out, lg, ta, tb, rows
+
+
+# --------------------------------------------------------------------------
+# prefill
+# --------------------------------------------------------------------------
+
+def plan_prefill_chunks(seq_lens, query_lens, workspace_tokens: int, logits_budget_bytes: int):
+    """Greedy chunk plan: list of (req_begin, req_end, q_begin, q_end)."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(query_lens, dtype=np.int32)
+    cap = 16
+    while True:
+        buf = np.zeros((cap, 4), np.int32)
+        n = _load().ora_plan_prefill_chunks(_p(sl), _p(ql), sl.shape[0], workspace_tokens,
+                                            logits_budget_bytes, _p(buf), cap)
+        if n >= 0:
+            return [tuple(int(v) for v in buf[i]) for i in range(n)]
+        cap *= 4
+
+
+def prefill_rows(seq_lens, query_start_loc):
+    """Per query token: (request id, number of visible keys)."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    total = int(qsl[-1])
+    req = np.zeros(total, np.int64)
+    ln = np.zeros(total, np.int64)
+    _load().ora_prefill_rows(_p(sl), _p(qsl), sl.shape[0], _p(req), _p(ln))
+    return req, ln
+
+
+def prefill_topk(q_bf16_bits, w, cache, block_table, seq_lens, query_start_loc, k: int,
+                 rows=None, want_logits: bool = False, threads: int = 0):
+    """The prefill indexer: query token i of request r sees keys [0, len_i).
+    Chunking does not change the result, so the oracle scores rows directly."""
+    q8, _, wp = quantize_q(q_bf16_bits, w)
+    req, ln = prefill_rows(seq_lens, query_start_loc)
+    if rows is None:
+        rows = np.arange(ln.shape[0], dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    out, lg, ta, tb = score_select_rows(q8, wp, cache, block_table, rows, req[rows], ln[rows],
+                                        k, want_logits, threads)
+    return out, lg, ta, tb, rows

@@ -1,0 +1,380 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+Each test ties one oracle function to the pages' worked examples, a library
+routine, a closed form, brute force or an invariant, chosen so that a dropped
+term, a wrong sign or index or a transposed operand fails.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+# --------------------------------------------------------------------------
+# e4m3fn codec
+# --------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_golden_codes():
+    for line in _golden_lines("e4m3_codes.txt"):
+        code, val = line.split()
+        got = float(oracle.e4m3_decode([int(code, 16)])[0])
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_e4m3_decode_matches_torch_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def _torch_e4m3(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def test_e4m3_encode_roundtrip_midpoints_and_neighbours():
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = oracle.e4m3_decode(finite).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), finite)      # round trip, incl. -0
+    pos = np.sort(oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)          # exact in fp32
+    probes = np.concatenate([mids, np.nextafter(mids, np.float32(0)),
+                             np.nextafter(mids, np.float32(1000)), -mids])
+    assert np.array_equal(oracle.e4m3_encode(probes), _torch_e4m3(probes))
+    # ties go to the even code
+    enc = oracle.e4m3_encode(mids)
+    assert np.all((enc & 1) == 0)
+
+
+def test_e4m3_encode_random_and_saturation():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(-448, 448, 4000),
+                        rng.standard_normal(4000) * 1e-2,
+                        rng.standard_normal(2000) * 1e-3]).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(x), _torch_e4m3(x))
+    sat = oracle.e4m3_encode(np.array([448.0, 464.0, 1e6, np.inf, -np.inf, -500.0], np.float32))
+    assert list(sat) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+
+
+# --------------------------------------------------------------------------
+# q quantisation
+# --------------------------------------------------------------------------
+
+def _bf16(vals):
+    return torch.tensor(vals, dtype=torch.bfloat16)
+
+
+def test_quantize_q_hand_example():
+    head = [0.0] * 128
+    head[0], head[1], head[2] = 2.0, -1.0, 0.5
+    q = _bf16([[head, [0.0] * 128]])                              # 1 row, 2 heads
+    w = np.array([[0.25, -3.0]], np.float32)
+    q8, sq, wp = oracle.quantize_q(synth.bf16_bits(q), w)
+    # amax 2 -> inv 224 -> 448, -224, 112 -> codes 0x7E, 0xF6, 0x6E
+    assert list(q8[0, 0, :3]) == [0x7E, 0xF6, 0x6E]
+    assert np.all(q8[0, 0, 3:] == 0)
+    assert sq[0, 0] == 2.0 / 448.0 and wp[0, 0] == 0.25 * 2.0 / 448.0
+    # an all-zero head quantises to zero codes and a zero weight
+    assert np.all(q8[0, 1] == 0) and sq[0, 1] == 0.0 and wp[0, 1] == 0.0
+
+
+def test_quantize_q_matches_library_cast_and_bounds():
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(5, 64, 128, generator=g).to(torch.bfloat16)
+    q[1, 3] = 0.0
+    w = (torch.randn(5, 64, generator=g) / 8).numpy()
+    q8, sq, wp = oracle.quantize_q(synth.bf16_bits(q), w)
+    qf = q.float().numpy()
+    amax = np.abs(qf).max(axis=-1, keepdims=True)
+    safe = np.where(amax > 0, amax, np.float32(1.0)).astype(np.float32)
+    inv = np.float32(448.0) / safe                               # IEEE fp32 division
+    x = np.where(amax > 0, qf * inv, 0).astype(np.float32)       # fp32 product
+    ref = _torch_e4m3(x)
+    ref[1, 3] = 0
+    assert np.array_equal(q8, ref)
+    # the largest magnitude maps onto +-448 exactly
+    mx = np.abs(oracle.e4m3_decode(q8.reshape(-1, 128)[:64])).max(axis=-1)
+    assert np.all(mx == 448.0)
+    # dequantised q is within half an e4m3 step (relative 2^-4) of q for normal codes
+    codes = oracle.e4m3_decode(q8)
+    deq = codes * sq[..., None]
+    normal = (np.abs(codes) >= 2.0 ** -6) & (qf != 0)
+    rel = np.abs(deq - qf)[normal] / np.abs(qf)[normal]
+    assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)
+    assert np.allclose(wp, w * sq, rtol=0, atol=0)
+
+
+# --------------------------------------------------------------------------
+# row expansion
+# --------------------------------------------------------------------------
+
+def _worked_example():
+    d = {}
+    for line in _golden_lines("flatten_worked_example.txt"):
+        key, *vals = line.split()
+        d[key] = [int(v) for v in vals]
+    return d
+
+
+def test_expand_flatten_matches_pages_worked_example():
+    ex = _worked_example()
+    bt = np.arange(4 * 3, dtype=np.int32).reshape(4, 3) + 100
+    n_out = 10
+    lens, rbt, n = oracle.expand_rows(ex["seq_lens"], ex["decode_lens"], 4, mode=1,
+                                      block_table=bt, num_out_rows=n_out)
+    assert n == len(ex["flat_row_lens"])
+    assert list(lens[:n]) == ex["flat_row_lens"]
+    assert np.all(lens[n:] == 0)                                  # zero tail
+    owners = np.repeat(np.arange(4), ex["decode_lens"])
+    assert np.array_equal(rbt[:n], bt[owners])                    # request's row per token
+    assert np.all(rbt[n:, 0] == 0)                                # padded rows: column 0 = 0
+
+
+def test_expand_padded_grid_agrees_with_flatten_and_pads_zero():
+    ex = _worked_example()
+    lens, _, n = oracle.expand_rows(ex["seq_lens"], ex["decode_lens"], 4, mode=0)
+    grid = lens.reshape(4, 4)
+    dl = np.array(ex["decode_lens"])
+    for b in range(4):
+        assert np.all(grid[b, dl[b]:] == 0)                       # padded rows have seq_len 0
+    real = [int(grid[b, j]) for b in range(4) for j in range(dl[b])]
+    assert real == ex["flat_row_lens"]
+
+
+def test_expand_uniform_matches_token_rows_docstring():
+    # token j of a request with q query tokens sees seq_len - (q - 1 - j) keys
+    # ("vllm.models.minimax_m3.amd.mono.runner", token_rows).
+    seq = np.array([100, 50, 3000, 7], np.int32)
+    q = 3
+    lens, _, _ = oracle.expand_rows(seq, np.full(4, q, np.int32), q, mode=0)
+    for b in range(4):
+        for j in range(q):
+            assert lens[b * q + j] == seq[b] - (q - 1 - j)
+
+
+# --------------------------------------------------------------------------
+# scoring
+# --------------------------------------------------------------------------
+
+def _one_page_cache(k_codes, scales):
+    page = np.zeros((1, oracle.PAGE_BYTES), np.uint8)
+    for t, codes in enumerate(k_codes):
+        page[0, t * 128:t * 128 + 128] = codes
+    page[0, 8192:8192 + 4 * len(scales)] = np.asarray(scales, np.float32).view(np.uint8)
+    return page
+
+
+def test_logits_hand_computed_single_key():
+    k = np.zeros(128, np.uint8)
+    k[0] = 0x38                                                    # key = e_0, value 1.0
+    cache = _one_page_cache([k, k], [0.5, 0.0])
+    q = np.zeros((1, 2, 128), np.float32)
+    q[0, 0, 0] = 1.0                                               # head 0 aligned
+    q[0, 1, 0] = -1.0                                              # head 1 anti-aligned
+    w = np.array([[0.25, 7.0]], np.float32)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(torch.from_numpy(q).to(torch.bfloat16)), w)
+    lg, ta, tb = oracle.row_logits(q8[0], wp[0], cache, np.array([0], np.int32), 2)
+    # head 0: ReLU(0.5 * 1 * 1) * 0.25; head 1: ReLU(-0.5) = 0; key 1 has scale 0
+    assert lg[0] == 0.125 and lg[1] == 0.0
+    assert ta[0] == 0.125 and tb[0] == pytest.approx(0.5 * (0.25 + 7.0))
+
+
+def _dense_reference(q8, wp, cache, bt_row, length):
+    """Independent numpy restatement used only to pin the C loops."""
+    s = np.arange(length)
+    pages = bt_row[s // 64]
+    slots = s % 64
+    vals = cache[pages[:, None], slots[:, None] * 128 + np.arange(128)[None, :]]
+    kd = oracle.e4m3_decode(vals)                                  # [len, 128]
+    scale = cache[pages[:, None], 8192 + 4 * slots[:, None] + np.arange(4)[None, :]]
+    scale = scale.copy().view(np.float32)[:, 0].astype(np.float64)
+    qd = oracle.e4m3_decode(q8)                                    # [H, 128]
+    dots = kd @ qd.T                                               # [len, H]
+    return scale * (np.maximum(dots, 0) @ wp), dots
+
+
+def test_logits_match_dense_numpy_and_are_exact_dots():
+    d = synth.make_decode_from_lens([300, 130], [1, 1], 1, seed=11, bt_min_width=8)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(d.q), d.w.numpy())
+    cache = d.cache.numpy()
+    bt = d.block_table.numpy()
+    for r, L in enumerate([300, 130]):
+        lg, _, _ = oracle.row_logits(q8[r], wp[r], cache, bt[r], L)
+        ref, dots = _dense_reference(q8[r], wp[r], cache, bt[r], L)
+        assert np.allclose(lg, ref, rtol=1e-12, atol=1e-12)
+        # the fp64 dot of e4m3 values is exact: every product is a multiple of 2^-18
+        qi = (oracle.e4m3_decode(q8[r]) * 2 ** 9).astype(np.int64)
+        s = np.arange(L)
+        vals = cache[bt[r][s // 64][:, None], (s % 64)[:, None] * 128 + np.arange(128)]
+        ki = (oracle.e4m3_decode(vals) * 2 ** 9).astype(np.int64)
+        assert np.array_equal((ki @ qi.T).astype(np.float64) / 2 ** 18, dots)
+
+
+def test_logits_invariant_under_page_permutation_and_linear_in_w():
+    d = synth.make_decode_from_lens([700], [1], 1, seed=5)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(d.q), d.w.numpy())
+    cache = d.cache.numpy()
+    bt = d.block_table.numpy()[0]
+    lg, _, _ = oracle.row_logits(q8[0], wp[0], cache, bt, 700)
+    perm = np.random.default_rng(2).permutation(cache.shape[0])
+    cache2 = np.empty_like(cache)
+    cache2[perm] = cache                                           # page p moves to perm[p]
+    lg2, _, _ = oracle.row_logits(q8[0], wp[0], cache2, perm[bt].astype(np.int32), 700)
+    assert np.array_equal(lg, lg2)
+    lg3, _, _ = oracle.row_logits(q8[0], 2.0 * wp[0], cache, bt, 700)
+    assert np.array_equal(lg3, 2.0 * lg)
+    # a key whose slot is past the row length never influences the earlier logits
+    lg4, _, _ = oracle.row_logits(q8[0], wp[0], cache, bt, 650)
+    assert np.array_equal(lg4, lg[:650])
+
+
+# --------------------------------------------------------------------------
+# selection
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("k", [1, 7, 64])
+def test_topk_brute_force_small_rows(k):
+    rng = np.random.default_rng(k)
+    for length in [0, 1, k - 1, k, k + 1, 150, 300]:
+        if length < 0:
+            continue
+        lg = rng.integers(-20, 20, size=length).astype(np.float64)  # many ties
+        out = oracle.topk_row(lg, length, k)
+        if length <= k:
+            assert list(out) == list(range(length)) + [-1] * (k - length)
+        else:
+            brute = sorted(range(length), key=lambda i: (-lg[i], i))[:k]
+            assert list(out) == brute
+
+
+def test_causal_identity_for_short_rows():
+    # rows with len <= k select every key: exactly [0, len) followed by -1
+    # ("vllm.models.glm5next.common.sparse_indexer", _fill_short_decode_causal_indices)
+    d = synth.make_decode("tiny")
+    lens, _, _ = oracle.expand_rows(d.seq_lens.numpy(), d.decode_lens.numpy(), 1)
+    out, _, _, _, _ = oracle.decode_topk(synth.bf16_bits(d.q), d.w.numpy(), d.cache.numpy(),
+                                         d.block_table.numpy(), lens, 1, 2048, rows=[0, 1])
+    assert list(out[0]) == list(range(1000)) + [-1] * 1048
+    assert list(out[1]) == list(range(2048))
+
+
+def test_decode_topk_rows_are_valid_sets():
+    d = synth.make_decode_from_lens([2100, 2500], [1, 1], 1, seed=9)
+    lens, _, _ = oracle.expand_rows(d.seq_lens.numpy(), d.decode_lens.numpy(), 1)
+    out, lg, _, _, _ = oracle.decode_topk(synth.bf16_bits(d.q), d.w.numpy(), d.cache.numpy(),
+                                          d.block_table.numpy(), lens, 1, 2048,
+                                          want_logits=True)
+    for r in range(2):
+        sel = out[r]
+        assert len(set(sel.tolist())) == 2048 and sel.min() >= 0 and sel.max() < lens[r]
+        kth = np.sort(lg[r])[::-1][2047]
+        assert np.all(lg[r][sel] >= kth)
+        rest = np.setdiff1d(np.arange(lens[r]), sel)
+        assert np.all(lg[r][rest] <= kth)
+
+
+# --------------------------------------------------------------------------
+# prefill
+# --------------------------------------------------------------------------
+
+def _plans():
+    for line in _golden_lines("prefill_chunk_plans.txt"):
+        _, rest = line.split(" ", 1)
+        name, sl, ql, ws, budget, plan = [x.strip() for x in rest.split("|")]
+        yield (name, [int(x) for x in sl.split()], [int(x) for x in ql.split()], int(ws),
+               int(budget), [tuple(int(v) for v in p.split(":")) for p in plan.split()])
+
+
+@pytest.mark.parametrize("case", list(_plans()), ids=lambda c: c[0])
+def test_prefill_plan_golden(case):
+    _, sl, ql, ws, budget, plan = case
+    assert oracle.plan_prefill_chunks(sl, ql, ws, budget) == plan
+
+
+def test_prefill_plan_invariants_random():
+    rng = np.random.default_rng(4)
+    for _ in range(300):
+        n = int(rng.integers(1, 12))
+        sl = rng.integers(0, 5000, n)
+        ql = np.minimum(rng.integers(0, 3000, n), np.maximum(sl, 0))
+        ws = int(rng.integers(1, 20000))
+        budget = int(rng.integers(4, 4 * 10 ** 7))
+        elems = budget // 4
+        plan = oracle.plan_prefill_chunks(sl, ql, ws, budget)
+        # chunks cover every request with queries exactly once, in order
+        seen_q = {}
+        for (r0, r1, a, b) in plan:
+            assert 0 <= r0 < r1 <= n and 0 <= a < b
+            seen_q.setdefault((r0, r1), []).append((a, b))
+        covered = []
+        for (r0, r1), pieces in seen_q.items():
+            M = int(ql[r0:r1].sum())
+            N = int(sl[r0:r1].sum())
+            assert pieces[0][0] == 0 and pieces[-1][1] == M
+            for (a0, b0), (a1, b1) in zip(pieces, pieces[1:]):
+                assert b0 == a1
+            if r1 - r0 > 1:
+                assert N <= ws and M * N <= elems
+            max_q = max(1, elems // N) if N > 0 else M
+            assert all(b - a <= max_q for a, b in pieces)
+            covered.extend(range(r0, r1))
+        with_q = [i for i in range(n)]
+        assert sorted(set(covered)) == sorted(set(i for i in covered))
+        for i in with_q:
+            if any(r0 <= i < r1 for (r0, r1) in seen_q):
+                continue
+            # a request left out belongs to a chunk with no queries at all
+            assert ql[i] == 0
+
+
+def test_prefill_rows_causal_ranges():
+    # query i of a request with seq_len L and query_len Q sees keys [0, L - Q + 1 + i)
+    # (_build_prefill_chunk_metadata_kernel: cu_seqlen_ke - cu_seqlen_ks)
+    req, ln = oracle.prefill_rows([8, 10, 5], [0, 8, 11, 11])
+    assert list(req) == [0] * 8 + [1] * 3
+    assert list(ln[:8]) == list(range(1, 9))                      # L == Q: query i sees 0..i
+    assert list(ln[8:]) == [8, 9, 10]
+
+
+def test_fraction_exactness_of_score_scale():
+    # scale_s factors out of the head sum because it is >= 0: checked with exact
+    # rationals on one key against the unfactored sum.
+    k = np.zeros(128, np.uint8)
+    k[:4] = [0x38, 0xB8, 0x40, 0x01]
+    cache = _one_page_cache([k], [0.375])
+    q = torch.zeros(1, 3, 128)
+    q[0, 0, :4] = torch.tensor([1.0, 0.5, 0.25, 3.0])
+    q[0, 1, :4] = torch.tensor([-1.0, 0.0, 0.5, 0.0])
+    q[0, 2, :4] = torch.tensor([0.0, -2.0, 0.0, 1.0])
+    w = np.array([[0.5, -0.25, 2.0]], np.float32)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(q.to(torch.bfloat16)), w)
+    lg, _, _ = oracle.row_logits(q8[0], wp[0], cache, np.array([0], np.int32), 1)
+    kd = [Fraction(float(v)) for v in oracle.e4m3_decode(k)]
+    tot = Fraction(0)
+    for h in range(3):
+        qd = [Fraction(float(v)) for v in oracle.e4m3_decode(q8[0, h])]
+        dot = sum(a * b for a, b in zip(qd, kd))
+        tot += Fraction(float(wp[0, h])) * max(Fraction(0.375) * dot, Fraction(0))
+    assert abs(Fraction(float(lg[0])) - tot) <= abs(tot) * Fraction(1, 10 ** 15)
