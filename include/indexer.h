@@ -1,0 +1,228 @@
+/*
+ * indexer.h — C ABI of the GB300 (sm_103a) sparse-attention indexer.
+ *
+ * The indexer picks, for every query token, the k (<= 2048) cached keys that a
+ * sparse attention step will attend to:
+ *
+ *     logit[t, s] = sum_h w[t, h] * ReLU(scale_s * (q[t, h] . k_s)),   s < len_t
+ *     out[t]      = indices of the k largest logit[t, s]      (len_t >  k)
+ *     out[t]      = [0, 1, ..., len_t - 1, -1, ...]           (len_t <= k)
+ *
+ * over 64 index heads of dimension 128, reading the keys from a paged fp8 e4m3
+ * cache through a block table.
+ *
+ * Sources (web pages, by title and section):
+ *  [RUNNER]  "vllm.models.minimax_m3.amd.mono.runner" — token_rows: a request
+ *            of q query tokens becomes q rows, token j seeing
+ *            seq_len - (q - 1 - j) keys; StepTables: block table int32
+ *            [rows, width], seq_lens int32 [rows].
+ *  [INDEXER] "recipes/docker-images/glm52-nf3-hybrid/overlay/vllm/v1/attention/
+ *            backends/mla/indexer.py" — DeepseekV32IndexerBackend
+ *            (64-token blocks, cache shape (num_blocks, block_size, head_size),
+ *            head sizes 32/64/128), get_max_prefill_buffer_size (128 fp8 bytes +
+ *            4 scale bytes per entry), DeepSeekV32IndexerDecodeMetadata (2-D
+ *            (B, next_n) per-token seq_lens [b, j] = L_b - next_n + j + 1),
+ *            _prepare_decode_tensors (flatten path: worked example with
+ *            seq_lens [10, 7, 12, 0], decode_lens [3, 1, 4, 0]),
+ *            split_indexer_prefill_chunks (M*N logits-budget chunking),
+ *            _build_prefill_chunk_metadata_kernel (query i of a request sees
+ *            keys [0, seq_len - query_len + 1 + i)).
+ *  [GLM5]    "vllm.models.glm5next.common.sparse_indexer" — _decode_topk_seq_lens
+ *            (padded grid rows get seq_len 0), _fill_short_decode_causal_indices
+ *            (exact causal rows when every key would be selected),
+ *            _gather_workspace_shapes (fp8 values + 4-byte fp32 scale per token).
+ *  The scoring formula and k = 2048 are the method's statement; the pages only
+ *  name the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
+ *
+ * Data layout (all device memory unless a name ends in _host):
+ *  index cache  uint8 [num_pages, 8448]; page p holds 64 tokens as
+ *               [64 x 128 fp8 e4m3 codes][64 x fp32 scale] (the pages fix 132
+ *               bytes per token but not their order inside a page; values
+ *               first keeps every 128-byte key row 16-byte aligned for TMA).
+ *               Base address 16-byte aligned. Scales must be >= 0 and finite.
+ *  block_table  int32 [num_reqs, bt_width] with row stride bt_stride (elements);
+ *               entry c is the page holding tokens [64c, 64c + 64).
+ *  q            bf16 [rows, 64, 128] contiguous; weights fp32 [rows, 64].
+ *  out_idx      int32 [rows, topk] contiguous; request-relative token positions.
+ *               Rows with len > topk hold the selected set in no particular
+ *               order; rows with len <= topk hold the exact causal row.
+ *
+ * Conventions:
+ *  - The caller owns every buffer; the library never allocates device memory,
+ *    never synchronises the stream and never reads results back. Every call is
+ *    enqueued on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *  - Host-detectable problems return a status before anything is enqueued.
+ *  - Device-detectable problems (a block id outside [0, num_pages), a row
+ *    length < 0 or > bt_width*64, a pipeline wait that gave up) OR a bit into
+ *    *dev_error (nullable, a uint32 the caller zeroes) and never trap; the
+ *    affected rows' outputs are then unspecified. Bad lengths are clamped.
+ *  - Workspaces are caller-provided scratch of the size the *_workspace_bytes
+ *    query returns for the current device; contents need no initialisation and
+ *    are overwritten. Calls that share a workspace must not overlap.
+ */
+#ifndef SAIB_INDEXER_H
+#define SAIB_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  IDX_OK = 0,
+  IDX_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad alignment, bad mode */
+  IDX_ERR_UNSUPPORTED = 2,   /* heads != 64, head_dim != 128, topk outside [1, 2048], ... */
+  IDX_ERR_WORKSPACE = 3,     /* workspace smaller than the size query returned */
+  IDX_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  IDX_ERR_CAPACITY = 5       /* an output array is too small (chunk list) */
+} idx_status;
+
+/* Bits of the device error word. */
+#define IDX_DEV_BAD_BLOCK 1u /* a block-table entry outside [0, num_pages) was skipped */
+#define IDX_DEV_BAD_LEN 2u   /* a row length < 0 or > bt_width * 64 was clamped */
+#define IDX_DEV_TIMEOUT 4u   /* a pipeline wait gave up; the kernel returned early */
+#define IDX_DEV_OVERFLOW 8u  /* more token rows than the output holds (flatten mode) */
+
+#define IDX_NUM_HEADS 64
+#define IDX_HEAD_DIM 128
+#define IDX_PAGE_TOKENS 64
+#define IDX_PAGE_BYTES 8448
+#define IDX_MAX_TOPK 2048
+
+/* Human-readable name of a status code (static string). */
+const char* indexer_status_string(idx_status status);
+
+/*
+ * Decode row expansion ([INDEXER] _prepare_uniform_decode_kernel and the
+ * variable-length flatten branch of _prepare_decode_tensors; [RUNNER]
+ * token_rows; [GLM5] _decode_topk_seq_lens).
+ *
+ * Inputs: seq_lens int32 [num_reqs] (keys of the request including its new
+ * tokens), decode_lens int32 [num_reqs] (new tokens, 0 <= d <= next_n for
+ * mode 0), block_table as above.
+ * mode 0 (padded grid): row b*next_n + j gets len = L_b - d_b + j + 1 for
+ *   j < d_b and 0 otherwise; num_out_rows must be >= num_reqs*next_n.
+ * mode 1 (flatten): the d_b tokens of request b take consecutive rows starting
+ *   at sum_{b' < b} d_b' with the same len; rows from sum d_b up to
+ *   num_out_rows get len 0; more tokens than num_out_rows sets
+ *   IDX_DEV_OVERFLOW and drops the excess.
+ * row_block_table (nullable) int32 [num_out_rows, >= bt_width], row stride
+ *   out_stride: each token row gets its request's first bt_width entries;
+ *   in mode 1 rows past the last token get column 0 set to 0 (the rest is
+ *   left as it was).
+ */
+idx_status indexer_expand_decode_rows(const int32_t* seq_lens, const int32_t* decode_lens,
+                                      int32_t num_reqs, int32_t next_n,
+                                      const int32_t* block_table, int64_t bt_stride,
+                                      int32_t bt_width, int32_t mode, int32_t* row_seq_lens,
+                                      int32_t* row_block_table, int64_t out_stride,
+                                      int64_t num_out_rows, uint32_t* dev_error, void* stream);
+
+/*
+ * Per (row, head) fp8 quantisation of q, the reading this library takes for
+ * feeding bf16 q to an fp8 e4m3 MMA (the pages name an "fp8_fp4" paged MQA
+ * logits kernel but not its q path): amax = max_d |q|, inv = 448 / amax
+ * (fp32, correctly rounded), q8 = e4m3 round-to-nearest-even, saturating, of
+ * the fp32 product q * inv; sq = amax / 448; weights_scaled = w * sq. A head
+ * with amax == 0 gets q8 = 0 and weights_scaled = 0.
+ * q bf16 [rows, 64, 128]; weights fp32 [rows, 64]; q_fp8 uint8 [rows, 64, 128];
+ * weights_scaled fp32 [rows, 64]. The decode and prefill calls run this same
+ * step internally; it is exposed for inspection and tests.
+ */
+idx_status indexer_quantize_q(const void* q, const float* weights, int64_t num_rows,
+                              int32_t num_heads, int32_t head_dim, uint8_t* q_fp8,
+                              float* weights_scaled, void* stream);
+
+/* Bytes of workspace indexer_decode_topk / indexer_decode_logits need for
+ * num_reqs requests of next_n rows each, on the current CUDA device. */
+idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int32_t topk,
+                                          size_t* bytes);
+
+/*
+ * Decode top-k ([INDEXER] DeepSeekV32IndexerDecodeMetadata: the logits and top-k
+ * kernels see a (B, next_n) grid of per-token seq_lens; [GLM5]
+ * _fill_short_decode_causal_indices for rows with len <= topk).
+ *
+ * Token rows form a [num_reqs, next_n] grid: row b*next_n + j is token j of
+ * request b and reads block-table row b. row_seq_lens int32 [num_reqs*next_n]
+ * is the per-token key count (from indexer_expand_decode_rows; 0 = padded row,
+ * whose output is all -1). next_n is 1 or 2 (for longer speculative runs use
+ * mode 1 of the expansion with next_n = 1 and its row block table).
+ * num_heads must be 64, head_dim 128, 1 <= topk <= 2048.
+ * Writes out_idx [num_reqs*next_n, topk]. No logits row is written to memory.
+ */
+idx_status indexer_decode_topk(const void* q, const float* weights, const uint8_t* index_cache,
+                               int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                               int32_t bt_width, const int32_t* row_seq_lens, int32_t num_reqs,
+                               int32_t next_n, int32_t num_heads, int32_t head_dim, int32_t topk,
+                               int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_error, void* stream);
+
+/*
+ * The decode logits themselves, from the same quantisation, page gather and
+ * tensor-core scoring as indexer_decode_topk (for parity checks): for every
+ * token row t and key s < len_t writes out_logits[t * ld_logits + s]; other
+ * entries are left untouched. Same arguments as indexer_decode_topk (topk is
+ * only validated).
+ */
+idx_status indexer_decode_logits(const void* q, const float* weights, const uint8_t* index_cache,
+                                 int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                 int32_t bt_width, const int32_t* row_seq_lens, int32_t num_reqs,
+                                 int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                 int32_t topk, float* out_logits, int64_t ld_logits,
+                                 void* workspace, size_t workspace_bytes, uint32_t* dev_error,
+                                 void* stream);
+
+/*
+ * Host-only prefill chunk plan ([INDEXER] split_indexer_prefill_chunks): pack
+ * requests greedily while the summed key count N <= workspace_tokens and
+ * (summed query count M) * N <= logits_budget_bytes / 4; a request that fits
+ * alone in neither is taken by itself; cut each chunk's M queries into pieces
+ * of max(1, (logits_budget_bytes / 4) / N) (all of them when N == 0; a chunk
+ * with M == 0 yields no piece). Writes (req_begin, req_end, q_begin, q_end)
+ * rows into chunks [max_chunks, 4] (q relative to the chunk's first query) and
+ * the count into *num_chunks; IDX_ERR_CAPACITY if more are needed (then
+ * *num_chunks holds the count required). Host pointers only.
+ */
+idx_status indexer_plan_prefill_chunks(const int32_t* seq_lens_host,
+                                       const int32_t* query_lens_host, int32_t num_reqs,
+                                       int64_t workspace_tokens, int64_t logits_budget_bytes,
+                                       int32_t* chunks, int32_t max_chunks, int32_t* num_chunks);
+
+/* Bytes of workspace indexer_prefill_topk needs (host arrays as there). */
+idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
+                                           const int32_t* query_lens_host, int32_t num_reqs,
+                                           int32_t topk, int64_t workspace_tokens,
+                                           int64_t logits_budget_bytes, size_t* bytes);
+
+/*
+ * Prefill top-k ([INDEXER] split_indexer_prefill_chunks,
+ * build_prefill_chunk_metadata and _build_prefill_chunk_metadata_kernel).
+ * Query token i of request r (global row query_start_loc[r] + i) sees keys
+ * [0, seq_len_r - query_len_r + 1 + i) of request r (block-table row r).
+ * The chunk plan above is computed from the host copies and the chunks are
+ * enqueued in order; results do not depend on the plan (no logits are
+ * materialised; the plan bounds each launch's rows the way the pages bound
+ * their M x N logits buffer).
+ * q bf16 [total_q, 64, 128], weights fp32 [total_q, 64], seq_lens int32 [R],
+ * query_start_loc int32 [R + 1] (device), seq_lens_host / query_lens_host
+ * int32 [R] (host, equal to the device data; 0 <= query_len <= seq_len);
+ * out_idx int32 [total_q, topk].
+ */
+idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8_t* index_cache,
+                                int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                int32_t bt_width, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, const int32_t* seq_lens_host,
+                                const int32_t* query_lens_host, int32_t num_reqs,
+                                int32_t num_heads, int32_t head_dim, int32_t topk,
+                                int64_t workspace_tokens, int64_t logits_budget_bytes,
+                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_error, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAIB_INDEXER_H */

@@ -1,0 +1,244 @@
+"""Thin ctypes binding of the indexer's C ABI (``include/indexer.h``).
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers, sizes and the current CUDA stream to the function of the same name
+in ``libsaib.so`` and raises :class:`IndexerError` on a non-OK status. Torch is
+used for device memory (outputs and workspaces the caller did not pass) and
+streams. There is no fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsaib.so")
+
+IDX_OK = 0
+STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
+                3: "IDX_ERR_WORKSPACE", 4: "IDX_ERR_CUDA", 5: "IDX_ERR_CAPACITY"}
+DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_TIMEOUT, DEV_OVERFLOW = 1, 2, 4, 8
+NUM_HEADS, HEAD_DIM, PAGE_TOKENS, PAGE_BYTES, MAX_TOPK = 64, 128, 64, 8448, 2048
+
+# exported symbols and their ctypes signatures (kept in step with indexer.h)
+_P, _I32, _I64, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+SIGNATURES = {
+    "indexer_status_string": (C.c_char_p, [C.c_int]),
+    "indexer_expand_decode_rows": (C.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32, _P, _P,
+                                             _I64, _I64, _P, _P]),
+    "indexer_quantize_q": (C.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "indexer_decode_workspace_bytes": (C.c_int, [_I32, _I32, _I32, C.POINTER(_SZ)]),
+    "indexer_decode_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
+                                      _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "indexer_decode_logits": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
+                                        _I32, _I32, _P, _I64, _P, _SZ, _P, _P]),
+    "indexer_plan_prefill_chunks": (C.c_int, [_P, _P, _I32, _I64, _I64, _P, _I32,
+                                              C.POINTER(_I32)]),
+    "indexer_prefill_workspace_bytes": (C.c_int, [_P, _P, _I32, _I32, _I64, _I64,
+                                                  C.POINTER(_SZ)]),
+    "indexer_prefill_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P, _I32,
+                                       _I32, _I32, _I32, _I64, _I64, _P, _P, _SZ, _P, _P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class IndexerError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH):
+    """Loads libsaib.so (build it with ``build.build()`` first)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"indexer CUDA library not built ({path}); run "
+                               "sparse_attention_indexer_block_gb300.build.build()")
+        lib = C.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return C.c_void_p(t)
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _check(name, st):
+    if st != IDX_OK:
+        raise IndexerError(name, st)
+
+
+def _host_i32(t):
+    import numpy as np
+    if isinstance(t, torch.Tensor):
+        t = t.detach().cpu().numpy()
+    return np.ascontiguousarray(t, dtype=np.int32)
+
+
+def indexer_status_string(status: int) -> str:
+    return load().indexer_status_string(status).decode()
+
+
+def indexer_expand_decode_rows(seq_lens, decode_lens, next_n: int, mode: int = 0,
+                               block_table=None, row_seq_lens=None, row_block_table=None,
+                               num_out_rows: int | None = None, want_block_table: bool = False,
+                               dev_error=None, stream=None):
+    R = int(seq_lens.shape[0])
+    if num_out_rows is None:
+        num_out_rows = R * next_n
+    dev = seq_lens.device
+    if row_seq_lens is None:
+        row_seq_lens = torch.empty(num_out_rows, dtype=torch.int32, device=dev)
+    W, bt_stride, out_stride = 0, 0, 0
+    if block_table is not None:
+        W = int(block_table.shape[1])
+        bt_stride = int(block_table.stride(0))
+        if row_block_table is None and want_block_table:
+            row_block_table = torch.zeros((num_out_rows, W), dtype=torch.int32, device=dev)
+        if row_block_table is not None:
+            out_stride = int(row_block_table.stride(0))
+    st = load().indexer_expand_decode_rows(
+        _ptr(seq_lens), _ptr(decode_lens), R, next_n, _ptr(block_table), bt_stride, W, mode,
+        _ptr(row_seq_lens), _ptr(row_block_table), out_stride, num_out_rows, _ptr(dev_error),
+        _stream(stream))
+    _check("indexer_expand_decode_rows", st)
+    return row_seq_lens, row_block_table
+
+
+def indexer_quantize_q(q, weights, q_fp8=None, weights_scaled=None, stream=None):
+    rows = int(q.shape[0])
+    if q_fp8 is None:
+        q_fp8 = torch.empty((rows, NUM_HEADS, HEAD_DIM), dtype=torch.uint8, device=q.device)
+    if weights_scaled is None:
+        weights_scaled = torch.empty((rows, NUM_HEADS), dtype=torch.float32, device=q.device)
+    st = load().indexer_quantize_q(_ptr(q), _ptr(weights), rows, int(q.shape[1]),
+                                   int(q.shape[2]), _ptr(q_fp8), _ptr(weights_scaled),
+                                   _stream(stream))
+    _check("indexer_quantize_q", st)
+    return q_fp8, weights_scaled
+
+
+def indexer_decode_workspace_bytes(num_reqs: int, next_n: int, topk: int) -> int:
+    out = C.c_size_t(0)
+    _check("indexer_decode_workspace_bytes",
+           load().indexer_decode_workspace_bytes(num_reqs, next_n, topk, C.byref(out)))
+    return int(out.value)
+
+
+def decode_workspace(num_reqs: int, next_n: int, topk: int, device="cuda"):
+    n = indexer_decode_workspace_bytes(num_reqs, next_n, topk)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def indexer_decode_topk(q, weights, index_cache, block_table, row_seq_lens, next_n: int,
+                        topk: int = MAX_TOPK, out_idx=None, workspace=None, dev_error=None,
+                        stream=None):
+    R = int(block_table.shape[0])
+    rows = R * next_n
+    if out_idx is None:
+        out_idx = torch.empty((rows, topk), dtype=torch.int32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, next_n, topk, q.device)
+    st = load().indexer_decode_topk(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, next_n,
+        int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_idx), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_topk", st)
+    return out_idx
+
+
+def indexer_decode_logits(q, weights, index_cache, block_table, row_seq_lens, next_n: int,
+                          topk: int = MAX_TOPK, out_logits=None, workspace=None, dev_error=None,
+                          stream=None):
+    R = int(block_table.shape[0])
+    rows = R * next_n
+    ld = int(block_table.shape[1]) * PAGE_TOKENS
+    if out_logits is None:
+        out_logits = torch.full((rows, ld), float("nan"), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, next_n, topk, q.device)
+    st = load().indexer_decode_logits(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, next_n,
+        int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_logits), int(out_logits.stride(0)),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(dev_error),
+        _stream(stream))
+    _check("indexer_decode_logits", st)
+    return out_logits
+
+
+def indexer_plan_prefill_chunks(seq_lens, query_lens, workspace_tokens: int,
+                                logits_budget_bytes: int):
+    import numpy as np
+    sl, ql = _host_i32(seq_lens), _host_i32(query_lens)
+    lib = load()
+    cap = 64
+    while True:
+        buf = np.zeros((cap, 4), np.int32)
+        n = C.c_int32(0)
+        st = lib.indexer_plan_prefill_chunks(sl.ctypes.data, ql.ctypes.data, sl.shape[0],
+                                             workspace_tokens, logits_budget_bytes,
+                                             buf.ctypes.data, cap, C.byref(n))
+        if st == 5:  # capacity
+            cap = int(n.value)
+            continue
+        _check("indexer_plan_prefill_chunks", st)
+        return [tuple(int(v) for v in buf[i]) for i in range(n.value)]
+
+
+def indexer_prefill_workspace_bytes(seq_lens_host, query_lens_host, topk: int,
+                                    workspace_tokens: int, logits_budget_bytes: int) -> int:
+    sl, ql = _host_i32(seq_lens_host), _host_i32(query_lens_host)
+    out = C.c_size_t(0)
+    _check("indexer_prefill_workspace_bytes",
+           load().indexer_prefill_workspace_bytes(sl.ctypes.data, ql.ctypes.data, sl.shape[0], topk,
+                                                  workspace_tokens, logits_budget_bytes,
+                                                  C.byref(out)))
+    return int(out.value)
+
+
+def indexer_prefill_topk(q, weights, index_cache, block_table, seq_lens, query_start_loc,
+                         seq_lens_host, query_lens_host, topk: int = MAX_TOPK,
+                         workspace_tokens: int = 40 * 8192, logits_budget_bytes: int = 512 << 20,
+                         out_idx=None, workspace=None, dev_error=None, stream=None):
+    sl, ql = _host_i32(seq_lens_host), _host_i32(query_lens_host)
+    total_q = int(q.shape[0])
+    if out_idx is None:
+        out_idx = torch.empty((total_q, topk), dtype=torch.int32, device=q.device)
+    if workspace is None:
+        n = indexer_prefill_workspace_bytes(sl, ql, topk, workspace_tokens, logits_budget_bytes)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    st = load().indexer_prefill_topk(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(seq_lens),
+        _ptr(query_start_loc), sl.ctypes.data, ql.ctypes.data, sl.shape[0], int(q.shape[1]),
+        int(q.shape[2]), topk, workspace_tokens, logits_budget_bytes, _ptr(out_idx),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), _ptr(dev_error),
+        _stream(stream))
+    _check("indexer_prefill_topk", st)
+    return out_idx

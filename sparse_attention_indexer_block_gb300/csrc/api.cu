@@ -1,0 +1,410 @@
+// C ABI of the indexer: argument validation, workspace carve-up, the host
+// prefill chunk planner and the launch sequences.
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace saib {
+
+namespace {
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes, size_t align) {
+    off = round_up(off, align);
+    const size_t o = off;
+    off += bytes;
+    return o;
+  };
+  const int64_t nslots = static_cast<int64_t>(num_ctas) + num_wr;
+  L.wr = take(sizeof(WorkRow) * static_cast<size_t>(num_wr), 256);
+  L.wr_tile_start = take(4 * static_cast<size_t>(num_wr + 1), 256);
+  L.row_len = take(4 * static_cast<size_t>(rows), 256);
+  L.seg_counter = take(4 * static_cast<size_t>(num_wr), 256);
+  L.slot_count = take(4 * static_cast<size_t>(nslots * G), 256);
+  L.q8 = take(static_cast<size_t>(rows) * kQRowBytes, 1024);
+  L.wprime = take(4 * static_cast<size_t>(rows) * kHeads, 256);
+  L.slot_key = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
+  L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
+  L.total = round_up(off, 256);
+  return L;
+}
+
+int device_sm_count() {
+  static int cached[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 128 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 1;
+  if (dev < 128) cached[dev] = n;
+  return n;
+}
+
+idx_status encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return IDX_ERR_CUDA;
+  // [page][token][128 bytes]: one box is one page's 64 key rows (8 KB).
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kPageTokens),
+                              static_cast<cuuint64_t>(num_pages)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kPageBytes)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kDim), static_cast<cuuint32_t>(kPageTokens), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(cache), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IDX_OK : IDX_ERR_CUDA;
+}
+
+namespace {
+
+// Greedy chunking of prefill requests (split_indexer_prefill_chunks of the
+// vLLM sparse-indexer backend): pack requests while the summed key count stays
+// within the workspace and the M x N fp32 logits within the budget; a request
+// that fits alone in neither goes by itself; cut each chunk's queries into
+// pieces of max(1, budget_elems / N).
+struct Chunk {
+  int32_t r0, r1, q0, q1;
+};
+
+std::vector<Chunk> plan_chunks(const int32_t* sl, const int32_t* ql, int32_t n, int64_t ws_tokens,
+                               int64_t budget_bytes) {
+  std::vector<Chunk> out;
+  const int64_t elems = budget_bytes / 4;
+  int32_t end = 0;
+  while (end < n) {
+    const int32_t start = end;
+    int64_t m = 0, keys = 0;
+    for (; end < n; ++end) {
+      const int64_t nm = m + ql[end], nk = keys + sl[end];
+      if (nk > ws_tokens || nm * nk > elems) break;
+      m = nm;
+      keys = nk;
+    }
+    if (end == start) {
+      m = ql[end];
+      keys = sl[end];
+      ++end;
+    }
+    const int64_t piece = keys > 0 ? std::max<int64_t>(1, elems / keys) : m;
+    for (int64_t q = 0; q < m; q += piece)
+      out.push_back(Chunk{start, end, static_cast<int32_t>(q),
+                          static_cast<int32_t>(std::min(m, q + piece))});
+  }
+  return out;
+}
+
+// Work rows of a chunk: groups of up to 4 consecutive queries of one request.
+int64_t chunk_work_rows(const std::vector<int64_t>& qsl, const Chunk& c, int64_t* row_lo,
+                        int64_t* row_hi) {
+  *row_lo = qsl[c.r0] + c.q0;
+  *row_hi = qsl[c.r0] + c.q1;
+  int64_t nw = 0;
+  for (int32_t r = c.r0; r < c.r1; ++r) {
+    const int64_t lo = std::max(qsl[r], *row_lo), hi = std::min(qsl[r + 1], *row_hi);
+    if (hi > lo) nw += (hi - lo + 3) / 4;
+  }
+  return nw;
+}
+
+constexpr int kPrefillG = 4;
+
+idx_status check_common(const void* q, const float* w, const uint8_t* cache, int64_t num_pages,
+                        const int32_t* bt, int64_t bt_stride, int32_t bt_width, int32_t num_heads,
+                        int32_t head_dim, int32_t topk) {
+  if (!q || !w || !cache || !bt) return IDX_ERR_INVALID_ARG;
+  if (num_pages < 1 || num_pages > INT32_MAX || bt_width < 1 || bt_stride < bt_width)
+    return IDX_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(w, 4) || !aligned(cache, 16) || !aligned(bt, 4))
+    return IDX_ERR_INVALID_ARG;
+  if (num_heads != kHeads || head_dim != kDim) return IDX_ERR_UNSUPPORTED;
+  if (topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
+  return IDX_OK;
+}
+
+idx_status decode_common(bool logits, const void* q, const float* weights,
+                         const uint8_t* index_cache, int64_t num_pages, const int32_t* block_table,
+                         int64_t bt_stride, int32_t bt_width, const int32_t* row_seq_lens,
+                         int32_t num_reqs, int32_t next_n, int32_t num_heads, int32_t head_dim,
+                         int32_t topk, int32_t* out_idx, float* out_logits, int64_t ld_logits,
+                         void* workspace, size_t workspace_bytes, uint32_t* dev_error,
+                         void* stream) {
+  if (num_reqs < 0) return IDX_ERR_INVALID_ARG;
+  if (next_n != 1 && next_n != 2) return IDX_ERR_UNSUPPORTED;
+  idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                               num_heads, head_dim, topk);
+  if (st != IDX_OK) return st;
+  if (!row_seq_lens || !workspace || !aligned(workspace, 256)) return IDX_ERR_INVALID_ARG;
+  if (logits) {
+    if (!out_logits || ld_logits < static_cast<int64_t>(bt_width) * kPageTokens)
+      return IDX_ERR_INVALID_ARG;
+  } else if (!out_idx) {
+    return IDX_ERR_INVALID_ARG;
+  }
+  if (num_reqs == 0) return IDX_OK;
+  const int nC = device_sm_count();
+  const int64_t rows = static_cast<int64_t>(num_reqs) * next_n;
+  const WsLayout L = ws_layout(num_reqs, rows, next_n, topk, nC);
+  if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
+  CUtensorMap map;
+  if ((st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
+                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error};
+  if ((st = launch_decode_prep(a, ws, L, s)) != IDX_OK) return st;
+  ScoreParams p{};
+  p.cache = index_cache;
+  p.num_pages = num_pages;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
+  p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
+  p.num_wr = num_reqs;
+  p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
+  p.q8 = ws + L.q8;
+  p.wprime = reinterpret_cast<const float*>(ws + L.wprime);
+  p.seg_counter = reinterpret_cast<int32_t*>(ws + L.seg_counter);
+  p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
+  p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
+  p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+  p.out_idx = out_idx;
+  p.out_row_base = 0;
+  p.topk = topk;
+  p.out_logits = out_logits;
+  p.ld_logits = ld_logits;
+  p.dev_error = dev_error;
+  return launch_score(next_n, logits, p, map, nC, s);
+}
+
+}  // namespace
+}  // namespace saib
+
+using namespace saib;
+
+extern "C" {
+
+const char* indexer_status_string(idx_status status) {
+  switch (status) {
+    case IDX_OK: return "ok";
+    case IDX_ERR_INVALID_ARG: return "invalid argument";
+    case IDX_ERR_UNSUPPORTED: return "unsupported configuration";
+    case IDX_ERR_WORKSPACE: return "workspace too small";
+    case IDX_ERR_CUDA: return "CUDA error";
+    case IDX_ERR_CAPACITY: return "output capacity too small";
+  }
+  return "unknown status";
+}
+
+idx_status indexer_expand_decode_rows(const int32_t* seq_lens, const int32_t* decode_lens,
+                                      int32_t num_reqs, int32_t next_n,
+                                      const int32_t* block_table, int64_t bt_stride,
+                                      int32_t bt_width, int32_t mode, int32_t* row_seq_lens,
+                                      int32_t* row_block_table, int64_t out_stride,
+                                      int64_t num_out_rows, uint32_t* dev_error, void* stream) {
+  if (num_reqs < 0 || next_n < 1 || (mode != 0 && mode != 1) || num_out_rows < 0)
+    return IDX_ERR_INVALID_ARG;
+  if ((num_reqs > 0 && (!seq_lens || !decode_lens)) || (num_out_rows > 0 && !row_seq_lens))
+    return IDX_ERR_INVALID_ARG;
+  if (mode == 0 && num_out_rows < static_cast<int64_t>(num_reqs) * next_n)
+    return IDX_ERR_CAPACITY;
+  if (row_block_table && (!block_table || bt_width < 1 || bt_stride < bt_width ||
+                          out_stride < bt_width))
+    return IDX_ERR_INVALID_ARG;
+  if (num_reqs == 0 && (mode == 0 || num_out_rows == 0)) return IDX_OK;
+  return launch_expand(seq_lens, decode_lens, num_reqs, next_n, block_table, bt_stride, bt_width,
+                       mode, row_seq_lens, row_block_table, out_stride, num_out_rows, dev_error,
+                       static_cast<cudaStream_t>(stream));
+}
+
+idx_status indexer_quantize_q(const void* q, const float* weights, int64_t num_rows,
+                              int32_t num_heads, int32_t head_dim, uint8_t* q_fp8,
+                              float* weights_scaled, void* stream) {
+  if (num_rows < 0) return IDX_ERR_INVALID_ARG;
+  if (num_heads != kHeads || head_dim != kDim) return IDX_ERR_UNSUPPORTED;
+  if (num_rows == 0) return IDX_OK;
+  if (!q || !weights || !q_fp8 || !weights_scaled || !aligned(q, 16) || !aligned(q_fp8, 4))
+    return IDX_ERR_INVALID_ARG;
+  return launch_quantize_plain(static_cast<const __nv_bfloat16*>(q), weights, num_rows, q_fp8,
+                               weights_scaled, static_cast<cudaStream_t>(stream));
+}
+
+idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int32_t topk,
+                                          size_t* bytes) {
+  if (!bytes || num_reqs < 0) return IDX_ERR_INVALID_ARG;
+  if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk,
+                               device_sm_count());
+  *bytes = L.total;
+  return IDX_OK;
+}
+
+idx_status indexer_decode_topk(const void* q, const float* weights, const uint8_t* index_cache,
+                               int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                               int32_t bt_width, const int32_t* row_seq_lens, int32_t num_reqs,
+                               int32_t next_n, int32_t num_heads, int32_t head_dim, int32_t topk,
+                               int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_error, void* stream) {
+  return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       row_seq_lens, num_reqs, next_n, num_heads, head_dim, topk, out_idx, nullptr,
+                       0, workspace, workspace_bytes, dev_error, stream);
+}
+
+idx_status indexer_decode_logits(const void* q, const float* weights, const uint8_t* index_cache,
+                                 int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                 int32_t bt_width, const int32_t* row_seq_lens, int32_t num_reqs,
+                                 int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                 int32_t topk, float* out_logits, int64_t ld_logits,
+                                 void* workspace, size_t workspace_bytes, uint32_t* dev_error,
+                                 void* stream) {
+  return decode_common(true, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       row_seq_lens, num_reqs, next_n, num_heads, head_dim, topk, nullptr,
+                       out_logits, ld_logits, workspace, workspace_bytes, dev_error, stream);
+}
+
+idx_status indexer_plan_prefill_chunks(const int32_t* seq_lens_host,
+                                       const int32_t* query_lens_host, int32_t num_reqs,
+                                       int64_t workspace_tokens, int64_t logits_budget_bytes,
+                                       int32_t* chunks, int32_t max_chunks, int32_t* num_chunks) {
+  if (num_reqs < 0 || !num_chunks || max_chunks < 0 || (max_chunks > 0 && !chunks))
+    return IDX_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (!seq_lens_host || !query_lens_host)) return IDX_ERR_INVALID_ARG;
+  if (workspace_tokens < 0 || logits_budget_bytes < 0) return IDX_ERR_INVALID_ARG;
+  const std::vector<Chunk> plan =
+      plan_chunks(seq_lens_host, query_lens_host, num_reqs, workspace_tokens, logits_budget_bytes);
+  *num_chunks = static_cast<int32_t>(plan.size());
+  if (static_cast<int64_t>(plan.size()) > max_chunks) return IDX_ERR_CAPACITY;
+  for (size_t i = 0; i < plan.size(); ++i) {
+    chunks[4 * i + 0] = plan[i].r0;
+    chunks[4 * i + 1] = plan[i].r1;
+    chunks[4 * i + 2] = plan[i].q0;
+    chunks[4 * i + 3] = plan[i].q1;
+  }
+  return IDX_OK;
+}
+
+namespace {
+
+idx_status prefill_plan(const int32_t* sl, const int32_t* ql, int32_t num_reqs,
+                        int64_t workspace_tokens, int64_t budget, std::vector<Chunk>* plan,
+                        std::vector<int64_t>* qsl, int64_t* max_wr, int64_t* max_rows) {
+  if (num_reqs < 0 || (num_reqs > 0 && (!sl || !ql)) || workspace_tokens < 0 || budget < 0)
+    return IDX_ERR_INVALID_ARG;
+  qsl->assign(num_reqs + 1, 0);
+  for (int32_t r = 0; r < num_reqs; ++r) {
+    if (ql[r] < 0 || sl[r] < 0 || ql[r] > sl[r]) return IDX_ERR_INVALID_ARG;
+    (*qsl)[r + 1] = (*qsl)[r] + ql[r];
+  }
+  *plan = plan_chunks(sl, ql, num_reqs, workspace_tokens, budget);
+  *max_wr = 0;
+  *max_rows = 0;
+  for (const Chunk& c : *plan) {
+    int64_t lo, hi;
+    const int64_t nw = chunk_work_rows(*qsl, c, &lo, &hi);
+    *max_wr = std::max(*max_wr, nw);
+    *max_rows = std::max(*max_rows, hi - lo);
+  }
+  return IDX_OK;
+}
+
+}  // namespace
+
+idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
+                                           const int32_t* query_lens_host, int32_t num_reqs,
+                                           int32_t topk, int64_t workspace_tokens,
+                                           int64_t logits_budget_bytes, size_t* bytes) {
+  if (!bytes) return IDX_ERR_INVALID_ARG;
+  if (topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
+  std::vector<Chunk> plan;
+  std::vector<int64_t> qsl;
+  int64_t max_wr, max_rows;
+  const idx_status st = prefill_plan(seq_lens_host, query_lens_host, num_reqs, workspace_tokens,
+                                     logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows);
+  if (st != IDX_OK) return st;
+  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, device_sm_count()).total;
+  return IDX_OK;
+}
+
+idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8_t* index_cache,
+                                int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                int32_t bt_width, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, const int32_t* seq_lens_host,
+                                const int32_t* query_lens_host, int32_t num_reqs,
+                                int32_t num_heads, int32_t head_dim, int32_t topk,
+                                int64_t workspace_tokens, int64_t logits_budget_bytes,
+                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_error, void* stream) {
+  idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                               num_heads, head_dim, topk);
+  if (st != IDX_OK) return st;
+  if (!seq_lens || !query_start_loc || !out_idx || !workspace || !aligned(workspace, 256))
+    return IDX_ERR_INVALID_ARG;
+  std::vector<Chunk> plan;
+  std::vector<int64_t> qsl;
+  int64_t max_wr, max_rows;
+  if ((st = prefill_plan(seq_lens_host, query_lens_host, num_reqs, workspace_tokens,
+                         logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows)) != IDX_OK)
+    return st;
+  if (plan.empty()) return IDX_OK;
+  const int nC = device_sm_count();
+  const WsLayout L = ws_layout(max_wr, max_rows, kPrefillG, topk, nC);
+  if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
+  CUtensorMap map;
+  if ((st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  for (const Chunk& c : plan) {
+    int64_t lo, hi;
+    const int64_t nw = chunk_work_rows(qsl, c, &lo, &hi);
+    if (nw == 0) continue;
+    PrefillPrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, seq_lens, query_start_loc,
+                      c.r0, c.r1, lo, hi, static_cast<int32_t>(nw), topk, bt_width, out_idx,
+                      dev_error};
+    if ((st = launch_prefill_prep(a, ws, L, s)) != IDX_OK) return st;
+    ScoreParams p{};
+    p.cache = index_cache;
+    p.num_pages = num_pages;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
+    p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
+    p.num_wr = static_cast<int32_t>(nw);
+    p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
+    p.q8 = ws + L.q8;
+    p.wprime = reinterpret_cast<const float*>(ws + L.wprime);
+    p.seg_counter = reinterpret_cast<int32_t*>(ws + L.seg_counter);
+    p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
+    p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
+    p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+    p.out_idx = out_idx;
+    p.out_row_base = lo;
+    p.topk = topk;
+    p.dev_error = dev_error;
+    if ((st = launch_score(kPrefillG, false, p, map, nC, s)) != IDX_OK) return st;
+  }
+  return IDX_OK;
+}
+
+}  // extern "C"

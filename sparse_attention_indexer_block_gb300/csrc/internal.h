@@ -1,0 +1,92 @@
+// Internal launch interfaces shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace saib {
+
+// Everything the score/select kernel reads, for one launch.
+struct ScoreParams {
+  const uint8_t* cache;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const WorkRow* wr;
+  const int32_t* wr_tile_start;  // [num_wr + 1], exclusive prefix of tiles per work row
+  int32_t num_wr;
+  const int32_t* row_len;        // [rows] validated key count per token row
+  const uint8_t* q8;             // [rows, 8192] swizzled fp8 images of q
+  const float* wprime;           // [rows, 64] w * sq
+  int32_t* seg_counter;          // [num_wr] finished segments per work row
+  uint32_t* slot_key;            // [nslots, G, topk] candidate keys of finished segments
+  int32_t* slot_idx;             // [nslots, G, topk] their token indices
+  int32_t* slot_count;           // [nslots, G]
+  int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
+  int64_t out_row_base;
+  int32_t topk;
+  float* out_logits;             // logits mode only
+  int64_t ld_logits;
+  uint32_t* dev_error;
+};
+
+// Workspace carve-up shared by decode and prefill.
+struct WsLayout {
+  size_t wr, wr_tile_start, row_len, seg_counter, slot_count, q8, wprime, slot_key, slot_idx;
+  size_t total;
+};
+WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
+
+// Per-device facts and one-time setup.
+int device_sm_count();
+idx_status encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages);
+
+// Kernel launchers (return IDX_ERR_CUDA on a launch failure).
+idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, int32_t num_reqs,
+                         int32_t next_n, const int32_t* bt, int64_t bt_stride, int32_t bt_width,
+                         int32_t mode, int32_t* row_lens, int32_t* row_bt, int64_t out_stride,
+                         int64_t num_out_rows, uint32_t* err, cudaStream_t s);
+
+idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows,
+                                 uint8_t* q8, float* wprime, cudaStream_t s);
+
+struct DecodePrepArgs {
+  const __nv_bfloat16* q;
+  const float* w;
+  const int32_t* row_seq_lens;
+  int32_t num_reqs;
+  int32_t next_n;
+  int32_t topk;
+  int32_t bt_width;
+  int32_t score_all;  // logits mode: every row with len > 0 is scored
+  int32_t* out_idx;   // causal fill target (nullable in logits mode)
+  uint32_t* err;
+};
+idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
+                              cudaStream_t s);
+
+struct PrefillPrepArgs {
+  const __nv_bfloat16* q;
+  const float* w;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t req_begin, req_end;  // requests of the chunk
+  int64_t row_lo, row_hi;      // global query rows of the chunk
+  int32_t num_wr;              // work rows of the chunk (host count)
+  int32_t topk;
+  int32_t bt_width;
+  int32_t* out_idx;
+  uint32_t* err;
+};
+idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
+                               cudaStream_t s);
+
+// G = token rows per work row (1, 2 or 4); logits = write logits instead of selecting.
+idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
+                        int num_ctas, cudaStream_t s);
+
+}  // namespace saib

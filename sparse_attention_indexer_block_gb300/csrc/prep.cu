@@ -1,0 +1,385 @@
+// Row expansion, q quantisation, and the per-launch schedule + causal fill that
+// precede the score/select kernel.
+#include "internal.h"
+
+namespace saib {
+
+namespace {
+
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
+
+// Exclusive scan of one int per thread over a block of kPrepThreads threads.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int warp_tot[kPrepWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kPrepWarps ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    if (lane < kPrepWarps) warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int before = warp > 0 ? warp_tot[warp - 1] : 0;
+  *total = warp_tot[kPrepWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__device__ __forceinline__ int64_t clamp_len(int64_t v, int64_t bt_width, uint32_t* err,
+                                             bool report) {
+  const int64_t cap = bt_width * kPageTokens;
+  if (v < 0) {
+    if (report) set_error(err, IDX_DEV_BAD_LEN);
+    return 0;
+  }
+  if (v > cap) {
+    if (report) set_error(err, IDX_DEV_BAD_LEN);
+    return cap;
+  }
+  return v;
+}
+
+// One warp quantises one head of 128 bf16 values: lane l owns elements
+// [4l, 4l + 4). Returns the four e4m3 codes of the lane (element 4l in the
+// low byte) and, in *wp, w * amax / 448 (all lanes).
+__device__ __forceinline__ uint32_t quantize_head(const __nv_bfloat16* src, float w, int lane,
+                                                  float* wp) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  const float x0 = __uint_as_float(raw.x << 16);
+  const float x1 = __uint_as_float(raw.x & 0xffff0000u);
+  const float x2 = __uint_as_float(raw.y << 16);
+  const float x3 = __uint_as_float(raw.y & 0xffff0000u);
+  float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (amax == 0.0f) {
+    *wp = 0.0f;
+    return 0u;
+  }
+  const float inv = __fdiv_rn(448.0f, amax);
+  const uint32_t lo = cvt_e4m3x2(__fmul_rn(x0, inv), __fmul_rn(x1, inv));
+  const uint32_t hi = cvt_e4m3x2(__fmul_rn(x2, inv), __fmul_rn(x3, inv));
+  *wp = __fmul_rn(w, __fdiv_rn(amax, 448.0f));
+  return lo | (hi << 16);
+}
+
+// Byte offset, inside a token row's 8 KB fp8 image, of the 4 codes lane `lane`
+// holds for head h, in the layout the MMA reads: 128-byte rows (one per head)
+// whose 16-byte chunks are XOR-swizzled by (head & 7) — the 128-byte swizzle
+// a TMA copy would produce for a 1024-byte aligned tile.
+__device__ __forceinline__ uint32_t swizzled_offset(int h, int lane) {
+  return static_cast<uint32_t>(h) * 128u + ((static_cast<uint32_t>(lane >> 2) ^ (h & 7)) << 4) +
+         (static_cast<uint32_t>(lane & 3) << 2);
+}
+
+// -------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
+    const __nv_bfloat16* __restrict__ q, const float* __restrict__ w, int64_t rows,
+    uint8_t* __restrict__ q8, float* __restrict__ wprime) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * kPrepThreads) >> 5;
+  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
+    float wp;
+    const uint32_t c = quantize_head(q + idx * kDim, w[idx], lane, &wp);
+    *reinterpret_cast<uint32_t*>(q8 + idx * kDim + 4 * lane) = c;
+    if (lane == 0) wprime[idx] = wp;
+  }
+}
+
+// Block 0: work-row schedule (tile counts and their exclusive prefix), validated
+// row lengths and zeroed segment counters. Other blocks: q quantisation into
+// the swizzled images and the exact causal rows of short rows.
+__global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
+    DecodePrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
+    int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
+    float* __restrict__ wprime) {
+  const int G = a.next_n;
+  const int64_t rows = static_cast<int64_t>(a.num_reqs) * G;
+  if (blockIdx.x == 0) {
+    int carry = 0;
+    for (int base = 0; base < a.num_reqs; base += kPrepThreads) {
+      const int b = base + threadIdx.x;
+      int tiles = 0;
+      if (b < a.num_reqs) {
+        int maxlen = 0;
+        for (int g = 0; g < G; ++g) {
+          const int64_t r = static_cast<int64_t>(b) * G + g;
+          const int len = static_cast<int>(clamp_len(a.row_seq_lens[r], a.bt_width, a.err, true));
+          row_len[r] = len;
+          const bool active = a.score_all ? len > 0 : len > a.topk;
+          if (active) maxlen = max(maxlen, len);
+        }
+        tiles = (maxlen + kTileKeys - 1) / kTileKeys;
+        wr[b] = WorkRow{b, b * G, G, maxlen};
+        seg_counter[b] = 0;
+      }
+      int total;
+      const int excl = block_exclusive_scan(tiles, &total);
+      if (b < a.num_reqs) wts[b] = carry + excl;
+      carry += total;
+    }
+    if (threadIdx.x == 0) wts[a.num_reqs] = carry;
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
+  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
+    const int64_t r = idx / kHeads;
+    const int h = static_cast<int>(idx % kHeads);
+    float wp;
+    const uint32_t c = quantize_head(a.q + idx * kDim, a.w[idx], lane, &wp);
+    *reinterpret_cast<uint32_t*>(q8img + r * kQRowBytes + swizzled_offset(h, lane)) = c;
+    if (lane == 0) wprime[idx] = wp;
+  }
+  if (!a.score_all) {
+    for (int64_t r = gw; r < rows; r += nw) {
+      const int64_t len = clamp_len(a.row_seq_lens[r], a.bt_width, a.err, false);
+      if (len > a.topk) continue;
+      int32_t* o = a.out_idx + r * a.topk;
+      for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;
+    }
+  }
+}
+
+// Request owning global query row `row` among requests [r0, r1).
+__device__ __forceinline__ int find_request(const int32_t* qsl, int r0, int r1, int64_t row) {
+  int lo = r0, hi = r1 - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (qsl[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int64_t prefill_len(const PrefillPrepArgs& a, int r, int64_t row,
+                                               bool report) {
+  const int64_t qs = a.qsl[r], qe = a.qsl[r + 1];
+  const int64_t v = static_cast<int64_t>(a.seq_lens[r]) - (qe - qs) + 1 + (row - qs);
+  return clamp_len(v, a.bt_width, a.err, report);
+}
+
+// Block 0: work rows of the chunk (up to four consecutive queries of one
+// request each), their tile prefix and zeroed segment counters. Other blocks:
+// row lengths, q quantisation and the causal rows of short queries.
+__global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
+    PrefillPrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
+    int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
+    float* __restrict__ wprime) {
+  constexpr int G = 4;
+  const int64_t rows = a.row_hi - a.row_lo;
+  if (blockIdx.x == 0) {
+    int carry = 0;
+    for (int base = a.req_begin; base < a.req_end; base += kPrepThreads) {
+      const int r = base + threadIdx.x;
+      int nw = 0;
+      int64_t lo = 0, hi = 0;
+      if (r < a.req_end) {
+        lo = max(static_cast<int64_t>(a.qsl[r]), a.row_lo);
+        hi = min(static_cast<int64_t>(a.qsl[r + 1]), a.row_hi);
+        nw = hi > lo ? static_cast<int>((hi - lo + G - 1) / G) : 0;
+      }
+      int total;
+      const int excl = block_exclusive_scan(nw, &total);
+      for (int j = 0; j < nw; ++j) {
+        const int idx = carry + excl + j;
+        if (idx >= a.num_wr) {
+          set_error(a.err, IDX_DEV_OVERFLOW);
+          break;
+        }
+        const int64_t first = lo + static_cast<int64_t>(j) * G;
+        const int ntok = static_cast<int>(min(static_cast<int64_t>(G), hi - first));
+        int maxlen = 0;
+        for (int g = 0; g < ntok; ++g) {
+          const int len = static_cast<int>(prefill_len(a, r, first + g, true));
+          if (len > a.topk) maxlen = max(maxlen, len);
+        }
+        wr[idx] = WorkRow{r, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
+        wts[idx] = (maxlen + kTileKeys - 1) / kTileKeys;  // tile count, scanned below
+        seg_counter[idx] = 0;
+      }
+      carry += total;
+    }
+    if (carry != a.num_wr && threadIdx.x == 0) set_error(a.err, IDX_DEV_OVERFLOW);
+    for (int idx = carry + threadIdx.x; idx < a.num_wr; idx += kPrepThreads) {
+      wr[idx] = WorkRow{a.req_begin, 0, 0, 0};
+      wts[idx] = 0;
+      seg_counter[idx] = 0;
+    }
+    __syncthreads();
+    int run = 0;
+    for (int base = 0; base < a.num_wr; base += kPrepThreads) {
+      const int idx = base + threadIdx.x;
+      const int t = idx < a.num_wr ? wts[idx] : 0;
+      int total;
+      const int excl = block_exclusive_scan(t, &total);
+      if (idx < a.num_wr) wts[idx] = run + excl;
+      run += total;
+    }
+    if (threadIdx.x == 0) wts[a.num_wr] = run;
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
+  for (int64_t lr = gw; lr < rows; lr += nw) {
+    const int64_t row = a.row_lo + lr;
+    const int r = find_request(a.qsl, a.req_begin, a.req_end, row);
+    const int64_t len = prefill_len(a, r, row, false);
+    if (lane == 0) row_len[lr] = static_cast<int32_t>(len);
+    if (len <= a.topk) {
+      int32_t* o = a.out_idx + row * a.topk;
+      for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;
+    }
+  }
+  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
+    const int64_t lr = idx / kHeads;
+    const int h = static_cast<int>(idx % kHeads);
+    const int64_t src = (a.row_lo + lr) * kHeads + h;
+    float wp;
+    const uint32_t c = quantize_head(a.q + src * kDim, a.w[src], lane, &wp);
+    *reinterpret_cast<uint32_t*>(q8img + lr * kQRowBytes + swizzled_offset(h, lane)) = c;
+    if (lane == 0) wprime[idx] = wp;
+  }
+}
+
+// Row expansion. One warp per request: it writes the request's token rows and
+// copies its block-table row to each of them.
+__global__ void __launch_bounds__(kPrepThreads) expand_kernel(
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ decode_lens,
+    int32_t num_reqs, int32_t next_n, const int32_t* __restrict__ bt, int64_t bt_stride,
+    int32_t bt_width, int32_t mode, int32_t* __restrict__ row_lens, int32_t* __restrict__ row_bt,
+    int64_t out_stride, int64_t num_out_rows, uint32_t* err) {
+  __shared__ int64_t s_carry, s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b0 = blockIdx.x * kPrepWarps;
+  const int b = b0 + warp;
+  int64_t start = 0;
+  if (mode == 1) {
+    // tokens before this block's first request, and in all requests
+    int64_t before = 0, all = 0;
+    for (int i = threadIdx.x; i < num_reqs; i += kPrepThreads) {
+      const int64_t d = decode_lens[i];
+      all += d;
+      if (i < b0) before += d;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, off);
+      all += __shfl_xor_sync(0xffffffffu, all, off);
+    }
+    __shared__ int64_t s_before[kPrepWarps], s_all[kPrepWarps];
+    if (lane == 0) {
+      s_before[warp] = before;
+      s_all[warp] = all;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t x = 0, y = 0;
+      for (int i = 0; i < kPrepWarps; ++i) {
+        x += s_before[i];
+        y += s_all[i];
+      }
+      s_carry = x;
+      s_total = y;
+    }
+    __syncthreads();
+    int64_t mine = 0;
+    if (lane < warp && b0 + lane < num_reqs) mine = decode_lens[b0 + lane];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    start = s_carry + mine;
+  }
+  if (b < num_reqs) {
+    const int32_t L = seq_lens[b];
+    const int32_t d = decode_lens[b];
+    const int32_t nrows = mode == 0 ? next_n : d;
+    for (int j = 0; j < nrows; ++j) {
+      const int64_t row = mode == 0 ? static_cast<int64_t>(b) * next_n + j : start + j;
+      if (row >= num_out_rows) {
+        if (lane == 0) set_error(err, IDX_DEV_OVERFLOW);
+        break;
+      }
+      if (lane == 0) row_lens[row] = (j < d) ? L - d + j + 1 : 0;
+      if (row_bt) {
+        const int32_t* src = bt + static_cast<int64_t>(b) * bt_stride;
+        int32_t* dst = row_bt + row * out_stride;
+        for (int c = lane; c < bt_width; c += 32) dst[c] = src[c];
+      }
+    }
+  }
+  if (mode == 1) {
+    // rows after the last token: len 0 and block-table column 0 zeroed
+    const int64_t first = s_total;
+    for (int64_t row = first + static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x;
+         row < num_out_rows; row += static_cast<int64_t>(gridDim.x) * kPrepThreads) {
+      row_lens[row] = 0;
+      if (row_bt && bt_width > 0) row_bt[row * out_stride] = 0;
+    }
+  }
+}
+
+int prep_grid(int64_t work_warps) {
+  const int64_t blocks = (work_warps + kPrepWarps - 1) / kPrepWarps;
+  const int64_t cap = 4 * static_cast<int64_t>(device_sm_count());
+  return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
+}
+
+}  // namespace
+
+idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, int32_t num_reqs,
+                         int32_t next_n, const int32_t* bt, int64_t bt_stride, int32_t bt_width,
+                         int32_t mode, int32_t* row_lens, int32_t* row_bt, int64_t out_stride,
+                         int64_t num_out_rows, uint32_t* err, cudaStream_t s) {
+  int grid = (num_reqs + kPrepWarps - 1) / kPrepWarps;
+  if (grid < 1) grid = 1;
+  expand_kernel<<<grid, kPrepThreads, 0, s>>>(seq_lens, decode_lens, num_reqs, next_n, bt,
+                                              bt_stride, bt_width, mode, row_lens, row_bt,
+                                              out_stride, num_out_rows, err);
+  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows, uint8_t* q8,
+                                 float* wprime, cudaStream_t s) {
+  quantize_plain_kernel<<<prep_grid(rows * kHeads), kPrepThreads, 0, s>>>(q, w, rows, q8, wprime);
+  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
+                              cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(a.num_reqs) * a.next_n;
+  const int grid = 1 + prep_grid(rows * kHeads);
+  decode_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
+      a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
+      reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
+      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime));
+  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
+                               cudaStream_t s) {
+  const int64_t rows = a.row_hi - a.row_lo;
+  const int grid = 1 + prep_grid(rows * kHeads);
+  prefill_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
+      a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
+      reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
+      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime));
+  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+}
+
+}  // namespace saib

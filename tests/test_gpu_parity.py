@@ -1,0 +1,293 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Integer work (row expansion, q codes, short causal rows, chunk plans) must be
+bit-exact; logits must agree within 1e-3 relative to the per-key magnitude A
+plus fp32 summation slack (tests/_util.py); selected sets are checked with the
+tolerance band around the k-th value.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import sparse_attention_indexer_block_gb300 as saib
+from _util import check_logits, check_topk_row
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+    libbuild.build()
+    saib.load()
+    torch.cuda.set_device(DEV)
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _to(d):
+    return synth.DecodeInputs(q=d.q.to(DEV), w=d.w.to(DEV), cache=d.cache.to(DEV),
+                              block_table=d.block_table.to(DEV), seq_lens=d.seq_lens.to(DEV),
+                              decode_lens=d.decode_lens.to(DEV), next_n=d.next_n, topk=d.topk)
+
+
+def _expand(dd, err):
+    lens, _ = saib.indexer_expand_decode_rows(dd.seq_lens, dd.decode_lens, dd.next_n,
+                                              dev_error=err)
+    return lens
+
+
+def _oracle_rows(d, lens, k, rows=None):
+    return oracle.decode_topk(synth.bf16_bits(d.q), d.w.cpu().numpy(), d.cache.cpu().numpy(),
+                              d.block_table.cpu().numpy(), lens, d.next_n, k, rows=rows,
+                              want_logits=True)
+
+
+def _check_decode(d, k, rows=None):
+    dd = _to(d) if d.q.device.type == "cpu" else d
+    err = _err()
+    lens = _expand(dd, err)
+    out = saib.indexer_decode_topk(dd.q, dd.w, dd.cache, dd.block_table, lens, d.next_n, k,
+                                   dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lens_h = lens.cpu().numpy()
+    ref, lg, ta, tb, rows = _oracle_rows(d, lens_h, k, rows)
+    got = out.cpu().numpy()
+    open_keys = 0
+    for i, r in enumerate(rows):
+        open_keys += check_topk_row(got[r], lg[i], ta[i], tb[i], k, int(lens_h[r]))
+    return open_keys
+
+
+# ---------------------------------------------------------------------------
+# integer steps: bit-exact
+# ---------------------------------------------------------------------------
+
+def test_expand_rows_bit_exact():
+    ex = {"seq": [10, 7, 12, 0], "dl": [3, 1, 4, 0], "flat": [8, 9, 10, 7, 9, 10, 11, 12]}
+    bt = (torch.arange(12, dtype=torch.int32).reshape(4, 3) + 100).to(DEV)
+    seq = torch.tensor(ex["seq"], dtype=torch.int32, device=DEV)
+    dl = torch.tensor(ex["dl"], dtype=torch.int32, device=DEV)
+    err = _err()
+    lens, rbt = saib.indexer_expand_decode_rows(seq, dl, 4, mode=1, block_table=bt,
+                                                num_out_rows=11, want_block_table=True,
+                                                dev_error=err)
+    torch.cuda.synchronize()
+    assert lens.cpu().tolist() == ex["flat"] + [0, 0, 0]
+    ref_l, ref_bt, n = oracle.expand_rows(ex["seq"], ex["dl"], 4, 1, bt.cpu().numpy(), 11)
+    assert np.array_equal(lens.cpu().numpy(), ref_l)
+    assert np.array_equal(rbt.cpu().numpy()[:n], ref_bt[:n])
+    assert np.all(rbt.cpu().numpy()[n:, 0] == 0)
+    # padded grid, random
+    rng = np.random.default_rng(3)
+    for R, nn in [(1, 1), (37, 2), (300, 3), (1000, 1)]:
+        sl = rng.integers(0, 5000, R).astype(np.int32)
+        dlr = rng.integers(0, nn + 1, R).astype(np.int32)
+        W = 5
+        btr = rng.integers(0, 1000, (R, W)).astype(np.int32)
+        for mode in (0, 1):
+            out_rows = R * nn + 3
+            l, b = saib.indexer_expand_decode_rows(
+                torch.from_numpy(sl).to(DEV), torch.from_numpy(dlr).to(DEV), nn, mode=mode,
+                block_table=torch.from_numpy(btr).to(DEV), num_out_rows=out_rows,
+                want_block_table=True, dev_error=err)
+            rl, rb, n = oracle.expand_rows(sl, dlr, nn, mode, btr, out_rows)
+            torch.cuda.synchronize()
+            assert np.array_equal(l.cpu().numpy(), rl)
+            bb = b.cpu().numpy()
+            assert np.array_equal(bb[:n], rb[:n])
+            if mode == 0:
+                assert np.array_equal(bb[:R * nn], rb[:R * nn])
+    assert int(err.item()) == 0
+
+
+def test_quantize_q_bit_exact():
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(37, 64, 128, generator=g)
+    q[3, 5] = 0.0                                  # all-zero head
+    q[4, 6, :] *= 1e-30                            # tiny head
+    q[5, 7, 0] = 1e4                               # one large value: most codes underflow
+    q = q.to(torch.bfloat16)
+    w = torch.randn(37, 64, generator=g) / 8
+    q8, wp = saib.indexer_quantize_q(q.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    ref_q8, sq, ref_wp = oracle.quantize_q(synth.bf16_bits(q), w.numpy())
+    assert np.array_equal(q8.cpu().numpy(), ref_q8)
+    assert np.allclose(wp.cpu().numpy(), ref_wp, rtol=2 ** -22, atol=0)
+
+
+# ---------------------------------------------------------------------------
+# logits through the tensor-core path
+# ---------------------------------------------------------------------------
+
+def _check_logits_case(d):
+    dd = _to(d)
+    err = _err()
+    lens = _expand(dd, err)
+    lg_gpu = saib.indexer_decode_logits(dd.q, dd.w, dd.cache, dd.block_table, lens, d.next_n,
+                                        dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lens_h = lens.cpu().numpy()
+    _, lg, ta, tb, rows = _oracle_rows(d, lens_h, 2048)
+    g = lg_gpu.cpu().numpy()
+    worst = 0.0
+    for i, r in enumerate(rows):
+        L = int(lens_h[r])
+        worst = max(worst, check_logits(g[r, :L], lg[i], ta[i], tb[i]))
+    return worst
+
+
+def test_logits_tiny_workload():
+    _check_logits_case(synth.make_decode("tiny"))
+
+
+def test_logits_ragged_lengths_single_token():
+    lens = [1, 63, 64, 65, 127, 128, 129, 255, 256, 257, 1000, 5000]
+    d = synth.make_decode_from_lens(lens, [1] * len(lens), 1, seed=12)
+    _check_logits_case(d)
+
+
+def test_logits_two_token_rows():
+    sl = [300, 129, 2000, 64, 5]
+    dl = [2, 1, 2, 0, 2]
+    d = synth.make_decode_from_lens(sl, dl, 2, seed=13)
+    _check_logits_case(d)
+
+
+# ---------------------------------------------------------------------------
+# top-k sets
+# ---------------------------------------------------------------------------
+
+def test_topk_tiny_workload():
+    _check_decode(synth.make_decode("tiny"), 2048)
+
+
+@pytest.mark.parametrize("k", [1, 7, 64, 512])
+def test_topk_small_k_ragged(k):
+    lens = [0, 1, k, k + 1, 129, 700, 3000, 9000]
+    d = synth.make_decode_from_lens(lens, [1] * len(lens), 1, seed=100 + k)
+    _check_decode(d, k)
+
+
+def test_topk_boundary_lengths_k2048():
+    lens = [0, 1, 2047, 2048, 2049, 2100, 4095, 4096, 4097, 8191, 20000]
+    d = synth.make_decode_from_lens(lens, [1] * len(lens), 1, seed=31)
+    _check_decode(d, 2048)
+
+
+def test_topk_two_token_rows_mixed():
+    sl = [2048, 2049, 2050, 5000, 3000, 100, 70000]
+    dl = [2, 2, 1, 2, 0, 2, 2]
+    d = synth.make_decode_from_lens(sl, dl, 2, seed=32)
+    _check_decode(d, 2048)
+
+
+def test_topk_decode_batch_workload():
+    _check_decode(synth.make_decode("decode"), 2048)
+
+
+def test_topk_mtp_workload():
+    _check_decode(synth.make_decode("mtp"), 2048)
+
+
+def test_topk_long_context_sampled():
+    d = synth.make_decode("long", device=DEV)
+    rows = np.array([0, 1, 17, 63, 64, 100, 126, 127])
+    dh = synth.DecodeInputs(q=d.q.cpu(), w=d.w.cpu(), cache=d.cache.cpu(),
+                            block_table=d.block_table.cpu(), seq_lens=d.seq_lens.cpu(),
+                            decode_lens=d.decode_lens.cpu(), next_n=1, topk=2048)
+    err = _err()
+    lens = _expand(d, err)
+    out = saib.indexer_decode_topk(d.q, d.w, d.cache, d.block_table, lens, 1, 2048,
+                                   dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lens_h = lens.cpu().numpy()
+    _, lg, ta, tb, rows = _oracle_rows(dh, lens_h, 2048, rows)
+    got = out.cpu().numpy()
+    for i, r in enumerate(rows):
+        check_topk_row(got[r], lg[i], ta[i], tb[i], 2048, int(lens_h[r]))
+
+
+def test_workspace_reuse_across_shapes():
+    a = _to(synth.make_decode_from_lens([9000, 3000, 2500], [1, 1, 1], 1, seed=41))
+    b = synth.make_decode_from_lens([5000, 2049], [1, 1], 1, seed=42)
+    bb = _to(b)
+    ws = saib.decode_workspace(3, 1, 2048, DEV)
+    err = _err()
+    la = _expand(a, err)
+    saib.indexer_decode_topk(a.q, a.w, a.cache, a.block_table, la, 1, 2048, workspace=ws,
+                             dev_error=err)
+    lb = _expand(bb, err)
+    out = saib.indexer_decode_topk(bb.q, bb.w, bb.cache, bb.block_table, lb, 1, 2048,
+                                   workspace=ws, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lens_h = lb.cpu().numpy()
+    _, lg, ta, tb, rows = _oracle_rows(b, lens_h, 2048)
+    for i, r in enumerate(rows):
+        check_topk_row(out.cpu().numpy()[r], lg[i], ta[i], tb[i], 2048, int(lens_h[r]))
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+
+def _check_prefill(p, k, rows=None, budget=512 << 20, ws_tokens=40 * 8192):
+    err = _err()
+    out = saib.indexer_prefill_topk(p.q.to(DEV), p.w.to(DEV), p.cache.to(DEV),
+                                    p.block_table.to(DEV), p.seq_lens.to(DEV),
+                                    p.query_start_loc.to(DEV), p.seq_lens, p.query_lens, k,
+                                    ws_tokens, budget, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, lg, ta, tb, rows = oracle.prefill_topk(
+        synth.bf16_bits(p.q), p.w.numpy(), p.cache.numpy(), p.block_table.numpy(),
+        p.seq_lens.numpy(), p.query_start_loc.numpy(), k, rows=rows, want_logits=True)
+    _, ln = oracle.prefill_rows(p.seq_lens.numpy(), p.query_start_loc.numpy())
+    got = out.cpu().numpy()
+    for i, r in enumerate(rows):
+        check_topk_row(got[r], lg[i], ta[i], tb[i], k, int(ln[r]))
+
+
+def test_prefill_small_full():
+    p = synth.make_prefill(seed=51, seq_lens=[300, 517, 90], query_lens=[300, 211, 7])
+    _check_prefill(p, 64)
+    # a budget that forces query sub-chunks and a workspace bound between requests
+    _check_prefill(p, 64, budget=4 * 300 * 50, ws_tokens=600)
+
+
+def test_prefill_workload_sampled():
+    p = synth.make_prefill("prefill")
+    rows = np.array([0, 1, 2046, 2047, 2048, 2049, 5000, 8191, 8192, 8192 + 4095, 16383,
+                     24576 + 3000, 32767])
+    _check_prefill(p, 2048, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# device-side error reporting (no trap)
+# ---------------------------------------------------------------------------
+
+def test_bad_block_id_and_length_are_reported():
+    d = _to(synth.make_decode_from_lens([3000, 2500], [1, 1], 1, seed=61))
+    bt = d.block_table.clone()
+    bt[0, 3] = d.cache.shape[0] + 5                  # outside the cache
+    err = _err()
+    lens = _expand(d, err)
+    saib.indexer_decode_topk(d.q, d.w, d.cache, bt, lens, 1, 2048, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & saib.binding.DEV_BAD_BLOCK
+    err2 = _err()
+    lens2 = lens.clone()
+    lens2[1] = bt.shape[1] * 64 + 1                  # longer than the block table
+    saib.indexer_decode_topk(d.q, d.w, d.cache, d.block_table, lens2, 1, 2048, dev_error=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == saib.binding.DEV_BAD_LEN
