@@ -1,0 +1,424 @@
+"""Benchmark: decode top-2048 sparse-attention indexer on GB300.
+
+One step = one pass of the decode hot path over the decode-batch workload
+(32 requests, next_n 1, seq_lens uniform in [2048, 32768], 64 heads x 128,
+fp8 e4m3 paged index cache, top-2048): row expansion + q quantisation +
+paged gather + tensor-core scoring + causal mask + top-k, through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. ``value`` is indexed keys/s (sum over token rows of the
+keys each row scores) over all ranks, device-timed with CUDA events around a
+CUDA graph of K steps (inputs resident in HBM, cold L2: every step reads a
+different copy of the index cache, the copies together several times L2).
+``e2e`` is the same metric with pinned host buffers copied in and the indices
+copied out every step. ``--impl reference`` times the CPU oracle on the host
+cores instead (bounded sample per step). Multi-GPU runs are replicas: every
+rank runs its own batch (weak scaling), no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexed keys/sec for decode top-2048; % of HBM roofline (1×GB300)"
+WORKLOAD = "decode"
+WORKLOAD_DESC = ("decode batch: 32 requests, next_n 1, seq_lens uniform in [2048, 32768], "
+                 "64 index heads x head_dim 128, bf16 q, fp8 e4m3 paged index-K (page 64, "
+                 "fp32 per-token scale), random block table, top-2048")
+PAGE_KEY_BYTES = 132  # 128 fp8 values + 4-byte scale per key
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seed", type=int, default=0x5EED)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-i", str(self.gpu), "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self, min_mhz_load: float = 500.0):
+        sms, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, smax = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            sms.append(sm)
+            mx.append(smax)
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in sms if s >= min_mhz_load] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import synth
+    import sparse_attention_indexer_block_gb300 as saib
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    libbuild.build()
+    saib.load()
+
+    seed = args.seed + 1000 * rank
+    d = synth.make_decode(args.workload, seed=seed, device=dev)
+    R, G, k = d.num_reqs, d.next_n, d.topk
+    seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
+    dl_h = d.decode_lens.cpu().numpy().astype(np.int64)
+    # keys scored per step (sum of row lengths) and unique keys read
+    row_lens_h = np.concatenate([[L - dd + j + 1 if j < dd else 0 for j in range(G)]
+                                 for L, dd in zip(seq_h, dl_h)])
+    keys_per_step = int(row_lens_h.sum())
+    algo_bytes = int(seq_h.sum()) * PAGE_KEY_BYTES
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    cache_bytes = d.cache.numel()
+    n_copies = max(2, math.ceil(3 * l2 / cache_bytes) + 1)
+    caches = [d.cache] + [d.cache.clone() for _ in range(n_copies - 1)]
+    ws = saib.decode_workspace(R, G, k, dev)
+    out = torch.empty((R * G, k), dtype=torch.int32, device=dev)
+    lens = torch.empty(R * G, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        saib.indexer_expand_decode_rows(d.seq_lens, d.decode_lens, G, row_seq_lens=lens,
+                                        dev_error=err, stream=stream)
+        saib.indexer_decode_topk(d.q, d.w, caches[i % n_copies], d.block_table, lens, G, k,
+                                 out_idx=out, workspace=ws, dev_error=err, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+
+    # CUDA graph of the K timed steps (replayed in pieces of at most 1000 steps)
+    K = args.steps
+    piece = min(K, 1000)
+    graphs = []
+    done = 0
+    with torch.cuda.stream(stream):
+        while done < K:
+            n = min(piece, K - done)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(done, done + n):
+                    step(i)
+            graphs.append(g)
+            done += n
+    torch.cuda.synchronize()
+    launches = 3 * K  # expand, prep, score per step
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # soak (untimed) so the clock samples see the same load, then the timed region
+    t_soak = time.time()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            while time.time() - t_soak < 1.0:
+                for g in graphs:
+                    g.replay()
+                stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g in graphs:
+                g.replay()
+            e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+    value = keys_per_step * K * world / (ms / 1e3)
+
+    # live per-launch duration of the score/select kernel (eager, same rotation)
+    n_prof = min(K, 400)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            saib.indexer_profile_events(*evs[i])
+            step(i)
+        saib.indexer_profile_events(None, None)
+    torch.cuda.synchronize()
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_avg = statistics.mean(kern_ms)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = algo_bytes / (kern_avg / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                "measured" else "fallback 6.8 TB/s",
+                "kernel": "score_select_kernel<1,false>", "kernel_ms_avg": round(kern_avg, 5),
+                "kernel_ms_median": round(statistics.median(kern_ms), 5),
+                "algorithmic_bytes_per_launch": algo_bytes}
+
+    # end to end: pinned host inputs in, indices out, every step
+    host = {n: t.cpu().pin_memory() for n, t in
+            [("q", d.q), ("w", d.w), ("cache", d.cache), ("bt", d.block_table),
+             ("seq", d.seq_lens), ("dl", d.decode_lens)]}
+    dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty((R * G, k), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        saib.indexer_expand_decode_rows(dbuf["seq"], dbuf["dl"], G, row_seq_lens=lens,
+                                        dev_error=err, stream=stream)
+        saib.indexer_decode_topk(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"], lens, G, k,
+                                 out_idx=out, workspace=ws, dev_error=err, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    n_e2e = max(3, min(K, 50))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1) / n_e2e
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": keys_per_step * world / (e2e_ms / 1e3), "unit": "keys/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(d, row_lens_h)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD_DESC, "requests": R, "next_n": G, "topk": k,
+                           "keys_per_step": keys_per_step,
+                           "index_bytes_per_step": algo_bytes,
+                           "l2": f"cold: {n_copies} rotating index-cache copies "
+                                 f"({n_copies * cache_bytes / 2**20:.0f} MiB > 3 x L2 "
+                                 f"{l2 / 2**20:.0f} MiB)",
+                           "timing": "CUDA events around CUDA-graph replays of K steps",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clk.summary(), "gpu_launches": launches,
+                "hbm_gbs_index_stream": round(algo_bytes * K / (ms / 1e3) / 1e9, 1)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_inputs(d):
+    import oracle
+    import synth
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(d.q), d.w.cpu().numpy())
+    return (q8, wp, d.cache.cpu().numpy(), d.block_table.cpu().numpy())
+
+
+def cpu_baseline(d, row_lens_h, target_s: float = 10.0):
+    """The oracle as it stands on this host's cores: all rows of the workload,
+    repeated while under ~target_s seconds."""
+    import oracle
+    q8, wp, cache, bt = _oracle_inputs(d)
+    G = d.next_n
+    rows = np.nonzero(row_lens_h > 0)[0]
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.score_select_rows(q8, wp, cache, bt, rows, rows // G, row_lens_h[rows], d.topk,
+                                 threads=threads)
+        passes += 1
+        if time.perf_counter() - t0 > target_s or passes >= 3:
+            break
+    dt = time.perf_counter() - t0
+    keys = int(row_lens_h[rows].sum()) * passes
+    return {"value": keys / dt, "unit": "keys/s", "cores": threads, "kind": "oracle",
+            "sample": f"whole workload ({len(rows)} token rows, {keys // passes} keys) x {passes} "
+                      f"pass(es), {dt:.1f} s, {threads} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    oracle.build()
+    d = synth.make_decode(args.workload, seed=args.seed, device="cpu")
+    G, k = d.next_n, d.topk
+    seq_h = d.seq_lens.numpy().astype(np.int64)
+    dl_h = d.decode_lens.numpy().astype(np.int64)
+    row_lens_h = np.concatenate([[L - dd + j + 1 if j < dd else 0 for j in range(G)]
+                                 for L, dd in zip(seq_h, dl_h)])
+    q8, wp, cache, bt = _oracle_inputs(d)
+    threads = oracle.num_threads()
+    rows_all = np.nonzero(row_lens_h > 0)[0]
+    # calibrate: keys/s of the oracle on a prefix sample of every row
+    cal_len = np.minimum(row_lens_h[rows_all], k + 256)
+    t0 = time.perf_counter()
+    oracle.score_select_rows(q8, wp, cache, bt, rows_all, rows_all // G, cal_len, k,
+                             threads=threads)
+    rate = cal_len.sum() / (time.perf_counter() - t0)
+    budget_s = 150.0
+    per_step_keys = max(64, int(rate * budget_s / (args.steps + args.warmup)))
+    per_row = max(1, per_step_keys // len(rows_all))
+    sample_lens = np.minimum(row_lens_h[rows_all], per_row)
+
+    def step():
+        oracle.score_select_rows(q8, wp, cache, bt, rows_all, rows_all // G, sample_lens, k,
+                                 want_logits=True, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    keys = int(sample_lens.sum()) * args.steps
+    value = keys / dt
+    sample = (f"each step: up to the first {per_row} keys of each of the {len(rows_all)} token rows "
+              f"({int(sample_lens.sum())} keys), scored and selected")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "keys/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "requests": d.num_reqs, "next_n": G,
+                       "topk": k, "parallelism": "host threads"},
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -221,6 +221,15 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
                                 int32_t* out_idx, void* workspace, size_t workspace_bytes,
                                 uint32_t* dev_error, void* stream);
 
+/*
+ * Profiling hook (the live per-kernel timing a benchmark needs): while set,
+ * every decode/prefill call made from this host thread records start_event
+ * immediately before and stop_event immediately after each launch of the
+ * score/select kernel, on the call's stream (cudaEvent_t handles owned by the
+ * caller; NULL, NULL turns it off). Meant for eager calls, not stream capture.
+ */
+idx_status indexer_profile_events(void* start_event, void* stop_event);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     indexer_plan_prefill_chunks,
     indexer_prefill_topk,
     indexer_prefill_workspace_bytes,
+    indexer_profile_events,
     indexer_quantize_q,
     indexer_status_string,
     load,

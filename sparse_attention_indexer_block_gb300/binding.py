@@ -41,6 +41,7 @@ SIGNATURES = {
                                                   C.POINTER(_SZ)]),
     "indexer_prefill_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P, _I32,
                                        _I32, _I32, _I32, _I64, _I64, _P, _P, _SZ, _P, _P]),
+    "indexer_profile_events": (C.c_int, [_P, _P]),
 }
 
 _lock = threading.Lock()
@@ -242,3 +243,11 @@ def indexer_prefill_topk(q, weights, index_cache, block_table, seq_lens, query_s
         _stream(stream))
     _check("indexer_prefill_topk", st)
     return out_idx
+
+
+def indexer_profile_events(start_event=None, stop_event=None):
+    """Records the given torch.cuda.Event pair around every score/select launch
+    made from this thread (None, None turns it off)."""
+    a = C.c_void_p(start_event.cuda_event) if start_event is not None else None
+    b = C.c_void_p(stop_event.cuda_event) if stop_event is not None else None
+    _check("indexer_profile_events", load().indexer_profile_events(a, b))

@@ -12,6 +12,19 @@ namespace saib {
 
 namespace {
 
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+
+// Score/select launch bracketed by the profiling events when they are set.
+idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map, int nC,
+                       cudaStream_t s) {
+  if (g_prof_start && cudaEventRecord(g_prof_start, s) != cudaSuccess) return IDX_ERR_CUDA;
+  const idx_status st = launch_score(G, logits, p, map, nC, s);
+  if (st == IDX_OK && g_prof_stop && cudaEventRecord(g_prof_stop, s) != cudaSuccess)
+    return IDX_ERR_CUDA;
+  return st;
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -196,7 +209,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.out_logits = out_logits;
   p.ld_logits = ld_logits;
   p.dev_error = dev_error;
-  return launch_score(next_n, logits, p, map, nC, s);
+  return timed_score(next_n, logits, p, map, nC, s);
 }
 
 }  // namespace
@@ -205,6 +218,12 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
 using namespace saib;
 
 extern "C" {
+
+idx_status indexer_profile_events(void* start_event, void* stop_event) {
+  g_prof_start = static_cast<cudaEvent_t>(start_event);
+  g_prof_stop = static_cast<cudaEvent_t>(stop_event);
+  return IDX_OK;
+}
 
 const char* indexer_status_string(idx_status status) {
   switch (status) {
@@ -402,7 +421,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.out_row_base = lo;
     p.topk = topk;
     p.dev_error = dev_error;
-    if ((st = launch_score(kPrefillG, false, p, map, nC, s)) != IDX_OK) return st;
+    if ((st = timed_score(kPrefillG, false, p, map, nC, s)) != IDX_OK) return st;
   }
   return IDX_OK;
 }

@@ -442,7 +442,7 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
 template <int G>
 __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
                                  const bool (&active)[G], int64_t rs, int64_t re, int64_t t0,
-                                 int64_t t1, int64_t T) {
+                                 int64_t t1, int64_t T, int64_t nC) {
   using C = Cfg<G>;
   const int et = threadIdx.x - 64;
   const int K = p.topk;
@@ -454,7 +454,6 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
     write_rows<G>(p, s, wr, active);
     return;
   }
-  const int64_t nC = gridDim.x;
   const int64_t c_first = cta_of(rs, T, nC), c_last = cta_of(re - 1, T, nC);
   const int64_t slot = static_cast<int64_t>(blockIdx.x) + w;
 #pragma unroll
@@ -507,7 +506,7 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
 
 template <int G, bool kLogits>
 __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int64_t t0, int64_t t1,
-                         int64_t T) {
+                         int64_t T, int64_t nC) {
   using C = Cfg<G>;
   volatile int* abort_flag = &s.misc->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -549,7 +548,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
   bool ok = true;
   for (int64_t t = t0; t < t1; ++t) {
     if (t >= re) {
-      if (!kLogits) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T);
+      if (!kLogits) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
       do {
         ++w;
         re = p.wr_tile_start[w + 1];
@@ -627,7 +626,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       acc_phase ^= 1;
     }
   }
-  if (!kLogits && ok) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T);
+  if (!kLogits && ok) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
 }
 
 template <int G, bool kLogits>
@@ -641,10 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem s = carve<G>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // With fewer tiles than CTAs only the first T CTAs take part, so that every
+  // participating CTA owns at least one tile (segment counts rely on it).
   const int64_t T = p.wr_tile_start[p.num_wr];
-  const int64_t nC = gridDim.x;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * T / nC;
-  const int64_t t1 = static_cast<int64_t>(blockIdx.x + 1) * T / nC;
+  const int64_t nC = min(static_cast<int64_t>(gridDim.x), T);
+  const bool part = static_cast<int64_t>(blockIdx.x) < nC;
+  const int64_t t0 = part ? static_cast<int64_t>(blockIdx.x) * T / nC : 0;
+  const int64_t t1 = part ? static_cast<int64_t>(blockIdx.x + 1) * T / nC : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -674,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if (lane == 0) mma_issuer<G>(p, s, tmem, t0, t1);
     } else {
-      epilogue<G, kLogits>(p, s, tmem, t0, t1, T);
+      epilogue<G, kLogits>(p, s, tmem, t0, t1, T, nC);
     }
   }
   tc_fence_before();
