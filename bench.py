@@ -240,6 +240,10 @@ def run_ours(args, rank, world, local):
     n_prof = min(K, 400)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n_prof)]
+    for a, b in evs:  # torch creates the event handles on first record
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(n_prof):
             saib.indexer_profile_events(*evs[i])

@@ -230,6 +230,16 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
  */
 idx_status indexer_profile_events(void* start_event, void* stop_event);
 
+/*
+ * Tracing hook: while set, score/select launches made from this host thread
+ * write 32 uint64 per CTA into `buffer` (device memory, zeroed by the caller,
+ * >= 32 * 8 * (2 x SM count) bytes; smaller buffers disable it): %globaltimer
+ * stamps of the start, the first/last TMA, MMA and epilogue tile and the end,
+ * the ns and count of buffer compactions and merges, merge statistics and the
+ * CTA's tile count. NULL turns it off.
+ */
+idx_status indexer_trace_buffer(void* buffer, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     indexer_prefill_topk,
     indexer_prefill_workspace_bytes,
     indexer_profile_events,
+    indexer_trace_buffer,
     indexer_quantize_q,
     indexer_status_string,
     load,

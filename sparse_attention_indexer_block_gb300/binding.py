@@ -42,6 +42,7 @@ SIGNATURES = {
     "indexer_prefill_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P, _I32,
                                        _I32, _I32, _I32, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "indexer_profile_events": (C.c_int, [_P, _P]),
+    "indexer_trace_buffer": (C.c_int, [_P, _SZ]),
 }
 
 _lock = threading.Lock()
@@ -251,3 +252,13 @@ def indexer_profile_events(start_event=None, stop_event=None):
     a = C.c_void_p(start_event.cuda_event) if start_event is not None else None
     b = C.c_void_p(stop_event.cuda_event) if stop_event is not None else None
     _check("indexer_profile_events", load().indexer_profile_events(a, b))
+
+
+def indexer_trace_buffer(buffer=None):
+    """Per-CTA trace stamps of later score/select launches go to ``buffer``
+    (a uint64/int64 CUDA tensor of >= 16 * SM-count entries); None turns it off."""
+    if buffer is None:
+        _check("indexer_trace_buffer", load().indexer_trace_buffer(None, 0))
+    else:
+        _check("indexer_trace_buffer", load().indexer_trace_buffer(
+            _ptr(buffer), int(buffer.numel() * buffer.element_size())))

@@ -12,6 +12,8 @@ namespace saib {
 
 namespace {
 
+thread_local uint64_t* g_trace = nullptr;
+thread_local size_t g_trace_bytes = 0;
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 
@@ -30,6 +32,11 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+uint64_t* trace_buffer(size_t* bytes) {
+  *bytes = g_trace_bytes;
+  return g_trace;
+}
 
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) {
   WsLayout L{};
@@ -50,6 +57,10 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
   L.wprime = take(4 * static_cast<size_t>(rows) * kHeads, 256);
   L.slot_key = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
   L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
+  L.row_hist_words = static_cast<size_t>(num_ctas) * G * 1024;
+  L.row_hist = take(4 * L.row_hist_words, 256);
+  L.cta_row = take(4 * static_cast<size_t>(num_ctas), 256);
+  L.slot_thrbin = take(4 * static_cast<size_t>(nslots * G), 256);
   L.total = round_up(off, 256);
   return L;
 }
@@ -177,7 +188,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
     return IDX_ERR_INVALID_ARG;
   }
   if (num_reqs == 0) return IDX_OK;
-  const int nC = device_sm_count();
+  const int nC = score_ctas(next_n);
   const int64_t rows = static_cast<int64_t>(num_reqs) * next_n;
   const WsLayout L = ws_layout(num_reqs, rows, next_n, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
@@ -186,7 +197,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
-                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error};
+                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC};
   if ((st = launch_decode_prep(a, ws, L, s)) != IDX_OK) return st;
   ScoreParams p{};
   p.cache = index_cache;
@@ -195,6 +206,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.bt_stride = bt_stride;
   p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
   p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
+  p.cta_row = reinterpret_cast<const int32_t*>(ws + L.cta_row);
   p.num_wr = num_reqs;
   p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
   p.q8 = ws + L.q8;
@@ -203,12 +215,17 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
   p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
   p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+  p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
+  p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
   p.out_idx = out_idx;
   p.out_row_base = 0;
   p.topk = topk;
   p.out_logits = out_logits;
   p.ld_logits = ld_logits;
   p.dev_error = dev_error;
+  size_t tb = 0;
+  p.trace = trace_buffer(&tb);
+  if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
   return timed_score(next_n, logits, p, map, nC, s);
 }
 
@@ -218,6 +235,12 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
 using namespace saib;
 
 extern "C" {
+
+idx_status indexer_trace_buffer(void* buffer, size_t bytes) {
+  g_trace = static_cast<uint64_t*>(buffer);
+  g_trace_bytes = buffer ? bytes : 0;
+  return IDX_OK;
+}
 
 idx_status indexer_profile_events(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
@@ -275,7 +298,7 @@ idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int3
   if (!bytes || num_reqs < 0) return IDX_ERR_INVALID_ARG;
   if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk,
-                               device_sm_count());
+                               score_ctas(next_n));
   *bytes = L.total;
   return IDX_OK;
 }
@@ -362,7 +385,7 @@ idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
   const idx_status st = prefill_plan(seq_lens_host, query_lens_host, num_reqs, workspace_tokens,
                                      logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows);
   if (st != IDX_OK) return st;
-  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, device_sm_count()).total;
+  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, score_ctas(kPrefillG)).total;
   return IDX_OK;
 }
 
@@ -387,7 +410,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
                          logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows)) != IDX_OK)
     return st;
   if (plan.empty()) return IDX_OK;
-  const int nC = device_sm_count();
+  const int nC = score_ctas(kPrefillG);
   const WsLayout L = ws_layout(max_wr, max_rows, kPrefillG, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
   CUtensorMap map;
@@ -400,7 +423,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     if (nw == 0) continue;
     PrefillPrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, seq_lens, query_start_loc,
                       c.r0, c.r1, lo, hi, static_cast<int32_t>(nw), topk, bt_width, out_idx,
-                      dev_error};
+                      dev_error, nC};
     if ((st = launch_prefill_prep(a, ws, L, s)) != IDX_OK) return st;
     ScoreParams p{};
     p.cache = index_cache;
@@ -409,6 +432,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.bt_stride = bt_stride;
     p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
     p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
+    p.cta_row = reinterpret_cast<const int32_t*>(ws + L.cta_row);
     p.num_wr = static_cast<int32_t>(nw);
     p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
     p.q8 = ws + L.q8;
@@ -417,10 +441,15 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
     p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
     p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+    p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
+    p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
     p.out_idx = out_idx;
     p.out_row_base = lo;
     p.topk = topk;
     p.dev_error = dev_error;
+    size_t tb = 0;
+    p.trace = trace_buffer(&tb);
+    if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
     if ((st = timed_score(kPrefillG, false, p, map, nC, s)) != IDX_OK) return st;
   }
   return IDX_OK;

@@ -18,6 +18,7 @@ struct ScoreParams {
   int64_t bt_stride;
   const WorkRow* wr;
   const int32_t* wr_tile_start;  // [num_wr + 1], exclusive prefix of tiles per work row
+  const int32_t* cta_row;        // [grid] work row holding each CTA's first tile
   int32_t num_wr;
   const int32_t* row_len;        // [rows] validated key count per token row
   const uint8_t* q8;             // [rows, 8192] swizzled fp8 images of q
@@ -26,17 +27,30 @@ struct ScoreParams {
   uint32_t* slot_key;            // [nslots, G, topk] candidate keys of finished segments
   int32_t* slot_idx;             // [nslots, G, topk] their token indices
   int32_t* slot_count;           // [nslots, G]
+  int32_t* slot_thrbin;          // [nslots, G] row-histogram bin of the segment's final threshold
+  uint32_t* row_hist;            // [nC, G, 1024] histograms of split work rows (zeroed by prep)
   int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
   int64_t out_row_base;
   int32_t topk;
   float* out_logits;             // logits mode only
   int64_t ld_logits;
   uint32_t* dev_error;
+  uint64_t* trace;               // optional per-CTA timestamps (kTraceSlots per CTA)
+};
+
+// Per-CTA trace slots (ns from %globaltimer, or counts).
+enum TraceSlot {
+  kTrStart = 0, kTrFirstTma, kTrLastTma, kTrFirstMma, kTrLastMma, kTrFirstEpi, kTrLastEpi,
+  kTrFinal, kTrCompactNs, kTrCompactN, kTrMergeNs, kTrMergeN, kTrEnd, kTrTiles, kTrFinalizeNs,
+  kTrEndEpi, kTrMergeFallback, kTrMergeUnion, kTrMergeCut, kTrMergeSegs, kTrSeen, kTrMergeCutNs, kTrMergeLoadNs, kTrMergeRadixNs, kTrCompactRadixNs,
+  kTrRadixHistNs, kTrRadixBucketNs, kTrRadixPasses, kTrEpiWaitCyc, kTrEpiLdCyc,
+  kTrEpiMathCyc, kTrEpiVoteCyc, kTrEpiSelCyc, kTrSlots = 40
 };
 
 // Workspace carve-up shared by decode and prefill.
 struct WsLayout {
   size_t wr, wr_tile_start, row_len, seg_counter, slot_count, q8, wprime, slot_key, slot_idx;
+  size_t row_hist, row_hist_words, cta_row, slot_thrbin;
   size_t total;
 };
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
@@ -65,6 +79,7 @@ struct DecodePrepArgs {
   int32_t score_all;  // logits mode: every row with len > 0 is scored
   int32_t* out_idx;   // causal fill target (nullable in logits mode)
   uint32_t* err;
+  int32_t num_ctas;   // grid of the score/select launch that follows
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -81,12 +96,22 @@ struct PrefillPrepArgs {
   int32_t bt_width;
   int32_t* out_idx;
   uint32_t* err;
+  int32_t num_ctas;   // grid of the score/select launch that follows
 };
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);
 
 // G = token rows per work row (1, 2 or 4); logits = write logits instead of selecting.
+// Thread-local trace buffer set by indexer_trace_buffer (nullptr = off).
+uint64_t* trace_buffer(size_t* bytes);
+
 idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s);
+
+// CTAs per SM the score/select kernel runs with for work rows of G tokens.
+int score_ctas_per_sm(int G);
+
+// CTAs of one score/select launch on the current device.
+inline int score_ctas(int G) { return device_sm_count() * score_ctas_per_sm(G); }
 
 }  // namespace saib

@@ -100,13 +100,47 @@ __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
   }
 }
 
+// Block 0, after wts[0..num_wr] is written: the work row holding the first
+// tile of each participating CTA of the score/select launch (the kernel gives
+// CTA c tiles [c*T/nC, (c+1)*T/nC) with nC = min(grid, T)).
+__device__ void fill_cta_rows(const int32_t* wts, int num_wr, int grid, int32_t* cta_row) {
+  __syncthreads();
+  const int64_t T = wts[num_wr];
+  const int64_t nC = min(static_cast<int64_t>(grid), T);
+  for (int c = threadIdx.x; c < grid; c += kPrepThreads) {
+    int w = 0;
+    if (c < nC) {
+      const int64_t t = static_cast<int64_t>(c) * T / nC;
+      int lo = 0, hi = num_wr - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wts[mid] <= t) lo = mid;
+        else hi = mid - 1;
+      }
+      w = lo;
+    }
+    cta_row[c] = w;
+  }
+}
+
+// Zeroes n 32-bit words (16-byte aligned) with the blocks after block 0.
+__device__ __forceinline__ void zero_words(uint32_t* p, size_t n) {
+  const size_t tid = static_cast<size_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x;
+  const size_t nt = static_cast<size_t>(gridDim.x - 1) * kPrepThreads;
+  uint4* p4 = reinterpret_cast<uint4*>(p);
+  for (size_t i = tid; i < n / 4; i += nt) p4[i] = make_uint4(0, 0, 0, 0);
+  for (size_t i = (n / 4) * 4 + tid; i < n; i += nt) p[i] = 0;
+}
+
 // Block 0: work-row schedule (tile counts and their exclusive prefix), validated
-// row lengths and zeroed segment counters. Other blocks: q quantisation into
-// the swizzled images and the exact causal rows of short rows.
+// row lengths and zeroed segment counters. Other blocks: zeroed row histograms,
+// q quantisation into the swizzled images and the exact causal rows of short
+// rows.
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
     DecodePrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
-    float* __restrict__ wprime) {
+    float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
+    int32_t* __restrict__ cta_row) {
   const int G = a.next_n;
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * G;
   if (blockIdx.x == 0) {
@@ -133,8 +167,10 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
       carry += total;
     }
     if (threadIdx.x == 0) wts[a.num_reqs] = carry;
+    fill_cta_rows(wts, a.num_reqs, a.num_ctas, cta_row);
     return;
   }
+  zero_words(row_hist, row_hist_words);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
@@ -180,7 +216,8 @@ __device__ __forceinline__ int64_t prefill_len(const PrefillPrepArgs& a, int r, 
 __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     PrefillPrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
-    float* __restrict__ wprime) {
+    float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
+    int32_t* __restrict__ cta_row) {
   constexpr int G = 4;
   const int64_t rows = a.row_hi - a.row_lo;
   if (blockIdx.x == 0) {
@@ -232,8 +269,10 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
       run += total;
     }
     if (threadIdx.x == 0) wts[a.num_wr] = run;
+    fill_cta_rows(wts, a.num_wr, a.num_ctas, cta_row);
     return;
   }
+  zero_words(row_hist, row_hist_words);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
@@ -367,7 +406,9 @@ idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayo
   decode_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
       a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
-      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime));
+      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
+      reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
+      reinterpret_cast<int32_t*>(ws + L.cta_row));
   return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
@@ -378,7 +419,9 @@ idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLa
   prefill_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
       a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
-      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime));
+      ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
+      reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
+      reinterpret_cast<int32_t*>(ws + L.cta_row));
   return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

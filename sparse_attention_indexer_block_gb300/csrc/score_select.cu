@@ -33,14 +33,21 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
-constexpr int kEpiBarrier = 1;  // named barrier id of the epilogue warps
+constexpr int kEpiBarrier = 1;       // named barrier id of the epilogue warps
+constexpr int kTeardownBarrier = 2;  // used once, by all warps, before TMEM is freed
+constexpr int kSetupBarrier = 3;     // used once, by all warps, after barrier init and TMEM alloc
 
 template <int G>
 struct Cfg {
   static constexpr int N = 64 * G;
-  static constexpr int kStages = G == 1 ? 8 : (G == 2 ? 6 : 4);
-  static constexpr int kCap = G <= 2 ? 4096 : 2560;  // candidate slots per token row
-  static constexpr int kPer = kCap / kEpiThreads;
+  // next_n = 1 runs two CTAs per SM (one's selection work overlaps the other's
+  // streaming); wider work rows need the shared memory of a whole SM.
+  static constexpr int kCtasPerSm = G == 1 ? 2 : 1;
+  static constexpr int kStages = G == 1 ? 4 : (G == 2 ? 6 : 4);
+  static constexpr int kCap = G == 1 ? 3072 : (G == 2 ? 4096 : 2560);  // candidates per token row
+  static constexpr int kRegion = kCap / 4;          // per-warp append region
+  static constexpr int kPer = kRegion / 32;         // region entries per lane
+  static constexpr int kHistBins = 1024;
   static constexpr uint32_t kTmemCols = 2 * N <= 128 ? 128u : (2 * N <= 256 ? 256u : 512u);
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
   static constexpr int kKvOff = 0;
@@ -50,12 +57,12 @@ struct Cfg {
   static constexpr int kCandIdxOff = kCandKeyOff + G * kCap * 4;
   static constexpr int kWpOff = kCandIdxOff + G * kCap * 4;
   static constexpr int kHistOff = kWpOff + G * 256;
-  static constexpr int kBarOff = kHistOff + 1024;
+  static constexpr int kBarOff = kHistOff + kHistBins * 4;
   static constexpr int kNumBars = 2 * kStages + 9;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 256 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSmemBytes * kCtasPerSm + 1024 * kCtasPerSm <= 233472, "shared memory");
 };
 
 struct Misc {
@@ -67,6 +74,11 @@ struct Misc {
   int bucket, above, bcount;
   int is_last;
   int vote[2][4];
+  int scan[4];
+  uint32_t rmin[4], rmax[4];
+  int cut_n, fallback;
+  int epi_done;
+  int wcnt[4][4];  // [token][epilogue warp] entries in the warp's region
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
@@ -86,6 +98,7 @@ struct Smem {
   uint64_t* qempty;  // [2]
   uint64_t* done;
   Misc* misc;
+  uint64_t* trace;   // this CTA's trace slots, or nullptr
 };
 
 template <int G>
@@ -122,9 +135,18 @@ __device__ __forceinline__ int find_row(const int32_t* wts, int num_wr, int64_t 
   return lo;
 }
 
+// Row histogram over the top 10 bits of the order-preserving key: sign, the
+// 8 exponent bits and the leading mantissa bit (bins of half a binade).
+constexpr int kRowHistBins = 1024;
+__device__ __forceinline__ int row_bin(uint32_t key) { return static_cast<int>(key >> 22); }
+
 // CTA whose tile range [c*T/nC, (c+1)*T/nC) contains tile t.
 __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t T, int64_t nC) {
   return ((t + 1) * nC - 1) / T;
+}
+
+__device__ __forceinline__ void trace_set(const ScoreParams& p, int slot, uint64_t v) {
+  if (p.trace) p.trace[static_cast<int64_t>(blockIdx.x) * kTrSlots + slot] = v;
 }
 
 // ---------------------------------------------------------------------------
@@ -143,7 +165,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
   uint32_t qn[2] = {0, 0};
   int qslot = 0;
 
-  int w = find_row(p.wr_tile_start, p.num_wr, t0);
+  int w = p.cta_row[blockIdx.x];
   int64_t rs = p.wr_tile_start[w], re = p.wr_tile_start[w + 1];
   WorkRow wr = p.wr[w];
   bool ok = true;
@@ -196,6 +218,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
         }
       }
     }
+    if (t == t0) trace_set(p, kTrFirstTma, globaltimer_ns());
     mbar_arrive_expect_tx(&s.full[stage], bytes);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -211,6 +234,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
       phase ^= 1;
     }
   }
+  trace_set(p, kTrLastTma, globaltimer_ns());
   // Every copy this thread issued lands before the CTA may exit.
   int dummy = 0;
 #pragma unroll
@@ -232,7 +256,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
   uint32_t phase = 0, acc_phase = 0;
   uint32_t qn[2] = {0, 0};
   int qslot = 0;
-  int w = find_row(p.wr_tile_start, p.num_wr, t0);
+  int w = p.cta_row[blockIdx.x];
   int64_t re = p.wr_tile_start[w + 1];
   bool issued = false;
   bool ok = mbar_wait(&s.qfull[qslot], qn[qslot] & 1, abort_flag, p.dev_error);
@@ -251,6 +275,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
     if (!mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error)) break;
     if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1, abort_flag, p.dev_error)) break;
     tc_fence_after();
+    if (t == t0) trace_set(p, kTrFirstMma, globaltimer_ns());
     const uint32_t a_base = smem_u32(s.kv + stage * 16384);
     const uint32_t b_base = smem_u32(s.q + qslot * G * kQRowBytes);
     const uint32_t d = tmem + static_cast<uint32_t>(acc * C::N);
@@ -270,6 +295,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
       acc_phase ^= 1;
     }
   }
+  trace_set(p, kTrLastMma, globaltimer_ns());
   if (issued) {
     // all MMAs of this CTA complete before tensor memory is released
     mma_commit(s.done);
@@ -282,145 +308,306 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
 // epilogue: streaming top-k over a shared-memory candidate buffer
 // ---------------------------------------------------------------------------
 
-// Shrinks candidate buffer g to exactly K entries (its K largest keys, ties at
-// the K-th value broken arbitrarily) by an MSB-first 8-bit radix select over
-// the order-preserving keys, and raises the buffer's drop threshold to the
-// resolved prefix of the K-th key. Precondition: cnt[g] > K. Called by all
-// epilogue threads.
-template <int G>
-__device__ void compact(const Smem& s, int g, int K) {
-  using C = Cfg<G>;
-  const int et = threadIdx.x - 64;
-  const int lane = threadIdx.x & 31;
-  uint32_t* ck = s.ckey + g * C::kCap;
-  int32_t* ci = s.cidx + g * C::kCap;
-  Misc* m = s.misc;
-  const int n = m->cnt[g];
-  uint32_t prefix = 0, mask = 0;
-  int remaining = K;
-  const int iters = (n + kEpiThreads - 1) / kEpiThreads;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int b = et; b < 256; b += kEpiThreads) s.hist[b] = 0;
-    named_sync(kEpiBarrier, kEpiThreads);
-#pragma unroll 1
-    for (int j = 0; j < iters; ++j) {
-      const int e = j * kEpiThreads + et;
-      const uint32_t u = e < n ? ck[e] : 0u;
-      const bool act = e < n && (u & mask) == prefix;
-      const uint32_t digit = (u >> shift) & 0xffu;
-      const unsigned am = __ballot_sync(0xffffffffu, act);
-      if (act) {
-        const unsigned peers = __match_any_sync(am, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&s.hist[digit], static_cast<uint32_t>(__popc(peers)));
-      }
-    }
-    named_sync(kEpiBarrier, kEpiThreads);
-    if (et < 32) {
-      uint32_t c[8];
-      int local = 0;
+// Exclusive scan of one int per epilogue thread (in thread order); *total gets
+// the sum. Contains one epilogue barrier.
+__device__ __forceinline__ int epi_exclusive_scan(Misc* m, int v, int* total) {
+  const int lane = threadIdx.x & 31, ew = (threadIdx.x - 64) >> 5;
+  int x = v;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = s.hist[8 * lane + j];
-        local += static_cast<int>(c[j]);
-      }
-      int suf = local;  // keys in bins of this lane and above
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_down_sync(0xffffffffu, suf, off);
-        if (lane + off < 32) suf += v;
-      }
-      int above = suf - local;
-      if (above < remaining && remaining <= suf) {
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-          if (above + static_cast<int>(c[j]) >= remaining) {
-            m->bucket = 8 * lane + j;
-            m->above = above;
-            m->bcount = static_cast<int>(c[j]);
-            break;
-          }
-          above += static_cast<int>(c[j]);
-        }
-      }
-    }
-    named_sync(kEpiBarrier, kEpiThreads);
-    const int b = m->bucket;
-    prefix |= static_cast<uint32_t>(b) << shift;
-    mask |= 0xffu << shift;
-    remaining -= m->above;
-    const int bcount = m->bcount;
-    if (bcount == remaining) break;  // the whole bucket is selected
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
   }
-  // gather into registers, then write the selected keys to the front
+  if (lane == 31) m->scan[ew] = x;
+  named_sync(kEpiBarrier, kEpiThreads);
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = m->scan[i];
+    before += i < ew ? t : 0;
+    tot += t;
+  }
+  *total = tot;
+  return before + x - v;
+}
+
+// With hist[0, nb) complete (after an epilogue barrier; nb <= 1024): the bin
+// holding the `remaining`-th largest key, the number of keys in higher bins and
+// the bin's count, for every epilogue thread. Thread et reads (and zeroes)
+// bins [nb - (et+1)*per, nb - et*per); a scan in thread order orders the bins
+// from the top. The histogram is zero again after.
+__device__ __forceinline__ void take_bucket(uint32_t* hist, Misc* m, int nb, int remaining,
+                                            int* bucket, int* above, int* bcount) {
+  const int et = threadIdx.x - 64;
+  const int per = (nb + kEpiThreads - 1) / kEpiThreads;
+  const int hi = nb - 1 - et * per;  // thread et: bins [hi - per + 1, hi], from the top
+  const int lo = max(hi - per + 1, 0);
+  int c[8];
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = (j < per && hi - j >= lo) ? static_cast<int>(hist[hi - j]) : 0;
+    local += c[j];
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < per && hi - j >= lo) hist[hi - j] = 0;
+  int total;
+  const int excl = epi_exclusive_scan(m, local, &total);  // keys in higher bins
+  if (excl < remaining && remaining <= excl + local) {
+    int acc = excl;
+    bool found = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!found && acc + c[j] >= remaining) {
+        m->bucket = hi - j;
+        m->above = acc;
+        m->bcount = c[j];
+        found = true;
+      }
+      acc += c[j];
+    }
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  *bucket = m->bucket;
+  *above = m->above;
+  *bcount = m->bcount;
+}
+
+// Digit layout of the fixed MSB-first radix select over 32-bit keys: 10, 10,
+// 10 and 2 bits.
+constexpr int kFixedPasses = 4;
+__device__ __forceinline__ int digit_shift(int pass) {
+  return pass == 0 ? 22 : (pass == 1 ? 12 : (pass == 2 ? 2 : 0));
+}
+__device__ __forceinline__ int digit_bins(int pass) { return pass == 3 ? 4 : 1024; }
+
+// Warp-aggregated reservation of one slot per lane with `take` set; returns
+// the lane's position (counter base + rank among the taking lanes).
+__device__ __forceinline__ int warp_reserve(int* counter, bool take) {
+  const int lane = threadIdx.x & 31;
+  const unsigned tm = __ballot_sync(0xffffffffu, take);
+  if (!tm) return 0;
+  const int leader = __ffs(tm) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(tm));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(tm & ((1u << lane) - 1u));
+}
+
+// The K-th largest among the member keys of all epilogue threads (member j of
+// this thread: key u[j] with bit j of `mem` set; K <= member count): an
+// MSB-first radix select over v = key - min (10-bit digits below the top bit
+// of max - min, so the bins spread over the keys present) with one shared
+// histogram (zero on entry and on exit). Result: *mn (min member key), *hi and *pre (the member keys with
+// (key - mn) >> hi > pre are in, those equal to pre are tied) and *rem (how
+// many tied keys complete K). Contains epilogue barriers; all epilogue threads.
+template <int N>
+__device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, int K,
+                          uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out) {
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  Misc* m = s.misc;
+  uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+  for (int j = 0; j < N; ++j)
+    if ((mem >> j) & 1) {
+      mn = min(mn, u[j]);
+      mx = max(mx, u[j]);
+    }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    m->rmin[ew] = mn;
+    m->rmax[ew] = mx;
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  mn = min(min(m->rmin[0], m->rmin[1]), min(m->rmin[2], m->rmin[3]));
+  mx = max(max(m->rmax[0], m->rmax[1]), max(m->rmax[2], m->rmax[3]));
+  int hi = mx >= mn ? 32 - __clz(mx - mn) : 0;  // bits of v still to resolve
+  uint64_t pre = 0;                              // resolved high part: v >> hi
+  int remaining = K;
+#pragma unroll 1
+  while (hi > 0) {
+    const int lo = max(hi - 10, 0);
+    const int nb = 1 << (hi - lo);
+    const uint64_t ta = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const uint64_t v = u[j] - mn;
+      if (((mem >> j) & 1) && (v >> hi) == pre)
+        atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
+    }
+    named_sync(kEpiBarrier, kEpiThreads);
+    const uint64_t tb = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+    int bucket, above, bcount;
+    take_bucket(s.hist, m, nb, remaining, &bucket, &above, &bcount);
+    if (et == 0 && s.trace) {
+      s.trace[kTrRadixHistNs] += tb - ta;
+      s.trace[kTrRadixBucketNs] += globaltimer_ns() - tb;
+      s.trace[kTrRadixPasses] += 1;
+    }
+    pre = (pre << (hi - lo)) | static_cast<uint64_t>(bucket);
+    remaining -= above;
+    hi = lo;
+    if (bcount == remaining) break;  // the whole bin is taken
+  }
+  *mn_out = mn;
+  *hi_out = hi;
+  *pre_out = pre;
+  *rem_out = remaining;
+}
+
+// Position p of a packed candidate buffer: buffers are split into four
+// per-warp regions (appends need no shared counter); packed entries are dealt
+// round-robin over the regions so every region has the same room afterwards.
+template <int G>
+__device__ __forceinline__ int buf_at(int g, int p) {
+  return g * Cfg<G>::kCap + (p & 3) * Cfg<G>::kRegion + (p >> 2);
+}
+
+// Packs candidate buffer g (the four regions, counts in wcnt[g][*]) into its
+// K largest keys (all of them when there are <= K; ties at the K-th value
+// broken arbitrarily): the entries go to registers, radix_kth finds the K-th
+// key, one scan gives every kept entry its packed position. The drop
+// threshold becomes min + (resolved prefix of the K-th key): keys at or below
+// it cannot displace the K kept ones. Sets cnt[g] to the entries kept and
+// returns it; all epilogue threads.
+template <int G>
+__device__ int compact(const Smem& s, int g, int K) {
+  using C = Cfg<G>;
+  static_assert(C::kPer <= 64, "member mask");
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  uint32_t* ck = s.ckey;
+  int32_t* ci = s.cidx;
+  Misc* m = s.misc;
+  const uint64_t tc0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  const int n_w = m->wcnt[g][ew];
+  const int n = m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3];
   uint32_t ku[C::kPer];
   int32_t ki[C::kPer];
+  uint64_t mem = 0;
+  const int rbase = g * C::kCap + ew * C::kRegion;
 #pragma unroll
   for (int j = 0; j < C::kPer; ++j) {
-    const int e = j * kEpiThreads + et;
-    ku[j] = e < n ? ck[e] : 0u;
-    ki[j] = e < n ? ci[e] : 0;
+    const int r = j * 32 + lane;
+    ku[j] = r < n_w ? ck[rbase + r] : 0u;
+    ki[j] = r < n_w ? ci[rbase + r] : 0;
+    if (r < n_w) mem |= 1ull << j;
+  }
+  uint32_t mn = 0;
+  int hi = 0, remaining = 0;
+  uint64_t pre = 0;
+  const bool select = n > K;
+  if (select) {
+    const uint64_t tr0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+    radix_kth(s, ku, mem, K, &mn, &hi, &pre, &remaining);
+    if (et == 0 && s.trace) s.trace[kTrCompactRadixNs] += globaltimer_ns() - tr0;
+  }
+  // One scan of (tied << 16 | greater) gives every thread the counts before it;
+  // tied keys are taken in thread order until `remaining` of them are in.
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int j = 0; j < C::kPer; ++j) {
+    const bool in = (mem >> j) & 1;
+    const uint64_t top = static_cast<uint64_t>(ku[j] - mn) >> hi;
+    n_gt += (in && (!select || top > pre)) ? 1 : 0;
+    n_eq += (in && select && top == pre) ? 1 : 0;
+  }
+  int tot;
+  const int before = epi_exclusive_scan(m, (n_eq << 16) | n_gt, &tot);
+  const int eq_before = before >> 16;
+  int take_eq = min(max(remaining - eq_before, 0), n_eq);
+  int pos = (before & 0xffff) + min(eq_before, remaining);
+  const int kept = (tot & 0xffff) + min(tot >> 16, remaining);
+#pragma unroll
+  for (int j = 0; j < C::kPer; ++j) {
+    const bool in = (mem >> j) & 1;
+    const uint64_t top = static_cast<uint64_t>(ku[j] - mn) >> hi;
+    bool take = in && (!select || top > pre);
+    if (in && select && top == pre && take_eq > 0) {
+      take = true;
+      --take_eq;
+    }
+    if (take) {
+      ck[buf_at<G>(g, pos)] = ku[j];
+      ci[buf_at<G>(g, pos)] = ki[j];
+      ++pos;
+    }
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  if (et == 0) {
+    m->cnt[g] = kept;
+    if (select) m->thr[g] = max(m->thr[g], mn + static_cast<uint32_t>(pre << hi));
+    if (s.trace) {
+      s.trace[kTrCompactNs] += globaltimer_ns() - tc0;
+      s.trace[kTrCompactN] += 1;
+    }
+  }
+  if (lane == 0) m->wcnt[g][ew] = (kept - ew + 3) >> 2;
+  named_sync(kEpiBarrier, kEpiThreads);
+  return kept;
+}
+
+template <int G>
+__device__ void merge_slots(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
+                            int64_t c_last, int32_t* out) {
+  const int et = threadIdx.x - 64;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  uint32_t prefix = 0, mask = 0;
+  int remaining = K;
+  int total = 0;
+  for (int64_t c = c_first; c <= c_last; ++c) total += __ldcg(&p.slot_count[(c + w) * G + g]);
+  if (total > K) {
+#pragma unroll 1
+    for (int pass = 0; pass < kFixedPasses; ++pass) {
+      const int shift = digit_shift(pass), nb = digit_bins(pass);
+      for (int64_t c = c_first; c <= c_last; ++c) {
+        const int64_t slot = (c + w) * G + g;
+        const int n = __ldcg(&p.slot_count[slot]);
+        const uint32_t* keys = p.slot_key + slot * K;
+#pragma unroll 4
+        for (int e = et; e < n; e += kEpiThreads) {
+          const uint32_t u = __ldcg(&keys[e]);
+          if ((u & mask) == prefix)
+            atomicAdd(&s.hist[(u >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        }
+      }
+      named_sync(kEpiBarrier, kEpiThreads);
+      int bucket, above, bcount;
+      take_bucket(s.hist, s.misc, nb, remaining, &bucket, &above, &bcount);
+      prefix |= static_cast<uint32_t>(bucket) << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
+      remaining -= above;
+      if (bcount == remaining) break;
+    }
   }
   if (et == 0) {
     m->sel_out = 0;
     m->sel_tie = 0;
   }
   named_sync(kEpiBarrier, kEpiThreads);
-#pragma unroll
-  for (int j = 0; j < C::kPer; ++j) {
-    const int e = j * kEpiThreads + et;
-    const bool valid = e < n;
-    const uint32_t top = ku[j] & mask;
-    const bool gt = valid && top > prefix;
-    const bool eq = valid && top == prefix;
-    const unsigned em = __ballot_sync(0xffffffffu, eq);
-    int tie_rank = 0;
-    if (em) {
-      int base = 0;
-      const int leader = __ffs(em) - 1;
-      if (lane == leader) base = atomicAdd(&m->sel_tie, __popc(em));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      tie_rank = base + __popc(em & ((1u << lane) - 1u));
-    }
-    const bool take = gt || (eq && tie_rank < remaining);
-    const unsigned tm = __ballot_sync(0xffffffffu, take);
-    if (tm) {
-      int base = 0;
-      const int leader = __ffs(tm) - 1;
-      if (lane == leader) base = atomicAdd(&m->sel_out, __popc(tm));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      if (take) {
-        const int pos = base + __popc(tm & ((1u << lane) - 1u));
-        ck[pos] = ku[j];
-        ci[pos] = ki[j];
-      }
+  for (int64_t c = c_first; c <= c_last; ++c) {
+    const int64_t slot = (c + w) * G + g;
+    const int n = __ldcg(&p.slot_count[slot]);
+    const uint32_t* keys = p.slot_key + slot * K;
+    const int32_t* idxs = p.slot_idx + slot * K;
+    for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
+      const int e = e0 + et;
+      const uint32_t u = e < n ? __ldcg(&keys[e]) : 0u;
+      const uint32_t top = u & mask;
+      const bool gt = e < n && top > prefix;
+      const bool eq = e < n && top == prefix;
+      const int tie_rank = warp_reserve(&m->sel_tie, eq);
+      const bool take = gt || (eq && tie_rank < remaining);
+      const int pos = warp_reserve(&m->sel_out, take);
+      if (take && pos < K) out[pos] = __ldcg(&idxs[e]);
     }
   }
   named_sync(kEpiBarrier, kEpiThreads);
-  if (et == 0) {
-    m->cnt[g] = m->sel_out;
-    m->thr[g] = max(m->thr[g], prefix);
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-}
-
-// Appends (key, idx) to buffer g when it passes the buffer's threshold. The
-// caller guarantees room for one append per epilogue thread.
-__device__ __forceinline__ void append(const Smem& s, int g, int cap, bool pass, uint32_t key,
-                                       int32_t idx) {
-  const int lane = threadIdx.x & 31;
-  const unsigned am = __ballot_sync(0xffffffffu, pass);
-  if (!am) return;
-  int base = 0;
-  const int leader = __ffs(am) - 1;
-  if (lane == leader) base = atomicAdd(&s.misc->cnt[g], __popc(am));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (pass) {
-    const int pos = base + __popc(am & ((1u << lane) - 1u));
-    s.ckey[g * cap + pos] = key;
-    s.cidx[g * cap + pos] = idx;
-  }
+  for (int e = m->sel_out + et; e < K; e += kEpiThreads) out[e] = -1;
 }
 
 template <int G>
@@ -433,12 +620,206 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
     if (!active[g]) continue;
     const int n = s.misc->cnt[g];
     int32_t* o = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
-    for (int e = et; e < p.topk; e += kEpiThreads) o[e] = e < n ? s.cidx[g * C::kCap + e] : -1;
+    for (int e = et; e < p.topk; e += kEpiThreads) o[e] = e < n ? s.cidx[buf_at<G>(g, e)] : -1;
   }
 }
 
-// End of this CTA's part of work row w: reduce each buffer to <= k, then write
-// the output (sole segment) or publish a slot and merge if this is the last.
+
+// From a row histogram: cut = max(floor, the highest bin whose suffix count
+// (keys in bins >= it) reaches K) and above = the count in bins > cut; cut is
+// -1 when the histogram holds fewer than K keys and floor < 0.
+__device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, int floor,
+                                           int* cut, int* above) {
+  const int et = threadIdx.x - 64;
+  if (et == 0) {
+    m->bucket = -1;
+    m->above = 0;
+  }
+  constexpr int per = kRowHistBins / kEpiThreads;
+  const int hi = kRowHistBins - 1 - et * per;
+  int c[per];
+  int local = 0, local_above_floor = 0;
+#pragma unroll
+  for (int j = 0; j < per; ++j) {
+    c[j] = static_cast<int>(__ldcg(&gh[hi - j]));
+    local += c[j];
+    local_above_floor += hi - j > floor ? c[j] : 0;
+  }
+  int total;
+  const int excl = epi_exclusive_scan(m, local, &total);  // contains a barrier
+  if (excl < K && K <= excl + local) {
+    int acc = excl;
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      if (acc + c[j] >= K) {
+        m->bucket = hi - j;
+        m->above = acc;
+        break;
+      }
+      acc += c[j];
+    }
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  int cb = m->bucket, ab = m->above;
+  named_sync(kEpiBarrier, kEpiThreads);
+  if (cb < floor) {
+    int tot_above;
+    epi_exclusive_scan(m, local_above_floor, &tot_above);
+    named_sync(kEpiBarrier, kEpiThreads);
+    cb = floor;
+    ab = tot_above;
+  }
+  *cut = cb;
+  *above = ab;
+}
+
+// Merges work row w's segment slots for token g into `out` (K indices).
+// The row histogram is complete here (every segment added its keys before it
+// counted itself finished), so its cutoff bin is exact. The union of the
+// slots' keys is loaded into registers in one batch of independent loads;
+// entries in bins above the cutoff are selected outright, radix_kth picks the
+// missing ones among the cutoff bin's entries, and the selected entries'
+// indices are gathered in a second batch. Unions larger than the register
+// batch, or a histogram that disagrees with the slots, go to merge_slots.
+template <int G>
+__device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
+                          int64_t c_last, const uint32_t* gh, int32_t* out) {
+  constexpr int kMB = 48;  // union entries per thread (6144 per CTA)
+  const int et = threadIdx.x - 64;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  const int nseg = static_cast<int>(c_last - c_first + 1);
+  // The histogram holds every segment's final buffer, which is exact for all
+  // bins above each segment's threshold bin; the row's cutoff is at or above
+  // the highest of those bins.
+  int floor = et < nseg ? __ldcg(&p.slot_thrbin[(c_first + et + w) * G + g]) : -1;
+  floor = __reduce_max_sync(0xffffffffu, floor);
+  if ((et & 31) == 0) m->scan[et >> 5] = floor;
+  named_sync(kEpiBarrier, kEpiThreads);
+  floor = max(max(m->scan[0], m->scan[1]), max(m->scan[2], m->scan[3]));
+  named_sync(kEpiBarrier, kEpiThreads);
+  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  int cut, above;
+  row_cutoff(gh, m, K, floor, &cut, &above);
+  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  if (et == 0 && s.trace) s.trace[kTrMergeCutNs] += tq1 - tq0;
+  if (cut < 0 || nseg > kEpiThreads) {
+    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
+    merge_slots<G>(p, s, w, g, c_first, c_last, out);
+    return;
+  }
+  // start offsets of the segments' entries in one flat index space, kept in
+  // the token's candidate buffer (idle here; the histogram is radix_kth's)
+  int* seg_start = reinterpret_cast<int*>(s.ckey + g * Cfg<G>::kCap);
+  const int my_n = et < nseg ? __ldcg(&p.slot_count[(c_first + et + w) * G + g]) : 0;
+  int total;
+  const int my_start = epi_exclusive_scan(m, my_n, &total);
+  if (et <= nseg) seg_start[et] = et < nseg ? my_start : total;
+  named_sync(kEpiBarrier, kEpiThreads);
+  if (total > kMB * kEpiThreads) {
+    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1000000;
+    merge_slots<G>(p, s, w, g, c_first, c_last, out);
+    return;
+  }
+  uint32_t u[kMB];
+  uint64_t gt_mask = 0, eq_mask = 0;
+  {
+    int seg = 0;
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      const int i = j * kEpiThreads + et;
+      u[j] = 0u;
+      if (i < total) {
+        while (seg_start[seg + 1] <= i) ++seg;
+        const int64_t slot = (c_first + seg + w) * G + g;
+        u[j] = __ldcg(&p.slot_key[slot * K + (i - seg_start[seg])]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      const bool valid = j * kEpiThreads + et < total;
+      const int b = row_bin(u[j]);
+      if (valid && b > cut) gt_mask |= 1ull << j;
+      if (valid && b == cut) eq_mask |= 1ull << j;
+    }
+  }
+  int tge;
+  epi_exclusive_scan(m, (__popcll(eq_mask) << 16) | __popcll(gt_mask), &tge);
+  const int t_gt = tge & 0xffff, t_eq = tge >> 16;
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int need = K - above;
+  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  if (et == 0 && s.trace) {
+    s.trace[kTrMergeLoadNs] += tq2 - tq1;
+    s.trace[kTrMergeUnion] += static_cast<uint64_t>(total);
+    s.trace[kTrMergeCut] += static_cast<uint64_t>(t_eq);
+    s.trace[kTrMergeSegs] += static_cast<uint64_t>(nseg);
+  }
+  if (t_gt != above || t_eq < need) {
+    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1000;
+    merge_slots<G>(p, s, w, g, c_first, c_last, out);
+    return;
+  }
+  // among the cutoff bin's entries: the `need` largest
+  uint32_t mn = 0;
+  int hi = 0, remaining = need;
+  uint64_t pre = 0;
+  if (t_eq > need) radix_kth(s, u, eq_mask, need, &mn, &hi, &pre, &remaining);
+  if (et == 0 && s.trace) s.trace[kTrMergeRadixNs] += globaltimer_ns() - tq2;
+  uint64_t take_mask = gt_mask;
+  int n_tie = 0;
+#pragma unroll
+  for (int j = 0; j < kMB; ++j) {
+    if (!((eq_mask >> j) & 1)) continue;
+    const uint64_t top = t_eq > need ? static_cast<uint64_t>(u[j] - mn) >> hi : 0;
+    if (top > pre) take_mask |= 1ull << j;
+    else if (top == pre) ++n_tie;
+  }
+  int tt;
+  const int tie_before = epi_exclusive_scan(m, n_tie, &tt);
+  named_sync(kEpiBarrier, kEpiThreads);
+  int take_tie = min(max(remaining - tie_before, 0), n_tie);
+#pragma unroll
+  for (int j = 0; j < kMB; ++j) {
+    if (!((eq_mask >> j) & 1) || ((take_mask >> j) & 1)) continue;
+    const uint64_t top = t_eq > need ? static_cast<uint64_t>(u[j] - mn) >> hi : 0;
+    if (top == pre && take_tie > 0) {
+      take_mask |= 1ull << j;
+      --take_tie;
+    }
+  }
+  int t_take;
+  int pos = epi_exclusive_scan(m, __popcll(take_mask), &t_take);
+  {
+    // gather the selected entries' indices in one batch (into the key
+    // registers, which are no longer needed), then store them
+    int seg = 0;
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      if ((take_mask >> j) & 1) {
+        const int i = j * kEpiThreads + et;
+        while (seg_start[seg + 1] <= i) ++seg;
+        const int64_t slot = (c_first + seg + w) * G + g;
+        u[j] = static_cast<uint32_t>(__ldcg(&p.slot_idx[slot * K + (i - seg_start[seg])]));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      if ((take_mask >> j) & 1) {
+        if (pos < K) out[pos] = static_cast<int32_t>(u[j]);
+        ++pos;
+      }
+    }
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
+  named_sync(kEpiBarrier, kEpiThreads);
+}
+
+// End of this CTA's part of work row w: shrink each buffer to <= k; if the
+// CTA holds the whole row write the output, else publish the candidates that
+// can still make the row's top-k (bins at or above the row histogram's
+// current cutoff) to the segment's slot; the CTA that publishes last merges.
 template <int G>
 __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
                                  const bool (&active)[G], int64_t rs, int64_t re, int64_t t0,
@@ -446,62 +827,90 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
   using C = Cfg<G>;
   const int et = threadIdx.x - 64;
   const int K = p.topk;
+  Misc* m = s.misc;
+  const uint64_t tf0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   named_sync(kEpiBarrier, kEpiThreads);
 #pragma unroll
   for (int g = 0; g < G; ++g)
-    if (active[g] && s.misc->cnt[g] > K) compact<G>(s, g, K);
+    if (active[g]) compact<G>(s, g, K);  // pack (and cut to k)
   if (rs >= t0 && re <= t1) {
     write_rows<G>(p, s, wr, active);
+    if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     return;
   }
   const int64_t c_first = cta_of(rs, T, nC), c_last = cta_of(re - 1, T, nC);
+  uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
   const int64_t slot = static_cast<int64_t>(blockIdx.x) + w;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const int n = active[g] ? s.misc->cnt[g] : 0;
-    const int64_t base = (slot * G + g) * K;
-    for (int e = et; e < n; e += kEpiThreads) {
-      p.slot_key[base + e] = s.ckey[g * C::kCap + e];
-      p.slot_idx[base + e] = s.cidx[g * C::kCap + e];
+    uint32_t* gh = gh_base + g * kRowHistBins;
+    const int n = active[g] ? m->cnt[g] : 0;
+    // the segment's final buffer joins the row histogram
+    for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
+      const int e = e0 + et;
+      const bool valid = e < n;
+      const int b = valid ? row_bin(s.ckey[buf_at<G>(g, e)]) : 0;
+      const unsigned vm = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const unsigned peers = __match_any_sync(vm, b);
+        if (lane == __ffs(peers) - 1) atomicAdd(&gh[b], static_cast<uint32_t>(__popc(peers)));
+      }
     }
-    if (et == 0) p.slot_count[slot * G + g] = n;
+    // publish the candidates that can still make the row's top-k (bins at or
+    // above the histogram's current cutoff) and the threshold's bin
+    int cut = -1, above = 0;
+    if (active[g]) row_cutoff(gh, m, K, -1, &cut, &above);
+    const int64_t base = (slot * G + g) * K;
+    int keep = 0;
+#pragma unroll 4
+    for (int j = 0; j < (C::kCap + kEpiThreads - 1) / kEpiThreads; ++j) {
+      const int e = j * kEpiThreads + et;
+      keep += (e < n && row_bin(s.ckey[buf_at<G>(g, e)]) >= cut) ? 1 : 0;
+    }
+    int tot;
+    int pos = epi_exclusive_scan(m, keep, &tot);
+#pragma unroll 4
+    for (int j = 0; j < (C::kCap + kEpiThreads - 1) / kEpiThreads; ++j) {
+      const int e = j * kEpiThreads + et;
+      const uint32_t u = e < n ? s.ckey[buf_at<G>(g, e)] : 0u;
+      if (e < n && row_bin(u) >= cut) {
+        p.slot_key[base + pos] = u;
+        p.slot_idx[base + pos] = s.cidx[buf_at<G>(g, e)];
+        ++pos;
+      }
+    }
+    if (et == 0) {
+      p.slot_count[slot * G + g] = tot;
+      // a buffer that never filled dropped nothing: its histogram is exact
+      p.slot_thrbin[slot * G + g] = m->thr[g] ? row_bin(m->thr[g]) : -1;
+    }
+    named_sync(kEpiBarrier, kEpiThreads);
   }
   __threadfence();
   named_sync(kEpiBarrier, kEpiThreads);
   if (et == 0) {
     const int old = atomicAdd(&p.seg_counter[w], 1);
-    s.misc->is_last = (old == static_cast<int>(c_last - c_first));
+    m->is_last = (old == static_cast<int>(c_last - c_first));
   }
   named_sync(kEpiBarrier, kEpiThreads);
-  if (!s.misc->is_last) return;
+  if (!m->is_last) {
+    if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
+    return;
+  }
+  const uint64_t tm0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   __threadfence();
-  for (int64_t c = c_first; c <= c_last; ++c) {
-    if (c == blockIdx.x) continue;
-    const int64_t os = c + w;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (!active[g]) continue;
-      const int n = __ldcg(&p.slot_count[os * G + g]);
-      const int64_t base = (os * G + g) * K;
-      for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
-        named_sync(kEpiBarrier, kEpiThreads);
-        if (s.misc->cnt[g] + kEpiThreads > C::kCap) compact<G>(s, g, K);
-        const int e = e0 + et;
-        uint32_t key = 0;
-        int32_t idx = 0;
-        if (e < n) {
-          key = __ldcg(&p.slot_key[base + e]);
-          idx = __ldcg(&p.slot_idx[base + e]);
-        }
-        append(s, g, C::kCap, e < n && key > s.misc->thr[g], key, idx);
-      }
-    }
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
 #pragma unroll
   for (int g = 0; g < G; ++g)
-    if (active[g] && s.misc->cnt[g] > K) compact<G>(s, g, K);
-  write_rows<G>(p, s, wr, active);
+    if (active[g])
+      merge_row<G>(p, s, w, g, c_first, c_last, gh_base + g * kRowHistBins,
+                   p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk);
+  if (et == 0 && s.trace) {
+    const uint64_t now = globaltimer_ns();
+    s.trace[kTrMergeNs] += now - tm0;
+    s.trace[kTrMergeN] += 1;
+    s.trace[kTrFinalizeNs] += now - tf0;
+  }
 }
 
 template <int G, bool kLogits>
@@ -517,11 +926,16 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
 
-  int w = find_row(p.wr_tile_start, p.num_wr, t0);
+  int w = p.cta_row[blockIdx.x];
   int64_t rs = p.wr_tile_start[w], re = p.wr_tile_start[w + 1];
   WorkRow wr;
   int len[G];
   bool active[G];
+  int wcnt[G];        // entries in this warp's region of each token's buffer
+  uint32_t thr[G];    // each buffer's drop threshold
+  const int ew = et >> 5;
+
+  for (int b = et; b < C::kHistBins; b += kEpiThreads) s.hist[b] = 0u;  // zero between uses
 
   auto begin_row = [&]() {
     wr = p.wr[w];
@@ -534,6 +948,11 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       const int g = i / kHeads;
       s.wp[i] = g < wr.ntok ? p.wprime[static_cast<int64_t>(wr.row0 + g) * kHeads + i % kHeads] : 0.f;
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      wcnt[g] = 0;
+      thr[g] = 0u;
+    }
     if (et == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -543,11 +962,18 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     }
     named_sync(kEpiBarrier, kEpiThreads);
   };
+  auto publish_counts = [&]() {
+    if (lane == 0)
+#pragma unroll
+      for (int g = 0; g < G; ++g) s.misc->wcnt[g][ew] = wcnt[g];
+  };
   begin_row();
 
   bool ok = true;
+  long long cyc[5] = {0, 0, 0, 0, 0};  // per-phase clock totals (trace only)
   for (int64_t t = t0; t < t1; ++t) {
     if (t >= re) {
+      publish_counts();
       if (!kLogits) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
       do {
         ++w;
@@ -558,6 +984,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       begin_row();
     }
     const int i = static_cast<int>(t - rs);
+    const long long c0 = clock64();
     // lane 0 of each warp waits for the stage (scales) and the accumulator
     bool wok = true;
     if (lane == 0)
@@ -565,7 +992,10 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
             mbar_wait(&s.tfull[acc], acc_phase, abort_flag, p.dev_error);
     wok = __shfl_sync(0xffffffffu, wok ? 1 : 0, 0) != 0;
     __syncwarp();
+    const long long c1 = clock64();
+    long long c2 = c1;
     float logit[G];
+    if (t == t0 && et == 0 && s.trace) s.trace[kTrFirstEpi] = globaltimer_ns();
     if (wok) {
       tc_fence_after();
       const float scale = s.scales[stage * 128 + mrow];
@@ -576,14 +1006,26 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         tmem_ld32(col, v0);
         tmem_ld32(col + 32, v1);
         tmem_ld_wait();
-        const float* wg = s.wp + g * kHeads;
-        float a0 = 0.f, a1 = 0.f;
+        if (g == 0) c2 = clock64();
+        const float4* w4 = reinterpret_cast<const float4*>(s.wp + g * kHeads);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          a0 = fmaf(wg[j], fmaxf(v0[j], 0.f), a0);
-          a1 = fmaf(wg[32 + j], fmaxf(v1[j], 0.f), a1);
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = w4[q];
+          a0 = fmaf(x.x, fmaxf(v0[4 * q + 0], 0.f), a0);
+          a1 = fmaf(x.y, fmaxf(v0[4 * q + 1], 0.f), a1);
+          a2 = fmaf(x.z, fmaxf(v0[4 * q + 2], 0.f), a2);
+          a3 = fmaf(x.w, fmaxf(v0[4 * q + 3], 0.f), a3);
         }
-        logit[g] = (a0 + a1) * scale;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 x = w4[8 + q];
+          a0 = fmaf(x.x, fmaxf(v1[4 * q + 0], 0.f), a0);
+          a1 = fmaf(x.y, fmaxf(v1[4 * q + 1], 0.f), a1);
+          a2 = fmaf(x.z, fmaxf(v1[4 * q + 2], 0.f), a2);
+          a3 = fmaf(x.w, fmaxf(v1[4 * q + 3], 0.f), a3);
+        }
+        logit[g] = ((a0 + a1) + (a2 + a3)) * scale;
       }
       tc_fence_before();
       __syncwarp();
@@ -592,15 +1034,26 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         mbar_arrive(&s.empty[stage]);
       }
     }
-    // uniform decision across the four epilogue warps (double-buffered vote)
+    const long long c3 = clock64();
+    // Uniform decision across the four epilogue warps (double-buffered vote):
+    // bit 0 = this warp's waits succeeded, bit 1 + g = its region of token g's
+    // buffer has no room for another tile (then all warps compact it).
     const int par = static_cast<int>(t & 1);
-    if (lane == 0) s.misc->vote[par][warp - 2] = wok ? 1 : 0;
+    int need = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      need |= (!kLogits && active[g] && wcnt[g] + 32 > C::kRegion) ? 2 << g : 0;
+    publish_counts();
+    if (lane == 0) s.misc->vote[par][ew] = (wok ? 1 : 0) | need;
     named_sync(kEpiBarrier, kEpiThreads);
-    if (!(s.misc->vote[par][0] & s.misc->vote[par][1] & s.misc->vote[par][2] &
-          s.misc->vote[par][3])) {
+    const long long c4 = clock64();
+    const int v0 = s.misc->vote[par][0], v1 = s.misc->vote[par][1];
+    const int v2 = s.misc->vote[par][2], v3 = s.misc->vote[par][3];
+    if (!(v0 & v1 & v2 & v3 & 1)) {
       ok = false;
       break;
     }
+    const int needs = (v0 | v1 | v2 | v3) >> 1;
     const int key = i * kTileKeys + mrow;
     if (kLogits) {
 #pragma unroll
@@ -610,12 +1063,32 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     } else {
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        if (active[g] && s.misc->cnt[g] + kEpiThreads > C::kCap) compact<G>(s, g, p.topk);
+        if ((needs >> g) & 1) {
+          const int kept = compact<G>(s, g, p.topk);
+          wcnt[g] = (kept - ew + 3) >> 2;
+          thr[g] = s.misc->thr[g];
+        }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
+        // append to this warp's region: ballot + popc, no shared counter
         const uint32_t k = float_key(logit[g]);
-        append(s, g, C::kCap, active[g] && key < len[g] && k > s.misc->thr[g], k, key);
+        const bool pass = active[g] && key < len[g] && k > thr[g];
+        const unsigned pm = __ballot_sync(0xffffffffu, pass);
+        if (pass) {
+          const int at = g * C::kCap + ew * C::kRegion + wcnt[g] + __popc(pm & ((1u << lane) - 1u));
+          s.ckey[at] = k;
+          s.cidx[at] = key;
+        }
+        wcnt[g] += __popc(pm);
       }
+    }
+    {
+      const long long c5 = clock64();
+      cyc[0] += c1 - c0;
+      cyc[1] += c2 - c1;
+      cyc[2] += c3 - c2;
+      cyc[3] += c4 - c3;
+      cyc[4] += c5 - c4;
     }
     if (++stage == C::kStages) {
       stage = 0;
@@ -626,18 +1099,28 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       acc_phase ^= 1;
     }
   }
+  if (et == 0 && s.trace) {
+    s.trace[kTrLastEpi] = globaltimer_ns();
+    s.trace[kTrEpiWaitCyc] = cyc[0];
+    s.trace[kTrEpiLdCyc] = cyc[1];
+    s.trace[kTrEpiMathCyc] = cyc[2];
+    s.trace[kTrEpiVoteCyc] = cyc[3];
+    s.trace[kTrEpiSelCyc] = cyc[4];
+  }
+  publish_counts();
   if (!kLogits && ok) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
+  if (et == 0 && s.trace) s.trace[kTrFinal] = globaltimer_ns();
 }
 
 template <int G, bool kLogits>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
     score_select_kernel(const __grid_constant__ ScoreParams p,
                         const __grid_constant__ CUtensorMap map) {
   using C = Cfg<G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const Smem s = carve<G>(base);
+  Smem s = carve<G>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // With fewer tiles than CTAs only the first T CTAs take part, so that every
@@ -645,6 +1128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t T = p.wr_tile_start[p.num_wr];
   const int64_t nC = min(static_cast<int64_t>(gridDim.x), T);
   const bool part = static_cast<int64_t>(blockIdx.x) < nC;
+  s.trace = (p.trace && part) ? p.trace + static_cast<int64_t>(blockIdx.x) * kTrSlots : nullptr;
   const int64_t t0 = part ? static_cast<int64_t>(blockIdx.x) * T / nC : 0;
   const int64_t t1 = part ? static_cast<int64_t>(blockIdx.x + 1) * T / nC : 0;
 
@@ -661,26 +1145,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s.done, 1);
     s.misc->abort_flag = 0;
+    s.misc->epi_done = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&map);
+  __syncwarp();  // warp 0 reconverges before the block barrier (which counts whole warps)
   if (warp == 1) tmem_alloc(&s.misc->tmem_base, C::kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  named_sync(kSetupBarrier, kThreads);
   tc_fence_after();
   const uint32_t tmem = s.misc->tmem_base;
+  if (threadIdx.x == 0 && s.trace) {
+    s.trace[kTrStart] = globaltimer_ns();
+    s.trace[kTrTiles] = static_cast<uint64_t>(t1 - t0);
+  }
 
   if (t0 < t1) {
+    // One lane of each of warps 0 and 1 runs its role; the warp reconverges
+    // before the block barrier below (which counts whole warps).
     if (warp == 0) {
       if (lane == 0) producer<G>(p, &map, s, t0, t1);
+      __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) mma_issuer<G>(p, s, tmem, t0, t1);
+      __syncwarp();
     } else {
       epilogue<G, kLogits>(p, s, tmem, t0, t1, T, nC);
     }
   }
+  if (threadIdx.x == 64) *reinterpret_cast<volatile int*>(&s.misc->epi_done) = 1;
   tc_fence_before();
-  __syncthreads();
+  named_sync(kTeardownBarrier, kThreads);
+  if (threadIdx.x == 0 && s.trace) {
+    s.trace[kTrEnd] = globaltimer_ns();
+    s.trace[kTrSeen] = static_cast<uint64_t>(*reinterpret_cast<volatile int*>(&s.misc->epi_done));
+  }
+  if (threadIdx.x == 64 && s.trace) s.trace[kTrEndEpi] = globaltimer_ns();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -705,6 +1205,15 @@ idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_cta
 }
 
 }  // namespace
+
+int score_ctas_per_sm(int G) {
+  switch (G) {
+    case 1: return Cfg<1>::kCtasPerSm;
+    case 2: return Cfg<2>::kCtasPerSm;
+    case 4: return Cfg<4>::kCtasPerSm;
+    default: return 1;
+  }
+}
 
 idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s) {

@@ -292,3 +292,14 @@ def test_bad_block_id_and_length_are_reported():
     saib.indexer_decode_topk(d.q, d.w, d.cache, d.block_table, lens2, 1, 2048, dev_error=err2)
     torch.cuda.synchronize()
     assert int(err2.item()) == saib.binding.DEV_BAD_LEN
+
+
+def test_topk_all_equal_logits_degenerate():
+    # every key identical: all logits tie, so any k-subset is right; split rows
+    # then put the whole row into one histogram bin (the merge's fallback path)
+    d = synth.make_decode_from_lens([40000, 9000, 2100], [1, 1, 1], 1, seed=71)
+    c = d.cache.clone()
+    c[:, :8192] = c[0, :128].repeat(64)            # one key row everywhere
+    c[:, 8192:] = c[0, 8192:8196].repeat(64)       # and one scale
+    d.cache = c
+    _check_decode(d, 2048)
