@@ -240,6 +240,35 @@ idx_status indexer_profile_events(void* start_event, void* stop_event);
  */
 idx_status indexer_trace_buffer(void* buffer, size_t bytes);
 
+/*
+ * indexer_decode_topk without a caller workspace. The pages have no
+ * counterpart: this is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory where they run the indexer:
+ * code running while a stream is captured into a CUDA graph, serving loops
+ * that forbid allocator calls on their latency-critical path, or hosts whose
+ * device memory is owned by an allocator this code cannot call. The scratch is
+ * a 16 MiB device array inside the library (one per GPU that loads the
+ * library, held until the process exits); the call allocates nothing. Same
+ * arguments and results as indexer_decode_topk without the workspace.
+ *  - Limit: the batch must fit the scratch, i.e. indexer_decode_workspace_bytes
+ *    (num_reqs, next_n, topk) <= 16 MiB (about 400 requests at next_n = 1 with
+ *    top-2048); a larger batch returns IDX_ERR_WORKSPACE before any work.
+ *  - The first call on each device looks the scratch's device address up (this
+ *    may load the library's device code); make that first call before any
+ *    stream capture.
+ *  - All calls on a device share the scratch, which keeps the last call's
+ *    contents (each call re-initialises what it needs). Calls whose execution
+ *    overlaps on the GPU (other streams, other host threads) race on it.
+ */
+idx_status indexer_decode_topk_noalloc(const void* q, const float* weights,
+                                       const uint8_t* index_cache, int64_t num_pages,
+                                       const int32_t* block_table, int64_t bt_stride,
+                                       int32_t bt_width, const int32_t* row_seq_lens,
+                                       int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                       int32_t head_dim, int32_t topk, int32_t* out_idx,
+                                       uint32_t* dev_error, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

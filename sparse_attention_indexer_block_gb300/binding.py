@@ -43,6 +43,8 @@ SIGNATURES = {
                                        _I32, _I32, _I32, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "indexer_profile_events": (C.c_int, [_P, _P]),
     "indexer_trace_buffer": (C.c_int, [_P, _SZ]),
+    "indexer_decode_topk_noalloc": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
+                                              _I32, _I32, _I32, _P, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -262,3 +264,18 @@ def indexer_trace_buffer(buffer=None):
     else:
         _check("indexer_trace_buffer", load().indexer_trace_buffer(
             _ptr(buffer), int(buffer.numel() * buffer.element_size())))
+
+
+def indexer_decode_topk_noalloc(q, weights, index_cache, block_table, row_seq_lens, next_n: int,
+                                topk: int = MAX_TOPK, out_idx=None, dev_error=None, stream=None):
+    """indexer_decode_topk on the library's own scratch, for callers that
+    cannot allocate a workspace (the output buffer is the caller's)."""
+    R = int(block_table.shape[0])
+    if out_idx is None:
+        out_idx = torch.empty((R * next_n, topk), dtype=torch.int32, device=q.device)
+    st = load().indexer_decode_topk_noalloc(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, next_n,
+        int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_idx), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_topk_noalloc", st)
+    return out_idx
