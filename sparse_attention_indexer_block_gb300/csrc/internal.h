@@ -44,7 +44,8 @@ enum TraceSlot {
   kTrFinal, kTrCompactNs, kTrCompactN, kTrMergeNs, kTrMergeN, kTrEnd, kTrTiles, kTrFinalizeNs,
   kTrEndEpi, kTrMergeFallback, kTrMergeUnion, kTrMergeCut, kTrMergeSegs, kTrSeen, kTrMergeCutNs, kTrMergeLoadNs, kTrMergeRadixNs, kTrCompactRadixNs,
   kTrRadixHistNs, kTrRadixBucketNs, kTrRadixPasses, kTrEpiWaitCyc, kTrEpiLdCyc,
-  kTrEpiMathCyc, kTrEpiVoteCyc, kTrEpiSelCyc, kTrSlots = 40
+  kTrEpiMathCyc, kTrEpiVoteCyc, kTrEpiSelCyc, kTrFinPackNs, kTrFinHistNs, kTrFinCutNs,
+  kTrFinEmitNs, kTrFinPublishNs, kTrMergeTailNs, kTrSlots = 40
 };
 
 // Workspace carve-up shared by decode and prefill.

@@ -58,7 +58,7 @@ struct Cfg {
   static constexpr int kWpOff = kCandIdxOff + G * kCap * 4;
   static constexpr int kHistOff = kWpOff + G * 256;
   static constexpr int kBarOff = kHistOff + kHistBins * 4;
-  static constexpr int kNumBars = 2 * kStages + 9;
+  static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 256 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
@@ -79,6 +79,7 @@ struct Misc {
   int cut_n, fallback;
   int epi_done;
   int wcnt[4][4];  // [token][epilogue warp] entries in the warp's region
+  int staged_uses;  // phases of `staged` used so far
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
@@ -97,6 +98,7 @@ struct Smem {
   uint64_t* qfull;   // [2]
   uint64_t* qempty;  // [2]
   uint64_t* done;
+  uint64_t* staged;  // completion of the bulk copies that stage a merge's candidates
   Misc* misc;
   uint64_t* trace;   // this CTA's trace slots, or nullptr
 };
@@ -120,6 +122,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   s.qfull = s.tempty + 2;
   s.qempty = s.qfull + 2;
   s.done = s.qempty + 2;
+  s.staged = s.done + 1;
   s.misc = reinterpret_cast<Misc*>(base + C::kMiscOff);
   return s;
 }
@@ -458,6 +461,68 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
   *rem_out = remaining;
 }
 
+// radix_kth over keys held in shared memory: member e of the selection is
+// keys[e] for e < n with member(keys[e]). n is a multiple of 4 and keys is
+// 16-byte aligned: each thread reads four keys per 16-byte load.
+template <class Member>
+__device__ void radix_kth_smem(const Smem& s, const uint32_t* keys, int n, Member member, int K,
+                               uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out) {
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  Misc* m = s.misc;
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int n4 = n >> 2;
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int e = et; e < n4; e += kEpiThreads) {
+    const uint4 q = k4[e];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (member(u[c])) {
+        mn = min(mn, u[c]);
+        mx = max(mx, u[c]);
+      }
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    m->rmin[ew] = mn;
+    m->rmax[ew] = mx;
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  mn = min(min(m->rmin[0], m->rmin[1]), min(m->rmin[2], m->rmin[3]));
+  mx = max(max(m->rmax[0], m->rmax[1]), max(m->rmax[2], m->rmax[3]));
+  int hi = mx >= mn ? 32 - __clz(mx - mn) : 0;
+  uint64_t pre = 0;
+  int remaining = K;
+#pragma unroll 1
+  while (hi > 0) {
+    const int lo = max(hi - 10, 0);
+    const int nb = 1 << (hi - lo);
+    for (int e = et; e < n4; e += kEpiThreads) {
+      const uint4 q = k4[e];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint64_t v = u[c] - mn;
+        if (member(u[c]) && (v >> hi) == pre)
+          atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
+      }
+    }
+    named_sync(kEpiBarrier, kEpiThreads);
+    int bucket, above, bcount;
+    take_bucket(s.hist, m, nb, remaining, &bucket, &above, &bcount);
+    pre = (pre << (hi - lo)) | static_cast<uint64_t>(bucket);
+    remaining -= above;
+    hi = lo;
+    if (bcount == remaining) break;
+  }
+  *mn_out = mn;
+  *hi_out = hi;
+  *pre_out = pre;
+  *rem_out = remaining;
+}
+
 // Position p of a packed candidate buffer: buffers are split into four
 // per-warp regions (appends need no shared counter); packed entries are dealt
 // round-robin over the regions so every region has the same room afterwards.
@@ -610,20 +675,36 @@ __device__ void merge_slots(const ScoreParams& p, const Smem& s, int w, int g, i
   for (int e = m->sel_out + et; e < K; e += kEpiThreads) out[e] = -1;
 }
 
+// Entries of token g's buffer sit in four per-warp regions (counts in
+// wcnt[g][*]); warp w's lane l visits its region's entries l, l + 32, ...
+template <int G>
+__device__ __forceinline__ int region_entries(const Smem& s, int g) {
+  const int lane = threadIdx.x & 31, ew = (threadIdx.x - 64) >> 5;
+  const int nw = s.misc->wcnt[g][ew];
+  return lane < nw ? (nw - lane + 31) / 32 : 0;
+}
+
+// Output of a row held entirely by this CTA (its buffer holds <= k entries).
 template <int G>
 __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& wr,
                            const bool (&active)[G]) {
   using C = Cfg<G>;
   const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (!active[g]) continue;
-    const int n = s.misc->cnt[g];
+    const int mine = region_entries<G>(s, g);
+    int total;
+    int pos = epi_exclusive_scan(s.misc, mine, &total);
     int32_t* o = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
-    for (int e = et; e < p.topk; e += kEpiThreads) o[e] = e < n ? s.cidx[buf_at<G>(g, e)] : -1;
+    const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
+    for (int j = 0; j < mine; ++j)
+      if (pos < p.topk) o[pos++] = rx[lane + 32 * j];
+    for (int e = total + et; e < p.topk; e += kEpiThreads) o[e] = -1;
+    named_sync(kEpiBarrier, kEpiThreads);
   }
 }
-
 
 // From a row histogram: cut = max(floor, the highest bin whose suffix count
 // (keys in bins >= it) reaches K) and above = the count in bins > cut; cut is
@@ -765,7 +846,8 @@ __device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int
   int hi = 0, remaining = need;
   uint64_t pre = 0;
   if (t_eq > need) radix_kth(s, u, eq_mask, need, &mn, &hi, &pre, &remaining);
-  if (et == 0 && s.trace) s.trace[kTrMergeRadixNs] += globaltimer_ns() - tq2;
+  const uint64_t tq3 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  if (et == 0 && s.trace) s.trace[kTrMergeRadixNs] += tq3 - tq2;
   uint64_t take_mask = gt_mask;
   int n_tie = 0;
 #pragma unroll
@@ -814,6 +896,158 @@ __device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int
   named_sync(kEpiBarrier, kEpiThreads);
   for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
   named_sync(kEpiBarrier, kEpiThreads);
+  if (et == 0 && s.trace) s.trace[kTrMergeTailNs] += globaltimer_ns() - tq3;
+}
+
+// merge_row for a CTA whose own pipeline has finished (its shared-memory ring
+// is idle): the slots' keys and indices are staged into the ring by one bulk
+// copy per slot and segment (all completing on one mbarrier), then the cutoff
+// classification, the radix select among the cutoff bin's keys and the output
+// all run from shared memory. Returns false (having written nothing) when the
+// union does not fit the ring or the slots disagree with the histogram.
+template <int G>
+__device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int g,
+                                 int64_t c_first, int64_t c_last, const uint32_t* gh,
+                                 int32_t* out) {
+  using C = Cfg<G>;
+  constexpr int kStageCap = C::kStages * 16384 / 8;  // entries (key + index) in the ring
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  const int nseg = static_cast<int>(c_last - c_first + 1);
+  if (nseg > kEpiThreads || (K & 3) != 0) return false;
+  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  // the row's cutoff, floored by the segments' threshold bins (see merge_row)
+  int floor = et < nseg ? __ldcg(&p.slot_thrbin[(c_first + et + w) * G + g]) : -1;
+  const int my_n = et < nseg ? __ldcg(&p.slot_count[(c_first + et + w) * G + g]) : 0;
+  floor = __reduce_max_sync(0xffffffffu, floor);
+  if (lane == 0) m->scan[et >> 5] = floor;
+  named_sync(kEpiBarrier, kEpiThreads);
+  floor = max(max(m->scan[0], m->scan[1]), max(m->scan[2], m->scan[3]));
+  named_sync(kEpiBarrier, kEpiThreads);
+  int cut, above;
+  row_cutoff(gh, m, K, floor, &cut, &above);
+  if (cut < 0) return false;
+  // staging offsets: each segment's entries start on a 16-byte boundary
+  const int my_r = (my_n + 3) & ~3;
+  int total_r;
+  const int my_off = epi_exclusive_scan(m, my_r, &total_r);
+  if (total_r > kStageCap) return false;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
+  int32_t* idxs = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
+  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int use = m->staged_uses;
+  if (et < nseg && my_n > 0) {
+    const int64_t slot = (c_first + et + w) * G + g;
+    const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
+    bulk_load(keys + my_off, p.slot_key + slot * K, bytes, s.staged);
+    bulk_load(idxs + my_off, p.slot_idx + slot * K, bytes, s.staged);
+  }
+  if (et == 0) mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * 8u);
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(s.staged, use & 1, &m->abort_flag, p.dev_error);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  // the padding after a segment's entries becomes key 0, which no logit maps to
+  if (ok && et < nseg)
+    for (int e = my_off + my_n; e < my_off + my_r; ++e) keys[e] = 0u;
+  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
+  named_sync(kEpiBarrier, kEpiThreads);
+  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
+  if (et == 0) m->staged_uses = use + 1;
+  if (!all_ok) return false;
+  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  // classify (four keys per 16-byte load)
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int n4 = total_r >> 2;
+  int n_gt = 0, n_eq = 0;
+  for (int e = et; e < n4; e += kEpiThreads) {
+    const uint4 q = k4[e];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int b = row_bin(u[c]);
+      n_gt += (u[c] != 0u && b > cut) ? 1 : 0;
+      n_eq += (u[c] != 0u && b == cut) ? 1 : 0;
+    }
+  }
+  int tge;
+  epi_exclusive_scan(m, (n_eq << 16) | n_gt, &tge);
+  const int t_gt = tge & 0xffff, t_eq = tge >> 16;
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int need = K - above;
+  if (et == 0 && s.trace) {
+    s.trace[kTrMergeLoadNs] += tq1 - tq0;
+    s.trace[kTrMergeUnion] += static_cast<uint64_t>(total_r);
+    s.trace[kTrMergeCut] += static_cast<uint64_t>(t_eq);
+    s.trace[kTrMergeSegs] += static_cast<uint64_t>(nseg);
+  }
+  if (t_gt != above || t_eq < need) return false;
+  auto in_cut = [cut](uint32_t u) { return u != 0u && row_bin(u) == cut; };
+  uint32_t mn = 0;
+  int hi = 0, remaining = need;
+  uint64_t pre = 0;
+  const bool select = t_eq > need;
+  if (select) radix_kth_smem(s, keys, total_r, in_cut, need, &mn, &hi, &pre, &remaining);
+  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  // output: keys above the cutoff bin, cutoff-bin keys above the resolved
+  // prefix, and `remaining` of the tied ones (in thread order)
+  // per key: 1 = taken, 2 = tied at the K-th value, 0 = out
+  auto klass = [&](uint32_t u) -> int {
+    if (u == 0u) return 0;
+    const int b = row_bin(u);
+    if (b > cut) return 1;
+    if (b < cut) return 0;
+    if (!select) return 1;
+    const uint64_t top = static_cast<uint64_t>(u - mn) >> hi;
+    return top > pre ? 1 : (top == pre ? 2 : 0);
+  };
+  int n_take = 0, n_tie = 0;
+  for (int e = et; e < n4; e += kEpiThreads) {
+    const uint4 q = k4[e];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int k = klass(u[c]);
+      n_take += k == 1 ? 1 : 0;
+      n_tie += k == 2 ? 1 : 0;
+    }
+  }
+  int tt;
+  const int before = epi_exclusive_scan(m, (n_tie << 16) | n_take, &tt);
+  const int tie_before = before >> 16;
+  int take_tie = min(max(remaining - tie_before, 0), n_tie);
+  int pos = (before & 0xffff) + (select ? min(tie_before, remaining) : 0);
+  const int t_take = (tt & 0xffff) + (select ? min(tt >> 16, remaining) : 0);
+  const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  for (int e = et; e < n4; e += kEpiThreads) {
+    const uint4 q = k4[e];
+    const int4 xi = x4[e];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int k = klass(u[c]);
+      bool take = k == 1;
+      if (k == 2 && take_tie > 0) {
+        take = true;
+        --take_tie;
+      }
+      if (take) {
+        if (pos < K) out[pos] = x[c];
+        ++pos;
+      }
+    }
+  }
+  for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
+  named_sync(kEpiBarrier, kEpiThreads);
+  if (et == 0 && s.trace) {
+    s.trace[kTrMergeRadixNs] += tq2 - tq1;
+    s.trace[kTrMergeTailNs] += globaltimer_ns() - tq2;
+  }
+  return true;
 }
 
 // End of this CTA's part of work row w: shrink each buffer to <= k; if the
@@ -829,10 +1063,14 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
   const int K = p.topk;
   Misc* m = s.misc;
   const uint64_t tf0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
   named_sync(kEpiBarrier, kEpiThreads);
 #pragma unroll
   for (int g = 0; g < G; ++g)
-    if (active[g]) compact<G>(s, g, K);  // pack (and cut to k)
+    if (active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
+      compact<G>(s, g, K);  // cut to k (the regions stay the layout)
+  uint64_t tf1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  if (et == 0 && s.trace) s.trace[kTrFinPackNs] += tf1 - tf0;
   if (rs >= t0 && re <= t1) {
     write_rows<G>(p, s, wr, active);
     if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
@@ -841,42 +1079,48 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
   const int64_t c_first = cta_of(rs, T, nC), c_last = cta_of(re - 1, T, nC);
   uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
   const int64_t slot = static_cast<int64_t>(blockIdx.x) + w;
-  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     uint32_t* gh = gh_base + g * kRowHistBins;
-    const int n = active[g] ? m->cnt[g] : 0;
-    // the segment's final buffer joins the row histogram
-    for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
-      const int e = e0 + et;
-      const bool valid = e < n;
-      const int b = valid ? row_bin(s.ckey[buf_at<G>(g, e)]) : 0;
-      const unsigned vm = __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const unsigned peers = __match_any_sync(vm, b);
-        if (lane == __ffs(peers) - 1) atomicAdd(&gh[b], static_cast<uint32_t>(__popc(peers)));
+    const int mine = active[g] ? region_entries<G>(s, g) : 0;
+    const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
+    const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
+    // the segment's final buffer joins the row histogram: counted in shared
+    // memory, then the non-zero bins are added to the global one (and the
+    // shared bins zeroed again)
+    for (int j = 0; j < mine; ++j) atomicAdd(&s.hist[row_bin(rk[lane + 32 * j])], 1u);
+    named_sync(kEpiBarrier, kEpiThreads);
+    for (int b = et; b < kRowHistBins; b += kEpiThreads) {
+      const uint32_t c = s.hist[b];
+      if (c) {
+        atomicAdd(&gh[b], c);
+        s.hist[b] = 0u;
       }
+    }
+    if (et == 0 && s.trace) {
+      const uint64_t now = globaltimer_ns();
+      s.trace[kTrFinHistNs] += now - tf1;
+      tf1 = now;
     }
     // publish the candidates that can still make the row's top-k (bins at or
     // above the histogram's current cutoff) and the threshold's bin
     int cut = -1, above = 0;
     if (active[g]) row_cutoff(gh, m, K, -1, &cut, &above);
+    if (et == 0 && s.trace) {
+      const uint64_t now = globaltimer_ns();
+      s.trace[kTrFinCutNs] += now - tf1;
+      tf1 = now;
+    }
     const int64_t base = (slot * G + g) * K;
     int keep = 0;
-#pragma unroll 4
-    for (int j = 0; j < (C::kCap + kEpiThreads - 1) / kEpiThreads; ++j) {
-      const int e = j * kEpiThreads + et;
-      keep += (e < n && row_bin(s.ckey[buf_at<G>(g, e)]) >= cut) ? 1 : 0;
-    }
+    for (int j = 0; j < mine; ++j) keep += row_bin(rk[lane + 32 * j]) >= cut ? 1 : 0;
     int tot;
     int pos = epi_exclusive_scan(m, keep, &tot);
-#pragma unroll 4
-    for (int j = 0; j < (C::kCap + kEpiThreads - 1) / kEpiThreads; ++j) {
-      const int e = j * kEpiThreads + et;
-      const uint32_t u = e < n ? s.ckey[buf_at<G>(g, e)] : 0u;
-      if (e < n && row_bin(u) >= cut) {
+    for (int j = 0; j < mine; ++j) {
+      const uint32_t u = rk[lane + 32 * j];
+      if (row_bin(u) >= cut) {
         p.slot_key[base + pos] = u;
-        p.slot_idx[base + pos] = s.cidx[buf_at<G>(g, e)];
+        p.slot_idx[base + pos] = rx[lane + 32 * j];
         ++pos;
       }
     }
@@ -886,6 +1130,11 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
       p.slot_thrbin[slot * G + g] = m->thr[g] ? row_bin(m->thr[g]) : -1;
     }
     named_sync(kEpiBarrier, kEpiThreads);
+    if (et == 0 && s.trace) {
+      const uint64_t now = globaltimer_ns();
+      s.trace[kTrFinEmitNs] += now - tf1;
+      tf1 = now;
+    }
   }
   __threadfence();
   named_sync(kEpiBarrier, kEpiThreads);
@@ -894,17 +1143,23 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
     m->is_last = (old == static_cast<int>(c_last - c_first));
   }
   named_sync(kEpiBarrier, kEpiThreads);
+  if (et == 0 && s.trace) s.trace[kTrFinPublishNs] += globaltimer_ns() - tf1;
   if (!m->is_last) {
     if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     return;
   }
   const uint64_t tm0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   __threadfence();
+  // A CTA whose tiles are all done (re >= t1) has an idle ring to stage in.
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-    if (active[g])
-      merge_row<G>(p, s, w, g, c_first, c_last, gh_base + g * kRowHistBins,
-                   p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk);
+  for (int g = 0; g < G; ++g) {
+    if (!active[g]) continue;
+    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
+    const uint32_t* gh = gh_base + g * kRowHistBins;
+    if (re >= t1 && merge_row_staged<G>(p, s, w, g, c_first, c_last, gh, out)) continue;
+    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
+    merge_row<G>(p, s, w, g, c_first, c_last, gh, out);
+  }
   if (et == 0 && s.trace) {
     const uint64_t now = globaltimer_ns();
     s.trace[kTrMergeNs] += now - tm0;
@@ -1144,8 +1399,10 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
       mbar_init(&s.qempty[i], 1);
     }
     mbar_init(s.done, 1);
+    mbar_init(s.staged, 1);
     s.misc->abort_flag = 0;
     s.misc->epi_done = 0;
+    s.misc->staged_uses = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&map);
