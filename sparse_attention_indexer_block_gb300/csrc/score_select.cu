@@ -60,7 +60,8 @@ struct Cfg {
   static constexpr int kBarOff = kHistOff + kHistBins * 4;
   static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 256 + 1024;  // + alignment slack
+  static constexpr int kTraceOff = kMiscOff + 256;  // trace slots (kept in shared memory)
+  static constexpr int kSmemBytes = kTraceOff + kTrSlots * 8 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
   static_assert(kSmemBytes * kCtasPerSm + 1024 * kCtasPerSm <= 233472, "shared memory");
 };
@@ -100,7 +101,7 @@ struct Smem {
   uint64_t* done;
   uint64_t* staged;  // completion of the bulk copies that stage a merge's candidates
   Misc* misc;
-  uint64_t* trace;   // this CTA's trace slots, or nullptr
+  uint64_t* trace;   // this CTA's trace slots (shared memory, copied out at exit), or nullptr
 };
 
 template <int G>
@@ -127,17 +128,6 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
   return s;
 }
 
-// Largest work row w with wts[w] <= t (zero-tile rows share their start).
-__device__ __forceinline__ int find_row(const int32_t* wts, int num_wr, int64_t t) {
-  int lo = 0, hi = num_wr - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (wts[mid] <= t) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
-
 // Row histogram over the top 10 bits of the order-preserving key: sign, the
 // 8 exponent bits and the leading mantissa bit (bins of half a binade).
 constexpr int kRowHistBins = 1024;
@@ -148,8 +138,8 @@ __device__ __forceinline__ int64_t cta_of(int64_t t, int64_t T, int64_t nC) {
   return ((t + 1) * nC - 1) / T;
 }
 
-__device__ __forceinline__ void trace_set(const ScoreParams& p, int slot, uint64_t v) {
-  if (p.trace) p.trace[static_cast<int64_t>(blockIdx.x) * kTrSlots + slot] = v;
+__device__ __forceinline__ void trace_set(const Smem& s, int slot, uint64_t v) {
+  if (s.trace) s.trace[slot] = v;
 }
 
 // ---------------------------------------------------------------------------
@@ -221,7 +211,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
         }
       }
     }
-    if (t == t0) trace_set(p, kTrFirstTma, globaltimer_ns());
+    if (t == t0) trace_set(s, kTrFirstTma, globaltimer_ns());
     mbar_arrive_expect_tx(&s.full[stage], bytes);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -237,7 +227,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
       phase ^= 1;
     }
   }
-  trace_set(p, kTrLastTma, globaltimer_ns());
+  trace_set(s, kTrLastTma, globaltimer_ns());
   // Every copy this thread issued lands before the CTA may exit.
   int dummy = 0;
 #pragma unroll
@@ -278,7 +268,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
     if (!mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error)) break;
     if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1, abort_flag, p.dev_error)) break;
     tc_fence_after();
-    if (t == t0) trace_set(p, kTrFirstMma, globaltimer_ns());
+    if (t == t0) trace_set(s, kTrFirstMma, globaltimer_ns());
     const uint32_t a_base = smem_u32(s.kv + stage * 16384);
     const uint32_t b_base = smem_u32(s.q + qslot * G * kQRowBytes);
     const uint32_t d = tmem + static_cast<uint32_t>(acc * C::N);
@@ -298,7 +288,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
       acc_phase ^= 1;
     }
   }
-  trace_set(p, kTrLastMma, globaltimer_ns());
+  trace_set(s, kTrLastMma, globaltimer_ns());
   if (issued) {
     // all MMAs of this CTA complete before tensor memory is released
     mma_commit(s.done);
@@ -454,68 +444,6 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
     remaining -= above;
     hi = lo;
     if (bcount == remaining) break;  // the whole bin is taken
-  }
-  *mn_out = mn;
-  *hi_out = hi;
-  *pre_out = pre;
-  *rem_out = remaining;
-}
-
-// radix_kth over keys held in shared memory: member e of the selection is
-// keys[e] for e < n with member(keys[e]). n is a multiple of 4 and keys is
-// 16-byte aligned: each thread reads four keys per 16-byte load.
-template <class Member>
-__device__ void radix_kth_smem(const Smem& s, const uint32_t* keys, int n, Member member, int K,
-                               uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out) {
-  const int et = threadIdx.x - 64;
-  const int lane = threadIdx.x & 31, ew = et >> 5;
-  Misc* m = s.misc;
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int n4 = n >> 2;
-  uint32_t mn = 0xffffffffu, mx = 0u;
-  for (int e = et; e < n4; e += kEpiThreads) {
-    const uint4 q = k4[e];
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (member(u[c])) {
-        mn = min(mn, u[c]);
-        mx = max(mx, u[c]);
-      }
-  }
-  mn = __reduce_min_sync(0xffffffffu, mn);
-  mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) {
-    m->rmin[ew] = mn;
-    m->rmax[ew] = mx;
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  mn = min(min(m->rmin[0], m->rmin[1]), min(m->rmin[2], m->rmin[3]));
-  mx = max(max(m->rmax[0], m->rmax[1]), max(m->rmax[2], m->rmax[3]));
-  int hi = mx >= mn ? 32 - __clz(mx - mn) : 0;
-  uint64_t pre = 0;
-  int remaining = K;
-#pragma unroll 1
-  while (hi > 0) {
-    const int lo = max(hi - 10, 0);
-    const int nb = 1 << (hi - lo);
-    for (int e = et; e < n4; e += kEpiThreads) {
-      const uint4 q = k4[e];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint64_t v = u[c] - mn;
-        if (member(u[c]) && (v >> hi) == pre)
-          atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
-      }
-    }
-    named_sync(kEpiBarrier, kEpiThreads);
-    int bucket, above, bcount;
-    take_bucket(s.hist, m, nb, remaining, &bucket, &above, &bcount);
-    pre = (pre << (hi - lo)) | static_cast<uint64_t>(bucket);
-    remaining -= above;
-    hi = lo;
-    if (bcount == remaining) break;
   }
   *mn_out = mn;
   *hi_out = hi;
@@ -709,20 +637,29 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
 // From a row histogram: cut = max(floor, the highest bin whose suffix count
 // (keys in bins >= it) reaches K) and above = the count in bins > cut; cut is
 // -1 when the histogram holds fewer than K keys and floor < 0.
-__device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, int floor,
-                                           int* cut, int* above) {
+// Row-histogram bins held by epilogue thread et in the cutoff scans:
+// [hi - kCutPer + 1, hi] with hi = kRowHistBins - 1 - et * kCutPer, c[j] = bin hi - j.
+constexpr int kCutPer = kRowHistBins / kEpiThreads;
+__device__ __forceinline__ int cut_hi() { return kRowHistBins - 1 - (threadIdx.x - 64) * kCutPer; }
+
+__device__ __forceinline__ void load_row_bins(const uint32_t* gh, int (&c)[kCutPer]) {
+  const int hi = cut_hi();
+#pragma unroll
+  for (int j = 0; j < kCutPer; ++j) c[j] = static_cast<int>(__ldcg(&gh[hi - j]));
+}
+
+// row_cutoff over counts already held by the threads (c as in load_row_bins).
+__device__ __forceinline__ void row_cutoff_vals(const int (&c)[kCutPer], Misc* m, int K, int floor,
+                                                int* cut, int* above) {
   const int et = threadIdx.x - 64;
   if (et == 0) {
     m->bucket = -1;
     m->above = 0;
   }
-  constexpr int per = kRowHistBins / kEpiThreads;
-  const int hi = kRowHistBins - 1 - et * per;
-  int c[per];
+  const int hi = cut_hi();
   int local = 0, local_above_floor = 0;
 #pragma unroll
-  for (int j = 0; j < per; ++j) {
-    c[j] = static_cast<int>(__ldcg(&gh[hi - j]));
+  for (int j = 0; j < kCutPer; ++j) {
     local += c[j];
     local_above_floor += hi - j > floor ? c[j] : 0;
   }
@@ -731,7 +668,7 @@ __device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, i
   if (excl < K && K <= excl + local) {
     int acc = excl;
 #pragma unroll
-    for (int j = 0; j < per; ++j) {
+    for (int j = 0; j < kCutPer; ++j) {
       if (acc + c[j] >= K) {
         m->bucket = hi - j;
         m->above = acc;
@@ -752,6 +689,13 @@ __device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, i
   }
   *cut = cb;
   *above = ab;
+}
+
+__device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, int floor,
+                                           int* cut, int* above) {
+  int c[kCutPer];
+  load_row_bins(gh, c);
+  row_cutoff_vals(c, m, K, floor, cut, above);
 }
 
 // Merges work row w's segment slots for token g into `out` (K indices).
@@ -918,17 +862,13 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   const int nseg = static_cast<int>(c_last - c_first + 1);
   if (nseg > kEpiThreads || (K & 3) != 0) return false;
   const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // the row's cutoff, floored by the segments' threshold bins (see merge_row)
-  int floor = et < nseg ? __ldcg(&p.slot_thrbin[(c_first + et + w) * G + g]) : -1;
-  const int my_n = et < nseg ? __ldcg(&p.slot_count[(c_first + et + w) * G + g]) : 0;
-  floor = __reduce_max_sync(0xffffffffu, floor);
-  if (lane == 0) m->scan[et >> 5] = floor;
-  named_sync(kEpiBarrier, kEpiThreads);
-  floor = max(max(m->scan[0], m->scan[1]), max(m->scan[2], m->scan[3]));
-  named_sync(kEpiBarrier, kEpiThreads);
-  int cut, above;
-  row_cutoff(gh, m, K, floor, &cut, &above);
-  if (cut < 0) return false;
+  // the segments' counts and threshold bins and this thread's bins of the row
+  // histogram, loaded together
+  const int64_t sl = (c_first + et + w) * G + g;
+  int floor = et < nseg ? __ldcg(&p.slot_thrbin[sl]) : -1;
+  const int my_n = et < nseg ? __ldcg(&p.slot_count[sl]) : 0;
+  int hc[kCutPer];
+  load_row_bins(gh, hc);
   // staging offsets: each segment's entries start on a 16-byte boundary
   const int my_r = (my_n + 3) & ~3;
   int total_r;
@@ -940,12 +880,20 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   named_sync(kEpiBarrier, kEpiThreads);
   const int use = m->staged_uses;
   if (et < nseg && my_n > 0) {
-    const int64_t slot = (c_first + et + w) * G + g;
     const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
-    bulk_load(keys + my_off, p.slot_key + slot * K, bytes, s.staged);
-    bulk_load(idxs + my_off, p.slot_idx + slot * K, bytes, s.staged);
+    bulk_load(keys + my_off, p.slot_key + sl * K, bytes, s.staged);
+    bulk_load(idxs + my_off, p.slot_idx + sl * K, bytes, s.staged);
   }
   if (et == 0) mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * 8u);
+  // while the copies are in flight: the row's cutoff, floored by the
+  // segments' threshold bins (see merge_row)
+  floor = __reduce_max_sync(0xffffffffu, floor);
+  if (lane == 0) m->rmin[et >> 5] = static_cast<uint32_t>(floor);
+  named_sync(kEpiBarrier, kEpiThreads);
+  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
+              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
+  int cut, above;
+  row_cutoff_vals(hc, m, K, floor, &cut, &above);
   bool ok = true;
   if (lane == 0) ok = mbar_wait(s.staged, use & 1, &m->abort_flag, p.dev_error);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -957,20 +905,28 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   named_sync(kEpiBarrier, kEpiThreads);
   const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
   if (et == 0) m->staged_uses = use + 1;
-  if (!all_ok) return false;
+  if (!all_ok || cut < 0) return false;
   const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // classify (four keys per 16-byte load)
+  // One pass classifies every key against the cutoff bin (keys carry the row
+  // bin in their top 10 bits) and histograms the next 10 bits of the keys in
+  // it; further passes resolve 10 and then 2 more bits only while the bucket
+  // holding the K-th key is not taken whole. Four keys per 16-byte load.
   const uint4* k4 = reinterpret_cast<const uint4*>(keys);
   const int n4 = total_r >> 2;
+  const uint32_t ucut = static_cast<uint32_t>(cut);
   int n_gt = 0, n_eq = 0;
   for (int e = et; e < n4; e += kEpiThreads) {
     const uint4 q = k4[e];
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int b = row_bin(u[c]);
-      n_gt += (u[c] != 0u && b > cut) ? 1 : 0;
-      n_eq += (u[c] != 0u && b == cut) ? 1 : 0;
+      if (u[c] == 0u) continue;
+      const uint32_t b = u[c] >> 22;
+      n_gt += b > ucut ? 1 : 0;
+      if (b == ucut) {
+        ++n_eq;
+        atomicAdd(&s.hist[(u[c] >> 12) & 1023u], 1u);
+      }
     }
   }
   int tge;
@@ -984,61 +940,126 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     s.trace[kTrMergeCut] += static_cast<uint64_t>(t_eq);
     s.trace[kTrMergeSegs] += static_cast<uint64_t>(nseg);
   }
-  if (t_gt != above || t_eq < need) return false;
-  auto in_cut = [cut](uint32_t u) { return u != 0u && row_bin(u) == cut; };
-  uint32_t mn = 0;
-  int hi = 0, remaining = need;
-  uint64_t pre = 0;
-  const bool select = t_eq > need;
-  if (select) radix_kth_smem(s, keys, total_r, in_cut, need, &mn, &hi, &pre, &remaining);
-  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // output: keys above the cutoff bin, cutoff-bin keys above the resolved
-  // prefix, and `remaining` of the tied ones (in thread order)
-  // per key: 1 = taken, 2 = tied at the K-th value, 0 = out
-  auto klass = [&](uint32_t u) -> int {
-    if (u == 0u) return 0;
-    const int b = row_bin(u);
-    if (b > cut) return 1;
-    if (b < cut) return 0;
-    if (!select) return 1;
-    const uint64_t top = static_cast<uint64_t>(u - mn) >> hi;
-    return top > pre ? 1 : (top == pre ? 2 : 0);
-  };
-  int n_take = 0, n_tie = 0;
-  for (int e = et; e < n4; e += kEpiThreads) {
-    const uint4 q = k4[e];
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+  const bool fail = t_gt != above || t_eq < need;
+  if (fail || t_eq == need) {
+    for (int b = et; b < 1024; b += kEpiThreads) s.hist[b] = 0u;
+    named_sync(kEpiBarrier, kEpiThreads);
+    if (fail) return false;
+  }
+  // a key is in when key >> sh > pre; keys with key >> sh == pre are tied and
+  // `remaining` of them complete K (all of them when all_tied)
+  int sh = 22, remaining = need;
+  uint32_t pre = ucut;
+  bool all_tied = true;
+  if (t_eq > need) {
+    int bucket, ab, bc;
+    take_bucket(s.hist, m, 1024, remaining, &bucket, &ab, &bc);
+    pre = (pre << 10) | static_cast<uint32_t>(bucket);
+    sh = 12;
+    remaining -= ab;
+    if (bc != remaining) {
+      for (int e = et; e < n4; e += kEpiThreads) {
+        const uint4 q = k4[e];
+        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int k = klass(u[c]);
-      n_take += k == 1 ? 1 : 0;
-      n_tie += k == 2 ? 1 : 0;
+        for (int c = 0; c < 4; ++c)
+          if (u[c] != 0u && (u[c] >> 12) == pre) atomicAdd(&s.hist[(u[c] >> 2) & 1023u], 1u);
+      }
+      named_sync(kEpiBarrier, kEpiThreads);
+      take_bucket(s.hist, m, 1024, remaining, &bucket, &ab, &bc);
+      pre = (pre << 10) | static_cast<uint32_t>(bucket);
+      sh = 2;
+      remaining -= ab;
+      if (bc != remaining) {
+        for (int e = et; e < n4; e += kEpiThreads) {
+          const uint4 q = k4[e];
+          const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (u[c] != 0u && (u[c] >> 2) == pre) atomicAdd(&s.hist[u[c] & 3u], 1u);
+        }
+        named_sync(kEpiBarrier, kEpiThreads);
+        take_bucket(s.hist, m, 4, remaining, &bucket, &ab, &bc);
+        pre = (pre << 2) | static_cast<uint32_t>(bucket);
+        sh = 0;
+        remaining -= ab;
+        all_tied = bc == remaining;
+      }
     }
   }
-  int tt;
-  const int before = epi_exclusive_scan(m, (n_tie << 16) | n_take, &tt);
-  const int tie_before = before >> 16;
-  int take_tie = min(max(remaining - tie_before, 0), n_tie);
-  int pos = (before & 0xffff) + (select ? min(tie_before, remaining) : 0);
-  const int t_take = (tt & 0xffff) + (select ? min(tt >> 16, remaining) : 0);
-  const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  // output: per key 1 = in, 2 = tied (`remaining` of the tied keys complete
+  // K, in warp-major order). A counting pass gives each warp its output and
+  // tie offsets; the writing pass places keys by ballot ranks (coalesced).
+  auto klass = [&](uint32_t u) -> uint32_t {
+    const uint32_t top = u >> sh;
+    return u == 0u ? 0u : (top > pre ? 1u : (top == pre ? (all_tied ? 1u : 2u) : 0u));
+  };
+  const int ew = et >> 5;
+  int n_in = 0, n_tie = 0;
   for (int e = et; e < n4; e += kEpiThreads) {
     const uint4 q = k4[e];
-    const int4 xi = x4[e];
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-    const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int k = klass(u[c]);
-      bool take = k == 1;
-      if (k == 2 && take_tie > 0) {
-        take = true;
-        --take_tie;
+      const uint32_t k = klass(u[c]);
+      n_in += k == 1u ? 1 : 0;
+      n_tie += k == 2u ? 1 : 0;
+    }
+  }
+  n_in = __reduce_add_sync(0xffffffffu, n_in);
+  n_tie = __reduce_add_sync(0xffffffffu, n_tie);
+  if (lane == 0) {
+    m->scan[ew] = n_in;
+    m->rmax[ew] = static_cast<uint32_t>(n_tie);
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  int tie_base = 0, ties_before_all = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    tie_base += i < ew ? static_cast<int>(m->rmax[i]) : 0;
+  }
+  int out_base = 0, t_take = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tb = ties_before_all;
+    const int wt = static_cast<int>(m->rmax[i]);
+    const int taken_ties = min(max(remaining - tb, 0), wt);
+    ties_before_all += wt;
+    const int w_take = m->scan[i] + taken_ties;
+    out_base += i < ew ? w_take : 0;
+    t_take += w_take;
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
+    const int e = e0 + lane;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    int4 xi = make_int4(0, 0, 0, 0);
+    if (e < n4) {
+      q = k4[e];
+      xi = x4[e];
+    }
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
+    uint32_t kc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) kc[c] = klass(u[c]);
+    if (!all_tied) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t tm = __ballot_sync(0xffffffffu, kc[c] == 2u);
+        if (kc[c] == 2u) kc[c] = tie_base + __popc(tm & lt) < remaining ? 1u : 0u;
+        tie_base += __popc(tm);
       }
-      if (take) {
-        if (pos < K) out[pos] = x[c];
-        ++pos;
-      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t im = __ballot_sync(0xffffffffu, kc[c] == 1u);
+      const int pos = out_base + __popc(im & lt);
+      if (kc[c] == 1u && pos < K) out[pos] = x[c];
+      out_base += __popc(im);
     }
   }
   for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
@@ -1082,13 +1103,13 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     uint32_t* gh = gh_base + g * kRowHistBins;
-    const int mine = active[g] ? region_entries<G>(s, g) : 0;
     const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
     // the segment's final buffer joins the row histogram: counted in shared
     // memory, then the non-zero bins are added to the global one (and the
     // shared bins zeroed again)
-    for (int j = 0; j < mine; ++j) atomicAdd(&s.hist[row_bin(rk[lane + 32 * j])], 1u);
+    const int nw = active[g] ? m->wcnt[g][ew] : 0;
+    for (int j = lane; j < nw; j += 32) atomicAdd(&s.hist[row_bin(rk[j])], 1u);
     named_sync(kEpiBarrier, kEpiThreads);
     for (int b = et; b < kRowHistBins; b += kEpiThreads) {
       const uint32_t c = s.hist[b];
@@ -1113,17 +1134,29 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
     }
     const int64_t base = (slot * G + g) * K;
     int keep = 0;
-    for (int j = 0; j < mine; ++j) keep += row_bin(rk[lane + 32 * j]) >= cut ? 1 : 0;
-    int tot;
-    int pos = epi_exclusive_scan(m, keep, &tot);
-    for (int j = 0; j < mine; ++j) {
-      const uint32_t u = rk[lane + 32 * j];
-      if (row_bin(u) >= cut) {
-        p.slot_key[base + pos] = u;
-        p.slot_idx[base + pos] = rx[lane + 32 * j];
-        ++pos;
-      }
+    for (int j = lane; j < nw; j += 32) keep += row_bin(rk[j]) >= cut ? 1 : 0;
+    keep = __reduce_add_sync(0xffffffffu, keep);
+    if (lane == 0) m->scan[ew] = keep;
+    named_sync(kEpiBarrier, kEpiThreads);
+    int pos = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pos += i < ew ? m->scan[i] : 0;
+      tot += m->scan[i];
     }
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int j0 = 0; j0 < nw; j0 += 32) {
+      const int j = j0 + lane;
+      const uint32_t u = j < nw ? rk[j] : 0u;
+      const bool kp = j < nw && row_bin(u) >= cut;
+      const uint32_t km = __ballot_sync(0xffffffffu, kp);
+      if (kp) {
+        p.slot_key[base + pos + __popc(km & lt)] = u;
+        p.slot_idx[base + pos + __popc(km & lt)] = rx[j];
+      }
+      pos += __popc(km);
+    }
+    named_sync(kEpiBarrier, kEpiThreads);
     if (et == 0) {
       p.slot_count[slot * G + g] = tot;
       // a buffer that never filled dropped nothing: its histogram is exact
@@ -1383,7 +1416,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
   const int64_t T = p.wr_tile_start[p.num_wr];
   const int64_t nC = min(static_cast<int64_t>(gridDim.x), T);
   const bool part = static_cast<int64_t>(blockIdx.x) < nC;
-  s.trace = (p.trace && part) ? p.trace + static_cast<int64_t>(blockIdx.x) * kTrSlots : nullptr;
+  s.trace = (p.trace && part) ? reinterpret_cast<uint64_t*>(base + C::kTraceOff) : nullptr;
   const int64_t t0 = part ? static_cast<int64_t>(blockIdx.x) * T / nC : 0;
   const int64_t t1 = part ? static_cast<int64_t>(blockIdx.x + 1) * T / nC : 0;
 
@@ -1403,6 +1436,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
     s.misc->abort_flag = 0;
     s.misc->epi_done = 0;
     s.misc->staged_uses = 0;
+    if (s.trace)
+      for (int i = 0; i < kTrSlots; ++i) s.trace[i] = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&map);
@@ -1438,6 +1473,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
     s.trace[kTrSeen] = static_cast<uint64_t>(*reinterpret_cast<volatile int*>(&s.misc->epi_done));
   }
   if (threadIdx.x == 64 && s.trace) s.trace[kTrEndEpi] = globaltimer_ns();
+  if (s.trace) {
+    named_sync(kTeardownBarrier, kThreads);
+    if (threadIdx.x < kTrSlots)
+      p.trace[static_cast<int64_t>(blockIdx.x) * kTrSlots + threadIdx.x] = s.trace[threadIdx.x];
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
