@@ -60,6 +60,39 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Each replica draws its own batch."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(values, world: int, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity for one rank).
+    The reduction runs on `device` (a CUDA device under NCCL, the CPU under gloo)."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank_step: int, steps: int, world: int, ms: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank (ms)."""
+    return units_per_rank_step * steps * world / (ms / 1e3)
+
+
+WORKLOAD_DESCS = {
+    "decode": WORKLOAD_DESC,
+    "mtp": ("MTP decode: 64 requests, next_n 2, decode_lens from {1, 2}, seq_lens uniform in "
+            "[4096, 65536], 64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
+    "long": ("long context: 128 requests, next_n 1, seq_len 131072, 1% heavy-tail keys, "
+             "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
+    "tiny": ("tiny decode: 4 requests, next_n 1, seq_lens {1000, 2048, 3000, 4096}, "
+             "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
+}
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -152,7 +185,7 @@ def run_ours(args, rank, world, local):
     libbuild.build()
     saib.load()
 
-    seed = args.seed + 1000 * rank
+    seed = rank_seed(args.seed, rank)
     d = synth.make_decode(args.workload, seed=seed, device=dev)
     R, G, k = d.num_reqs, d.next_n, d.topk
     seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
@@ -226,15 +259,10 @@ def run_ours(args, rank, world, local):
                 g.replay()
             e1.record(stream)
         barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the timed region")
-    value = keys_per_step * K * world / (ms / 1e3)
+    value = whole_job_rate(keys_per_step, K, world, ms)
 
     # live per-launch duration of the score/select kernel (eager, same rotation)
     n_prof = min(K, 400)
@@ -292,13 +320,8 @@ def run_ours(args, rank, world, local):
             e2e_step()
         f1.record(stream)
     barrier()
-    e2e_ms = f0.elapsed_time(f1) / n_e2e
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": keys_per_step * world / (e2e_ms / 1e3), "unit": "keys/s",
+    e2e_ms = max_over_ranks([f0.elapsed_time(f1) / n_e2e], world, dev)[0]
+    e2e = {"value": whole_job_rate(keys_per_step, 1, world, e2e_ms), "unit": "keys/s",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
 
@@ -311,7 +334,8 @@ def run_ours(args, rank, world, local):
                 "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
                 "data": "synthetic",
-                "config": {"workload": WORKLOAD_DESC, "requests": R, "next_n": G, "topk": k,
+                "config": {"workload": WORKLOAD_DESCS.get(args.workload, args.workload),
+                           "requests": R, "next_n": G, "topk": k,
                            "keys_per_step": keys_per_step,
                            "index_bytes_per_step": algo_bytes,
                            "l2": f"cold: {n_copies} rotating index-cache copies "
@@ -406,7 +430,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "requests": d.num_reqs, "next_n": G,
+            "config": {"workload": WORKLOAD_DESCS.get(args.workload, args.workload),
+                       "requests": d.num_reqs, "next_n": G,
                        "topk": k, "parallelism": "host threads"},
             "cpu_baseline": {"value": value, "unit": "keys/s", "cores": threads,
                              "kind": "oracle", "sample": sample},

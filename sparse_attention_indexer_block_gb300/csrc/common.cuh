@@ -224,6 +224,18 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch. Every kernel of this library is launched with
+// programmatic stream serialization, so it may start while the kernel before it
+// in the stream is still finishing: pdl_wait() blocks until that kernel has
+// completed and its memory operations are visible (it returns at once when
+// there is no such dependency), and must precede every global-memory access
+// that could depend on earlier work; pdl_trigger() lets the next kernel in the
+// stream begin launching (it still waits for this one before touching memory).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -89,6 +89,8 @@ __device__ __forceinline__ uint32_t swizzled_offset(int h, int lane) {
 __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
     const __nv_bfloat16* __restrict__ q, const float* __restrict__ w, int64_t rows,
     uint8_t* __restrict__ q8, float* __restrict__ wprime) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * kPrepThreads) >> 5;
@@ -141,6 +143,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
     float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
     int32_t* __restrict__ cta_row) {
+  pdl_trigger();
+  pdl_wait();
   const int G = a.next_n;
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * G;
   if (blockIdx.x == 0) {
@@ -218,6 +222,8 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
     float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
     int32_t* __restrict__ cta_row) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int G = 4;
   const int64_t rows = a.row_hi - a.row_lo;
   if (blockIdx.x == 0) {
@@ -304,6 +310,8 @@ __global__ void __launch_bounds__(kPrepThreads) expand_kernel(
     int32_t num_reqs, int32_t next_n, const int32_t* __restrict__ bt, int64_t bt_stride,
     int32_t bt_width, int32_t mode, int32_t* __restrict__ row_lens, int32_t* __restrict__ row_bt,
     int64_t out_stride, int64_t num_out_rows, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int64_t s_carry, s_total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b0 = blockIdx.x * kPrepWarps;
@@ -387,42 +395,47 @@ idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, in
                          int64_t num_out_rows, uint32_t* err, cudaStream_t s) {
   int grid = (num_reqs + kPrepWarps - 1) / kPrepWarps;
   if (grid < 1) grid = 1;
-  expand_kernel<<<grid, kPrepThreads, 0, s>>>(seq_lens, decode_lens, num_reqs, next_n, bt,
-                                              bt_stride, bt_width, mode, row_lens, row_bt,
-                                              out_stride, num_out_rows, err);
-  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return launch_pdl(expand_kernel, grid, kPrepThreads, 0, s, seq_lens, decode_lens, num_reqs,
+                    next_n, bt, bt_stride, bt_width, mode, row_lens, row_bt, out_stride,
+                    num_out_rows, err) == cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
 }
 
 idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows, uint8_t* q8,
                                  float* wprime, cudaStream_t s) {
-  quantize_plain_kernel<<<prep_grid(rows * kHeads), kPrepThreads, 0, s>>>(q, w, rows, q8, wprime);
-  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return launch_pdl(quantize_plain_kernel, prep_grid(rows * kHeads), kPrepThreads, 0, s, q, w, rows,
+                    q8, wprime) == cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
 }
 
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * a.next_n;
   const int grid = 1 + prep_grid(rows * kHeads);
-  decode_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
-      a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
+  const cudaError_t e = launch_pdl(
+      decode_prep_kernel, grid, kPrepThreads, 0, s, a, reinterpret_cast<WorkRow*>(ws + L.wr),
+      reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
       ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
       reinterpret_cast<int32_t*>(ws + L.cta_row));
-  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s) {
   const int64_t rows = a.row_hi - a.row_lo;
   const int grid = 1 + prep_grid(rows * kHeads);
-  prefill_prep_kernel<<<grid, kPrepThreads, 0, s>>>(
-      a, reinterpret_cast<WorkRow*>(ws + L.wr), reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
+  const cudaError_t e = launch_pdl(
+      prefill_prep_kernel, grid, kPrepThreads, 0, s, a, reinterpret_cast<WorkRow*>(ws + L.wr),
+      reinterpret_cast<int32_t*>(ws + L.wr_tile_start),
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
       ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
       reinterpret_cast<int32_t*>(ws + L.cta_row));
-  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
 }  // namespace saib

@@ -1411,6 +1411,11 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
   Smem s = carve<G>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Shared-memory setup needs nothing from earlier kernels; everything after
+  // pdl_wait() may read what they wrote.
+  if (warp == 0 && lane == 0) prefetch_tensormap(&map);
+  pdl_wait();
+
   // With fewer tiles than CTAs only the first T CTAs take part, so that every
   // participating CTA owns at least one tile (segment counts rely on it).
   const int64_t T = p.wr_tile_start[p.num_wr];
@@ -1440,12 +1445,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
       for (int i = 0; i < kTrSlots; ++i) s.trace[i] = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tensormap(&map);
   __syncwarp();  // warp 0 reconverges before the block barrier (which counts whole warps)
   if (warp == 1) tmem_alloc(&s.misc->tmem_base, C::kTmemCols);
   tc_fence_before();
   named_sync(kSetupBarrier, kThreads);
   tc_fence_after();
+  pdl_trigger();
   const uint32_t tmem = s.misc->tmem_base;
   if (threadIdx.x == 0 && s.trace) {
     s.trace[kTrStart] = globaltimer_ns();
@@ -1497,8 +1502,10 @@ idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_cta
       return IDX_ERR_CUDA;
     configured_device = dev;
   }
-  score_select_kernel<G, kLogits><<<num_ctas, kThreads, C::kSmemBytes, s>>>(p, map);
-  return cudaPeekAtLastError() == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return launch_pdl(score_select_kernel<G, kLogits>, num_ctas, kThreads, C::kSmemBytes, s, p, map) ==
+                 cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
 }
 
 }  // namespace
