@@ -47,6 +47,9 @@ struct Cfg {
   static constexpr int kCap = G == 1 ? 3072 : (G == 2 ? 4096 : 2560);  // candidates per token row
   static constexpr int kRegion = kCap / 4;          // per-warp append region
   static constexpr int kPer = kRegion / 32;         // region entries per lane
+  // a full buffer is cut to at most k + kSlack entries (whichever bucket
+  // boundary the radix search reaches first)
+  static constexpr int kSlack = kCap / 24;
   static constexpr int kHistBins = 1024;
   static constexpr uint32_t kTmemCols = 2 * N <= 128 ? 128u : (2 * N <= 256 ? 256u : 512u);
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
@@ -394,10 +397,14 @@ __device__ __forceinline__ int warp_reserve(int* counter, bool take) {
 // of max - min, so the bins spread over the keys present) with one shared
 // histogram (zero on entry and on exit). Result: *mn (min member key), *hi and *pre (the member keys with
 // (key - mn) >> hi > pre are in, those equal to pre are tied) and *rem (how
-// many tied keys complete K). Contains epilogue barriers; all epilogue threads.
+// many tied keys complete K). With slack > 0 the search may stop early at a
+// bucket that holds at most `slack` keys beyond K: the whole bucket is then
+// taken (*rem = its count), so up to K + slack keys are in. Contains epilogue
+// barriers; all epilogue threads.
 template <int N>
 __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, int K,
-                          uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out) {
+                          uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out,
+                          int slack = 0) {
   const int et = threadIdx.x - 64;
   const int lane = threadIdx.x & 31, ew = et >> 5;
   Misc* m = s.misc;
@@ -443,7 +450,10 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
     pre = (pre << (hi - lo)) | static_cast<uint64_t>(bucket);
     remaining -= above;
     hi = lo;
-    if (bcount == remaining) break;  // the whole bin is taken
+    if (bcount - remaining <= slack) {  // the whole bin is taken
+      remaining = bcount;
+      break;
+    }
   }
   *mn_out = mn;
   *hi_out = hi;
@@ -467,7 +477,7 @@ __device__ __forceinline__ int buf_at(int g, int p) {
 // it cannot displace the K kept ones. Sets cnt[g] to the entries kept and
 // returns it; all epilogue threads.
 template <int G>
-__device__ int compact(const Smem& s, int g, int K) {
+__device__ int compact(const Smem& s, int g, int K, int slack = 0) {
   using C = Cfg<G>;
   static_assert(C::kPer <= 64, "member mask");
   const int et = threadIdx.x - 64;
@@ -495,7 +505,7 @@ __device__ int compact(const Smem& s, int g, int K) {
   const bool select = n > K;
   if (select) {
     const uint64_t tr0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-    radix_kth(s, ku, mem, K, &mn, &hi, &pre, &remaining);
+    radix_kth(s, ku, mem, K, &mn, &hi, &pre, &remaining, slack);
     if (et == 0 && s.trace) s.trace[kTrCompactRadixNs] += globaltimer_ns() - tr0;
   }
   // One scan of (tied << 16 | greater) gives every thread the counts before it;
@@ -873,18 +883,25 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   const int my_r = (my_n + 3) & ~3;
   int total_r;
   const int my_off = epi_exclusive_scan(m, my_r, &total_r);
-  if (total_r > kStageCap) return false;
+  if (total_r > 2 * kStageCap) return false;
+  // Keys and indices are staged when both fit; otherwise only the keys, and
+  // the selected entries' indices are gathered from the slots at the end
+  // (segment staging offsets kept in the idle candidate-index buffer).
+  const bool with_idx = total_r <= kStageCap;
   uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
   int32_t* idxs = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
+  int32_t* seg_off = s.cidx;
+  if (!with_idx && et <= nseg) seg_off[et] = et < nseg ? my_off : total_r;
   fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
   named_sync(kEpiBarrier, kEpiThreads);
   const int use = m->staged_uses;
   if (et < nseg && my_n > 0) {
     const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
     bulk_load(keys + my_off, p.slot_key + sl * K, bytes, s.staged);
-    bulk_load(idxs + my_off, p.slot_idx + sl * K, bytes, s.staged);
+    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * K, bytes, s.staged);
   }
-  if (et == 0) mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * 8u);
+  if (et == 0)
+    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * (with_idx ? 8u : 4u));
   // while the copies are in flight: the row's cutoff, floored by the
   // segments' threshold bins (see merge_row)
   floor = __reduce_max_sync(0xffffffffu, floor);
@@ -1032,6 +1049,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   }
   named_sync(kEpiBarrier, kEpiThreads);
   const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  int32_t* src = reinterpret_cast<int32_t*>(s.ckey);  // staged position of output p
   const uint32_t lt = (1u << lane) - 1u;
   for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
     const int e = e0 + lane;
@@ -1039,7 +1057,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     int4 xi = make_int4(0, 0, 0, 0);
     if (e < n4) {
       q = k4[e];
-      xi = x4[e];
+      if (with_idx) xi = x4[e];
     }
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
     const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
@@ -1058,8 +1076,25 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     for (int c = 0; c < 4; ++c) {
       const uint32_t im = __ballot_sync(0xffffffffu, kc[c] == 1u);
       const int pos = out_base + __popc(im & lt);
-      if (kc[c] == 1u && pos < K) out[pos] = x[c];
+      if (kc[c] == 1u && pos < K) {
+        if (with_idx) out[pos] = x[c];
+        else src[pos] = 4 * e + c;
+      }
       out_base += __popc(im);
+    }
+  }
+  if (!with_idx) {
+    named_sync(kEpiBarrier, kEpiThreads);
+    for (int q = et; q < min(t_take, K); q += kEpiThreads) {
+      const int e = src[q];
+      int lo = 0, hi = nseg - 1;  // the segment holding staged position e
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (seg_off[mid] <= e) lo = mid;
+        else hi = mid - 1;
+      }
+      const int64_t seg_slot = (c_first + lo + w) * G + g;
+      out[q] = __ldcg(&p.slot_idx[seg_slot * K + (e - seg_off[lo])]);
     }
   }
   for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
@@ -1352,7 +1387,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
 #pragma unroll
       for (int g = 0; g < G; ++g)
         if ((needs >> g) & 1) {
-          const int kept = compact<G>(s, g, p.topk);
+          const int kept = compact<G>(s, g, p.topk, C::kSlack);
           wcnt[g] = (kept - ew + 3) >> 2;
           thr[g] = s.misc->thr[g];
         }
