@@ -61,6 +61,9 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
   L.row_hist = take(4 * L.row_hist_words, 256);
   L.cta_row = take(4 * static_cast<size_t>(num_ctas), 256);
   L.slot_thrbin = take(4 * static_cast<size_t>(nslots * G), 256);
+  L.cta_tile = take(4 * static_cast<size_t>(num_ctas + 1), 256);
+  L.row_vs = take(4 * static_cast<size_t>(num_wr + 1), 256);
+  L.row_ctas = take(8 * static_cast<size_t>(num_wr), 256);
   L.total = round_up(off, 256);
   return L;
 }
@@ -196,8 +199,12 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   if ((st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // A work row that ends inside a CTA's range costs that CTA a segment
+  // finalisation (publication, often a buffer cut) worth about this many
+  // tiles of streaming; the split gives such CTAs correspondingly fewer tiles.
+  const int32_t row_penalty = logits ? 0 : (next_n == 1 ? 6 : 12);
   DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
-                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC};
+                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty};
   if ((st = launch_decode_prep(a, ws, L, s)) != IDX_OK) return st;
   ScoreParams p{};
   p.cache = index_cache;
@@ -207,6 +214,8 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
   p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
   p.cta_row = reinterpret_cast<const int32_t*>(ws + L.cta_row);
+  p.cta_tile = reinterpret_cast<const int32_t*>(ws + L.cta_tile);
+  p.row_ctas = reinterpret_cast<const int2*>(ws + L.row_ctas);
   p.num_wr = num_reqs;
   p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
   p.q8 = ws + L.q8;
@@ -423,7 +432,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     if (nw == 0) continue;
     PrefillPrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, seq_lens, query_start_loc,
                       c.r0, c.r1, lo, hi, static_cast<int32_t>(nw), topk, bt_width, out_idx,
-                      dev_error, nC};
+                      dev_error, nC, 0};
     if ((st = launch_prefill_prep(a, ws, L, s)) != IDX_OK) return st;
     ScoreParams p{};
     p.cache = index_cache;
@@ -433,6 +442,10 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.wr = reinterpret_cast<const WorkRow*>(ws + L.wr);
     p.wr_tile_start = reinterpret_cast<const int32_t*>(ws + L.wr_tile_start);
     p.cta_row = reinterpret_cast<const int32_t*>(ws + L.cta_row);
+    p.cta_tile = reinterpret_cast<const int32_t*>(ws + L.cta_tile);
+    p.row_ctas = reinterpret_cast<const int2*>(ws + L.row_ctas);
+  p.cta_tile = reinterpret_cast<const int32_t*>(ws + L.cta_tile);
+  p.row_ctas = reinterpret_cast<const int2*>(ws + L.row_ctas);
     p.num_wr = static_cast<int32_t>(nw);
     p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
     p.q8 = ws + L.q8;

@@ -40,6 +40,8 @@ struct ScoreParams {
   const WorkRow* wr;
   const int32_t* wr_tile_start;  // [num_wr + 1], exclusive prefix of tiles per work row
   const int32_t* cta_row;        // [grid] work row holding each CTA's first tile
+  const int32_t* cta_tile;       // [grid + 1] first tile of each CTA (cost-balanced split)
+  const int2* row_ctas;          // [num_wr] first and last CTA holding each work row's tiles
   int32_t num_wr;
   const int32_t* row_len;        // [rows] validated key count per token row
   const uint8_t* q8;             // [rows, 8192] swizzled fp8 images of q
@@ -72,7 +74,7 @@ enum TraceSlot {
 // Workspace carve-up shared by decode and prefill.
 struct WsLayout {
   size_t wr, wr_tile_start, row_len, seg_counter, slot_count, q8, wprime, slot_key, slot_idx;
-  size_t row_hist, row_hist_words, cta_row, slot_thrbin;
+  size_t row_hist, row_hist_words, cta_row, slot_thrbin, cta_tile, row_vs, row_ctas;
   size_t total;
 };
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
@@ -101,7 +103,8 @@ struct DecodePrepArgs {
   int32_t score_all;  // logits mode: every row with len > 0 is scored
   int32_t* out_idx;   // causal fill target (nullable in logits mode)
   uint32_t* err;
-  int32_t num_ctas;   // grid of the score/select launch that follows
+  int32_t num_ctas;     // grid of the score/select launch that follows
+  int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -118,7 +121,8 @@ struct PrefillPrepArgs {
   int32_t bt_width;
   int32_t* out_idx;
   uint32_t* err;
-  int32_t num_ctas;   // grid of the score/select launch that follows
+  int32_t num_ctas;     // grid of the score/select launch that follows
+  int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
 };
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);

@@ -1,5 +1,7 @@
 // Row expansion, q quantisation, and the per-launch schedule + causal fill that
 // precede the score/select kernel.
+#include <climits>
+
 #include "internal.h"
 
 namespace saib {
@@ -105,14 +107,96 @@ __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
 // Block 0, after wts[0..num_wr] is written: the work row holding the first
 // tile of each participating CTA of the score/select launch (the kernel gives
 // CTA c tiles [c*T/nC, (c+1)*T/nC) with nC = min(grid, T)).
-__device__ void fill_cta_rows(const int32_t* wts, int num_wr, int grid, int32_t* cta_row) {
+// Inclusive prefix max of one int per thread over a block of kPrepThreads
+// threads; *total = the block's max.
+__device__ int block_inclusive_max(int v, int* total) {
+  __shared__ int warp_max[kPrepWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v = max(v, y);
+  }
+  if (lane == 31) warp_max[warp] = v;
   __syncthreads();
-  const int64_t T = wts[num_wr];
-  const int64_t nC = min(static_cast<int64_t>(grid), T);
+  int before = INT_MIN, all = INT_MIN;
+  for (int i = 0; i < kPrepWarps; ++i) {
+    if (i < warp) before = max(before, warp_max[i]);
+    all = max(all, warp_max[i]);
+  }
+  __syncthreads();
+  *total = all;
+  return max(before, v);
+}
+
+// Virtual start of every work row: its first tile plus `penalty` for every
+// earlier work row that has tiles (each such row's end costs a finalisation).
+// Block 0 only, after wts is complete.
+__device__ void row_virtual_starts(const int32_t* wts, int num_wr, int penalty, int32_t* vs) {
+  __syncthreads();
+  int carry = 0;
+  for (int base = 0; base < num_wr; base += kPrepThreads) {
+    const int w = base + threadIdx.x;
+    const int nz = w < num_wr && wts[w + 1] > wts[w] ? 1 : 0;
+    int total;
+    const int excl = block_exclusive_scan(nz, &total);
+    if (w < num_wr) vs[w] = wts[w] + penalty * (carry + excl);
+    carry += total;
+  }
+  if (threadIdx.x == 0) vs[num_wr] = wts[num_wr] + penalty * carry;
+}
+
+constexpr int kMaxPlanCtas = 2048;
+
+// The score/select kernel's work split. CTA c of nC = min(grid, T) takes the
+// tiles [cta_tile[c], cta_tile[c+1]): the virtual sequence (tiles plus a
+// penalty after each work row's end) is cut evenly and mapped back to tiles,
+// then every CTA is given at least one tile. Also the work row of each CTA's
+// first tile and each work row's first and last CTA. Block 0 only.
+__device__ void plan_ctas(const int32_t* wts, const int32_t* vs, int num_wr, int grid,
+                          int32_t* cta_tile, int32_t* cta_row, int2* row_ctas) {
+  __shared__ int32_t s_ct[kMaxPlanCtas + 1];
+  __syncthreads();
+  const int T = wts[num_wr];
+  const int nC = min(grid, T);
+  const int64_t V = vs[num_wr];
+  const bool even = nC > kMaxPlanCtas;  // too many CTAs to plan here: plain even split
+  if (!even) {
+    int carry = INT_MIN;  // max of t - c over the earlier chunks
+    for (int base = 0; base <= nC; base += kPrepThreads) {
+      const int c = base + threadIdx.x;
+      int u = INT_MIN;
+      if (c <= nC) {
+        int t = T;
+        if (c < nC) {
+          const int64_t v = static_cast<int64_t>(c) * V / nC;
+          int lo = 0, hi = num_wr - 1;  // work row holding virtual position v
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (vs[mid] <= v) lo = mid;
+            else hi = mid - 1;
+          }
+          t = wts[lo] + static_cast<int>(min(v - vs[lo], static_cast<int64_t>(wts[lo + 1] - wts[lo])));
+        }
+        // CTA c starts in [c, T - nC + c]; a prefix max of t - c then makes
+        // the starts strictly increasing
+        u = max(min(t, T - nC + c), c) - c;
+      }
+      int chunk;
+      const int incl = block_inclusive_max(u, &chunk);
+      if (c <= nC) s_ct[c] = max(carry, incl) + c;
+      carry = max(carry, chunk);
+    }
+  }
+  __syncthreads();
+  auto start = [&](int c) -> int {
+    return even ? static_cast<int>(static_cast<int64_t>(c) * T / nC) : s_ct[c];
+  };
+  for (int c = threadIdx.x; c <= nC; c += kPrepThreads) cta_tile[c] = start(c);
   for (int c = threadIdx.x; c < grid; c += kPrepThreads) {
     int w = 0;
     if (c < nC) {
-      const int64_t t = static_cast<int64_t>(c) * T / nC;
+      const int t = start(c);
       int lo = 0, hi = num_wr - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -122,6 +206,19 @@ __device__ void fill_cta_rows(const int32_t* wts, int num_wr, int grid, int32_t*
       w = lo;
     }
     cta_row[c] = w;
+  }
+  auto cta_of = [&](int t) {  // the CTA whose range holds tile t
+    int lo = 0, hi = nC - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (start(mid) <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  };
+  for (int w = threadIdx.x; w < num_wr; w += kPrepThreads) {
+    const int rs = wts[w], re = wts[w + 1];
+    row_ctas[w] = re > rs ? make_int2(cta_of(rs), cta_of(re - 1)) : make_int2(0, -1);
   }
 }
 
@@ -142,7 +239,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
     DecodePrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
     float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
-    int32_t* __restrict__ cta_row) {
+    int32_t* __restrict__ cta_row, int32_t* __restrict__ cta_tile, int32_t* __restrict__ row_vs,
+    int2* __restrict__ row_ctas) {
   pdl_trigger();
   pdl_wait();
   const int G = a.next_n;
@@ -171,7 +269,8 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
       carry += total;
     }
     if (threadIdx.x == 0) wts[a.num_reqs] = carry;
-    fill_cta_rows(wts, a.num_reqs, a.num_ctas, cta_row);
+    row_virtual_starts(wts, a.num_reqs, a.row_penalty, row_vs);
+    plan_ctas(wts, row_vs, a.num_reqs, a.num_ctas, cta_tile, cta_row, row_ctas);
     return;
   }
   zero_words(row_hist, row_hist_words);
@@ -221,7 +320,8 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     PrefillPrepArgs a, WorkRow* __restrict__ wr, int32_t* __restrict__ wts,
     int32_t* __restrict__ row_len, int32_t* __restrict__ seg_counter, uint8_t* __restrict__ q8img,
     float* __restrict__ wprime, uint32_t* __restrict__ row_hist, size_t row_hist_words,
-    int32_t* __restrict__ cta_row) {
+    int32_t* __restrict__ cta_row, int32_t* __restrict__ cta_tile, int32_t* __restrict__ row_vs,
+    int2* __restrict__ row_ctas) {
   pdl_trigger();
   pdl_wait();
   constexpr int G = 4;
@@ -275,7 +375,8 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
       run += total;
     }
     if (threadIdx.x == 0) wts[a.num_wr] = run;
-    fill_cta_rows(wts, a.num_wr, a.num_ctas, cta_row);
+    row_virtual_starts(wts, a.num_wr, a.row_penalty, row_vs);
+    plan_ctas(wts, row_vs, a.num_wr, a.num_ctas, cta_tile, cta_row, row_ctas);
     return;
   }
   zero_words(row_hist, row_hist_words);
@@ -420,7 +521,8 @@ idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayo
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
       ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
-      reinterpret_cast<int32_t*>(ws + L.cta_row));
+      reinterpret_cast<int32_t*>(ws + L.cta_row), reinterpret_cast<int32_t*>(ws + L.cta_tile),
+      reinterpret_cast<int32_t*>(ws + L.row_vs), reinterpret_cast<int2*>(ws + L.row_ctas));
   return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 
@@ -434,7 +536,8 @@ idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLa
       reinterpret_cast<int32_t*>(ws + L.row_len), reinterpret_cast<int32_t*>(ws + L.seg_counter),
       ws + L.q8, reinterpret_cast<float*>(ws + L.wprime),
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
-      reinterpret_cast<int32_t*>(ws + L.cta_row));
+      reinterpret_cast<int32_t*>(ws + L.cta_row), reinterpret_cast<int32_t*>(ws + L.cta_tile),
+      reinterpret_cast<int32_t*>(ws + L.row_vs), reinterpret_cast<int2*>(ws + L.row_ctas));
   return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
 }
 

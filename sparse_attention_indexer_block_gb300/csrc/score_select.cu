@@ -84,6 +84,7 @@ struct Misc {
   int epi_done;
   int wcnt[4][4];  // [token][epilogue warp] entries in the warp's region
   int staged_uses;  // phases of `staged` used so far
+  int pending_row;  // work row this CTA must merge once its own tiles are done, or -1
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
@@ -136,10 +137,6 @@ __device__ __forceinline__ Smem carve(uint8_t* base) {
 constexpr int kRowHistBins = 1024;
 __device__ __forceinline__ int row_bin(uint32_t key) { return static_cast<int>(key >> 22); }
 
-// CTA whose tile range [c*T/nC, (c+1)*T/nC) contains tile t.
-__device__ __forceinline__ int64_t cta_of(int64_t t, int64_t T, int64_t nC) {
-  return ((t + 1) * nC - 1) / T;
-}
 
 __device__ __forceinline__ void trace_set(const Smem& s, int slot, uint64_t v) {
   if (s.trace) s.trace[slot] = v;
@@ -1106,6 +1103,31 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   return true;
 }
 
+// Merge of work row w (every segment published) into its output rows, by a
+// CTA whose own tiles are all done: staged in the idle ring, else from the
+// slots directly.
+template <int G>
+__device__ void merge_work_row(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
+                               const bool (&active)[G], int64_t c_first, int64_t c_last) {
+  const int et = threadIdx.x - 64;
+  const uint64_t tm0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  __threadfence();
+  const uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (!active[g]) continue;
+    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
+    const uint32_t* gh = gh_base + g * kRowHistBins;
+    if (merge_row_staged<G>(p, s, w, g, c_first, c_last, gh, out)) continue;
+    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
+    merge_row<G>(p, s, w, g, c_first, c_last, gh, out);
+  }
+  if (et == 0 && s.trace) {
+    s.trace[kTrMergeNs] += globaltimer_ns() - tm0;
+    s.trace[kTrMergeN] += 1;
+  }
+}
+
 // End of this CTA's part of work row w: shrink each buffer to <= k; if the
 // CTA holds the whole row write the output, else publish the candidates that
 // can still make the row's top-k (bins at or above the row histogram's
@@ -1132,7 +1154,8 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
     if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     return;
   }
-  const int64_t c_first = cta_of(rs, T, nC), c_last = cta_of(re - 1, T, nC);
+  const int2 rc = p.row_ctas[w];
+  const int64_t c_first = rc.x, c_last = rc.y;
   uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
   const int64_t slot = static_cast<int64_t>(blockIdx.x) + w;
 #pragma unroll
@@ -1212,28 +1235,11 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
   }
   named_sync(kEpiBarrier, kEpiThreads);
   if (et == 0 && s.trace) s.trace[kTrFinPublishNs] += globaltimer_ns() - tf1;
-  if (!m->is_last) {
-    if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
-    return;
-  }
-  const uint64_t tm0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  __threadfence();
-  // A CTA whose tiles are all done (re >= t1) has an idle ring to stage in.
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (!active[g]) continue;
-    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
-    const uint32_t* gh = gh_base + g * kRowHistBins;
-    if (re >= t1 && merge_row_staged<G>(p, s, w, g, c_first, c_last, gh, out)) continue;
-    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
-    merge_row<G>(p, s, w, g, c_first, c_last, gh, out);
-  }
-  if (et == 0 && s.trace) {
-    const uint64_t now = globaltimer_ns();
-    s.trace[kTrMergeNs] += now - tm0;
-    s.trace[kTrMergeN] += 1;
-    s.trace[kTrFinalizeNs] += now - tf0;
-  }
+  // The last segment to publish merges the row. A CTA with tiles still to
+  // stream defers the merge to its end, when its ring is idle for staging.
+  if (m->is_last && re < t1 && et == 0) m->pending_row = w;
+  if (m->is_last && re >= t1) merge_work_row<G>(p, s, w, wr, active, c_first, c_last);
+  if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
 }
 
 template <int G, bool kLogits>
@@ -1431,7 +1437,19 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     s.trace[kTrEpiSelCyc] = cyc[4];
   }
   publish_counts();
-  if (!kLogits && ok) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
+  if (!kLogits && ok) {
+    finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
+    const int pw = s.misc->pending_row;  // set (by thread 0) before barriers all passed since
+    if (pw >= 0) {
+      const WorkRow pwr = p.wr[pw];
+      bool pact[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        pact[g] = g < pwr.ntok && p.row_len[pwr.row0 + g] > p.topk;
+      const int2 rc = p.row_ctas[pw];
+      merge_work_row<G>(p, s, pw, pwr, pact, rc.x, rc.y);
+    }
+  }
   if (et == 0 && s.trace) s.trace[kTrFinal] = globaltimer_ns();
 }
 
@@ -1457,8 +1475,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
   const int64_t nC = min(static_cast<int64_t>(gridDim.x), T);
   const bool part = static_cast<int64_t>(blockIdx.x) < nC;
   s.trace = (p.trace && part) ? reinterpret_cast<uint64_t*>(base + C::kTraceOff) : nullptr;
-  const int64_t t0 = part ? static_cast<int64_t>(blockIdx.x) * T / nC : 0;
-  const int64_t t1 = part ? static_cast<int64_t>(blockIdx.x + 1) * T / nC : 0;
+  const int64_t t0 = part ? p.cta_tile[blockIdx.x] : 0;
+  const int64_t t1 = part ? p.cta_tile[blockIdx.x + 1] : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -1476,6 +1494,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
     s.misc->abort_flag = 0;
     s.misc->epi_done = 0;
     s.misc->staged_uses = 0;
+    s.misc->pending_row = -1;
     if (s.trace)
       for (int i = 0; i < kTrSlots; ++i) s.trace[i] = 0;
     fence_barrier_init();
