@@ -170,6 +170,107 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def measured_peak_fp8_tflops():
+    """Dense fp8 tensor peak: the measured bf16 burst figure x 2 (the nominal
+    fp8:bf16 ratio), or the fallback 1.9 PFLOP/s bf16 x 2."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 burst x 2"
+    except (OSError, KeyError, ValueError):
+        return 3800.0, "fallback 1.9 PFLOP/s bf16 x 2"
+
+
+def run_prefill(args, rank, world, local):
+    """Prefill indexer (4 requests x 8192 causal queries, top-2048 per query)
+    through indexer_prefill_topk, M*N logits-budget chunking included. The
+    score is a dense fp8 contraction (64 heads x 128 per key and query), so the
+    roofline is the fp8 tensor peak."""
+    import torch
+
+    import synth
+    import sparse_attention_indexer_block_gb300 as saib
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    libbuild.build()
+    saib.load()
+    d = synth.make_prefill("prefill", seed=rank_seed(args.seed, rank), device=dev)
+    sl = d.seq_lens.cpu().numpy().astype(np.int64)
+    ql = d.query_lens.cpu().numpy().astype(np.int64)
+    # keys scored per step: query i of a request sees seq_len - query_len + i + 1 keys
+    keys_per_step = int(sum(((L - n) * n + n * (n + 1) // 2) for L, n in zip(sl, ql)))
+    flops_per_step = keys_per_step * 64 * 128 * 2
+    k = d.topk
+    out = torch.empty((int(ql.sum()), k), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    chunks = saib.indexer_plan_prefill_chunks(sl, ql, 40 * 8192, 512 << 20)
+    ws_n = saib.indexer_prefill_workspace_bytes(sl, ql, k, 40 * 8192, 512 << 20)
+    ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        saib.indexer_prefill_topk(d.q, d.w, d.cache, d.block_table, d.seq_lens, d.query_start_loc,
+                                  sl, ql, k, out_idx=out, workspace=ws, dev_error=err,
+                                  stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+    K = args.steps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(K):
+                step()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_soak = time.time()
+        with torch.cuda.stream(stream):
+            while time.time() - t_soak < 1.0:
+                g.replay()
+                stream.synchronize()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
+    peak, peak_src = measured_peak_fp8_tflops()
+    tflops = flops_per_step * K / (ms / 1e3) / 1e12
+    if rank == 0:
+        line = {"metric": "indexed keys/sec for prefill top-2048 (fp8 tensor roofline)",
+                "value": whole_job_rate(keys_per_step, K, world, ms), "unit": "keys/s",
+                "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms / K,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+                "config": {"workload": "prefill: 4 requests x 8192 queries causally over 8192 "
+                                       "keys, 64 heads x 128, top-2048, 512 MiB logits budget",
+                           "keys_per_step": keys_per_step, "flops_per_step": flops_per_step,
+                           "timing": "CUDA events around a CUDA graph of K calls (whole path)",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                             "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                             "traffic": None, "peak_source": peak_src,
+                             "scope": "whole prefill call (prep + score/select, all chunks)"},
+                "clocks": clk.summary(), "gpu_launches": 2 * len(chunks) * K}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -445,6 +546,8 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload == "prefill":
+        run_prefill(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 

@@ -53,12 +53,10 @@ __device__ __forceinline__ int64_t clamp_len(int64_t v, int64_t bt_width, uint32
   return v;
 }
 
-// One warp quantises one head of 128 bf16 values: lane l owns elements
-// [4l, 4l + 4). Returns the four e4m3 codes of the lane (element 4l in the
+// One warp quantises one head of 128 bf16 values (raw: the lane's 8 bytes of
+// it): lane l owns elements [4l, 4l + 4). Returns the four e4m3 codes of the lane (element 4l in the
 // low byte) and, in *wp, w * amax / 448 (all lanes).
-__device__ __forceinline__ uint32_t quantize_head(const __nv_bfloat16* src, float w, int lane,
-                                                  float* wp) {
-  const uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+__device__ __forceinline__ uint32_t quantize_head(uint2 raw, float w, int lane, float* wp) {
   const float x0 = __uint_as_float(raw.x << 16);
   const float x1 = __uint_as_float(raw.x & 0xffff0000u);
   const float x2 = __uint_as_float(raw.y << 16);
@@ -86,6 +84,45 @@ __device__ __forceinline__ uint32_t swizzled_offset(int h, int lane) {
          (static_cast<uint32_t>(lane & 3) << 2);
 }
 
+// Quantises tasks [0, ntasks) (task = one head of one token row, source head
+// src0 + task) with warp gw of nw: four tasks per round, all four loads issued
+// before any is used. Codes go to the swizzled per-row image (kSwizzled) or
+// to a plain [task, 128] array; w * amax / 448 to wprime[task].
+template <bool kSwizzled>
+__device__ __forceinline__ void quantize_tasks(const __nv_bfloat16* __restrict__ q,
+                                               const float* __restrict__ w, int64_t src0,
+                                               int64_t ntasks, uint8_t* __restrict__ q8,
+                                               float* __restrict__ wprime, int64_t gw, int64_t nw) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = gw * 4; base < ntasks; base += nw * 4) {
+    uint2 raw[4];
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      raw[u] = make_uint2(0u, 0u);
+      wv[u] = 0.0f;
+      if (base + u < ntasks) {
+        const int64_t src = src0 + base + u;
+        raw[u] = *reinterpret_cast<const uint2*>(q + src * kDim + 4 * lane);
+        wv[u] = w[src];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t idx = base + u;
+      if (idx >= ntasks) break;
+      float wp;
+      const uint32_t c = quantize_head(raw[u], wv[u], lane, &wp);
+      if (kSwizzled)
+        *reinterpret_cast<uint32_t*>(q8 + (idx / kHeads) * kQRowBytes +
+                                     swizzled_offset(static_cast<int>(idx % kHeads), lane)) = c;
+      else
+        *reinterpret_cast<uint32_t*>(q8 + idx * kDim + 4 * lane) = c;
+      if (lane == 0) wprime[idx] = wp;
+    }
+  }
+}
+
 // -------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
@@ -96,12 +133,7 @@ __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * kPrepThreads) >> 5;
-  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
-    float wp;
-    const uint32_t c = quantize_head(q + idx * kDim, w[idx], lane, &wp);
-    *reinterpret_cast<uint32_t*>(q8 + idx * kDim + 4 * lane) = c;
-    if (lane == 0) wprime[idx] = wp;
-  }
+  quantize_tasks<false>(q, w, 0, rows * kHeads, q8, wprime, gw, nw);
 }
 
 // Block 0, after wts[0..num_wr] is written: the work row holding the first
@@ -146,7 +178,9 @@ __device__ void row_virtual_starts(const int32_t* wts, int num_wr, int penalty, 
   if (threadIdx.x == 0) vs[num_wr] = wts[num_wr] + penalty * carry;
 }
 
-constexpr int kMaxPlanCtas = 2048;
+constexpr int kMaxPlanCtas = 1024;
+// Work rows whose tile starts block 0 keeps in shared memory while planning.
+constexpr int kPlanRows = 1024;
 
 // The score/select kernel's work split. CTA c of nC = min(grid, T) takes the
 // tiles [cta_tile[c], cta_tile[c+1]): the virtual sequence (tiles plus a
@@ -246,6 +280,10 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
   const int G = a.next_n;
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * G;
   if (blockIdx.x == 0) {
+    // tile starts and virtual starts, in shared memory when they fit (the
+    // planner's searches then stay on chip)
+    __shared__ int32_t s_wts[kPlanRows + 1], s_vs[kPlanRows + 1];
+    const bool cached = a.num_reqs <= kPlanRows;
     int carry = 0;
     for (int base = 0; base < a.num_reqs; base += kPrepThreads) {
       const int b = base + threadIdx.x;
@@ -265,26 +303,27 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
       }
       int total;
       const int excl = block_exclusive_scan(tiles, &total);
-      if (b < a.num_reqs) wts[b] = carry + excl;
+      if (b < a.num_reqs) {
+        wts[b] = carry + excl;
+        if (cached) s_wts[b] = carry + excl;
+      }
       carry += total;
     }
-    if (threadIdx.x == 0) wts[a.num_reqs] = carry;
-    row_virtual_starts(wts, a.num_reqs, a.row_penalty, row_vs);
-    plan_ctas(wts, row_vs, a.num_reqs, a.num_ctas, cta_tile, cta_row, row_ctas);
+    if (threadIdx.x == 0) {
+      wts[a.num_reqs] = carry;
+      if (cached) s_wts[a.num_reqs] = carry;
+    }
+    const int32_t* pw = cached ? s_wts : wts;
+    int32_t* pv = cached ? s_vs : row_vs;
+    row_virtual_starts(pw, a.num_reqs, a.row_penalty, pv);
+    plan_ctas(pw, pv, a.num_reqs, a.num_ctas, cta_tile, cta_row, row_ctas);
     return;
   }
   zero_words(row_hist, row_hist_words);
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
-  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
-    const int64_t r = idx / kHeads;
-    const int h = static_cast<int>(idx % kHeads);
-    float wp;
-    const uint32_t c = quantize_head(a.q + idx * kDim, a.w[idx], lane, &wp);
-    *reinterpret_cast<uint32_t*>(q8img + r * kQRowBytes + swizzled_offset(h, lane)) = c;
-    if (lane == 0) wprime[idx] = wp;
-  }
+  quantize_tasks<true>(a.q, a.w, 0, rows * kHeads, q8img, wprime, gw, nw);
   if (!a.score_all) {
     for (int64_t r = gw; r < rows; r += nw) {
       const int64_t len = clamp_len(a.row_seq_lens[r], a.bt_width, a.err, false);
@@ -327,6 +366,10 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
   constexpr int G = 4;
   const int64_t rows = a.row_hi - a.row_lo;
   if (blockIdx.x == 0) {
+    // requests in batches of kPrepThreads: a scan of their work-row counts,
+    // then every thread fills work rows of the batch
+    __shared__ int s_off[kPrepThreads + 1];
+    __shared__ int64_t s_lo[kPrepThreads], s_hi[kPrepThreads];
     int carry = 0;
     for (int base = a.req_begin; base < a.req_end; base += kPrepThreads) {
       const int r = base + threadIdx.x;
@@ -339,24 +382,37 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
       }
       int total;
       const int excl = block_exclusive_scan(nw, &total);
-      for (int j = 0; j < nw; ++j) {
-        const int idx = carry + excl + j;
+      s_off[threadIdx.x] = excl;
+      s_lo[threadIdx.x] = lo;
+      s_hi[threadIdx.x] = hi;
+      __syncthreads();
+      const int nreq = min(kPrepThreads, a.req_end - base);
+      for (int i = threadIdx.x; i < total; i += kPrepThreads) {
+        const int idx = carry + i;
         if (idx >= a.num_wr) {
           set_error(a.err, IDX_DEV_OVERFLOW);
           break;
         }
-        const int64_t first = lo + static_cast<int64_t>(j) * G;
-        const int ntok = static_cast<int>(min(static_cast<int64_t>(G), hi - first));
+        int k0 = 0, k1 = nreq - 1;  // the request of batch work row i
+        while (k0 < k1) {
+          const int mid = (k0 + k1 + 1) >> 1;
+          if (s_off[mid] <= i) k0 = mid;
+          else k1 = mid - 1;
+        }
+        const int rq = base + k0;
+        const int64_t first = s_lo[k0] + static_cast<int64_t>(i - s_off[k0]) * G;
+        const int ntok = static_cast<int>(min(static_cast<int64_t>(G), s_hi[k0] - first));
         int maxlen = 0;
         for (int g = 0; g < ntok; ++g) {
-          const int len = static_cast<int>(prefill_len(a, r, first + g, true));
+          const int len = static_cast<int>(prefill_len(a, rq, first + g, true));
           if (len > a.topk) maxlen = max(maxlen, len);
         }
-        wr[idx] = WorkRow{r, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
+        wr[idx] = WorkRow{rq, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
         wts[idx] = (maxlen + kTileKeys - 1) / kTileKeys;  // tile count, scanned below
         seg_counter[idx] = 0;
       }
       carry += total;
+      __syncthreads();
     }
     if (carry != a.num_wr && threadIdx.x == 0) set_error(a.err, IDX_DEV_OVERFLOW);
     for (int idx = carry + threadIdx.x; idx < a.num_wr; idx += kPrepThreads) {
@@ -393,15 +449,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
       for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;
     }
   }
-  for (int64_t idx = gw; idx < rows * kHeads; idx += nw) {
-    const int64_t lr = idx / kHeads;
-    const int h = static_cast<int>(idx % kHeads);
-    const int64_t src = (a.row_lo + lr) * kHeads + h;
-    float wp;
-    const uint32_t c = quantize_head(a.q + src * kDim, a.w[src], lane, &wp);
-    *reinterpret_cast<uint32_t*>(q8img + lr * kQRowBytes + swizzled_offset(h, lane)) = c;
-    if (lane == 0) wprime[idx] = wp;
-  }
+  quantize_tasks<true>(a.q, a.w, a.row_lo * kHeads, rows * kHeads, q8img, wprime, gw, nw);
 }
 
 // Row expansion. One warp per request: it writes the request's token rows and
@@ -484,7 +532,7 @@ __global__ void __launch_bounds__(kPrepThreads) expand_kernel(
 
 int prep_grid(int64_t work_warps) {
   const int64_t blocks = (work_warps + kPrepWarps - 1) / kPrepWarps;
-  const int64_t cap = 4 * static_cast<int64_t>(device_sm_count());
+  const int64_t cap = 8 * static_cast<int64_t>(device_sm_count());
   return static_cast<int>(blocks < 1 ? 1 : (blocks > cap ? cap : blocks));
 }
 
