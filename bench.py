@@ -170,6 +170,32 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def profiled_traffic(workload: str):
+    """DRAM bytes per score/select launch from the committed ncu summary of
+    the decode-batch workload, or None when that summary was taken on other
+    kernel sources (or another workload is being run)."""
+    if workload != "decode":
+        return None
+    import hashlib
+    csrc = os.path.join(ROOT, "sparse_attention_indexer_block_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("score_select.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    fields = {}
+    try:
+        with open(os.path.join(ROOT, "profiles", "score_select_decode_batch.md")) as f:
+            for line in f:
+                k, _, v = line.strip().partition(":")
+                if k in ("source_sha256_16", "dram_bytes_per_launch"):
+                    fields[k] = v.strip()
+    except OSError:
+        return None
+    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
 def measured_peak_fp8_tflops():
     """Dense fp8 tensor peak: the measured bf16 burst figure x 2 (the nominal
     fp8:bf16 ratio), or the fallback 1.9 PFLOP/s bf16 x 2."""
@@ -384,10 +410,12 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peak_gbs()
     achieved = algo_bytes / (kern_avg / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None,
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                 "measured" else "fallback 6.8 TB/s",
-                "kernel": "score_select_kernel<1,false>", "kernel_ms_avg": round(kern_avg, 5),
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                   "profiles/score_select_decode_batch.md (same kernel sources)"),
+                "kernel": f"score_select_kernel<{G},false>", "kernel_ms_avg": round(kern_avg, 5),
                 "kernel_ms_median": round(statistics.median(kern_ms), 5),
                 "algorithmic_bytes_per_launch": algo_bytes}
 
