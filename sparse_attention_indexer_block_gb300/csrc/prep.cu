@@ -130,7 +130,6 @@ __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
     uint8_t* __restrict__ q8, float* __restrict__ wprime) {
   pdl_trigger();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * kPrepThreads) >> 5;
   quantize_tasks<false>(q, w, 0, rows * kHeads, q8, wprime, gw, nw);
