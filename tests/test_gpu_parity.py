@@ -191,6 +191,21 @@ def test_topk_two_token_rows_mixed():
     _check_decode(d, 2048)
 
 
+def test_topk_single_long_request_many_segments():
+    """One 131072-key request spread over every CTA: far more segments than
+    the staged merge takes, so the merge runs from registers or, for a large
+    union, by the radix over the slots."""
+    d = synth.make_decode_from_lens([131072], [1], 1, seed=51)
+    _check_decode(d, 2048)
+
+
+def test_topk_uneven_pair_two_token_rows():
+    """A long two-token request next to a short one (next_n 2): one work row
+    covers almost every CTA, the other sits inside one."""
+    d = synth.make_decode_from_lens([65536, 3000], [2, 1], 2, seed=52)
+    _check_decode(d, 2048)
+
+
 def test_topk_decode_batch_workload():
     _check_decode(synth.make_decode("decode"), 2048)
 
