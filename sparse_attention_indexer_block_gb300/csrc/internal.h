@@ -105,6 +105,10 @@ struct DecodePrepArgs {
   uint32_t* err;
   int32_t num_ctas;     // grid of the score/select launch that follows
   int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
+  // When CTAs stream long segments (>= 64 tiles each), a row end also restarts
+  // a segment's drop threshold (more buffer cuts): the penalty grows by the
+  // per-CTA tile share divided by this (0: no growth).
+  int32_t row_penalty_div;
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);

@@ -314,7 +314,10 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
     }
     const int32_t* pw = cached ? s_wts : wts;
     int32_t* pv = cached ? s_vs : row_vs;
-    row_virtual_starts(pw, a.num_reqs, a.row_penalty, pv);
+    int penalty = a.row_penalty;
+    const int share = carry / max(1, min(a.num_ctas, carry));  // tiles per CTA
+    if (a.row_penalty_div > 0 && share >= 64) penalty += share / a.row_penalty_div;
+    row_virtual_starts(pw, a.num_reqs, penalty, pv);
     plan_ctas(pw, pv, a.num_reqs, a.num_ctas, cta_tile, cta_row, row_ctas);
     return;
   }
