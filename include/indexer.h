@@ -248,12 +248,13 @@ idx_status indexer_trace_buffer(void* buffer, size_t bytes);
  * code running while a stream is captured into a CUDA graph, serving loops
  * that forbid allocator calls on their latency-critical path, or hosts whose
  * device memory is owned by an allocator this code cannot call. The scratch is
- * a 16 MiB device array inside the library (one per GPU that loads the
+ * a 32 MiB device array inside the library (one per GPU that loads the
  * library, held until the process exits); the call allocates nothing. Same
  * arguments and results as indexer_decode_topk without the workspace.
  *  - Limit: the batch must fit the scratch, i.e. indexer_decode_workspace_bytes
- *    (num_reqs, next_n, topk) <= 16 MiB (about 400 requests at next_n = 1 with
- *    top-2048); a larger batch returns IDX_ERR_WORKSPACE before any work.
+ *    (num_reqs, next_n, topk) <= 32 MiB (about 750 requests at next_n = 1, 270
+ *    at next_n = 2, top-2048, 152 SMs); a larger batch returns
+ *    IDX_ERR_WORKSPACE before any work.
  *  - The first call on each device looks the scratch's device address up (this
  *    may load the library's device code); make that first call before any
  *    stream capture.

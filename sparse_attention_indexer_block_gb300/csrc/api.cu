@@ -55,8 +55,9 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
   L.slot_count = take(4 * static_cast<size_t>(nslots * G), 256);
   L.q8 = take(static_cast<size_t>(rows) * kQRowBytes, 1024);
   L.wprime = take(4 * static_cast<size_t>(rows) * kHeads, 256);
-  L.slot_key = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
-  L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * topk, 256);
+  const size_t cap = static_cast<size_t>(candidate_capacity(G));
+  L.slot_key = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
+  L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
   L.row_hist_words = static_cast<size_t>(num_ctas) * G * 1024;
   L.row_hist = take(4 * L.row_hist_words, 256);
   L.cta_row = take(4 * static_cast<size_t>(num_ctas), 256);
@@ -225,6 +226,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.seg_counter = reinterpret_cast<int32_t*>(ws + L.seg_counter);
   p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
   p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
+  p.slot_cap = candidate_capacity(next_n);
   p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
   p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
   p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
@@ -455,6 +457,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.seg_counter = reinterpret_cast<int32_t*>(ws + L.seg_counter);
     p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
     p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
+    p.slot_cap = candidate_capacity(4);
     p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
     p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
     p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);

@@ -47,10 +47,11 @@ struct ScoreParams {
   const uint8_t* q8;             // [rows, 8192] swizzled fp8 images of q
   const float* wprime;           // [rows, 64] w * sq
   int32_t* seg_counter;          // [num_wr] finished segments per work row
-  uint32_t* slot_key;            // [nslots, G, topk] candidate keys of finished segments
-  int32_t* slot_idx;             // [nslots, G, topk] their token indices
+  uint32_t* slot_key;            // [nslots, G, slot_cap] candidate keys of finished segments
+  int32_t* slot_idx;             // [nslots, G, slot_cap] their token indices
   int32_t* slot_count;           // [nslots, G]
   int32_t* slot_thrbin;          // [nslots, G] row-histogram bin of the segment's final threshold
+  int32_t slot_cap;              // entries per slot (the candidate buffer's capacity)
   uint32_t* row_hist;            // [nC, G, 1024] histograms of split work rows (zeroed by prep)
   int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
   int64_t out_row_base;
@@ -70,6 +71,10 @@ enum TraceSlot {
   kTrEpiMathCyc, kTrEpiVoteCyc, kTrEpiSelCyc, kTrFinPackNs, kTrFinHistNs, kTrFinCutNs,
   kTrFinEmitNs, kTrFinPublishNs, kTrMergeTailNs, kTrSlots = 40
 };
+
+// Candidate-buffer capacity per token row of the score/select kernel for work
+// rows of G tokens; a published segment slot holds up to this many entries.
+constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : (G == 2 ? 4096 : 2560); }
 
 // Workspace carve-up shared by decode and prefill.
 struct WsLayout {

@@ -44,7 +44,7 @@ struct Cfg {
   // streaming); wider work rows need the shared memory of a whole SM.
   static constexpr int kCtasPerSm = G == 1 ? 2 : 1;
   static constexpr int kStages = G == 1 ? 4 : (G == 2 ? 6 : 4);
-  static constexpr int kCap = G == 1 ? 3072 : (G == 2 ? 4096 : 2560);  // candidates per token row
+  static constexpr int kCap = candidate_capacity(G);  // candidates per token row
   static constexpr int kRegion = kCap / 4;          // per-warp append region
   static constexpr int kPer = kRegion / 32;         // region entries per lane
   // a full buffer is cut to at most k + kSlack entries (whichever bucket
@@ -66,6 +66,7 @@ struct Cfg {
   static constexpr int kTraceOff = kMiscOff + 256;  // trace slots (kept in shared memory)
   static constexpr int kSmemBytes = kTraceOff + kTrSlots * 8 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
+  static_assert(kCap >= IDX_MAX_TOPK, "a slot must hold any k");
   static_assert(kSmemBytes * kCtasPerSm + 1024 * kCtasPerSm <= 233472, "shared memory");
 };
 
@@ -567,7 +568,7 @@ __device__ void merge_slots(const ScoreParams& p, const Smem& s, int w, int g, i
       for (int64_t c = c_first; c <= c_last; ++c) {
         const int64_t slot = (c + w) * G + g;
         const int n = __ldcg(&p.slot_count[slot]);
-        const uint32_t* keys = p.slot_key + slot * K;
+        const uint32_t* keys = p.slot_key + slot * p.slot_cap;
 #pragma unroll 4
         for (int e = et; e < n; e += kEpiThreads) {
           const uint32_t u = __ldcg(&keys[e]);
@@ -592,8 +593,8 @@ __device__ void merge_slots(const ScoreParams& p, const Smem& s, int w, int g, i
   for (int64_t c = c_first; c <= c_last; ++c) {
     const int64_t slot = (c + w) * G + g;
     const int n = __ldcg(&p.slot_count[slot]);
-    const uint32_t* keys = p.slot_key + slot * K;
-    const int32_t* idxs = p.slot_idx + slot * K;
+    const uint32_t* keys = p.slot_key + slot * p.slot_cap;
+    const int32_t* idxs = p.slot_idx + slot * p.slot_cap;
     for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
       const int e = e0 + et;
       const uint32_t u = e < n ? __ldcg(&keys[e]) : 0u;
@@ -764,7 +765,7 @@ __device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int
       if (i < total) {
         while (seg_start[seg + 1] <= i) ++seg;
         const int64_t slot = (c_first + seg + w) * G + g;
-        u[j] = __ldcg(&p.slot_key[slot * K + (i - seg_start[seg])]);
+        u[j] = __ldcg(&p.slot_key[slot * p.slot_cap + (i - seg_start[seg])]);
       }
     }
 #pragma unroll
@@ -833,7 +834,7 @@ __device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int
         const int i = j * kEpiThreads + et;
         while (seg_start[seg + 1] <= i) ++seg;
         const int64_t slot = (c_first + seg + w) * G + g;
-        u[j] = static_cast<uint32_t>(__ldcg(&p.slot_idx[slot * K + (i - seg_start[seg])]));
+        u[j] = static_cast<uint32_t>(__ldcg(&p.slot_idx[slot * p.slot_cap + (i - seg_start[seg])]));
       }
     }
 #pragma unroll
@@ -867,7 +868,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   const int K = p.topk;
   Misc* m = s.misc;
   const int nseg = static_cast<int>(c_last - c_first + 1);
-  if (nseg > kEpiThreads || (K & 3) != 0) return false;
+  if (nseg > kEpiThreads) return false;
   const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   // the segments' counts and threshold bins and this thread's bins of the row
   // histogram, loaded together
@@ -894,8 +895,8 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
   const int use = m->staged_uses;
   if (et < nseg && my_n > 0) {
     const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
-    bulk_load(keys + my_off, p.slot_key + sl * K, bytes, s.staged);
-    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * K, bytes, s.staged);
+    bulk_load(keys + my_off, p.slot_key + sl * p.slot_cap, bytes, s.staged);
+    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * p.slot_cap, bytes, s.staged);
   }
   if (et == 0)
     mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * (with_idx ? 8u : 4u));
@@ -1091,7 +1092,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
         else hi = mid - 1;
       }
       const int64_t seg_slot = (c_first + lo + w) * G + g;
-      out[q] = __ldcg(&p.slot_idx[seg_slot * K + (e - seg_off[lo])]);
+      out[q] = __ldcg(&p.slot_idx[seg_slot * p.slot_cap + (e - seg_off[lo])]);
     }
   }
   for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
@@ -1143,13 +1144,17 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
   const uint64_t tf0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   const int lane = threadIdx.x & 31, ew = et >> 5;
   named_sync(kEpiBarrier, kEpiThreads);
+  // A row held whole by this CTA is written from the buffer, cut to exactly
+  // k; a segment publishes its whole buffer (up to kCap entries, the slot's
+  // capacity), filtered by the row histogram's cutoff below.
+  const bool whole = rs >= t0 && re <= t1;
 #pragma unroll
   for (int g = 0; g < G; ++g)
-    if (active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
+    if (whole && active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
       compact<G>(s, g, K);  // cut to k (the regions stay the layout)
   uint64_t tf1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   if (et == 0 && s.trace) s.trace[kTrFinPackNs] += tf1 - tf0;
-  if (rs >= t0 && re <= t1) {
+  if (whole) {
     write_rows<G>(p, s, wr, active);
     if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     return;
@@ -1190,7 +1195,7 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
       s.trace[kTrFinCutNs] += now - tf1;
       tf1 = now;
     }
-    const int64_t base = (slot * G + g) * K;
+    const int64_t base = (slot * G + g) * p.slot_cap;
     int keep = 0;
     for (int j = lane; j < nw; j += 32) keep += row_bin(rk[j]) >= cut ? 1 : 0;
     keep = __reduce_add_sync(0xffffffffu, keep);
