@@ -204,7 +204,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   // finalisation (publication, often a buffer cut) worth about this many
   // tiles of streaming; the split gives such CTAs correspondingly fewer tiles.
   const int32_t row_penalty = logits ? 0 : (next_n == 1 ? 6 : 12);
-  const int32_t row_penalty_div = logits ? 0 : (next_n == 1 ? 10 : 12);
+  const int32_t row_penalty_div = logits ? 0 : (next_n == 1 ? 25 : 24);
   DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
                    topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty,
                    row_penalty_div};
