@@ -1318,7 +1318,8 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       begin_row();
     }
     const int i = static_cast<int>(t - rs);
-    const long long c0 = clock64();
+    const bool tr = s.trace != nullptr;  // per-phase clocks only when tracing
+    const long long c0 = tr ? clock64() : 0;
     // lane 0 of each warp waits for the stage (scales) and the accumulator
     bool wok = true;
     if (lane == 0)
@@ -1326,7 +1327,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
             mbar_wait(&s.tfull[acc], acc_phase, abort_flag, p.dev_error);
     wok = __shfl_sync(0xffffffffu, wok ? 1 : 0, 0) != 0;
     __syncwarp();
-    const long long c1 = clock64();
+    const long long c1 = tr ? clock64() : 0;
     long long c2 = c1;
     float logit[G];
     if (t == t0 && et == 0 && s.trace) s.trace[kTrFirstEpi] = globaltimer_ns();
@@ -1340,7 +1341,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         tmem_ld32(col, v0);
         tmem_ld32(col + 32, v1);
         tmem_ld_wait();
-        if (g == 0) c2 = clock64();
+        if (g == 0 && tr) c2 = clock64();
         const float4* w4 = reinterpret_cast<const float4*>(s.wp + g * kHeads);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
@@ -1368,7 +1369,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         mbar_arrive(&s.empty[stage]);
       }
     }
-    const long long c3 = clock64();
+    const long long c3 = tr ? clock64() : 0;
     // Uniform decision across the four epilogue warps (double-buffered vote):
     // bit 0 = this warp's waits succeeded, bit 1 + g = its region of token g's
     // buffer has no room for another tile (then all warps compact it).
@@ -1380,7 +1381,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     publish_counts();
     if (lane == 0) s.misc->vote[par][ew] = (wok ? 1 : 0) | need;
     named_sync(kEpiBarrier, kEpiThreads);
-    const long long c4 = clock64();
+    const long long c4 = tr ? clock64() : 0;
     const int v0 = s.misc->vote[par][0], v1 = s.misc->vote[par][1];
     const int v2 = s.misc->vote[par][2], v3 = s.misc->vote[par][3];
     if (!(v0 & v1 & v2 & v3 & 1)) {
@@ -1416,7 +1417,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         wcnt[g] += __popc(pm);
       }
     }
-    {
+    if (tr) {
       const long long c5 = clock64();
       cyc[0] += c1 - c0;
       cyc[1] += c2 - c1;
