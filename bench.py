@@ -297,6 +297,79 @@ def run_prefill(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_insert(args, rank, world, local):
+    """Index-key cache insert (the step that fills the cache the indexer
+    reads): 1 Mi new tokens of bf16 keys quantised per token and written to
+    their slots (pages in random order, tokens of a page contiguous, as a
+    prefill's new tokens land). HBM-bound: 256 B of keys + 8 B of slot read
+    and 132 B written per token."""
+    import torch
+
+    import sparse_attention_indexer_block_gb300 as saib
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    libbuild.build()
+    saib.load()
+    T = 1 << 20
+    g = torch.Generator(device=dev).manual_seed(rank_seed(args.seed, rank))
+    pages = T // 64
+    n_copies = 2  # alternate two input/output sets so no step finds its data in L2
+    ks = [torch.randn((T, 128), generator=g, device=dev).to(torch.bfloat16)
+          for _ in range(n_copies)]
+    perm = torch.randperm(pages, generator=g, device=dev)
+    slots = (perm.repeat_interleave(64) * 64 + torch.arange(T, device=dev) % 64).to(torch.int64)
+    caches = [torch.zeros((pages, 8448), dtype=torch.uint8, device=dev) for _ in range(n_copies)]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    bytes_per_step = T * (256 + 8 + 132)
+
+    def step(i):
+        saib.indexer_insert_keys(ks[i % n_copies], slots, caches[i % n_copies], dev_error=err,
+                                 stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(K):
+                step(i)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+    peak, peak_kind = measured_peak_gbs()
+    gbs = bytes_per_step * K / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "index-key cache insert: tokens/s (HBM roofline)",
+            "value": whole_job_rate(T, K, world, ms), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 -> fp8_e4m3 + fp32 scale",
+            "data": "synthetic",
+            "config": {"workload": "insert 1 Mi tokens x 128 bf16 into a paged fp8 cache",
+                       "bytes_per_step": bytes_per_step,
+                       "timing": "CUDA events around a CUDA graph of K calls",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
+                         "peak_source": peak_kind},
+            "clocks": clk.summary(), "gpu_launches": K}), flush=True)
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -576,6 +649,8 @@ def main():
         run_reference(args, rank, world)
     elif args.workload == "prefill":
         run_prefill(args, rank, world, local)
+    elif args.workload == "insert":
+        run_insert(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 

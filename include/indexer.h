@@ -135,6 +135,25 @@ idx_status indexer_quantize_q(const void* q, const float* weights, int64_t num_r
                               int32_t num_heads, int32_t head_dim, uint8_t* q_fp8,
                               float* weights_scaled, void* stream);
 
+/*
+ * Index-key cache insert: the step that fills the paged cache the decode and
+ * prefill calls read ([INDEXER] DeepseekV32IndexerMetadata.slot_mapping gives
+ * every new token its cache slot; get_max_prefill_buffer_size and [GLM5]
+ * _gather_workspace_shapes fix 128 fp8 values + one fp32 scale per token; the
+ * insert kernel itself is not shown on the pages). Token i's keys
+ * k bf16 [num_tokens, 128] are quantised with the token's own scale
+ * scale = amax / 448 (amax = max_d |k|, fp32, correctly rounded) into codes
+ * e4m3_rne_satfinite(k / scale) (fp32, correctly rounded quotient) and written
+ * to slot s = slot_mapping[i] (int64): page s / 64, token s % 64, in the page
+ * layout above. A negative slot is padding and skipped; a slot >= num_pages*64
+ * ORs IDX_DEV_BAD_BLOCK and is skipped; a token with amax == 0 gets zero codes
+ * and scale 0. Two tokens with the same slot race. k 8-byte aligned,
+ * slot_mapping 8-byte aligned, index_cache 16-byte aligned.
+ */
+idx_status indexer_insert_keys(const void* k, const int64_t* slot_mapping, int64_t num_tokens,
+                               int32_t head_dim, uint8_t* index_cache, int64_t num_pages,
+                               uint32_t* dev_error, void* stream);
+
 /* Bytes of workspace indexer_decode_topk / indexer_decode_logits need for
  * num_reqs requests of next_n rows each, on the current CUDA device. */
 idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int32_t topk,

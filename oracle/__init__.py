@@ -60,6 +60,8 @@ def _load():
         lib.ora_e4m3_encode.argtypes = [C.c_float]
         lib.ora_quantize_q.restype = None
         lib.ora_quantize_q.argtypes = [P, P, i64, i32, i32, P, P, P]
+        lib.ora_insert_keys.restype = None
+        lib.ora_insert_keys.argtypes = [P, P, i64, P, i64]
         lib.ora_expand_rows.restype = i64
         lib.ora_expand_rows.argtypes = [P, P, i32, i32, i32, P, i64, i32, P, P, i64, i64]
         lib.ora_row_logits.restype = C.c_int
@@ -128,6 +130,22 @@ def quantize_q(q_bf16_bits: np.ndarray, w: np.ndarray):
     wp = np.empty((rows, H), np.float64)
     _load().ora_quantize_q(_p(q), _p(w), rows, H, D, _p(q8), _p(sq), _p(wp))
     return q8, sq, wp
+
+
+# --------------------------------------------------------------------------
+# index-key cache insert
+# --------------------------------------------------------------------------
+
+def insert_keys(k_bf16_bits: np.ndarray, slots, cache: np.ndarray) -> np.ndarray:
+    """Quantises each token of k (uint16 raw bf16 [n, 128]) with scale =
+    amax/448 and codes e4m3(x/scale) (fp32 steps) into a copy of cache (uint8
+    [pages, 8448]) at slots (int64 [n]; negative or out-of-range skipped).
+    Restates the insert step behind the INDEXER page's slot_mapping."""
+    k = np.ascontiguousarray(k_bf16_bits, dtype=np.uint16)
+    sl = np.ascontiguousarray(slots, dtype=np.int64)
+    out = np.array(cache, dtype=np.uint8, copy=True, order="C")
+    _load().ora_insert_keys(_p(k), _p(sl), int(k.shape[0]), _p(out), int(out.shape[0]))
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -139,6 +139,38 @@ void ora_quantize_q(const uint16_t* q_bf16, const float* w, int64_t rows, int32_
 }
 
 /* ------------------------------------------------------------------------ */
+/* Index-key cache insert                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* The step that fills the paged cache ("recipes/.../indexer.py",
+ * DeepseekV32IndexerMetadata.slot_mapping: every new token has a cache slot;
+ * get_max_prefill_buffer_size and the glm5next _gather_workspace_shapes: 128
+ * fp8 values + one fp32 scale per token). Token i (k_bf16 [n, 128] raw bf16)
+ * gets scale = amax / 448 (fp32 division) and codes e4m3(x / scale) (fp32
+ * division, round to nearest even, saturating); slot s = slots[i] is page
+ * s / 64, token s % 64. Negative or out-of-range slots are skipped; amax == 0
+ * gives zero codes and scale 0. */
+void ora_insert_keys(const uint16_t* k_bf16, const int64_t* slots, int64_t n, uint8_t* cache,
+                     int64_t num_pages) {
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t s = slots[i];
+    if (s < 0 || s >= num_pages * ORA_PAGE_TOKENS) continue;
+    const uint16_t* src = k_bf16 + i * ORA_DIM;
+    float amax = 0.0f;
+    for (int d = 0; d < ORA_DIM; ++d) {
+      const float a = fabsf(bf16_to_float(src[d]));
+      if (a > amax) amax = a;
+    }
+    uint8_t* page = cache + (s / ORA_PAGE_TOKENS) * ORA_PAGE_BYTES;
+    const int64_t tok = s % ORA_PAGE_TOKENS;
+    const float scale = amax / 448.0f; /* fp32 division */
+    for (int d = 0; d < ORA_DIM; ++d)
+      page[tok * ORA_DIM + d] = amax == 0.0f ? 0x00 : ora_e4m3_encode(bf16_to_float(src[d]) / scale);
+    memcpy(page + ORA_SCALE_OFFSET + tok * 4, &scale, 4);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Decode row expansion                                                      */
 /* ------------------------------------------------------------------------ */
 

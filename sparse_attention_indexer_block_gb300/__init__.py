@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     indexer_decode_topk_noalloc,
     indexer_decode_workspace_bytes,
     indexer_expand_decode_rows,
+    indexer_insert_keys,
     indexer_plan_prefill_chunks,
     indexer_prefill_topk,
     indexer_prefill_workspace_bytes,

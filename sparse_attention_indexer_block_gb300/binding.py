@@ -30,6 +30,7 @@ SIGNATURES = {
     "indexer_expand_decode_rows": (C.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32, _P, _P,
                                              _I64, _I64, _P, _P]),
     "indexer_quantize_q": (C.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
+    "indexer_insert_keys": (C.c_int, [_P, _P, _I64, _I32, _P, _I64, _P, _P]),
     "indexer_decode_workspace_bytes": (C.c_int, [_I32, _I32, _I32, C.POINTER(_SZ)]),
     "indexer_decode_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
                                       _I32, _I32, _P, _P, _SZ, _P, _P]),
@@ -144,6 +145,16 @@ def indexer_quantize_q(q, weights, q_fp8=None, weights_scaled=None, stream=None)
                                    _stream(stream))
     _check("indexer_quantize_q", st)
     return q_fp8, weights_scaled
+
+
+def indexer_insert_keys(k, slot_mapping, index_cache, dev_error=None, stream=None):
+    """Quantises k (bf16 [T, 128]) per token and writes it into the paged
+    index cache (uint8 [pages, 8448]) at slot_mapping (int64 [T]); in place."""
+    st = load().indexer_insert_keys(_ptr(k), _ptr(slot_mapping), int(k.shape[0]), int(k.shape[1]),
+                                    _ptr(index_cache), int(index_cache.shape[0]),
+                                    _ptr(dev_error), _stream(stream))
+    _check("indexer_insert_keys", st)
+    return index_cache
 
 
 def indexer_decode_workspace_bytes(num_reqs: int, next_n: int, topk: int) -> int:

@@ -306,6 +306,19 @@ idx_status indexer_quantize_q(const void* q, const float* weights, int64_t num_r
                                weights_scaled, static_cast<cudaStream_t>(stream));
 }
 
+idx_status indexer_insert_keys(const void* k, const int64_t* slot_mapping, int64_t num_tokens,
+                               int32_t head_dim, uint8_t* index_cache, int64_t num_pages,
+                               uint32_t* dev_error, void* stream) {
+  if (num_tokens < 0 || num_pages < 0) return IDX_ERR_INVALID_ARG;
+  if (head_dim != kDim) return IDX_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return IDX_OK;
+  if (!k || !slot_mapping || !index_cache || !aligned(k, 8) || !aligned(slot_mapping, 8) ||
+      !aligned(index_cache, 16))
+    return IDX_ERR_INVALID_ARG;
+  return launch_insert_keys(static_cast<const __nv_bfloat16*>(k), slot_mapping, num_tokens,
+                            index_cache, num_pages, dev_error, static_cast<cudaStream_t>(stream));
+}
+
 idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int32_t topk,
                                           size_t* bytes) {
   if (!bytes || num_reqs < 0) return IDX_ERR_INVALID_ARG;

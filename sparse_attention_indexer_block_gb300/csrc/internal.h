@@ -94,6 +94,9 @@ idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, in
                          int32_t mode, int32_t* row_lens, int32_t* row_bt, int64_t out_stride,
                          int64_t num_out_rows, uint32_t* err, cudaStream_t s);
 
+idx_status launch_insert_keys(const __nv_bfloat16* k, const int64_t* slots, int64_t n,
+                              uint8_t* cache, int64_t num_pages, uint32_t* err, cudaStream_t s);
+
 idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows,
                                  uint8_t* q8, float* wprime, cudaStream_t s);
 

@@ -532,6 +532,66 @@ __global__ void __launch_bounds__(kPrepThreads) expand_kernel(
   }
 }
 
+// Index-key cache insert: token i's 128 bf16 values are quantised with their
+// own fp32 scale amax / 448 (correctly rounded) into e4m3 codes of x / scale
+// (correctly rounded quotient, round-to-nearest-even, saturating) and written
+// to slot slot_mapping[i] of the paged cache (page slot / 64, token slot % 64;
+// values then scales in the page). A negative slot is padding and skipped; a
+// slot past the cache sets IDX_DEV_BAD_BLOCK and is skipped; amax == 0 writes
+// zero codes and scale 0. One warp per token, four tokens' loads per round.
+__global__ void __launch_bounds__(kPrepThreads) insert_keys_kernel(
+    const __nv_bfloat16* __restrict__ k, const int64_t* __restrict__ slots, int64_t n,
+    uint8_t* __restrict__ cache, int64_t num_pages, uint32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * kPrepThreads) >> 5;
+  const int64_t nslot = num_pages * kPageTokens;
+  for (int64_t base = gw * 4; base < n; base += nw * 4) {
+    uint2 raw[4];
+    int64_t sl[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      raw[u] = make_uint2(0u, 0u);
+      sl[u] = -1;
+      if (base + u < n) {
+        raw[u] = *reinterpret_cast<const uint2*>(k + (base + u) * kDim + 4 * lane);
+        sl[u] = slots[base + u];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (base + u >= n) break;
+      if (sl[u] < 0) continue;  // same slot in every lane: warp-uniform
+      if (sl[u] >= nslot) {
+        if (lane == 0) set_error(err, IDX_DEV_BAD_BLOCK);
+        continue;
+      }
+      const float x0 = __uint_as_float(raw[u].x << 16);
+      const float x1 = __uint_as_float(raw[u].x & 0xffff0000u);
+      const float x2 = __uint_as_float(raw[u].y << 16);
+      const float x3 = __uint_as_float(raw[u].y & 0xffff0000u);
+      float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      float scale = 0.0f;
+      uint32_t codes = 0u;
+      if (amax > 0.0f) {
+        scale = __fdiv_rn(amax, 448.0f);
+        codes = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale))) |
+                (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(x2, scale), __fdiv_rn(x3, scale)))
+                 << 16);
+      }
+      uint8_t* page = cache + (sl[u] / kPageTokens) * kPageBytes;
+      const int tok = static_cast<int>(sl[u] % kPageTokens);
+      *reinterpret_cast<uint32_t*>(page + tok * kDim + 4 * lane) = codes;
+      if (lane == 0) *reinterpret_cast<float*>(page + kPageValueBytes + tok * 4) = scale;
+    }
+  }
+}
+
 int prep_grid(int64_t work_warps) {
   const int64_t blocks = (work_warps + kPrepWarps - 1) / kPrepWarps;
   const int64_t cap = 8 * static_cast<int64_t>(device_sm_count());
@@ -549,6 +609,14 @@ idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, in
   return launch_pdl(expand_kernel, grid, kPrepThreads, 0, s, seq_lens, decode_lens, num_reqs,
                     next_n, bt, bt_stride, bt_width, mode, row_lens, row_bt, out_stride,
                     num_out_rows, err) == cudaSuccess
+             ? IDX_OK
+             : IDX_ERR_CUDA;
+}
+
+idx_status launch_insert_keys(const __nv_bfloat16* k, const int64_t* slots, int64_t n,
+                              uint8_t* cache, int64_t num_pages, uint32_t* err, cudaStream_t s) {
+  return launch_pdl(insert_keys_kernel, prep_grid((n + 3) / 4), kPrepThreads, 0, s, k, slots, n,
+                    cache, num_pages, err) == cudaSuccess
              ? IDX_OK
              : IDX_ERR_CUDA;
 }

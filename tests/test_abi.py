@@ -113,6 +113,16 @@ def test_expand_and_quantize_validation(lib):
     assert q(FAKE, FAKE, 0, 64, 128, FAKE, FAKE, None) == 0
 
 
+def test_insert_keys_validation(lib):
+    f = lib.indexer_insert_keys
+    assert f(FAKE, FAKE, 4, 64, FAKE, 8, None, None) == 2      # head_dim must be 128
+    assert f(FAKE, FAKE, -1, 128, FAKE, 8, None, None) == 1    # negative count
+    assert f(FAKE, FAKE, 4, 128, FAKE, -1, None, None) == 1    # negative page count
+    assert f(None, FAKE, 4, 128, FAKE, 8, None, None) == 1     # missing keys
+    assert f(FAKE, FAKE, 4, 128, FAKE + 8, 8, None, None) == 1  # cache not 16-byte aligned
+    assert f(FAKE, FAKE, 0, 128, FAKE, 8, None, None) == 0     # nothing to do
+
+
 def test_prefill_validation(lib):
     sl = np.array([10, 5], np.int32)
     ql = np.array([11, 5], np.int32)   # query_len > seq_len is invalid

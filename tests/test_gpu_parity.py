@@ -318,3 +318,42 @@ def test_topk_all_equal_logits_degenerate():
     c[:, 8192:] = c[0, 8192:8196].repeat(64)       # and one scale
     d.cache = c
     _check_decode(d, 2048)
+
+
+# ---------------------------------------------------------------------------
+# index-key cache insert: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [3, 4999])
+def test_insert_keys_bit_exact(n):
+    pages = (n + 63) // 64 + 7
+    g = torch.Generator().manual_seed(n)
+    x = torch.randn((n, 128), generator=g)
+    x *= torch.exp(torch.randn((n, 1), generator=g) * 3)  # token scales over many octaves
+    x[n // 2] = 0.0                                         # an all-zero token
+    k = x.to(torch.bfloat16)
+    rng = np.random.default_rng(n)
+    slots = rng.permutation(pages * 64)[:n].astype(np.int64)
+    slots[rng.random(n) < 0.1] = -1                         # padding tokens
+    base = rng.integers(0, 256, (pages, 8448), dtype=np.uint8)
+    cache = torch.from_numpy(base.copy()).to(DEV)
+    err = _err()
+    saib.indexer_insert_keys(k.to(DEV), torch.from_numpy(slots).to(DEV), cache, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bits = k.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(cache.cpu().numpy(), oracle.insert_keys(bits, slots, base))
+
+
+def test_insert_keys_out_of_range_slot_is_reported_and_skipped():
+    pages = 4
+    k = torch.randn((8, 128)).to(torch.bfloat16)
+    slots = np.array([0, 5, pages * 64, 70, -3, 255, pages * 64 + 9, 130], np.int64)
+    base = np.zeros((pages, 8448), np.uint8)
+    cache = torch.from_numpy(base.copy()).to(DEV)
+    err = _err()
+    saib.indexer_insert_keys(k.to(DEV), torch.from_numpy(slots).to(DEV), cache, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1  # IDX_DEV_BAD_BLOCK
+    bits = k.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(cache.cpu().numpy(), oracle.insert_keys(bits, slots, base))

@@ -138,6 +138,71 @@ def _worked_example():
     return d
 
 
+# --------------------------------------------------------------------------
+# index-key cache insert
+# --------------------------------------------------------------------------
+
+def _bf16_tokens(n, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn((n, 128), generator=g) * scale).to(torch.bfloat16)
+    return x, x.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_insert_keys_matches_torch_quantisation():
+    """The insert equals torch's per-token quantisation (amax/448 scale,
+    x/scale cast by torch's own float8_e4m3fn conversion) slot by slot."""
+    n, pages = 300, 6
+    x, bits = _bf16_tokens(n, 5, scale=3.0)
+    rng = np.random.default_rng(5)
+    slots = rng.permutation(pages * 64)[:n].astype(np.int64)
+    got = oracle.insert_keys(bits, slots, np.zeros((pages, 8448), np.uint8))
+    xf = x.float()
+    amax = xf.abs().amax(dim=-1, keepdim=True)
+    scale = amax / 448.0
+    codes = (xf / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    sbytes = scale.reshape(-1).numpy().astype(np.float32).view(np.uint8).reshape(n, 4)
+    for i, sl in enumerate(slots):
+        pg, t = divmod(int(sl), 64)
+        assert np.array_equal(got[pg, t * 128:(t + 1) * 128], codes[i])
+        assert np.array_equal(got[pg, 8192 + 4 * t:8192 + 4 * t + 4], sbytes[i])
+
+
+def test_insert_keys_hand_example_zero_token_and_skips():
+    """A hand-worked token (amax 448 -> scale 1: codes of 448, 1, -0.5, 0 are
+    0x7E, 0x38, 0xB0, 0x00), an all-zero token (zero codes, scale 0), padding
+    and out-of-range slots skipped, every other byte untouched."""
+    x = torch.zeros((4, 128), dtype=torch.float32)
+    x[0, :4] = torch.tensor([448.0, 1.0, -0.5, 0.0])
+    x[2, 5] = -2.0
+    x[3, 0] = 1.0
+    bits = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    base = np.full((2, 8448), 0xA5, np.uint8)
+    got = oracle.insert_keys(bits, np.array([70, 3, -1, 128], np.int64), base)
+    row = got[1, 6 * 128:7 * 128]
+    assert list(row[:4]) == [0x7E, 0x38, 0xB0, 0x00] and not row[4:].any()
+    assert np.frombuffer(got[1, 8192 + 24:8192 + 28].tobytes(), np.float32)[0] == 1.0
+    assert not got[0, 3 * 128:4 * 128].any()
+    assert np.frombuffer(got[0, 8192 + 12:8192 + 16].tobytes(), np.float32)[0] == 0.0
+    touched = np.zeros_like(base, bool)
+    touched[1, 6 * 128:7 * 128] = touched[1, 8192 + 24:8192 + 28] = True
+    touched[0, 3 * 128:4 * 128] = touched[0, 8192 + 12:8192 + 16] = True
+    assert (got[~touched] == 0xA5).all()  # slot -1 (token 2) and slot 128 (token 3) skipped
+
+
+def test_insert_keys_dequantisation_error_bound():
+    """code * scale is within e4m3's rounding bound of x: half a step, i.e.
+    2^-4 relative for normal codes, 2^-10 * scale below the normal range."""
+    x, bits = _bf16_tokens(64, 6, scale=0.01)
+    got = oracle.insert_keys(bits, np.arange(64, dtype=np.int64), np.zeros((1, 8448), np.uint8))
+    codes = got[0, :8192].reshape(64, 128)
+    scale = np.frombuffer(got[0, 8192:].tobytes(), np.float32).astype(np.float64)
+    deq = oracle.e4m3_decode(codes) * scale[:, None]
+    xf = x.double().numpy()
+    bound = np.maximum(np.abs(xf) * 2.0 ** -4, 2.0 ** -10 * scale[:, None]) * (1 + 1e-6)
+    assert (np.abs(deq - xf) <= bound).all()
+    assert np.allclose(np.abs(xf).max(axis=1), 448.0 * scale, rtol=1e-6)
+
+
 def test_expand_flatten_matches_pages_worked_example():
     ex = _worked_example()
     bt = np.arange(4 * 3, dtype=np.int32).reshape(4, 3) + 100
