@@ -34,6 +34,9 @@
  *    sq = amax / 448; the head weight becomes w * sq. amax == 0 gives q8 = 0,
  *    sq = 0. The fp32 steps decide integer codes, so they are done in fp32 here
  *    exactly as the kernel does them; everything else is fp64.
+ *  - Cache insert (not shown on the pages): slot s is page s / 64, token
+ *    s % 64 (negative = padding); scale = amax / 448 and codes e4m3(x / scale),
+ *    fp32 steps like the q quantisation; amax == 0 gives zero codes, scale 0.
  *  - Since scale_s >= 0, ReLU(scale_s * x) = scale_s * ReLU(x).
  *  - Rows with len <= k output [0, 1, ..., len-1, -1, ...]; rows with len > k
  *    output the k indices of the largest logits; ties are broken here by the
