@@ -281,6 +281,13 @@ def test_prefill_small_full():
     _check_prefill(p, 64, budget=4 * 300 * 50, ws_tokens=600)
 
 
+def test_prefill_few_queries_over_long_context():
+    """Chunked-prefill shape: 8 new queries over 100000 keys (two work rows of
+    four queries, each spread over many CTAs and merged from their slots)."""
+    p = synth.make_prefill(seed=53, seq_lens=[100000, 3000], query_lens=[8, 5])
+    _check_prefill(p, 2048)
+
+
 def test_prefill_workload_sampled():
     p = synth.make_prefill("prefill")
     rows = np.array([0, 1, 2046, 2047, 2048, 2049, 5000, 8191, 8192, 8192 + 4095, 16383,
