@@ -177,11 +177,16 @@ def profiled_traffic(workload: str):
     if workload != "decode":
         return None
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "sparse_attention_indexer_block_gb300", "csrc")
     h = hashlib.sha256()
     for name in ("score_select.cu", "common.cuh", "internal.h"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        # code only: comments and whitespace do not change the kernel
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     fields = {}
     try:
         with open(os.path.join(ROOT, "profiles", "score_select_decode_batch.md")) as f:

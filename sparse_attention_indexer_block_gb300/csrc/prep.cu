@@ -135,9 +135,6 @@ __global__ void __launch_bounds__(kPrepThreads) quantize_plain_kernel(
   quantize_tasks<false>(q, w, 0, rows * kHeads, q8, wprime, gw, nw);
 }
 
-// Block 0, after wts[0..num_wr] is written: the work row holding the first
-// tile of each participating CTA of the score/select launch (the kernel gives
-// CTA c tiles [c*T/nC, (c+1)*T/nC) with nC = min(grid, T)).
 // Inclusive prefix max of one int per thread over a block of kPrepThreads
 // threads; *total = the block's max.
 __device__ int block_inclusive_max(int v, int* total) {

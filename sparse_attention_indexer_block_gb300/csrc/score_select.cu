@@ -1129,10 +1129,11 @@ __device__ void merge_work_row(const ScoreParams& p, const Smem& s, int w, const
   }
 }
 
-// End of this CTA's part of work row w: shrink each buffer to <= k; if the
-// CTA holds the whole row write the output, else publish the candidates that
-// can still make the row's top-k (bins at or above the row histogram's
-// current cutoff) to the segment's slot; the CTA that publishes last merges.
+// End of this CTA's part of work row w: if the CTA holds the whole row, cut
+// each buffer to k and write the output; else publish the candidates that can
+// still make the row's top-k (bins at or above the row histogram's current
+// cutoff; a slot holds a whole buffer) to the segment's slot; the CTA that
+// publishes last merges (now, or at its end if it still has tiles to stream).
 template <int G>
 __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
                                  const bool (&active)[G], int64_t rs, int64_t re, int64_t t0,
