@@ -851,76 +851,27 @@ __device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int
   if (et == 0 && s.trace) s.trace[kTrMergeTailNs] += globaltimer_ns() - tq3;
 }
 
-// merge_row for a CTA whose own pipeline has finished (its shared-memory ring
-// is idle): the slots' keys and indices are staged into the ring by one bulk
-// copy per slot and segment (all completing on one mbarrier), then the cutoff
-// classification, the radix select among the cutoff bin's keys and the output
-// all run from shared memory. Returns false (having written nothing) when the
-// union does not fit the ring or the slots disagree with the histogram.
+// Where the selection finds each staged key's token index.
+enum StagedIdx {
+  kIdxStaged = 0,     // aux[e]: the indices were staged beside the keys
+  kIdxSlotByPos = 1,  // slot entry at staged position e (segment offsets in cidx)
+  kIdxSlotBySrc = 2,  // slot entry at union position aux[e] (segment offsets in cidx)
+};
+
+// Selection of work row w's k (token g) from keys staged in shared memory:
+// keys[0, total_r) (total_r a multiple of 4 and keys 16-byte aligned; key 0
+// is padding), cut = the row's exact cutoff bin and above = the count in the
+// bins above it. Returns false (having written nothing final) when the staged
+// keys disagree with the histogram.
 template <int G>
-__device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int g,
-                                 int64_t c_first, int64_t c_last, const uint32_t* gh,
-                                 int32_t* out) {
-  using C = Cfg<G>;
-  constexpr int kStageCap = C::kStages * 16384 / 8;  // entries (key + index) in the ring
+__device__ bool select_staged(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
+                              int nseg, const uint32_t* keys, const int32_t* aux, int total_r,
+                              int cut, int above, int32_t* out, int mode, uint64_t tq0) {
   const int et = threadIdx.x - 64;
   const int lane = threadIdx.x & 31;
   const int K = p.topk;
   Misc* m = s.misc;
-  const int nseg = static_cast<int>(c_last - c_first + 1);
-  if (nseg > kEpiThreads) return false;
-  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // the segments' counts and threshold bins and this thread's bins of the row
-  // histogram, loaded together
-  const int64_t sl = (c_first + et + w) * G + g;
-  int floor = et < nseg ? __ldcg(&p.slot_thrbin[sl]) : -1;
-  const int my_n = et < nseg ? __ldcg(&p.slot_count[sl]) : 0;
-  int hc[kCutPer];
-  load_row_bins(gh, hc);
-  // staging offsets: each segment's entries start on a 16-byte boundary
-  const int my_r = (my_n + 3) & ~3;
-  int total_r;
-  const int my_off = epi_exclusive_scan(m, my_r, &total_r);
-  if (total_r > 2 * kStageCap) return false;
-  // Keys and indices are staged when both fit; otherwise only the keys, and
-  // the selected entries' indices are gathered from the slots at the end
-  // (segment staging offsets kept in the idle candidate-index buffer).
-  const bool with_idx = total_r <= kStageCap;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
-  int32_t* idxs = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
-  int32_t* seg_off = s.cidx;
-  if (!with_idx && et <= nseg) seg_off[et] = et < nseg ? my_off : total_r;
-  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int use = m->staged_uses;
-  if (et < nseg && my_n > 0) {
-    const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
-    bulk_load(keys + my_off, p.slot_key + sl * p.slot_cap, bytes, s.staged);
-    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * p.slot_cap, bytes, s.staged);
-  }
-  if (et == 0)
-    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * (with_idx ? 8u : 4u));
-  // while the copies are in flight: the row's cutoff, floored by the
-  // segments' threshold bins (see merge_row)
-  floor = __reduce_max_sync(0xffffffffu, floor);
-  if (lane == 0) m->rmin[et >> 5] = static_cast<uint32_t>(floor);
-  named_sync(kEpiBarrier, kEpiThreads);
-  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
-              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
-  int cut, above;
-  row_cutoff_vals(hc, m, K, floor, &cut, &above);
-  bool ok = true;
-  if (lane == 0) ok = mbar_wait(s.staged, use & 1, &m->abort_flag, p.dev_error);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  // the padding after a segment's entries becomes key 0, which no logit maps to
-  if (ok && et < nseg)
-    for (int e = my_off + my_n; e < my_off + my_r; ++e) keys[e] = 0u;
-  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
-  named_sync(kEpiBarrier, kEpiThreads);
-  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
-  if (et == 0) m->staged_uses = use + 1;
-  if (!all_ok || cut < 0) return false;
+  const int32_t* seg_off = s.cidx;
   const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   // One pass classifies every key against the cutoff bin (keys carry the row
   // bin in their top 10 bits) and histograms the next 10 bits of the keys in
@@ -1046,7 +997,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     t_take += w_take;
   }
   named_sync(kEpiBarrier, kEpiThreads);
-  const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  const int4* x4 = reinterpret_cast<const int4*>(aux);
   int32_t* src = reinterpret_cast<int32_t*>(s.ckey);  // staged position of output p
   const uint32_t lt = (1u << lane) - 1u;
   for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
@@ -1055,7 +1006,7 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     int4 xi = make_int4(0, 0, 0, 0);
     if (e < n4) {
       q = k4[e];
-      if (with_idx) xi = x4[e];
+      if (mode == kIdxStaged) xi = x4[e];
     }
     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
     const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
@@ -1075,16 +1026,17 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
       const uint32_t im = __ballot_sync(0xffffffffu, kc[c] == 1u);
       const int pos = out_base + __popc(im & lt);
       if (kc[c] == 1u && pos < K) {
-        if (with_idx) out[pos] = x[c];
+        if (mode == kIdxStaged) out[pos] = x[c];
         else src[pos] = 4 * e + c;
       }
       out_base += __popc(im);
     }
   }
-  if (!with_idx) {
+  if (mode != kIdxStaged) {
     named_sync(kEpiBarrier, kEpiThreads);
     for (int q = et; q < min(t_take, K); q += kEpiThreads) {
-      const int e = src[q];
+      int e = src[q];
+      if (mode == kIdxSlotBySrc) e = aux[e];  // staged position -> position in the slots' union
       int lo = 0, hi = nseg - 1;  // the segment holding staged position e
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -1102,6 +1054,171 @@ __device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int
     s.trace[kTrMergeTailNs] += globaltimer_ns() - tq2;
   }
   return true;
+}
+
+
+// Merge for rows with more segments than epilogue threads, or a union of slot
+// entries larger than the ring: every thread walks the slots' union (four
+// coalesced loads in flight per round) and appends the entries in bins at or
+// above the exact cutoff, with their union position, to the ring; the
+// selection then runs on that filtered set and gathers the chosen indices
+// from the slots. Returns false when the filtered set does not fit either.
+template <int G>
+__device__ bool merge_row_gathered(const ScoreParams& p, const Smem& s, int w, int g,
+                                   int64_t c_first, int64_t c_last, const uint32_t* gh,
+                                   int32_t* out) {
+  using C = Cfg<G>;
+  constexpr int kStageCap = C::kStages * 16384 / 8;
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  const int nseg = static_cast<int>(c_last - c_first + 1);
+  int32_t* seg_off = s.cidx;  // [nseg + 1] union offsets of the segments
+  if (nseg + 1 > G * C::kCap) return false;
+  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  named_sync(kEpiBarrier, kEpiThreads);
+  int floor = -1, carry = 0;
+  for (int base = 0; base < nseg; base += kEpiThreads) {
+    const int i = base + et;
+    int n = 0;
+    if (i < nseg) {
+      const int64_t sl = (c_first + i + w) * G + g;
+      n = __ldcg(&p.slot_count[sl]);
+      floor = max(floor, __ldcg(&p.slot_thrbin[sl]));
+    }
+    int tot;
+    const int excl = epi_exclusive_scan(m, n, &tot);
+    if (i < nseg) seg_off[i] = carry + excl;
+    carry += tot;
+    named_sync(kEpiBarrier, kEpiThreads);
+  }
+  const int total = carry;
+  if (et == 0) {
+    seg_off[nseg] = total;
+    m->sel_out = 0;
+  }
+  floor = __reduce_max_sync(0xffffffffu, floor);
+  if (lane == 0) m->rmin[ew] = static_cast<uint32_t>(floor);
+  named_sync(kEpiBarrier, kEpiThreads);
+  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
+              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
+  int cut, above;
+  row_cutoff(gh, m, K, floor, &cut, &above);
+  if (cut < 0) return false;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
+  int32_t* src = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
+  const uint32_t lt = (1u << lane) - 1u;
+  int seg = 0;  // this thread's segment; its union positions only grow
+  for (int i0 = ew * 128; i0 < total; i0 += 4 * kEpiThreads) {
+    uint32_t u4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      u4[u] = 0u;
+      if (i < total) {
+        while (seg_off[seg + 1] <= i) ++seg;
+        const int64_t sl = (c_first + seg + w) * G + g;
+        u4[u] = __ldcg(&p.slot_key[sl * p.slot_cap + (i - seg_off[seg])]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * 32 + lane;
+      const bool kp = i < total && row_bin(u4[u]) >= cut;
+      const uint32_t km = __ballot_sync(0xffffffffu, kp);
+      int b = 0;
+      if (lane == 0 && km) b = atomicAdd(&m->sel_out, __popc(km));
+      b = __shfl_sync(0xffffffffu, b, 0);
+      const int pos = b + __popc(km & lt);
+      if (kp && pos < kStageCap) {
+        keys[pos] = u4[u];
+        src[pos] = i;
+      }
+    }
+  }
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int kept = m->sel_out;
+  const int kept_r = (kept + 3) & ~3;
+  if (kept_r > kStageCap) return false;
+  for (int e = kept + et; e < kept_r; e += kEpiThreads) keys[e] = 0u;  // padding
+  named_sync(kEpiBarrier, kEpiThreads);
+  return select_staged<G>(p, s, w, g, c_first, nseg, keys, src, kept_r, cut, above, out,
+                          kIdxSlotBySrc, tq0);
+}
+
+// merge_row for a CTA whose own pipeline has finished (its shared-memory ring
+// is idle): the slots' keys and indices are staged into the ring by one bulk
+// copy per slot and segment (all completing on one mbarrier), then the cutoff
+// classification, the radix select among the cutoff bin's keys and the output
+// all run from shared memory. Returns false (having written nothing) when the
+// union does not fit the ring or the slots disagree with the histogram.
+template <int G>
+__device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int g,
+                                 int64_t c_first, int64_t c_last, const uint32_t* gh,
+                                 int32_t* out) {
+  using C = Cfg<G>;
+  constexpr int kStageCap = C::kStages * 16384 / 8;  // entries (key + index) in the ring
+  const int et = threadIdx.x - 64;
+  const int lane = threadIdx.x & 31;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  const int nseg = static_cast<int>(c_last - c_first + 1);
+  if (nseg > kEpiThreads) return merge_row_gathered<G>(p, s, w, g, c_first, c_last, gh, out);
+  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  // the segments' counts and threshold bins and this thread's bins of the row
+  // histogram, loaded together
+  const int64_t sl = (c_first + et + w) * G + g;
+  int floor = et < nseg ? __ldcg(&p.slot_thrbin[sl]) : -1;
+  const int my_n = et < nseg ? __ldcg(&p.slot_count[sl]) : 0;
+  int hc[kCutPer];
+  load_row_bins(gh, hc);
+  // staging offsets: each segment's entries start on a 16-byte boundary
+  const int my_r = (my_n + 3) & ~3;
+  int total_r;
+  const int my_off = epi_exclusive_scan(m, my_r, &total_r);
+  if (total_r > 2 * kStageCap) return merge_row_gathered<G>(p, s, w, g, c_first, c_last, gh, out);
+  // Keys and indices are staged when both fit; otherwise only the keys, and
+  // the selected entries' indices are gathered from the slots at the end
+  // (segment staging offsets kept in the idle candidate-index buffer).
+  const bool with_idx = total_r <= kStageCap;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
+  int32_t* idxs = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
+  int32_t* seg_off = s.cidx;
+  if (!with_idx && et <= nseg) seg_off[et] = et < nseg ? my_off : total_r;
+  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
+  named_sync(kEpiBarrier, kEpiThreads);
+  const int use = m->staged_uses;
+  if (et < nseg && my_n > 0) {
+    const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
+    bulk_load(keys + my_off, p.slot_key + sl * p.slot_cap, bytes, s.staged);
+    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * p.slot_cap, bytes, s.staged);
+  }
+  if (et == 0)
+    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * (with_idx ? 8u : 4u));
+  // while the copies are in flight: the row's cutoff, floored by the
+  // segments' threshold bins (see merge_row)
+  floor = __reduce_max_sync(0xffffffffu, floor);
+  if (lane == 0) m->rmin[et >> 5] = static_cast<uint32_t>(floor);
+  named_sync(kEpiBarrier, kEpiThreads);
+  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
+              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
+  int cut, above;
+  row_cutoff_vals(hc, m, K, floor, &cut, &above);
+  bool ok = true;
+  if (lane == 0) ok = mbar_wait(s.staged, use & 1, &m->abort_flag, p.dev_error);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  // the padding after a segment's entries becomes key 0, which no logit maps to
+  if (ok && et < nseg)
+    for (int e = my_off + my_n; e < my_off + my_r; ++e) keys[e] = 0u;
+  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
+  named_sync(kEpiBarrier, kEpiThreads);
+  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
+  if (et == 0) m->staged_uses = use + 1;
+  if (!all_ok || cut < 0) return false;
+  return select_staged<G>(p, s, w, g, c_first, nseg, keys, with_idx ? idxs : nullptr, total_r, cut,
+                          above, out, with_idx ? kIdxStaged : kIdxSlotByPos, tq0);
 }
 
 // Merge of work row w (every segment published) into its output rows, by a
