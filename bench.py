@@ -170,23 +170,28 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
+def kernel_code_hash(root: str) -> str:
+    """First 16 hex digits of the sha256 of the score/select kernel's code
+    (score_select.cu, common.cuh, internal.h without comments or whitespace)."""
+    import hashlib
+    import re
+    csrc = os.path.join(root, "sparse_attention_indexer_block_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("score_select.cu", "common.cuh", "internal.h"):
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per score/select launch from the committed ncu summary of
     the decode-batch workload, or None when that summary was taken on other
     kernel sources (or another workload is being run)."""
     if workload != "decode":
         return None
-    import hashlib
-    import re
-    csrc = os.path.join(ROOT, "sparse_attention_indexer_block_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in ("score_select.cu", "common.cuh", "internal.h"):
-        with open(os.path.join(csrc, name)) as f:
-            text = f.read()
-        # code only: comments and whitespace do not change the kernel
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
     fields = {}
     try:
         with open(os.path.join(ROOT, "profiles", "score_select_decode_batch.md")) as f:
@@ -196,7 +201,7 @@ def profiled_traffic(workload: str):
                     fields[k] = v.strip()
     except OSError:
         return None
-    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+    if fields.get("source_sha256_16") != kernel_code_hash(ROOT):
         return None
     return int(fields["dram_bytes_per_launch"])
 
