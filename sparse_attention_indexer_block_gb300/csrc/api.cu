@@ -1,6 +1,7 @@
 // C ABI of the indexer: argument validation, workspace carve-up, the host
 // prefill chunk planner and the launch sequences.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -70,14 +71,17 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
 }
 
 int device_sm_count() {
-  static int cached[128] = {0};
+  static std::atomic<int> cached[kMaxDevices];  // 0 = not looked up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 128 && cached[dev] > 0) return cached[dev];
+  if (dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     n = 1;
-  if (dev < 128) cached[dev] = n;
+  if (dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -84,7 +84,8 @@ struct WsLayout {
 };
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
 
-// Per-device facts and one-time setup.
+// Per-device facts and one-time setup (devices 0 .. kMaxDevices-1 are cached).
+constexpr int kMaxDevices = 128;
 int device_sm_count();
 idx_status encode_cache_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages);
 

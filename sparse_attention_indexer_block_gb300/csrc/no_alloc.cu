@@ -26,11 +26,11 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 // device with that device current (the first lookup may load the library's
 // device code).
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[128] = {};
+void* g_scratch_ptr[saib::kMaxDevices] = {};
 
 idx_status scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return IDX_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= saib::kMaxDevices) return IDX_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[dev]) {
     void* ptr = nullptr;

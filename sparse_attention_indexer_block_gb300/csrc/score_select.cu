@@ -25,6 +25,8 @@
 //   logit[t, s] = sum_h w[t, h] ReLU(scale_s (q[t, h] . k_s))
 //               = scale_s * sum_h (w[t, h] sq[t, h]) ReLU(q8[t, h] . k8_s),
 // since scale_s >= 0 and q = q8 * sq per (token, head).
+#include <atomic>
+
 #include "internal.h"
 
 namespace saib {
@@ -1670,15 +1672,17 @@ __global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
 template <int G, bool kLogits>
 idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_ctas, cudaStream_t s) {
   using C = Cfg<G>;
-  static int configured_device = -1;
+  // the dynamic shared-memory limit is a per-device attribute of the kernel:
+  // set once per device (any host thread; setting it twice is harmless)
+  static std::atomic<bool> configured[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return IDX_ERR_CUDA;
-  if (configured_device != dev) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return IDX_ERR_CUDA;
+  if (dev >= kMaxDevices || !configured[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(score_select_kernel<G, kLogits>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return IDX_ERR_CUDA;
-    configured_device = dev;
+    if (dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
   }
   return launch_pdl(score_select_kernel<G, kLogits>, num_ctas, kThreads, C::kSmemBytes, s, p, map) ==
                  cudaSuccess
