@@ -59,6 +59,10 @@
  *  - Workspaces are caller-provided scratch of the size the *_workspace_bytes
  *    query returns for the current device; contents need no initialisation and
  *    are overwritten. Calls that share a workspace must not overlap.
+ *  - Kernels are launched with programmatic dependent launch: a kernel may be
+ *    scheduled while the previous work in the stream finishes, but it waits
+ *    for that work to complete before it reads or writes any memory, so the
+ *    stream's ordering is what the caller sees.
  */
 #ifndef SAIB_INDEXER_H
 #define SAIB_INDEXER_H
