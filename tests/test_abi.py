@@ -36,6 +36,46 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(binding.SIGNATURES), "binding and header disagree"
 
 
+def _declarations():
+    """name -> list of parameter type strings, parsed from the header."""
+    text = open(os.path.join(ROOT, "include", "indexer.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(indexer_\w+)\s*\(([^)]*)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        out[m.group(1)] = [re.sub(r"\s*\b\w+$", "", p) if not p.endswith("*") else p
+                           for p in params]
+    return out
+
+
+def _kind(ctype):
+    if ctype in (C.c_void_p, C.c_char_p) or (isinstance(ctype, type) and
+                                            issubclass(ctype, C._Pointer)):
+        return "ptr"
+    return f"int{C.sizeof(ctype) * 8}"
+
+
+def _header_kind(t):
+    if "*" in t:
+        return "ptr"
+    base = t.replace("const", "").strip()
+    return {"int32_t": "int32", "idx_status": "int32", "int64_t": "int64",
+            "size_t": "int64"}[base]
+
+
+def test_binding_signatures_match_header_parameters():
+    """Every binding signature has the header's parameter count, and each
+    parameter the same kind (pointer, 32- or 64-bit integer), so a call cannot
+    shift or truncate an argument."""
+    decls = _declarations()
+    assert set(decls) == set(binding.SIGNATURES)
+    for name, params in decls.items():
+        _, argtypes = binding.SIGNATURES[name]
+        assert len(argtypes) == len(params), f"{name}: {len(argtypes)} vs {len(params)}"
+        for i, (t, a) in enumerate(zip(params, argtypes)):
+            assert _header_kind(t) == _kind(a), f"{name} parameter {i}: {t} vs {a}"
+
+
 def test_status_strings(lib):
     assert saib.indexer_status_string(0) == "ok"
     assert saib.indexer_status_string(3) == "workspace too small"
