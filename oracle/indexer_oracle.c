@@ -26,7 +26,7 @@
  *    and top-k = 2048 come from the statement of the method; the pages only name
  *    the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent or ambiguous (each one stated here):
  *  - Page byte layout: each 64-token page is [64 x 128 fp8 e4m3 values]
  *    followed by [64 x fp32 scales] = 8448 bytes (64 * 132).
  *  - q reaches an fp8 MMA, so q is quantised per (token, head): amax = max|q|,

@@ -360,6 +360,67 @@ def test_decode_topk_rows_are_valid_sets():
         assert np.all(lg[r][rest] <= kth)
 
 
+def _brute_topk(lg, k):
+    return sorted(range(len(lg)), key=lambda i: (-lg[i], i))[:k]
+
+
+def test_decode_topk_two_token_rows_read_their_requests_block_table():
+    """next_n = 2: token row b*2 + j reads q row b*2 + j and block-table row b,
+    with j < d_b seeing L_b - d_b + j + 1 keys and padded rows none
+    ("recipes/.../indexer.py", _prepare_decode_tensors: each token of a request
+    reads that request's block table; "vllm.models.glm5next.common.
+    sparse_indexer", _decode_topk_seq_lens: padded rows 0). Pinned by the
+    numpy restatement of the scores and brute-force sorts, on requests whose
+    block tables hold different pages."""
+    sl, dl, k = [2300, 2200, 2600], [2, 1, 2], 256
+    d = synth.make_decode_from_lens(sl, dl, 2, seed=19)
+    bt = d.block_table.numpy()
+    assert len(set(bt[0][:36]) & set(bt[1][:35])) == 0            # distinct pages
+    lens, _, _ = oracle.expand_rows(np.array(sl), np.array(dl), 2)
+    hand = [2299, 2300, 2200, 0, 2599, 2600]
+    assert list(lens) == hand
+    out, lg, _, _, rows = oracle.decode_topk(synth.bf16_bits(d.q), d.w.numpy(), d.cache.numpy(),
+                                             bt, lens, 2, k, want_logits=True)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(d.q), d.w.numpy())
+    cache = d.cache.numpy()
+    for r in rows:
+        b, L = r // 2, hand[r]
+        if L == 0:
+            assert list(out[r]) == [-1] * k
+            continue
+        ref, _ = _dense_reference(q8[r], wp[r], cache, bt[b], L)
+        assert np.allclose(lg[r], ref, rtol=1e-12, atol=1e-12)
+        # the same q row scored against another request's pages differs
+        other, _ = _dense_reference(q8[r], wp[r], cache, bt[(b + 1) % 3], min(L, 2200))
+        assert not np.allclose(ref[:len(other)], other)
+        assert sorted(out[r].tolist()) == sorted(_brute_topk(lg[r], k))
+
+
+def test_prefill_topk_routes_queries_to_their_request():
+    """Query row i of request r (rows query_start_loc[r] + i) reads request r's
+    block table and sees keys [0, L_r - Q_r + 1 + i) ("recipes/.../indexer.py",
+    _build_prefill_chunk_metadata_kernel). Pinned by the numpy restatement and
+    brute-force sorts; the rows are routed here by walking query_start_loc."""
+    sl, ql, k = [300, 517, 90], [3, 5, 2], 64
+    p = synth.make_prefill(seed=23, seq_lens=sl, query_lens=ql)
+    bt = p.block_table.numpy()
+    out, lg, _, _, rows = oracle.prefill_topk(synth.bf16_bits(p.q), p.w.numpy(), p.cache.numpy(),
+                                              bt, p.seq_lens.numpy(),
+                                              p.query_start_loc.numpy(), k, want_logits=True)
+    q8, _, wp = oracle.quantize_q(synth.bf16_bits(p.q), p.w.numpy())
+    cache = p.cache.numpy()
+    route = []
+    for r, (L, Q) in enumerate(zip(sl, ql)):
+        for i in range(Q):
+            route.append((r, L - Q + 1 + i))
+    assert list(rows) == list(range(sum(ql)))
+    assert [ln for _, ln in route] == [298, 299, 300, 513, 514, 515, 516, 517, 89, 90]
+    for row, (r, L) in enumerate(route):
+        ref, _ = _dense_reference(q8[row], wp[row], cache, bt[r], L)
+        assert np.allclose(lg[row], ref, rtol=1e-12, atol=1e-12)
+        assert sorted(out[row].tolist()) == sorted(_brute_topk(lg[row], k))
+
+
 # --------------------------------------------------------------------------
 # prefill
 # --------------------------------------------------------------------------

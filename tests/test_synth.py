@@ -1,6 +1,8 @@
-"""The synthetic input recipe (CPU only): workload shapes, seeded draws and the
-paged layout are what the design notes state, so parity and benchmark runs
-measure the configurations they claim."""
+"""The synthetic input recipe (CPU only): the five workloads (tiny, decode
+batch, MTP, long context, prefill) have the shapes and distributions stated in
+synth's docstring, the draws are seeded, and the paged layout is
+[64 x 128 fp8][64 x fp32 scale] per page, so parity and benchmark runs measure
+the configurations they claim."""
 import numpy as np
 import torch
 
