@@ -63,6 +63,11 @@
  *    scheduled while the previous work in the stream finishes, but it waits
  *    for that work to complete before it reads or writes any memory, so the
  *    stream's ordering is what the caller sees.
+ *  - The top-k score/select kernel is a cooperative launch (one or two CTAs
+ *    per SM, all resident at once): the CTAs that share a request's keys wait
+ *    for one another's candidates before selecting (each wait gives up after
+ *    2 s and sets IDX_DEV_TIMEOUT). It fails with IDX_ERR_CUDA rather than
+ *    run partly resident.
  */
 #ifndef SAIB_INDEXER_H
 #define SAIB_INDEXER_H
@@ -88,6 +93,7 @@ typedef enum {
 #define IDX_DEV_BAD_LEN 2u   /* a row length < 0 or > bt_width * 64 was clamped */
 #define IDX_DEV_TIMEOUT 4u   /* a pipeline wait gave up; the kernel returned early */
 #define IDX_DEV_OVERFLOW 8u  /* more token rows than the output holds (flatten mode) */
+#define IDX_DEV_INTERNAL 16u /* the split-row selection's counts disagreed (a library bug) */
 
 #define IDX_NUM_HEADS 64
 #define IDX_HEAD_DIM 128
@@ -97,6 +103,10 @@ typedef enum {
 
 /* Human-readable name of a status code (static string). */
 const char* indexer_status_string(idx_status status);
+
+/* The CUDA error behind the last IDX_ERR_CUDA this host thread got from a
+ * launch or CUDA call of the library (static string; "no error" if none). */
+const char* indexer_last_cuda_error(void);
 
 /*
  * Decode row expansion ([INDEXER] _prepare_uniform_decode_kernel and the
@@ -184,6 +194,29 @@ idx_status indexer_decode_topk(const void* q, const float* weights, const uint8_
                                uint32_t* dev_error, void* stream);
 
 /*
+ * Introspection of the on-device work split (for tests): where, inside a
+ * decode workspace for (num_reqs, next_n, topk) on the current device, the
+ * prep kernel leaves the plan the score/select kernel follows, as byte
+ * offsets into the workspace:
+ *   offsets[0] wr_tile_start int32 [num_reqs + 1]: first 128-key tile of each
+ *              request (the tile sequence is the requests' tiles in order);
+ *              entry num_reqs is the total T
+ *   offsets[1] cta_tile int32 [min(grid, T) + 1]: CTA c streams tiles
+ *              [cta_tile[c], cta_tile[c + 1])
+ *   offsets[2] row_ctas int32 pairs [num_reqs]: first and last CTA holding a
+ *              request's tiles ((0, -1) for a request with none)
+ *   offsets[3] cta_row int32 [grid]: the request holding CTA c's first tile
+ * *grid gets the launch's CTA count; penalty[0..1] the row-end penalty in
+ * tiles and its growth divisor (the split charges a CTA that finishes a
+ * request inside its range penalty[0] + (T / min(grid, T)) / penalty[1] extra
+ * tiles when that share is >= 64, else penalty[0]). Host only; no device
+ * work. The arrays are valid after an indexer_decode_topk call on the
+ * workspace until the next call.
+ */
+idx_status indexer_debug_decode_plan(int32_t num_reqs, int32_t next_n, int32_t topk,
+                                     int64_t* offsets, int32_t* grid, int32_t* penalty);
+
+/*
  * The decode logits themselves, from the same quantisation, page gather and
  * tensor-core scoring as indexer_decode_topk (for parity checks): for every
  * token row t and key s < len_t writes out_logits[t * ld_logits + s]; other
@@ -255,13 +288,28 @@ idx_status indexer_profile_events(void* start_event, void* stop_event);
 
 /*
  * Tracing hook: while set, score/select launches made from this host thread
- * write 32 uint64 per CTA into `buffer` (device memory, zeroed by the caller,
- * >= 32 * 8 * (2 x SM count) bytes; smaller buffers disable it): %globaltimer
+ * write 64 uint64 per tile stream (two per CTA, one CTA per SM) into `buffer`
+ * (device memory, zeroed by the caller, >= 64 * 8 * (2 x SM count) bytes;
+ * smaller buffers disable it): %globaltimer
  * stamps of the start, the first/last TMA, MMA and epilogue tile and the end,
- * the ns and count of buffer compactions and merges, merge statistics and the
- * CTA's tile count. NULL turns it off.
+ * the ns and count of buffer compactions, segment publication, split-row
+ * selection (waits, scans, final picks) and merges, and the CTA's tile count.
+ * NULL turns it off.
  */
 idx_status indexer_trace_buffer(void* buffer, size_t bytes);
+
+/*
+ * Failure-detection hook (for tests of the give-up path): score/select
+ * launches made from this host thread give up every pipeline and split-row
+ * wait after limit_ns nanoseconds instead of 2 s (0 restores 2 s). With
+ * stall_split_rows != 0 their split-row waits also wait for one segment more
+ * than the row has, a count nothing completes, so those waits run into the
+ * limit. A wait that gives up ORs IDX_DEV_TIMEOUT into *dev_error; the kernel
+ * then drains its own copies and tensor-core work, frees its tensor memory
+ * and returns, leaving the call's outputs unspecified. Not for production
+ * calls.
+ */
+idx_status indexer_debug_wait_limit(uint64_t limit_ns, int32_t stall_split_rows);
 
 /*
  * indexer_decode_topk without a caller workspace. The pages have no
@@ -271,11 +319,11 @@ idx_status indexer_trace_buffer(void* buffer, size_t bytes);
  * code running while a stream is captured into a CUDA graph, serving loops
  * that forbid allocator calls on their latency-critical path, or hosts whose
  * device memory is owned by an allocator this code cannot call. The scratch is
- * a 32 MiB device array inside the library (one per GPU that loads the
+ * a 64 MiB device array inside the library (one per GPU that loads the
  * library, held until the process exits); the call allocates nothing. Same
  * arguments and results as indexer_decode_topk without the workspace.
  *  - Limit: the batch must fit the scratch, i.e. indexer_decode_workspace_bytes
- *    (num_reqs, next_n, topk) <= 32 MiB (about 750 requests at next_n = 1, 270
+ *    (num_reqs, next_n, topk) <= 64 MiB (about 1050 requests at next_n = 1, 430
  *    at next_n = 2, top-2048, 152 SMs); a larger batch returns
  *    IDX_ERR_WORKSPACE before any work.
  *  - The first call on each device looks the scratch's device address up (this

@@ -27,6 +27,7 @@ NUM_HEADS, HEAD_DIM, PAGE_TOKENS, PAGE_BYTES, MAX_TOPK = 64, 128, 64, 8448, 2048
 _P, _I32, _I64, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
 SIGNATURES = {
     "indexer_status_string": (C.c_char_p, [C.c_int]),
+    "indexer_last_cuda_error": (C.c_char_p, []),
     "indexer_expand_decode_rows": (C.c_int, [_P, _P, _I32, _I32, _P, _I64, _I32, _I32, _P, _P,
                                              _I64, _I64, _P, _P]),
     "indexer_quantize_q": (C.c_int, [_P, _P, _I64, _I32, _I32, _P, _P, _P]),
@@ -44,6 +45,9 @@ SIGNATURES = {
                                        _I32, _I32, _I32, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "indexer_profile_events": (C.c_int, [_P, _P]),
     "indexer_trace_buffer": (C.c_int, [_P, _SZ]),
+    "indexer_debug_wait_limit": (C.c_int, [C.c_uint64, _I32]),
+    "indexer_debug_decode_plan": (C.c_int, [_I32, _I32, _I32, C.POINTER(_I64),
+                                            C.POINTER(_I32), C.POINTER(_I32)]),
     "indexer_decode_topk_noalloc": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
                                               _I32, _I32, _I32, _P, _P, _P]),
 }
@@ -53,8 +57,9 @@ _lib = None
 
 
 class IndexerError(RuntimeError):
-    def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        msg = f"{fn} failed: {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.status = status
 
 
@@ -94,7 +99,8 @@ def _stream(stream):
 
 def _check(name, st):
     if st != IDX_OK:
-        raise IndexerError(name, st)
+        detail = load().indexer_last_cuda_error().decode() if st == 4 else ""
+        raise IndexerError(name, st, detail)
 
 
 def _host_i32(t):
@@ -269,12 +275,34 @@ def indexer_profile_events(start_event=None, stop_event=None):
 
 def indexer_trace_buffer(buffer=None):
     """Per-CTA trace stamps of later score/select launches go to ``buffer``
-    (a uint64/int64 CUDA tensor of >= 16 * SM-count entries); None turns it off."""
+    (a uint64/int64 CUDA tensor of >= 128 * SM-count entries: 64 per tile
+    stream, two streams per SM); None turns it off."""
     if buffer is None:
         _check("indexer_trace_buffer", load().indexer_trace_buffer(None, 0))
     else:
         _check("indexer_trace_buffer", load().indexer_trace_buffer(
             _ptr(buffer), int(buffer.numel() * buffer.element_size())))
+
+
+def indexer_debug_decode_plan(num_reqs: int, next_n: int, topk: int = MAX_TOPK):
+    """Where the decode work split lives in a workspace: returns (offsets
+    dict of byte offsets, grid, (penalty, divisor))."""
+    offs = (_I64 * 4)()
+    grid = _I32(0)
+    pen = (_I32 * 2)()
+    _check("indexer_debug_decode_plan",
+           load().indexer_debug_decode_plan(num_reqs, next_n, topk, offs, C.byref(grid), pen))
+    names = ("wr_tile_start", "cta_tile", "row_ctas", "cta_row")
+    return dict(zip(names, [int(v) for v in offs])), int(grid.value), (int(pen[0]), int(pen[1]))
+
+
+def indexer_debug_wait_limit(limit_ns: int = 0, stall_split_rows: bool = False):
+    """Score/select launches from this thread give up their waits after
+    ``limit_ns`` (0 restores the 2 s default); with ``stall_split_rows`` their
+    split-row waits wait for a segment that never comes. For failure-detection
+    tests."""
+    _check("indexer_debug_wait_limit",
+           load().indexer_debug_wait_limit(int(limit_ns), 1 if stall_split_rows else 0))
 
 
 def indexer_decode_topk_noalloc(q, weights, index_cache, block_table, row_seq_lens, next_n: int,

@@ -13,6 +13,7 @@ namespace saib {
 
 namespace {
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
 thread_local uint64_t* g_trace = nullptr;
 thread_local size_t g_trace_bytes = 0;
 thread_local cudaEvent_t g_prof_start = nullptr;
@@ -21,18 +22,40 @@ thread_local cudaEvent_t g_prof_stop = nullptr;
 // Score/select launch bracketed by the profiling events when they are set.
 idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map, int nC,
                        cudaStream_t s) {
-  if (g_prof_start && cudaEventRecord(g_prof_start, s) != cudaSuccess) return IDX_ERR_CUDA;
+  if (g_prof_start) {
+    const idx_status st = cuda_status(cudaEventRecord(g_prof_start, s));
+    if (st != IDX_OK) return st;
+  }
   const idx_status st = launch_score(G, logits, p, map, nC, s);
-  if (st == IDX_OK && g_prof_stop && cudaEventRecord(g_prof_stop, s) != cudaSuccess)
-    return IDX_ERR_CUDA;
+  if (st == IDX_OK && g_prof_stop) return cuda_status(cudaEventRecord(g_prof_stop, s));
   return st;
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Give-up time of the kernels' waits: 2 s, or the test setting of this thread;
+// with g_stall_rows the split-row waits wait for a segment that never comes.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+thread_local uint64_t g_wait_ns = kDefaultWaitNs;
+thread_local int32_t g_stall_rows = 0;
+
+// The split-row selection state of a launch: counters, cutoff-bin lists and
+// the wait limit.
+void set_split_lists(ScoreParams* p, uint8_t* ws, const WsLayout& L, int G) {
+  p->row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
+  p->tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
+  p->elist_key = reinterpret_cast<uint32_t*>(ws + L.elist_key);
+  p->elist_idx = reinterpret_cast<int32_t*>(ws + L.elist_idx);
+  p->elist_cap = elist_capacity(G);
+  p->wait_ns = g_wait_ns;
+  p->wait_extra = g_stall_rows ? 1 : 0;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
 
 uint64_t* trace_buffer(size_t* bytes) {
   *bytes = g_trace_bytes;
@@ -49,23 +72,31 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
     return o;
   };
   const int64_t nslots = static_cast<int64_t>(num_ctas) + num_wr;
+  const int64_t nsplit = max_split_rows(num_wr, num_ctas);
   L.wr = take(sizeof(WorkRow) * static_cast<size_t>(num_wr), 256);
   L.wr_tile_start = take(4 * static_cast<size_t>(num_wr + 1), 256);
   L.row_len = take(4 * static_cast<size_t>(rows), 256);
+  // per work row its segment counter, per token row its output / list
+  // position pair and tie counter (all zeroed by the prep kernel)
   L.seg_counter = take(4 * static_cast<size_t>(num_wr), 256);
+  L.row_pos = take(8 * static_cast<size_t>(num_wr) * G, 256);
+  L.tie_count = take(4 * static_cast<size_t>(num_wr) * G, 256);
   L.slot_count = take(4 * static_cast<size_t>(nslots * G), 256);
   L.q8 = take(static_cast<size_t>(rows) * kQRowBytes, 1024);
   L.wprime = take(4 * static_cast<size_t>(rows) * kHeads, 256);
   const size_t cap = static_cast<size_t>(candidate_capacity(G));
   L.slot_key = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
   L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
-  L.row_hist_words = static_cast<size_t>(num_ctas) * G * 1024;
+  L.row_hist_words = static_cast<size_t>(nsplit) * G * 4096;  // four digit levels
   L.row_hist = take(4 * L.row_hist_words, 256);
   L.cta_row = take(4 * static_cast<size_t>(num_ctas), 256);
   L.slot_thrbin = take(4 * static_cast<size_t>(nslots * G), 256);
   L.cta_tile = take(4 * static_cast<size_t>(num_ctas + 1), 256);
   L.row_vs = take(4 * static_cast<size_t>(num_wr + 1), 256);
   L.row_ctas = take(8 * static_cast<size_t>(num_wr), 256);
+  const size_t ecap = static_cast<size_t>(elist_capacity(G));
+  L.elist_key = take(4 * static_cast<size_t>(nsplit) * G * ecap, 256);
+  L.elist_idx = take(4 * static_cast<size_t>(nsplit) * G * ecap, 256);
   L.total = round_up(off, 256);
   return L;
 }
@@ -148,7 +179,10 @@ std::vector<Chunk> plan_chunks(const int32_t* sl, const int32_t* ql, int32_t n, 
   return out;
 }
 
-// Work rows of a chunk: groups of up to 4 consecutive queries of one request.
+// Prefill work rows: up to two consecutive queries of one request.
+constexpr int kPrefillG = 2;
+
+// Work rows of a chunk: groups of up to kPrefillG consecutive queries of one request.
 int64_t chunk_work_rows(const std::vector<int64_t>& qsl, const Chunk& c, int64_t* row_lo,
                         int64_t* row_hi) {
   *row_lo = qsl[c.r0] + c.q0;
@@ -156,12 +190,11 @@ int64_t chunk_work_rows(const std::vector<int64_t>& qsl, const Chunk& c, int64_t
   int64_t nw = 0;
   for (int32_t r = c.r0; r < c.r1; ++r) {
     const int64_t lo = std::max(qsl[r], *row_lo), hi = std::min(qsl[r + 1], *row_hi);
-    if (hi > lo) nw += (hi - lo + 3) / 4;
+    if (hi > lo) nw += (hi - lo + kPrefillG - 1) / kPrefillG;
   }
   return nw;
 }
 
-constexpr int kPrefillG = 4;
 
 idx_status check_common(const void* q, const float* w, const uint8_t* cache, int64_t num_pages,
                         const int32_t* bt, int64_t bt_stride, int32_t bt_width, int32_t num_heads,
@@ -174,6 +207,15 @@ idx_status check_common(const void* q, const float* w, const uint8_t* cache, int
   if (num_heads != kHeads || head_dim != kDim) return IDX_ERR_UNSUPPORTED;
   if (topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
   return IDX_OK;
+}
+
+// A work row that ends inside a CTA's range costs that CTA a segment
+// finalisation (publication, sometimes a buffer cut) worth about `penalty`
+// tiles of streaming; the split gives such CTAs correspondingly fewer tiles.
+// When each CTA streams >= 64 tiles the penalty grows by the share / `div`.
+void decode_row_penalty(bool logits, int next_n, int32_t* penalty, int32_t* div) {
+  *penalty = logits ? 0 : (next_n == 1 ? 6 : 12);
+  *div = logits ? 0 : (next_n == 1 ? 25 : 24);
 }
 
 idx_status decode_common(bool logits, const void* q, const float* weights,
@@ -196,7 +238,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
     return IDX_ERR_INVALID_ARG;
   }
   if (num_reqs == 0) return IDX_OK;
-  const int nC = score_ctas(next_n);
+  const int nC = score_streams();
   const int64_t rows = static_cast<int64_t>(num_reqs) * next_n;
   const WsLayout L = ws_layout(num_reqs, rows, next_n, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
@@ -204,11 +246,8 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   if ((st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // A work row that ends inside a CTA's range costs that CTA a segment
-  // finalisation (publication, often a buffer cut) worth about this many
-  // tiles of streaming; the split gives such CTAs correspondingly fewer tiles.
-  const int32_t row_penalty = logits ? 0 : (next_n == 1 ? 6 : 12);
-  const int32_t row_penalty_div = logits ? 0 : (next_n == 1 ? 25 : 24);
+  int32_t row_penalty, row_penalty_div;
+  decode_row_penalty(logits, next_n, &row_penalty, &row_penalty_div);
   DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
                    topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty,
                    row_penalty_div};
@@ -234,6 +273,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
   p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
   p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
+  set_split_lists(&p, ws, L, next_n);
   p.out_idx = out_idx;
   p.out_row_base = 0;
   p.topk = topk;
@@ -243,7 +283,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   size_t tb = 0;
   p.trace = trace_buffer(&tb);
   if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-  return timed_score(next_n, logits, p, map, nC, s);
+  return timed_score(next_n, logits, p, map, score_grid(), s);
 }
 
 }  // namespace
@@ -259,10 +299,20 @@ idx_status indexer_trace_buffer(void* buffer, size_t bytes) {
   return IDX_OK;
 }
 
+idx_status indexer_debug_wait_limit(uint64_t limit_ns, int32_t stall_split_rows) {
+  g_wait_ns = limit_ns ? limit_ns : kDefaultWaitNs;
+  g_stall_rows = stall_split_rows;
+  return IDX_OK;
+}
+
 idx_status indexer_profile_events(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);
   return IDX_OK;
+}
+
+const char* indexer_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 const char* indexer_status_string(idx_status status) {
@@ -328,8 +378,23 @@ idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int3
   if (!bytes || num_reqs < 0) return IDX_ERR_INVALID_ARG;
   if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk,
-                               score_ctas(next_n));
+                               score_streams());
   *bytes = L.total;
+  return IDX_OK;
+}
+
+idx_status indexer_debug_decode_plan(int32_t num_reqs, int32_t next_n, int32_t topk,
+                                     int64_t* offsets, int32_t* grid, int32_t* penalty) {
+  if (!offsets || !grid || !penalty || num_reqs < 0) return IDX_ERR_INVALID_ARG;
+  if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
+  const int nC = score_streams();
+  const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk, nC);
+  offsets[0] = static_cast<int64_t>(L.wr_tile_start);
+  offsets[1] = static_cast<int64_t>(L.cta_tile);
+  offsets[2] = static_cast<int64_t>(L.row_ctas);
+  offsets[3] = static_cast<int64_t>(L.cta_row);
+  *grid = nC;
+  decode_row_penalty(false, next_n, &penalty[0], &penalty[1]);
   return IDX_OK;
 }
 
@@ -415,7 +480,7 @@ idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
   const idx_status st = prefill_plan(seq_lens_host, query_lens_host, num_reqs, workspace_tokens,
                                      logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows);
   if (st != IDX_OK) return st;
-  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, score_ctas(kPrefillG)).total;
+  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, score_streams()).total;
   return IDX_OK;
 }
 
@@ -440,7 +505,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
                          logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows)) != IDX_OK)
     return st;
   if (plan.empty()) return IDX_OK;
-  const int nC = score_ctas(kPrefillG);
+  const int nC = score_streams();
   const WsLayout L = ws_layout(max_wr, max_rows, kPrefillG, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
   CUtensorMap map;
@@ -465,8 +530,6 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.cta_row = reinterpret_cast<const int32_t*>(ws + L.cta_row);
     p.cta_tile = reinterpret_cast<const int32_t*>(ws + L.cta_tile);
     p.row_ctas = reinterpret_cast<const int2*>(ws + L.row_ctas);
-  p.cta_tile = reinterpret_cast<const int32_t*>(ws + L.cta_tile);
-  p.row_ctas = reinterpret_cast<const int2*>(ws + L.row_ctas);
     p.num_wr = static_cast<int32_t>(nw);
     p.row_len = reinterpret_cast<const int32_t*>(ws + L.row_len);
     p.q8 = ws + L.q8;
@@ -474,10 +537,11 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.seg_counter = reinterpret_cast<int32_t*>(ws + L.seg_counter);
     p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
     p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
-    p.slot_cap = candidate_capacity(4);
+    p.slot_cap = candidate_capacity(kPrefillG);
     p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
     p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
     p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
+    set_split_lists(&p, ws, L, kPrefillG);
     p.out_idx = out_idx;
     p.out_row_base = lo;
     p.topk = topk;
@@ -485,7 +549,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     size_t tb = 0;
     p.trace = trace_buffer(&tb);
     if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-    if ((st = timed_score(kPrefillG, false, p, map, nC, s)) != IDX_OK) return st;
+    if ((st = timed_score(kPrefillG, false, p, map, score_grid(), s)) != IDX_OK) return st;
   }
   return IDX_OK;
 }

@@ -115,6 +115,41 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy view of global memory (including
+// data it acquired from other CTAs) before its later bulk copies read global
+// memory through the async proxy.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until the global counter *ctr reaches `target` (other CTAs of the same
+// cooperative launch add to it after releasing their writes; the load that
+// sees it acquires them). Gives up after limit_ns: sets IDX_DEV_TIMEOUT, raises
+// the CTA abort flag and returns false.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, volatile int* abort_flag,
+                                           uint32_t* err, uint64_t limit_ns) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if ((it & 7) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        set_error(err, IDX_DEV_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // -------------------------------------------------------------------------
 // TMA / bulk copies (global -> shared, completion on an mbarrier)
 // -------------------------------------------------------------------------

@@ -12,22 +12,42 @@
 
 namespace saib {
 
+// Records a failed CUDA call's error for indexer_last_cuda_error (this host
+// thread) and maps it to a status.
+void record_cuda_error(cudaError_t e);
+inline idx_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return IDX_OK;
+  record_cuda_error(e);
+  return IDX_ERR_CUDA;
+}
+
 // Launches `kernel` on `stream` with programmatic stream serialization (the
-// kernel calls pdl_wait() before it reads anything earlier work wrote).
+// kernel calls pdl_wait() before it reads anything earlier work wrote). A
+// cooperative launch (all CTAs resident at once, or the launch fails) is for
+// kernels whose CTAs wait on one another.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                              cudaStream_t stream, Args&&... args) {
+inline cudaError_t launch_pdl_ex(bool cooperative, void (*kernel)(KArgs...), unsigned grid,
+                                 unsigned block, size_t smem, cudaStream_t stream,
+                                 Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cooperative ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  return launch_pdl_ex(false, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
 }
 
 
@@ -52,7 +72,15 @@ struct ScoreParams {
   int32_t* slot_count;           // [nslots, G]
   int32_t* slot_thrbin;          // [nslots, G] row-histogram bin of the segment's final threshold
   int32_t slot_cap;              // entries per slot (the candidate buffer's capacity)
-  uint32_t* row_hist;            // [nC, G, 1024] histograms of split work rows (zeroed by prep)
+  uint32_t* row_hist;            // [nsplit, G, 1024] histograms of split work rows (zeroed by prep)
+  unsigned long long* row_pos;   // [num_wr, G] output positions taken (low word) and cutoff-list
+                                 // entries (high word) so far (zeroed by prep)
+  uint32_t* elist_key;           // [nsplit, G, elist_cap] keys in a split row's cutoff bin
+  int32_t* elist_idx;            // [nsplit, G, elist_cap] their token indices
+  int32_t* tie_count;            // [num_wr, G] equal keys taken at the last digit (zeroed by prep)
+  int32_t elist_cap;             // entries per cutoff-bin list
+  uint64_t wait_ns;              // give-up time of every pipeline and row wait
+  int32_t wait_extra;            // added to the split-row wait target (test hook; 0)
   int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
   int64_t out_row_base;
   int32_t topk;
@@ -69,17 +97,37 @@ enum TraceSlot {
   kTrEndEpi, kTrMergeFallback, kTrMergeUnion, kTrMergeCut, kTrMergeSegs, kTrSeen, kTrMergeCutNs, kTrMergeLoadNs, kTrMergeRadixNs, kTrCompactRadixNs,
   kTrRadixHistNs, kTrRadixBucketNs, kTrRadixPasses, kTrEpiWaitCyc, kTrEpiLdCyc,
   kTrEpiMathCyc, kTrEpiVoteCyc, kTrEpiSelCyc, kTrFinPackNs, kTrFinHistNs, kTrFinCutNs,
-  kTrFinEmitNs, kTrFinPublishNs, kTrMergeTailNs, kTrSlots = 40
+  kTrFinEmitNs, kTrFinPublishNs, kTrMergeTailNs, kTrSelWaitNs, kTrSelScanNs, kTrSelFinalNs,
+  kTrSelRows, kTrSelLast, kTrSelList, kTrSelFallback, kTrRndLoadNs, kTrRndCutNs, kTrRndPassNs,
+  kTrRndAtomicNs, kTrRndArriveNs, kTrRndListSize, kTrPassCountCyc, kTrPassScanCyc,
+  kTrPassWriteCyc, kTrPassSyncCyc, kTrPickHistCyc, kTrPickScanCyc, kTrPickSplitCyc,
+  kTrPickOutCyc, kTrSlots = 64
 };
 
 // Candidate-buffer capacity per token row of the score/select kernel for work
-// rows of G tokens; a published segment slot holds up to this many entries.
-constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : (G == 2 ? 4096 : 2560); }
+// rows of G (1 or 2) tokens; a published segment slot holds up to this many
+// entries.
+constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : 2560; }
+
+// Pipeline stages (128-key tiles in flight) of the score/select kernel.
+constexpr int score_stages(int G) { return G == 1 ? 8 : 4; }
+
+// Capacity of a split row's cutoff-bin list (entries per token row): each of
+// the kernel's two epilogue groups stages a list as key + index pairs in half
+// of the idle stage ring.
+constexpr int elist_capacity(int G) { return score_stages(G) * 16384 / 2 / 8; }
+
+// Split work rows (rows whose tiles several CTAs share) that one launch can
+// have: each starts in a different CTA, and there is at most one per work row.
+inline int64_t max_split_rows(int64_t num_wr, int num_ctas) {
+  return num_wr < num_ctas ? num_wr : num_ctas;
+}
 
 // Workspace carve-up shared by decode and prefill.
 struct WsLayout {
   size_t wr, wr_tile_start, row_len, seg_counter, slot_count, q8, wprime, slot_key, slot_idx;
   size_t row_hist, row_hist_words, cta_row, slot_thrbin, cta_tile, row_vs, row_ctas;
+  size_t row_pos, elist_key, elist_idx, tie_count;
   size_t total;
 };
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
@@ -118,6 +166,8 @@ struct DecodePrepArgs {
   // a segment's drop threshold (more buffer cuts): the penalty grows by the
   // per-CTA tile share divided by this (0: no growth).
   int32_t row_penalty_div;
+  unsigned long long* row_pos = nullptr;  // [num_reqs, next_n], zeroed (set by the launcher)
+  int32_t* tie_count = nullptr;           // [num_reqs, next_n], zeroed (set by the launcher)
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -136,21 +186,23 @@ struct PrefillPrepArgs {
   uint32_t* err;
   int32_t num_ctas;     // grid of the score/select launch that follows
   int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
+  unsigned long long* row_pos = nullptr;  // [num_wr, 2], zeroed (set by the launcher)
+  int32_t* tie_count = nullptr;           // [num_wr, 2], zeroed (set by the launcher)
 };
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);
 
-// G = token rows per work row (1, 2 or 4); logits = write logits instead of selecting.
+// G = token rows per work row (1 or 2); logits = write logits instead of selecting.
 // Thread-local trace buffer set by indexer_trace_buffer (nullptr = off).
 uint64_t* trace_buffer(size_t* bytes);
 
 idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s);
 
-// CTAs per SM the score/select kernel runs with for work rows of G tokens.
-int score_ctas_per_sm(int G);
-
-// CTAs of one score/select launch on the current device.
-inline int score_ctas(int G) { return device_sm_count() * score_ctas_per_sm(G); }
+// The score/select kernel runs one CTA per SM, each CTA two tile streams
+// ("virtual CTAs"): the work split is planned over score_streams() ranges and
+// the launch has score_grid() CTAs.
+inline int score_grid() { return device_sm_count(); }
+inline int score_streams() { return 2 * device_sm_count(); }
 
 }  // namespace saib

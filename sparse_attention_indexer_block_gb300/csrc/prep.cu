@@ -252,6 +252,18 @@ __device__ void plan_ctas(const int32_t* wts, const int32_t* vs, int num_wr, int
   }
 }
 
+// Zeroes work row w's counters: its segment counter and, per token row, its
+// output / cutoff-list position pair and tie counter ([num_wr, G] each).
+__device__ __forceinline__ void zero_row_counters(int32_t* seg_counter,
+                                                  unsigned long long* row_pos,
+                                                  int32_t* tie_count, int G, int w) {
+  seg_counter[w] = 0;
+  for (int g = 0; g < G; ++g) {
+    row_pos[static_cast<int64_t>(w) * G + g] = 0ull;
+    tie_count[static_cast<int64_t>(w) * G + g] = 0;
+  }
+}
+
 // Zeroes n 32-bit words (16-byte aligned) with the blocks after block 0.
 __device__ __forceinline__ void zero_words(uint32_t* p, size_t n) {
   const size_t tid = static_cast<size_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x;
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
         }
         tiles = (maxlen + kTileKeys - 1) / kTileKeys;
         wr[b] = WorkRow{b, b * G, G, maxlen};
-        seg_counter[b] = 0;
+        zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, b);
       }
       int total;
       const int excl = block_exclusive_scan(tiles, &total);
@@ -351,7 +363,7 @@ __device__ __forceinline__ int64_t prefill_len(const PrefillPrepArgs& a, int r, 
   return clamp_len(v, a.bt_width, a.err, report);
 }
 
-// Block 0: work rows of the chunk (up to four consecutive queries of one
+// Block 0: work rows of the chunk (up to two consecutive queries of one
 // request each), their tile prefix and zeroed segment counters. Other blocks:
 // row lengths, q quantisation and the causal rows of short queries.
 __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     int2* __restrict__ row_ctas) {
   pdl_trigger();
   pdl_wait();
-  constexpr int G = 4;
+  constexpr int G = 2;
   const int64_t rows = a.row_hi - a.row_lo;
   if (blockIdx.x == 0) {
     // requests in batches of kPrepThreads: a scan of their work-row counts,
@@ -408,7 +420,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
         }
         wr[idx] = WorkRow{rq, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
         wts[idx] = (maxlen + kTileKeys - 1) / kTileKeys;  // tile count, scanned below
-        seg_counter[idx] = 0;
+        zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, idx);
       }
       carry += total;
       __syncthreads();
@@ -417,7 +429,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     for (int idx = carry + threadIdx.x; idx < a.num_wr; idx += kPrepThreads) {
       wr[idx] = WorkRow{a.req_begin, 0, 0, 0};
       wts[idx] = 0;
-      seg_counter[idx] = 0;
+      zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, idx);
     }
     __syncthreads();
     int run = 0;
@@ -603,31 +615,28 @@ idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, in
                          int64_t num_out_rows, uint32_t* err, cudaStream_t s) {
   int grid = (num_reqs + kPrepWarps - 1) / kPrepWarps;
   if (grid < 1) grid = 1;
-  return launch_pdl(expand_kernel, grid, kPrepThreads, 0, s, seq_lens, decode_lens, num_reqs,
+  return cuda_status(launch_pdl(expand_kernel, grid, kPrepThreads, 0, s, seq_lens, decode_lens, num_reqs,
                     next_n, bt, bt_stride, bt_width, mode, row_lens, row_bt, out_stride,
-                    num_out_rows, err) == cudaSuccess
-             ? IDX_OK
-             : IDX_ERR_CUDA;
+                    num_out_rows, err));
 }
 
 idx_status launch_insert_keys(const __nv_bfloat16* k, const int64_t* slots, int64_t n,
                               uint8_t* cache, int64_t num_pages, uint32_t* err, cudaStream_t s) {
-  return launch_pdl(insert_keys_kernel, prep_grid((n + 3) / 4), kPrepThreads, 0, s, k, slots, n,
-                    cache, num_pages, err) == cudaSuccess
-             ? IDX_OK
-             : IDX_ERR_CUDA;
+  return cuda_status(launch_pdl(insert_keys_kernel, prep_grid((n + 3) / 4), kPrepThreads, 0, s, k, slots, n,
+                    cache, num_pages, err));
 }
 
 idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows, uint8_t* q8,
                                  float* wprime, cudaStream_t s) {
-  return launch_pdl(quantize_plain_kernel, prep_grid(rows * kHeads), kPrepThreads, 0, s, q, w, rows,
-                    q8, wprime) == cudaSuccess
-             ? IDX_OK
-             : IDX_ERR_CUDA;
+  return cuda_status(launch_pdl(quantize_plain_kernel, prep_grid(rows * kHeads), kPrepThreads, 0, s, q, w, rows,
+                    q8, wprime));
 }
 
-idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
+idx_status launch_decode_prep(const DecodePrepArgs& args, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s) {
+  DecodePrepArgs a = args;
+  a.row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
+  a.tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * a.next_n;
   const int grid = 1 + prep_grid(rows * kHeads);
   const cudaError_t e = launch_pdl(
@@ -638,11 +647,14 @@ idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayo
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
       reinterpret_cast<int32_t*>(ws + L.cta_row), reinterpret_cast<int32_t*>(ws + L.cta_tile),
       reinterpret_cast<int32_t*>(ws + L.row_vs), reinterpret_cast<int2*>(ws + L.row_ctas));
-  return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return cuda_status(e);
 }
 
-idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
+idx_status launch_prefill_prep(const PrefillPrepArgs& args, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s) {
+  PrefillPrepArgs a = args;
+  a.row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
+  a.tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
   const int64_t rows = a.row_hi - a.row_lo;
   const int grid = 1 + prep_grid(rows * kHeads);
   const cudaError_t e = launch_pdl(
@@ -653,7 +665,7 @@ idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLa
       reinterpret_cast<uint32_t*>(ws + L.row_hist), L.row_hist_words,
       reinterpret_cast<int32_t*>(ws + L.cta_row), reinterpret_cast<int32_t*>(ws + L.cta_tile),
       reinterpret_cast<int32_t*>(ws + L.row_vs), reinterpret_cast<int2*>(ws + L.row_ctas));
-  return e == cudaSuccess ? IDX_OK : IDX_ERR_CUDA;
+  return cuda_status(e);
 }
 
 }  // namespace saib

@@ -1,25 +1,31 @@
 // Score + select: the persistent kernel of the indexer.
 //
-// Every CTA (one per SM) owns a contiguous range of 128-key tiles of the
-// global tile sequence (work rows in order, each work row cut into
-// ceil(maxlen / 128) tiles). Per CTA, warp-specialised:
-//   warp 0  TMA producer: two 64-token pages per tile (8 KB of fp8 keys via a
-//           3-D tensor map with the 128-byte swizzle, 256 B of fp32 scales via
-//           a bulk copy each) into a ring of shared-memory stages; the work
-//           row's fp8 q image (G x 8 KB) into one of two q slots.
-//   warp 1  MMA issuer: D[128 keys x 64G] = K_tile[128 x 128] . Q[64G x 128]^T
-//           as four tcgen05 kind::f8f6f4 MMAs (K = 32 each) into one of two
-//           tensor-memory accumulators.
-//   warps 2-5  epilogue: each thread owns one key (one TMEM lane), loads its
-//           64 head dots per token, applies ReLU, the folded head weights
-//           w * sq and the key's scale, and feeds the logit to a streaming
-//           top-k: a shared-memory candidate buffer per token, a threshold
-//           below which keys are dropped, and a radix select that shrinks the
-//           buffer back to k when it fills. No logits row leaves the SM.
-// A work row covered by several CTAs is a set of segments: each segment's
-// (<= k) candidates go to a workspace slot and the CTA that finishes the last
-// segment merges the slots through the same buffer (an atomic counter per work
-// row decides which CTA that is).
+// One CTA per SM (tensor-core kernels are scheduled one CTA per SM), launched
+// cooperatively so that all CTAs are resident at once. A CTA runs two
+// independent tile streams: the global sequence of 128-key tiles (work rows in
+// order, each work row cut into ceil(maxlen / 128) tiles) is split into
+// 2 x gridDim contiguous ranges ("virtual CTAs"), and CTA c streams ranges 2c
+// and 2c + 1 side by side, each with its own pipeline. Warp-specialised, per
+// stream j:
+//   warp 2j      TMA producer: two 64-token pages per tile (8 KB of fp8 keys
+//                via a 3-D tensor map with the 128-byte swizzle, 256 B of fp32
+//                scales via a bulk copy each) into the stream's half of the
+//                ring of shared-memory stages; the work row's fp8 q image
+//                (G x 8 KB) into one of the stream's two q slots.
+//   warp 2j + 1  MMA issuer: D[128 keys x 64G] = K_tile[128 x 128] .
+//                Q[64G x 128]^T as four tcgen05 kind::f8f6f4 MMAs (K = 32 each)
+//                into one of the stream's two tensor-memory accumulators.
+//   warps 4-7 (stream 0) and 8-11 (stream 1)  epilogue group: each thread owns
+//           one key (one TMEM lane), loads its 64 head dots per token, applies
+//           ReLU, the folded head weights w * sq and the key's scale, and feeds
+//           the logit to a streaming top-k: a shared-memory candidate buffer
+//           per token, a threshold below which keys are dropped, and a radix
+//           select that shrinks the buffer back to k when it fills. No logits
+//           row leaves the SM.
+// A work row covered by several streams is a set of segments. Each segment
+// publishes its candidates and their row-bin histogram; once a stream has
+// finished all its tiles, the streams that share a split row select it
+// together (select_split_rows).
 //
 // Scoring (the method's statement; the pages name the kernel only):
 //   logit[t, s] = sum_h w[t, h] ReLU(scale_s (q[t, h] . k_s))
@@ -33,64 +39,90 @@ namespace saib {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
-constexpr int kEpiBarrier = 1;       // named barrier id of the epilogue warps
+constexpr int kThreads = 384;        // warps 0-3 TMA / MMA per stream, warps 4-11 two epilogue groups
+constexpr int kEpiBase = 128;        // first epilogue thread
+constexpr int kEpiThreads = 128;     // threads of one epilogue group
 constexpr int kTeardownBarrier = 2;  // used once, by all warps, before TMEM is freed
 constexpr int kSetupBarrier = 3;     // used once, by all warps, after barrier init and TMEM alloc
+constexpr int kJointBarrier = 5;     // both epilogue groups, once, after their streams
+// (named barrier 1 belongs to epilogue group 0, 4 to group 1)
+
+// Epilogue group of this thread (0: warps 4-7, 1: warps 8-11), its thread
+// index in the group and the group's named barrier.
+__device__ __forceinline__ int epi_group() { return (static_cast<int>(threadIdx.x) - kEpiBase) >> 7; }
+__device__ __forceinline__ int epi_tid() { return (static_cast<int>(threadIdx.x) - kEpiBase) & 127; }
+__device__ __forceinline__ void epi_sync() { named_sync(1 + 3 * epi_group(), kEpiThreads); }
 
 template <int G>
 struct Cfg {
   static constexpr int N = 64 * G;
-  // next_n = 1 runs two CTAs per SM (one's selection work overlaps the other's
-  // streaming); wider work rows need the shared memory of a whole SM.
-  static constexpr int kCtasPerSm = G == 1 ? 2 : 1;
-  static constexpr int kStages = G == 1 ? 4 : (G == 2 ? 6 : 4);
+  static constexpr int kStages = score_stages(G);      // both streams
+  static constexpr int kStreamStages = kStages / 2;
   static constexpr int kCap = candidate_capacity(G);  // candidates per token row
-  static constexpr int kRegion = kCap / 4;          // per-warp append region
-  static constexpr int kPer = kRegion / 32;         // region entries per lane
+  static constexpr int kRegion = kCap / 4;            // per-warp append region
+  static constexpr int kPer = kRegion / 32;           // region entries per lane
   // a full buffer is cut to at most k + kSlack entries (whichever bucket
   // boundary the radix search reaches first)
   static constexpr int kSlack = kCap / 24;
   static constexpr int kHistBins = 1024;
-  static constexpr uint32_t kTmemCols = 2 * N <= 128 ? 128u : (2 * N <= 256 ? 256u : 512u);
+  static constexpr uint32_t kTmemCols = 4 * N;  // four accumulators: two per stream
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
+  // Shared memory: the stage ring, the q slots (2 streams x 2), the scales,
+  // then one block per epilogue group, the mbarriers and the CTA-wide words.
   static constexpr int kKvOff = 0;
   static constexpr int kQOff = kKvOff + kStages * 16384;
-  static constexpr int kScaleOff = kQOff + 2 * G * kQRowBytes;
-  static constexpr int kCandKeyOff = kScaleOff + kStages * 512;
-  static constexpr int kCandIdxOff = kCandKeyOff + G * kCap * 4;
-  static constexpr int kWpOff = kCandIdxOff + G * kCap * 4;
-  static constexpr int kHistOff = kWpOff + G * 256;
-  static constexpr int kBarOff = kHistOff + kHistBins * 4;
-  static constexpr int kNumBars = 2 * kStages + 10;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTraceOff = kMiscOff + 256;  // trace slots (kept in shared memory)
-  static constexpr int kSmemBytes = kTraceOff + kTrSlots * 8 + 1024;  // + alignment slack
+  static constexpr int kScaleOff = kQOff + 4 * G * kQRowBytes;
+  static constexpr int kGroupOff = kScaleOff + kStages * 512;
+  static constexpr int kGCandKey = 0;
+  static constexpr int kGCandIdx = kGCandKey + G * kCap * 4;
+  static constexpr int kGWp = kGCandIdx + G * kCap * 4;
+  static constexpr int kGHist = kGWp + G * 256;
+  static constexpr int kGMisc = kGHist + kHistBins * 4;
+  static constexpr int kGTrace = kGMisc + 256;
+  static constexpr int kGroupBytes = kGTrace + kTrSlots * 8;
+  static constexpr int kBarOff = kGroupOff + 2 * kGroupBytes;
+  static constexpr int kNumBars = 2 * kStages + 4 * 4 + 2 + 2;
+  static constexpr int kSharedOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kSharedOff + 64 + 1024;  // + alignment slack
+  // the idle ring, halved, holds one cutoff-bin list per group (key + index)
+  static constexpr int kListCap = kStages * 16384 / 2 / 8;
+  static_assert(kListCap == elist_capacity(G), "cutoff-bin list capacity");
   static_assert(kCap % kEpiThreads == 0, "capacity");
   static_assert(kCap >= IDX_MAX_TOPK, "a slot must hold any k");
-  static_assert(kSmemBytes * kCtasPerSm + 1024 * kCtasPerSm <= 233472, "shared memory");
+  static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(kGroupBytes % 16 == 0 && kGTrace % 8 == 0, "alignment");
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-struct Misc {
+// Words shared by all roles of the CTA.
+struct CtaShared {
   uint32_t tmem_base;
   int abort_flag;
-  int cnt[4];
-  uint32_t thr[4];
-  int sel_out, sel_tie;
+  int epi_done;
+};
+
+// Scratch of one epilogue group.
+struct Misc {
+  int cnt[2];
+  uint32_t thr[2];
   int bucket, above, bcount;
   int is_last;
   int vote[2][4];
   int scan[4];
   uint32_t rmin[4], rmax[4];
-  int cut_n, fallback;
-  int epi_done;
-  int wcnt[4][4];  // [token][epilogue warp] entries in the warp's region
+  int wcnt[2][4];   // [token][epilogue warp] entries in the warp's region
   int staged_uses;  // phases of `staged` used so far
-  int pending_row;  // work row this CTA must merge once its own tiles are done, or -1
+  int pend[2];      // split work rows this group published a segment of (at most two)
+  int npend;
+  int sel_ok;
+  int bcast[4];     // values one thread hands to the group
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
+// The shared memory the roles of stream j (its producer, MMA issuer and
+// epilogue group j) see: the common ring, q slots, scales and barriers, and
+// the group's own candidate buffers, weights, histogram, scratch and trace
+// slots.
 struct Smem {
   uint8_t* kv;
   uint8_t* q;
@@ -99,81 +131,130 @@ struct Smem {
   int32_t* cidx;
   float* wp;
   uint32_t* hist;
-  uint64_t* full;
-  uint64_t* empty;
-  uint64_t* tfull;   // [2]
-  uint64_t* tempty;  // [2]
-  uint64_t* qfull;   // [2]
-  uint64_t* qempty;  // [2]
-  uint64_t* done;
-  uint64_t* staged;  // completion of the bulk copies that stage a merge's candidates
+  uint64_t* full;    // [kStages]: stream j owns stages [j, j + 1) * kStreamStages
+  uint64_t* empty;   // [kStages]
+  uint64_t* tfull;   // [4] accumulator 2j + b of stream j
+  uint64_t* tempty;  // [4]
+  uint64_t* qfull;   // [4] q slot 2j + b of stream j
+  uint64_t* qempty;  // [4]
+  uint64_t* done;    // [2] each stream's MMAs complete
+  uint64_t* staged;  // this group's completion of the bulk copies that stage a list
   Misc* misc;
-  uint64_t* trace;   // this CTA's trace slots (shared memory, copied out at exit), or nullptr
+  CtaShared* cs;
+  uint64_t* trace;   // this stream's trace slots (shared memory, copied out at exit), or nullptr
+  int group;
 };
 
 template <int G>
-__device__ __forceinline__ Smem carve(uint8_t* base) {
+__device__ __forceinline__ Smem carve(uint8_t* base, int group) {
   using C = Cfg<G>;
   Smem s;
   s.kv = base + C::kKvOff;
   s.q = base + C::kQOff;
   s.scales = reinterpret_cast<float*>(base + C::kScaleOff);
-  s.ckey = reinterpret_cast<uint32_t*>(base + C::kCandKeyOff);
-  s.cidx = reinterpret_cast<int32_t*>(base + C::kCandIdxOff);
-  s.wp = reinterpret_cast<float*>(base + C::kWpOff);
-  s.hist = reinterpret_cast<uint32_t*>(base + C::kHistOff);
+  uint8_t* gb = base + C::kGroupOff + group * C::kGroupBytes;
+  s.ckey = reinterpret_cast<uint32_t*>(gb + C::kGCandKey);
+  s.cidx = reinterpret_cast<int32_t*>(gb + C::kGCandIdx);
+  s.wp = reinterpret_cast<float*>(gb + C::kGWp);
+  s.hist = reinterpret_cast<uint32_t*>(gb + C::kGHist);
+  s.misc = reinterpret_cast<Misc*>(gb + C::kGMisc);
+  s.trace = reinterpret_cast<uint64_t*>(gb + C::kGTrace);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::kBarOff);
   s.full = bars;
   s.empty = bars + C::kStages;
   s.tfull = bars + 2 * C::kStages;
-  s.tempty = s.tfull + 2;
-  s.qfull = s.tempty + 2;
-  s.qempty = s.qfull + 2;
-  s.done = s.qempty + 2;
-  s.staged = s.done + 1;
-  s.misc = reinterpret_cast<Misc*>(base + C::kMiscOff);
+  s.tempty = s.tfull + 4;
+  s.qfull = s.tempty + 4;
+  s.qempty = s.qfull + 4;
+  s.done = s.qempty + 4;
+  s.staged = s.done + 2 + group;
+  s.cs = reinterpret_cast<CtaShared*>(base + C::kSharedOff);
+  s.group = group;
   return s;
 }
+
+// One of the CTA's two tile streams: virtual CTA v = 2 * blockIdx.x + j owns
+// tiles [t0, t1) of the launch's tile sequence.
+struct Stream {
+  int64_t t0, t1;
+  int v;
+};
 
 // Row histogram over the top 10 bits of the order-preserving key: sign, the
 // 8 exponent bits and the leading mantissa bit (bins of half a binade).
 constexpr int kRowHistBins = 1024;
 __device__ __forceinline__ int row_bin(uint32_t key) { return static_cast<int>(key >> 22); }
 
+// Index of split work row w (first virtual CTA v_first) among the launch's
+// row histograms and cutoff-bin lists: the work row itself when the launch
+// has no more work rows than virtual CTAs, else its first virtual CTA (split
+// rows start in different virtual CTAs). Either way below
+// max_split_rows(num_wr, 2 * gridDim.x).
+__device__ __forceinline__ int64_t split_slot(const ScoreParams& p, int w, int v_first) {
+  return p.num_wr <= 2 * static_cast<int>(gridDim.x) ? w : v_first;
+}
 
 __device__ __forceinline__ void trace_set(const Smem& s, int slot, uint64_t v) {
   if (s.trace) s.trace[slot] = v;
 }
 
 // ---------------------------------------------------------------------------
-// producer (one thread)
+// producer (one thread per stream)
 // ---------------------------------------------------------------------------
-template <int G>
-__device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Smem& s, int64_t t0,
-                         int64_t t1) {
-  using C = Cfg<G>;
-  volatile int* abort_flag = &s.misc->abort_flag;
-  int stage = 0;
-  uint32_t phase = 0;
-  int last_par[C::kStages];
+
+// The pages of tile `tile` of a work row (-1: none, or outside the cache).
+struct TilePages {
+  int pid[2];
+};
+
+__device__ __forceinline__ TilePages tile_pages(const ScoreParams& p, const int32_t* bt_row,
+                                                int npages, int tile) {
+  TilePages tp;
 #pragma unroll
-  for (int i = 0; i < C::kStages; ++i) last_par[i] = -1;
+  for (int h = 0; h < 2; ++h) {
+    tp.pid[h] = -1;
+    const int pg = 2 * tile + h;
+    if (pg < npages) {
+      const int32_t pv = bt_row[pg];
+      if (pv >= 0 && static_cast<int64_t>(pv) < p.num_pages) tp.pid[h] = pv;
+      else set_error(p.dev_error, IDX_DEV_BAD_BLOCK);
+    }
+  }
+  return tp;
+}
+
+template <int G>
+__device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Smem& s,
+                         const Stream& st) {
+  using C = Cfg<G>;
+  constexpr int S = C::kStreamStages;
+  volatile int* abort_flag = &s.cs->abort_flag;
+  const int j = s.group;
+  uint64_t* full = s.full + j * S;
+  uint64_t* empty = s.empty + j * S;
+  uint8_t* kv = s.kv + j * S * 16384;
+  float* scales = s.scales + j * S * 128;
+  int last_par[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) last_par[i] = -1;
   uint32_t qn[2] = {0, 0};
   int qslot = 0;
 
-  int w = p.cta_row[blockIdx.x];
+  int w = p.cta_row[st.v];
   int64_t rs = p.wr_tile_start[w], re = p.wr_tile_start[w + 1];
   WorkRow wr = p.wr[w];
   bool ok = true;
 
   auto load_q = [&]() -> bool {
-    if (qn[qslot] > 0 && !mbar_wait(&s.qempty[qslot], (qn[qslot] - 1) & 1, abort_flag, p.dev_error))
+    const int q = 2 * j + qslot;
+    if (qn[qslot] > 0 &&
+        !mbar_wait(&s.qempty[q], (qn[qslot] - 1) & 1, abort_flag, p.dev_error, p.wait_ns))
       return false;
     const uint32_t bytes = static_cast<uint32_t>(wr.ntok) * kQRowBytes;
-    mbar_arrive_expect_tx(&s.qfull[qslot], bytes);
+    mbar_arrive_expect_tx(&s.qfull[q], bytes);
     if (bytes)
-      bulk_load(s.q + qslot * G * kQRowBytes, p.q8 + static_cast<int64_t>(wr.row0) * kQRowBytes,
-                bytes, &s.qfull[qslot]);
+      bulk_load(s.q + q * G * kQRowBytes, p.q8 + static_cast<int64_t>(wr.row0) * kQRowBytes,
+                bytes, &s.qfull[q]);
     ++qn[qslot];
     return true;
   };
@@ -181,8 +262,13 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
   ok = load_q();
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(wr.req) * p.bt_stride;
   int npages = (wr.maxlen + kPageTokens - 1) / kPageTokens;
+  // the page ids of the next tile are read one tile ahead (their load latency
+  // overlaps the wait for a free stage)
+  TilePages next = tile_pages(p, bt_row, npages, static_cast<int>(st.t0 - rs));
 
-  for (int64_t t = t0; ok && t < t1; ++t) {
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t t = st.t0; ok && t < st.t1; ++t) {
     if (*abort_flag) break;
     if (t >= re) {
       do {
@@ -195,37 +281,26 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
       if (!load_q()) break;
       bt_row = p.block_table + static_cast<int64_t>(wr.req) * p.bt_stride;
       npages = (wr.maxlen + kPageTokens - 1) / kPageTokens;
+      next = tile_pages(p, bt_row, npages, static_cast<int>(t - rs));
     }
-    const int i = static_cast<int>(t - rs);
-    if (!mbar_wait(&s.empty[stage], phase ^ 1, abort_flag, p.dev_error)) break;
-    int pid[2];
+    const TilePages cur = next;
+    if (t + 1 < st.t1 && t + 1 < re) next = tile_pages(p, bt_row, npages, static_cast<int>(t + 1 - rs));
+    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
     uint32_t bytes = 0;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      pid[j] = -1;
-      const int pg = 2 * i + j;
-      if (pg < npages) {
-        const int32_t v = bt_row[pg];
-        if (v >= 0 && static_cast<int64_t>(v) < p.num_pages) {
-          pid[j] = v;
-          bytes += kPageValueBytes + 256;
-        } else {
-          set_error(p.dev_error, IDX_DEV_BAD_BLOCK);
-        }
-      }
-    }
-    if (t == t0) trace_set(s, kTrFirstTma, globaltimer_ns());
-    mbar_arrive_expect_tx(&s.full[stage], bytes);
+    for (int h = 0; h < 2; ++h) bytes += cur.pid[h] >= 0 ? kPageValueBytes + 256 : 0;
+    if (t == st.t0) trace_set(s, kTrFirstTma, globaltimer_ns());
+    mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (pid[j] < 0) continue;
-      tma_load_3d(s.kv + stage * 16384 + j * kPageValueBytes, map, 0, 0, pid[j], &s.full[stage]);
-      bulk_load(s.scales + stage * 128 + j * 64,
-                p.cache + static_cast<int64_t>(pid[j]) * kPageBytes + kPageValueBytes, 256,
-                &s.full[stage]);
+    for (int h = 0; h < 2; ++h) {
+      if (cur.pid[h] < 0) continue;
+      tma_load_3d(kv + stage * 16384 + h * kPageValueBytes, map, 0, 0, cur.pid[h], &full[stage]);
+      bulk_load(scales + stage * 128 + h * 64,
+                p.cache + static_cast<int64_t>(cur.pid[h]) * kPageBytes + kPageValueBytes, 256,
+                &full[stage]);
     }
     last_par[stage] = static_cast<int>(phase);
-    if (++stage == C::kStages) {
+    if (++stage == S) {
       stage = 0;
       phase ^= 1;
     }
@@ -234,72 +309,75 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
   // Every copy this thread issued lands before the CTA may exit.
   int dummy = 0;
 #pragma unroll
-  for (int i = 0; i < C::kStages; ++i)
-    if (last_par[i] >= 0) mbar_wait(&s.full[i], static_cast<uint32_t>(last_par[i]), &dummy, p.dev_error);
-  for (int j = 0; j < 2; ++j)
-    if (qn[j] > 0) mbar_wait(&s.qfull[j], (qn[j] - 1) & 1, &dummy, p.dev_error);
+  for (int i = 0; i < S; ++i)
+    if (last_par[i] >= 0)
+      mbar_wait(&full[i], static_cast<uint32_t>(last_par[i]), &dummy, p.dev_error);
+  for (int q = 0; q < 2; ++q)
+    if (qn[q] > 0) mbar_wait(&s.qfull[2 * j + q], (qn[q] - 1) & 1, &dummy, p.dev_error);
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuer (one thread per stream)
 // ---------------------------------------------------------------------------
 template <int G>
-__device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, int64_t t0,
-                           int64_t t1) {
+__device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, const Stream& st) {
   using C = Cfg<G>;
-  volatile int* abort_flag = &s.misc->abort_flag;
-  int stage = 0, acc = 0;
-  uint32_t phase = 0, acc_phase = 0;
+  constexpr int S = C::kStreamStages;
+  volatile int* abort_flag = &s.cs->abort_flag;
+  const int j = s.group;
+  uint64_t* full = s.full + j * S;
+  uint64_t* empty = s.empty + j * S;
+  const uint8_t* kv = s.kv + j * S * 16384;
+  int stage = 0;
+  uint32_t phase = 0;
   uint32_t qn[2] = {0, 0};
   int qslot = 0;
-  int w = p.cta_row[blockIdx.x];
+  int w = p.cta_row[st.v];
   int64_t re = p.wr_tile_start[w + 1];
   bool issued = false;
-  bool ok = mbar_wait(&s.qfull[qslot], qn[qslot] & 1, abort_flag, p.dev_error);
-  for (int64_t t = t0; ok && t < t1; ++t) {
+  bool ok = mbar_wait(&s.qfull[2 * j], 0, abort_flag, p.dev_error, p.wait_ns);
+  for (int64_t t = st.t0, k = 0; ok && t < st.t1; ++t, ++k) {
     if (*abort_flag) break;
     if (t >= re) {
-      mma_commit(&s.qempty[qslot]);  // q slot free once this row's MMAs finish
+      mma_commit(&s.qempty[2 * j + qslot]);  // q slot free once this row's MMAs finish
       ++qn[qslot];
       do {
         ++w;
         re = p.wr_tile_start[w + 1];
       } while (t >= re);
       qslot ^= 1;
-      if (!mbar_wait(&s.qfull[qslot], qn[qslot] & 1, abort_flag, p.dev_error)) break;
+      if (!mbar_wait(&s.qfull[2 * j + qslot], qn[qslot] & 1, abort_flag, p.dev_error, p.wait_ns))
+        break;
     }
-    if (!mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error)) break;
-    if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1, abort_flag, p.dev_error)) break;
+    const int acc = 2 * j + static_cast<int>(k & 1);
+    const uint32_t acc_par = static_cast<uint32_t>((k >> 1) & 1);
+    if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_error, p.wait_ns)) break;
+    if (!mbar_wait(&s.tempty[acc], acc_par ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
     tc_fence_after();
-    if (t == t0) trace_set(s, kTrFirstMma, globaltimer_ns());
-    const uint32_t a_base = smem_u32(s.kv + stage * 16384);
-    const uint32_t b_base = smem_u32(s.q + qslot * G * kQRowBytes);
+    if (k == 0) trace_set(s, kTrFirstMma, globaltimer_ns());
+    const uint32_t a_base = smem_u32(kv + stage * 16384);
+    const uint32_t b_base = smem_u32(s.q + (2 * j + qslot) * G * kQRowBytes);
     const uint32_t d = tmem + static_cast<uint32_t>(acc * C::N);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_f8(d, sw128_kmajor_desc(a_base + kk * 32), sw128_kmajor_desc(b_base + kk * 32),
              C::kIdesc, kk > 0 ? 1u : 0u);
-    mma_commit(&s.empty[stage]);
+    mma_commit(&empty[stage]);
     mma_commit(&s.tfull[acc]);
     issued = true;
-    if (++stage == C::kStages) {
+    if (++stage == S) {
       stage = 0;
       phase ^= 1;
-    }
-    if (++acc == 2) {
-      acc = 0;
-      acc_phase ^= 1;
     }
   }
   trace_set(s, kTrLastMma, globaltimer_ns());
   if (issued) {
-    // all MMAs of this CTA complete before tensor memory is released
-    mma_commit(s.done);
+    // all of this stream's MMAs complete before tensor memory is released
+    mma_commit(&s.done[j]);
     int dummy = 0;
-    mbar_wait(s.done, 0, &dummy, p.dev_error);
+    mbar_wait(&s.done[j], 0, &dummy, p.dev_error);
   }
 }
-
 // ---------------------------------------------------------------------------
 // epilogue: streaming top-k over a shared-memory candidate buffer
 // ---------------------------------------------------------------------------
@@ -307,7 +385,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, i
 // Exclusive scan of one int per epilogue thread (in thread order); *total gets
 // the sum. Contains one epilogue barrier.
 __device__ __forceinline__ int epi_exclusive_scan(Misc* m, int v, int* total) {
-  const int lane = threadIdx.x & 31, ew = (threadIdx.x - 64) >> 5;
+  const int lane = threadIdx.x & 31, ew = epi_tid() >> 5;
   int x = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -315,7 +393,7 @@ __device__ __forceinline__ int epi_exclusive_scan(Misc* m, int v, int* total) {
     if (lane >= off) x += y;
   }
   if (lane == 31) m->scan[ew] = x;
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   int before = 0, tot = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -334,7 +412,7 @@ __device__ __forceinline__ int epi_exclusive_scan(Misc* m, int v, int* total) {
 // from the top. The histogram is zero again after.
 __device__ __forceinline__ void take_bucket(uint32_t* hist, Misc* m, int nb, int remaining,
                                             int* bucket, int* above, int* bcount) {
-  const int et = threadIdx.x - 64;
+  const int et = epi_tid();
   const int per = (nb + kEpiThreads - 1) / kEpiThreads;
   const int hi = nb - 1 - et * per;  // thread et: bins [hi - per + 1, hi], from the top
   const int lo = max(hi - per + 1, 0);
@@ -364,31 +442,10 @@ __device__ __forceinline__ void take_bucket(uint32_t* hist, Misc* m, int nb, int
       acc += c[j];
     }
   }
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   *bucket = m->bucket;
   *above = m->above;
   *bcount = m->bcount;
-}
-
-// Digit layout of the fixed MSB-first radix select over 32-bit keys: 10, 10,
-// 10 and 2 bits.
-constexpr int kFixedPasses = 4;
-__device__ __forceinline__ int digit_shift(int pass) {
-  return pass == 0 ? 22 : (pass == 1 ? 12 : (pass == 2 ? 2 : 0));
-}
-__device__ __forceinline__ int digit_bins(int pass) { return pass == 3 ? 4 : 1024; }
-
-// Warp-aggregated reservation of one slot per lane with `take` set; returns
-// the lane's position (counter base + rank among the taking lanes).
-__device__ __forceinline__ int warp_reserve(int* counter, bool take) {
-  const int lane = threadIdx.x & 31;
-  const unsigned tm = __ballot_sync(0xffffffffu, take);
-  if (!tm) return 0;
-  const int leader = __ffs(tm) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(tm));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return base + __popc(tm & ((1u << lane) - 1u));
 }
 
 // The K-th largest among the member keys of all epilogue threads (member j of
@@ -405,7 +462,7 @@ template <int N>
 __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, int K,
                           uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out,
                           int slack = 0) {
-  const int et = threadIdx.x - 64;
+  const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
   Misc* m = s.misc;
   uint32_t mn = 0xffffffffu, mx = 0u;
@@ -421,7 +478,7 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
     m->rmin[ew] = mn;
     m->rmax[ew] = mx;
   }
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   mn = min(min(m->rmin[0], m->rmin[1]), min(m->rmin[2], m->rmin[3]));
   mx = max(max(m->rmax[0], m->rmax[1]), max(m->rmax[2], m->rmax[3]));
   int hi = mx >= mn ? 32 - __clz(mx - mn) : 0;  // bits of v still to resolve
@@ -438,7 +495,7 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
       if (((mem >> j) & 1) && (v >> hi) == pre)
         atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
     }
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
     const uint64_t tb = (et == 0 && s.trace) ? globaltimer_ns() : 0;
     int bucket, above, bcount;
     take_bucket(s.hist, m, nb, remaining, &bucket, &above, &bcount);
@@ -480,7 +537,7 @@ template <int G>
 __device__ int compact(const Smem& s, int g, int K, int slack = 0) {
   using C = Cfg<G>;
   static_assert(C::kPer <= 64, "member mask");
-  const int et = threadIdx.x - 64;
+  const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
   uint32_t* ck = s.ckey;
   int32_t* ci = s.cidx;
@@ -539,7 +596,7 @@ __device__ int compact(const Smem& s, int g, int K, int slack = 0) {
       ++pos;
     }
   }
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   if (et == 0) {
     m->cnt[g] = kept;
     if (select) m->thr[g] = max(m->thr[g], mn + static_cast<uint32_t>(pre << hi));
@@ -549,75 +606,15 @@ __device__ int compact(const Smem& s, int g, int K, int slack = 0) {
     }
   }
   if (lane == 0) m->wcnt[g][ew] = (kept - ew + 3) >> 2;
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   return kept;
-}
-
-template <int G>
-__device__ void merge_slots(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
-                            int64_t c_last, int32_t* out) {
-  const int et = threadIdx.x - 64;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  uint32_t prefix = 0, mask = 0;
-  int remaining = K;
-  int total = 0;
-  for (int64_t c = c_first; c <= c_last; ++c) total += __ldcg(&p.slot_count[(c + w) * G + g]);
-  if (total > K) {
-#pragma unroll 1
-    for (int pass = 0; pass < kFixedPasses; ++pass) {
-      const int shift = digit_shift(pass), nb = digit_bins(pass);
-      for (int64_t c = c_first; c <= c_last; ++c) {
-        const int64_t slot = (c + w) * G + g;
-        const int n = __ldcg(&p.slot_count[slot]);
-        const uint32_t* keys = p.slot_key + slot * p.slot_cap;
-#pragma unroll 4
-        for (int e = et; e < n; e += kEpiThreads) {
-          const uint32_t u = __ldcg(&keys[e]);
-          if ((u & mask) == prefix)
-            atomicAdd(&s.hist[(u >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-        }
-      }
-      named_sync(kEpiBarrier, kEpiThreads);
-      int bucket, above, bcount;
-      take_bucket(s.hist, s.misc, nb, remaining, &bucket, &above, &bcount);
-      prefix |= static_cast<uint32_t>(bucket) << shift;
-      mask |= static_cast<uint32_t>(nb - 1) << shift;
-      remaining -= above;
-      if (bcount == remaining) break;
-    }
-  }
-  if (et == 0) {
-    m->sel_out = 0;
-    m->sel_tie = 0;
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  for (int64_t c = c_first; c <= c_last; ++c) {
-    const int64_t slot = (c + w) * G + g;
-    const int n = __ldcg(&p.slot_count[slot]);
-    const uint32_t* keys = p.slot_key + slot * p.slot_cap;
-    const int32_t* idxs = p.slot_idx + slot * p.slot_cap;
-    for (int e0 = 0; e0 < n; e0 += kEpiThreads) {
-      const int e = e0 + et;
-      const uint32_t u = e < n ? __ldcg(&keys[e]) : 0u;
-      const uint32_t top = u & mask;
-      const bool gt = e < n && top > prefix;
-      const bool eq = e < n && top == prefix;
-      const int tie_rank = warp_reserve(&m->sel_tie, eq);
-      const bool take = gt || (eq && tie_rank < remaining);
-      const int pos = warp_reserve(&m->sel_out, take);
-      if (take && pos < K) out[pos] = __ldcg(&idxs[e]);
-    }
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  for (int e = m->sel_out + et; e < K; e += kEpiThreads) out[e] = -1;
 }
 
 // Entries of token g's buffer sit in four per-warp regions (counts in
 // wcnt[g][*]); warp w's lane l visits its region's entries l, l + 32, ...
 template <int G>
 __device__ __forceinline__ int region_entries(const Smem& s, int g) {
-  const int lane = threadIdx.x & 31, ew = (threadIdx.x - 64) >> 5;
+  const int lane = threadIdx.x & 31, ew = epi_tid() >> 5;
   const int nw = s.misc->wcnt[g][ew];
   return lane < nw ? (nw - lane + 31) / 32 : 0;
 }
@@ -627,7 +624,7 @@ template <int G>
 __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& wr,
                            const bool (&active)[G]) {
   using C = Cfg<G>;
-  const int et = threadIdx.x - 64;
+  const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -640,7 +637,7 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
     for (int j = 0; j < mine; ++j)
       if (pos < p.topk) o[pos++] = rx[lane + 32 * j];
     for (int e = total + et; e < p.topk; e += kEpiThreads) o[e] = -1;
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
   }
 }
 
@@ -650,7 +647,7 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
 // Row-histogram bins held by epilogue thread et in the cutoff scans:
 // [hi - kCutPer + 1, hi] with hi = kRowHistBins - 1 - et * kCutPer, c[j] = bin hi - j.
 constexpr int kCutPer = kRowHistBins / kEpiThreads;
-__device__ __forceinline__ int cut_hi() { return kRowHistBins - 1 - (threadIdx.x - 64) * kCutPer; }
+__device__ __forceinline__ int cut_hi() { return kRowHistBins - 1 - epi_tid() * kCutPer; }
 
 __device__ __forceinline__ void load_row_bins(const uint32_t* gh, int (&c)[kCutPer]) {
   const int hi = cut_hi();
@@ -659,12 +656,15 @@ __device__ __forceinline__ void load_row_bins(const uint32_t* gh, int (&c)[kCutP
 }
 
 // row_cutoff over counts already held by the threads (c as in load_row_bins).
+// *bcount (nullable) gets the cutoff bin's count when the cutoff is the bin
+// holding the K-th key (not raised to `floor`), else -1.
 __device__ __forceinline__ void row_cutoff_vals(const int (&c)[kCutPer], Misc* m, int K, int floor,
-                                                int* cut, int* above) {
-  const int et = threadIdx.x - 64;
+                                                int* cut, int* above, int* bcount = nullptr) {
+  const int et = epi_tid();
   if (et == 0) {
     m->bucket = -1;
     m->above = 0;
+    m->bcount = -1;
   }
   const int hi = cut_hi();
   int local = 0, local_above_floor = 0;
@@ -682,18 +682,20 @@ __device__ __forceinline__ void row_cutoff_vals(const int (&c)[kCutPer], Misc* m
       if (acc + c[j] >= K) {
         m->bucket = hi - j;
         m->above = acc;
+        m->bcount = c[j];
         break;
       }
       acc += c[j];
     }
   }
-  named_sync(kEpiBarrier, kEpiThreads);
-  int cb = m->bucket, ab = m->above;
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
+  int cb = m->bucket, ab = m->above, bc = m->bcount;
+  epi_sync();
+  if (bcount) *bcount = cb >= floor ? bc : -1;
   if (cb < floor) {
     int tot_above;
     epi_exclusive_scan(m, local_above_floor, &tot_above);
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
     cb = floor;
     ab = tot_above;
   }
@@ -702,598 +704,82 @@ __device__ __forceinline__ void row_cutoff_vals(const int (&c)[kCutPer], Misc* m
 }
 
 __device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, int floor,
-                                           int* cut, int* above) {
+                                           int* cut, int* above, int* bcount = nullptr) {
   int c[kCutPer];
   load_row_bins(gh, c);
-  row_cutoff_vals(c, m, K, floor, cut, above);
+  row_cutoff_vals(c, m, K, floor, cut, above, bcount);
 }
 
-// Merges work row w's segment slots for token g into `out` (K indices).
-// The row histogram is complete here (every segment added its keys before it
-// counted itself finished), so its cutoff bin is exact. The union of the
-// slots' keys is loaded into registers in one batch of independent loads;
-// entries in bins above the cutoff are selected outright, radix_kth picks the
-// missing ones among the cutoff bin's entries, and the selected entries'
-// indices are gathered in a second batch. Unions larger than the register
-// batch, or a histogram that disagrees with the slots, go to merge_slots.
-template <int G>
-__device__ void merge_row(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
-                          int64_t c_last, const uint32_t* gh, int32_t* out) {
-  constexpr int kMB = 48;  // union entries per thread (6144 per CTA)
-  const int et = threadIdx.x - 64;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  const int nseg = static_cast<int>(c_last - c_first + 1);
-  // The histogram holds every segment's final buffer, which is exact for all
-  // bins above each segment's threshold bin; the row's cutoff is at or above
-  // the highest of those bins.
-  int floor = et < nseg ? __ldcg(&p.slot_thrbin[(c_first + et + w) * G + g]) : -1;
-  floor = __reduce_max_sync(0xffffffffu, floor);
-  if ((et & 31) == 0) m->scan[et >> 5] = floor;
-  named_sync(kEpiBarrier, kEpiThreads);
-  floor = max(max(m->scan[0], m->scan[1]), max(m->scan[2], m->scan[3]));
-  named_sync(kEpiBarrier, kEpiThreads);
-  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  int cut, above;
-  row_cutoff(gh, m, K, floor, &cut, &above);
-  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  if (et == 0 && s.trace) s.trace[kTrMergeCutNs] += tq1 - tq0;
-  if (cut < 0 || nseg > kEpiThreads) {
-    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
-    merge_slots<G>(p, s, w, g, c_first, c_last, out);
-    return;
-  }
-  // start offsets of the segments' entries in one flat index space, kept in
-  // the token's candidate buffer (idle here; the histogram is radix_kth's)
-  int* seg_start = reinterpret_cast<int*>(s.ckey + g * Cfg<G>::kCap);
-  const int my_n = et < nseg ? __ldcg(&p.slot_count[(c_first + et + w) * G + g]) : 0;
-  int total;
-  const int my_start = epi_exclusive_scan(m, my_n, &total);
-  if (et <= nseg) seg_start[et] = et < nseg ? my_start : total;
-  named_sync(kEpiBarrier, kEpiThreads);
-  if (total > kMB * kEpiThreads) {
-    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1000000;
-    merge_slots<G>(p, s, w, g, c_first, c_last, out);
-    return;
-  }
-  uint32_t u[kMB];
-  uint64_t gt_mask = 0, eq_mask = 0;
-  {
-    int seg = 0;
-#pragma unroll
-    for (int j = 0; j < kMB; ++j) {
-      const int i = j * kEpiThreads + et;
-      u[j] = 0u;
-      if (i < total) {
-        while (seg_start[seg + 1] <= i) ++seg;
-        const int64_t slot = (c_first + seg + w) * G + g;
-        u[j] = __ldcg(&p.slot_key[slot * p.slot_cap + (i - seg_start[seg])]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kMB; ++j) {
-      const bool valid = j * kEpiThreads + et < total;
-      const int b = row_bin(u[j]);
-      if (valid && b > cut) gt_mask |= 1ull << j;
-      if (valid && b == cut) eq_mask |= 1ull << j;
-    }
-  }
-  int tge;
-  epi_exclusive_scan(m, (__popcll(eq_mask) << 16) | __popcll(gt_mask), &tge);
-  const int t_gt = tge & 0xffff, t_eq = tge >> 16;
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int need = K - above;
-  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  if (et == 0 && s.trace) {
-    s.trace[kTrMergeLoadNs] += tq2 - tq1;
-    s.trace[kTrMergeUnion] += static_cast<uint64_t>(total);
-    s.trace[kTrMergeCut] += static_cast<uint64_t>(t_eq);
-    s.trace[kTrMergeSegs] += static_cast<uint64_t>(nseg);
-  }
-  if (t_gt != above || t_eq < need) {
-    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1000;
-    merge_slots<G>(p, s, w, g, c_first, c_last, out);
-    return;
-  }
-  // among the cutoff bin's entries: the `need` largest
-  uint32_t mn = 0;
-  int hi = 0, remaining = need;
-  uint64_t pre = 0;
-  if (t_eq > need) radix_kth(s, u, eq_mask, need, &mn, &hi, &pre, &remaining);
-  const uint64_t tq3 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  if (et == 0 && s.trace) s.trace[kTrMergeRadixNs] += tq3 - tq2;
-  uint64_t take_mask = gt_mask;
-  int n_tie = 0;
-#pragma unroll
-  for (int j = 0; j < kMB; ++j) {
-    if (!((eq_mask >> j) & 1)) continue;
-    const uint64_t top = t_eq > need ? static_cast<uint64_t>(u[j] - mn) >> hi : 0;
-    if (top > pre) take_mask |= 1ull << j;
-    else if (top == pre) ++n_tie;
-  }
-  int tt;
-  const int tie_before = epi_exclusive_scan(m, n_tie, &tt);
-  named_sync(kEpiBarrier, kEpiThreads);
-  int take_tie = min(max(remaining - tie_before, 0), n_tie);
-#pragma unroll
-  for (int j = 0; j < kMB; ++j) {
-    if (!((eq_mask >> j) & 1) || ((take_mask >> j) & 1)) continue;
-    const uint64_t top = t_eq > need ? static_cast<uint64_t>(u[j] - mn) >> hi : 0;
-    if (top == pre && take_tie > 0) {
-      take_mask |= 1ull << j;
-      --take_tie;
-    }
-  }
-  int t_take;
-  int pos = epi_exclusive_scan(m, __popcll(take_mask), &t_take);
-  {
-    // gather the selected entries' indices in one batch (into the key
-    // registers, which are no longer needed), then store them
-    int seg = 0;
-#pragma unroll
-    for (int j = 0; j < kMB; ++j) {
-      if ((take_mask >> j) & 1) {
-        const int i = j * kEpiThreads + et;
-        while (seg_start[seg + 1] <= i) ++seg;
-        const int64_t slot = (c_first + seg + w) * G + g;
-        u[j] = static_cast<uint32_t>(__ldcg(&p.slot_idx[slot * p.slot_cap + (i - seg_start[seg])]));
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kMB; ++j) {
-      if ((take_mask >> j) & 1) {
-        if (pos < K) out[pos] = static_cast<int32_t>(u[j]);
-        ++pos;
-      }
-    }
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
-  named_sync(kEpiBarrier, kEpiThreads);
-  if (et == 0 && s.trace) s.trace[kTrMergeTailNs] += globaltimer_ns() - tq3;
+// ---------------------------------------------------------------------------
+// segments of split rows
+// ---------------------------------------------------------------------------
+
+// Words of one (split row, token row) histogram block: the row-bin histogram
+// of the candidates (level 0) and the finer levels the selection may need.
+constexpr int kRowHistWords = 4 * kRowHistBins;
+
+// The key digits the split-row selection resolves, most significant first:
+// level 0 is the row bin (bits 31..22), then bits 21..12, 11..2 and 1..0.
+__device__ __forceinline__ int level_shift(int L) {
+  return L == 0 ? 22 : (L == 1 ? 12 : (L == 2 ? 2 : 0));
+}
+__device__ __forceinline__ int level_bins(int L) { return L == 3 ? 4 : 1024; }
+// Key u has the resolved prefix `pre` of the levels above L.
+__device__ __forceinline__ bool level_match(uint32_t u, int L, uint32_t pre) {
+  return L == 0 || (u >> level_shift(L - 1)) == pre;
+}
+__device__ __forceinline__ uint32_t level_digit(uint32_t u, int L) {
+  return (u >> level_shift(L)) & static_cast<uint32_t>(level_bins(L) - 1);
 }
 
-// Where the selection finds each staged key's token index.
-enum StagedIdx {
-  kIdxStaged = 0,     // aux[e]: the indices were staged beside the keys
-  kIdxSlotByPos = 1,  // slot entry at staged position e (segment offsets in cidx)
-  kIdxSlotBySrc = 2,  // slot entry at union position aux[e] (segment offsets in cidx)
-};
-
-// Selection of work row w's k (token g) from keys staged in shared memory:
-// keys[0, total_r) (total_r a multiple of 4 and keys 16-byte aligned; key 0
-// is padding), cut = the row's exact cutoff bin and above = the count in the
-// bins above it. Returns false (having written nothing final) when the staged
-// keys disagree with the histogram.
+// End of this stream's part of work row w. A row held whole by this stream
+// is cut to k and written out. A split row's segment publishes: its final
+// buffer is added to the row histogram (level 0) and copied whole to the
+// segment's slot (keys and token indices), then the segment counts itself in
+// the row's counter; the selection runs once this stream has all its tiles
+// done (select_split_rows).
 template <int G>
-__device__ bool select_staged(const ScoreParams& p, const Smem& s, int w, int g, int64_t c_first,
-                              int nseg, const uint32_t* keys, const int32_t* aux, int total_r,
-                              int cut, int above, int32_t* out, int mode, uint64_t tq0) {
-  const int et = threadIdx.x - 64;
-  const int lane = threadIdx.x & 31;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  const int32_t* seg_off = s.cidx;
-  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // One pass classifies every key against the cutoff bin (keys carry the row
-  // bin in their top 10 bits) and histograms the next 10 bits of the keys in
-  // it; further passes resolve 10 and then 2 more bits only while the bucket
-  // holding the K-th key is not taken whole. Four keys per 16-byte load.
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int n4 = total_r >> 2;
-  const uint32_t ucut = static_cast<uint32_t>(cut);
-  int n_gt = 0, n_eq = 0;
-  for (int e = et; e < n4; e += kEpiThreads) {
-    const uint4 q = k4[e];
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (u[c] == 0u) continue;
-      const uint32_t b = u[c] >> 22;
-      n_gt += b > ucut ? 1 : 0;
-      if (b == ucut) {
-        ++n_eq;
-        atomicAdd(&s.hist[(u[c] >> 12) & 1023u], 1u);
-      }
-    }
-  }
-  int tge;
-  epi_exclusive_scan(m, (n_eq << 16) | n_gt, &tge);
-  const int t_gt = tge & 0xffff, t_eq = tge >> 16;
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int need = K - above;
-  if (et == 0 && s.trace) {
-    s.trace[kTrMergeLoadNs] += tq1 - tq0;
-    s.trace[kTrMergeUnion] += static_cast<uint64_t>(total_r);
-    s.trace[kTrMergeCut] += static_cast<uint64_t>(t_eq);
-    s.trace[kTrMergeSegs] += static_cast<uint64_t>(nseg);
-  }
-  const bool fail = t_gt != above || t_eq < need;
-  if (fail || t_eq == need) {
-    for (int b = et; b < 1024; b += kEpiThreads) s.hist[b] = 0u;
-    named_sync(kEpiBarrier, kEpiThreads);
-    if (fail) return false;
-  }
-  // a key is in when key >> sh > pre; keys with key >> sh == pre are tied and
-  // `remaining` of them complete K (all of them when all_tied)
-  int sh = 22, remaining = need;
-  uint32_t pre = ucut;
-  bool all_tied = true;
-  if (t_eq > need) {
-    int bucket, ab, bc;
-    take_bucket(s.hist, m, 1024, remaining, &bucket, &ab, &bc);
-    pre = (pre << 10) | static_cast<uint32_t>(bucket);
-    sh = 12;
-    remaining -= ab;
-    if (bc != remaining) {
-      for (int e = et; e < n4; e += kEpiThreads) {
-        const uint4 q = k4[e];
-        const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (u[c] != 0u && (u[c] >> 12) == pre) atomicAdd(&s.hist[(u[c] >> 2) & 1023u], 1u);
-      }
-      named_sync(kEpiBarrier, kEpiThreads);
-      take_bucket(s.hist, m, 1024, remaining, &bucket, &ab, &bc);
-      pre = (pre << 10) | static_cast<uint32_t>(bucket);
-      sh = 2;
-      remaining -= ab;
-      if (bc != remaining) {
-        for (int e = et; e < n4; e += kEpiThreads) {
-          const uint4 q = k4[e];
-          const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (u[c] != 0u && (u[c] >> 2) == pre) atomicAdd(&s.hist[u[c] & 3u], 1u);
-        }
-        named_sync(kEpiBarrier, kEpiThreads);
-        take_bucket(s.hist, m, 4, remaining, &bucket, &ab, &bc);
-        pre = (pre << 2) | static_cast<uint32_t>(bucket);
-        sh = 0;
-        remaining -= ab;
-        all_tied = bc == remaining;
-      }
-    }
-  }
-  const uint64_t tq2 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // output: per key 1 = in, 2 = tied (`remaining` of the tied keys complete
-  // K, in warp-major order). A counting pass gives each warp its output and
-  // tie offsets; the writing pass places keys by ballot ranks (coalesced).
-  auto klass = [&](uint32_t u) -> uint32_t {
-    const uint32_t top = u >> sh;
-    return u == 0u ? 0u : (top > pre ? 1u : (top == pre ? (all_tied ? 1u : 2u) : 0u));
-  };
-  const int ew = et >> 5;
-  int n_in = 0, n_tie = 0;
-  for (int e = et; e < n4; e += kEpiThreads) {
-    const uint4 q = k4[e];
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t k = klass(u[c]);
-      n_in += k == 1u ? 1 : 0;
-      n_tie += k == 2u ? 1 : 0;
-    }
-  }
-  n_in = __reduce_add_sync(0xffffffffu, n_in);
-  n_tie = __reduce_add_sync(0xffffffffu, n_tie);
-  if (lane == 0) {
-    m->scan[ew] = n_in;
-    m->rmax[ew] = static_cast<uint32_t>(n_tie);
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  int tie_base = 0, ties_before_all = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    tie_base += i < ew ? static_cast<int>(m->rmax[i]) : 0;
-  }
-  int out_base = 0, t_take = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int tb = ties_before_all;
-    const int wt = static_cast<int>(m->rmax[i]);
-    const int taken_ties = min(max(remaining - tb, 0), wt);
-    ties_before_all += wt;
-    const int w_take = m->scan[i] + taken_ties;
-    out_base += i < ew ? w_take : 0;
-    t_take += w_take;
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int4* x4 = reinterpret_cast<const int4*>(aux);
-  int32_t* src = reinterpret_cast<int32_t*>(s.ckey);  // staged position of output p
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
-    const int e = e0 + lane;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    int4 xi = make_int4(0, 0, 0, 0);
-    if (e < n4) {
-      q = k4[e];
-      if (mode == kIdxStaged) xi = x4[e];
-    }
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-    const int32_t x[4] = {xi.x, xi.y, xi.z, xi.w};
-    uint32_t kc[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) kc[c] = klass(u[c]);
-    if (!all_tied) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t tm = __ballot_sync(0xffffffffu, kc[c] == 2u);
-        if (kc[c] == 2u) kc[c] = tie_base + __popc(tm & lt) < remaining ? 1u : 0u;
-        tie_base += __popc(tm);
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t im = __ballot_sync(0xffffffffu, kc[c] == 1u);
-      const int pos = out_base + __popc(im & lt);
-      if (kc[c] == 1u && pos < K) {
-        if (mode == kIdxStaged) out[pos] = x[c];
-        else src[pos] = 4 * e + c;
-      }
-      out_base += __popc(im);
-    }
-  }
-  if (mode != kIdxStaged) {
-    named_sync(kEpiBarrier, kEpiThreads);
-    for (int q = et; q < min(t_take, K); q += kEpiThreads) {
-      int e = src[q];
-      if (mode == kIdxSlotBySrc) e = aux[e];  // staged position -> position in the slots' union
-      int lo = 0, hi = nseg - 1;  // the segment holding staged position e
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (seg_off[mid] <= e) lo = mid;
-        else hi = mid - 1;
-      }
-      const int64_t seg_slot = (c_first + lo + w) * G + g;
-      out[q] = __ldcg(&p.slot_idx[seg_slot * p.slot_cap + (e - seg_off[lo])]);
-    }
-  }
-  for (int e = t_take + et; e < K; e += kEpiThreads) out[e] = -1;
-  named_sync(kEpiBarrier, kEpiThreads);
-  if (et == 0 && s.trace) {
-    s.trace[kTrMergeRadixNs] += tq2 - tq1;
-    s.trace[kTrMergeTailNs] += globaltimer_ns() - tq2;
-  }
-  return true;
-}
-
-
-// Merge for rows with more segments than epilogue threads, or a union of slot
-// entries larger than the ring: every thread walks the slots' union (four
-// coalesced loads in flight per round) and appends the entries in bins at or
-// above the exact cutoff, with their union position, to the ring; the
-// selection then runs on that filtered set and gathers the chosen indices
-// from the slots. Returns false when the filtered set does not fit either.
-template <int G>
-__device__ bool merge_row_gathered(const ScoreParams& p, const Smem& s, int w, int g,
-                                   int64_t c_first, int64_t c_last, const uint32_t* gh,
-                                   int32_t* out) {
+__device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int w,
+                                 const WorkRow& wr, const bool (&active)[G], int64_t rs,
+                                 int64_t re, int64_t t0, int64_t t1) {
   using C = Cfg<G>;
-  constexpr int kStageCap = C::kStages * 16384 / 8;
-  const int et = threadIdx.x - 64;
-  const int lane = threadIdx.x & 31, ew = et >> 5;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  const int nseg = static_cast<int>(c_last - c_first + 1);
-  int32_t* seg_off = s.cidx;  // [nseg + 1] union offsets of the segments
-  if (nseg + 1 > G * C::kCap) return false;
-  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  named_sync(kEpiBarrier, kEpiThreads);
-  int floor = -1, carry = 0;
-  for (int base = 0; base < nseg; base += kEpiThreads) {
-    const int i = base + et;
-    int n = 0;
-    if (i < nseg) {
-      const int64_t sl = (c_first + i + w) * G + g;
-      n = __ldcg(&p.slot_count[sl]);
-      floor = max(floor, __ldcg(&p.slot_thrbin[sl]));
-    }
-    int tot;
-    const int excl = epi_exclusive_scan(m, n, &tot);
-    if (i < nseg) seg_off[i] = carry + excl;
-    carry += tot;
-    named_sync(kEpiBarrier, kEpiThreads);
-  }
-  const int total = carry;
-  if (et == 0) {
-    seg_off[nseg] = total;
-    m->sel_out = 0;
-  }
-  floor = __reduce_max_sync(0xffffffffu, floor);
-  if (lane == 0) m->rmin[ew] = static_cast<uint32_t>(floor);
-  named_sync(kEpiBarrier, kEpiThreads);
-  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
-              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
-  int cut, above;
-  row_cutoff(gh, m, K, floor, &cut, &above);
-  if (cut < 0) return false;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
-  int32_t* src = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
-  const uint32_t lt = (1u << lane) - 1u;
-  int seg = 0;  // this thread's segment; its union positions only grow
-  for (int i0 = ew * 128; i0 < total; i0 += 4 * kEpiThreads) {
-    uint32_t u4[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * 32 + lane;
-      u4[u] = 0u;
-      if (i < total) {
-        while (seg_off[seg + 1] <= i) ++seg;
-        const int64_t sl = (c_first + seg + w) * G + g;
-        u4[u] = __ldcg(&p.slot_key[sl * p.slot_cap + (i - seg_off[seg])]);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * 32 + lane;
-      const bool kp = i < total && row_bin(u4[u]) >= cut;
-      const uint32_t km = __ballot_sync(0xffffffffu, kp);
-      int b = 0;
-      if (lane == 0 && km) b = atomicAdd(&m->sel_out, __popc(km));
-      b = __shfl_sync(0xffffffffu, b, 0);
-      const int pos = b + __popc(km & lt);
-      if (kp && pos < kStageCap) {
-        keys[pos] = u4[u];
-        src[pos] = i;
-      }
-    }
-  }
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int kept = m->sel_out;
-  const int kept_r = (kept + 3) & ~3;
-  if (kept_r > kStageCap) return false;
-  for (int e = kept + et; e < kept_r; e += kEpiThreads) keys[e] = 0u;  // padding
-  named_sync(kEpiBarrier, kEpiThreads);
-  return select_staged<G>(p, s, w, g, c_first, nseg, keys, src, kept_r, cut, above, out,
-                          kIdxSlotBySrc, tq0);
-}
-
-// merge_row for a CTA whose own pipeline has finished (its shared-memory ring
-// is idle): the slots' keys and indices are staged into the ring by one bulk
-// copy per slot and segment (all completing on one mbarrier), then the cutoff
-// classification, the radix select among the cutoff bin's keys and the output
-// all run from shared memory. Returns false (having written nothing) when the
-// union does not fit the ring or the slots disagree with the histogram.
-template <int G>
-__device__ bool merge_row_staged(const ScoreParams& p, const Smem& s, int w, int g,
-                                 int64_t c_first, int64_t c_last, const uint32_t* gh,
-                                 int32_t* out) {
-  using C = Cfg<G>;
-  constexpr int kStageCap = C::kStages * 16384 / 8;  // entries (key + index) in the ring
-  const int et = threadIdx.x - 64;
-  const int lane = threadIdx.x & 31;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  const int nseg = static_cast<int>(c_last - c_first + 1);
-  if (nseg > kEpiThreads) return merge_row_gathered<G>(p, s, w, g, c_first, c_last, gh, out);
-  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  // the segments' counts and threshold bins and this thread's bins of the row
-  // histogram, loaded together
-  const int64_t sl = (c_first + et + w) * G + g;
-  int floor = et < nseg ? __ldcg(&p.slot_thrbin[sl]) : -1;
-  const int my_n = et < nseg ? __ldcg(&p.slot_count[sl]) : 0;
-  int hc[kCutPer];
-  load_row_bins(gh, hc);
-  // staging offsets: each segment's entries start on a 16-byte boundary
-  const int my_r = (my_n + 3) & ~3;
-  int total_r;
-  const int my_off = epi_exclusive_scan(m, my_r, &total_r);
-  if (total_r > 2 * kStageCap) return merge_row_gathered<G>(p, s, w, g, c_first, c_last, gh, out);
-  // Keys and indices are staged when both fit; otherwise only the keys, and
-  // the selected entries' indices are gathered from the slots at the end
-  // (segment staging offsets kept in the idle candidate-index buffer).
-  const bool with_idx = total_r <= kStageCap;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(s.kv);
-  int32_t* idxs = reinterpret_cast<int32_t*>(s.kv) + kStageCap;
-  int32_t* seg_off = s.cidx;
-  if (!with_idx && et <= nseg) seg_off[et] = et < nseg ? my_off : total_r;
-  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
-  named_sync(kEpiBarrier, kEpiThreads);
-  const int use = m->staged_uses;
-  if (et < nseg && my_n > 0) {
-    const uint32_t bytes = static_cast<uint32_t>(my_r) * 4u;
-    bulk_load(keys + my_off, p.slot_key + sl * p.slot_cap, bytes, s.staged);
-    if (with_idx) bulk_load(idxs + my_off, p.slot_idx + sl * p.slot_cap, bytes, s.staged);
-  }
-  if (et == 0)
-    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(total_r) * (with_idx ? 8u : 4u));
-  // while the copies are in flight: the row's cutoff, floored by the
-  // segments' threshold bins (see merge_row)
-  floor = __reduce_max_sync(0xffffffffu, floor);
-  if (lane == 0) m->rmin[et >> 5] = static_cast<uint32_t>(floor);
-  named_sync(kEpiBarrier, kEpiThreads);
-  floor = max(max(static_cast<int>(m->rmin[0]), static_cast<int>(m->rmin[1])),
-              max(static_cast<int>(m->rmin[2]), static_cast<int>(m->rmin[3])));
-  int cut, above;
-  row_cutoff_vals(hc, m, K, floor, &cut, &above);
-  bool ok = true;
-  if (lane == 0) ok = mbar_wait(s.staged, use & 1, &m->abort_flag, p.dev_error);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  // the padding after a segment's entries becomes key 0, which no logit maps to
-  if (ok && et < nseg)
-    for (int e = my_off + my_n; e < my_off + my_r; ++e) keys[e] = 0u;
-  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
-  named_sync(kEpiBarrier, kEpiThreads);
-  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
-  if (et == 0) m->staged_uses = use + 1;
-  if (!all_ok || cut < 0) return false;
-  return select_staged<G>(p, s, w, g, c_first, nseg, keys, with_idx ? idxs : nullptr, total_r, cut,
-                          above, out, with_idx ? kIdxStaged : kIdxSlotByPos, tq0);
-}
-
-// Merge of work row w (every segment published) into its output rows, by a
-// CTA whose own tiles are all done: staged in the idle ring, else from the
-// slots directly.
-template <int G>
-__device__ void merge_work_row(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
-                               const bool (&active)[G], int64_t c_first, int64_t c_last) {
-  const int et = threadIdx.x - 64;
-  const uint64_t tm0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  __threadfence();
-  const uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (!active[g]) continue;
-    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
-    const uint32_t* gh = gh_base + g * kRowHistBins;
-    if (merge_row_staged<G>(p, s, w, g, c_first, c_last, gh, out)) continue;
-    if (et == 0 && s.trace) s.trace[kTrMergeFallback] += 1;
-    merge_row<G>(p, s, w, g, c_first, c_last, gh, out);
-  }
-  if (et == 0 && s.trace) {
-    s.trace[kTrMergeNs] += globaltimer_ns() - tm0;
-    s.trace[kTrMergeN] += 1;
-  }
-}
-
-// End of this CTA's part of work row w: if the CTA holds the whole row, cut
-// each buffer to k and write the output; else publish the candidates that can
-// still make the row's top-k (bins at or above the row histogram's current
-// cutoff; a slot holds a whole buffer) to the segment's slot; the CTA that
-// publishes last merges (now, or at its end if it still has tiles to stream).
-template <int G>
-__device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, const WorkRow& wr,
-                                 const bool (&active)[G], int64_t rs, int64_t re, int64_t t0,
-                                 int64_t t1, int64_t T, int64_t nC) {
-  using C = Cfg<G>;
-  const int et = threadIdx.x - 64;
+  const int et = epi_tid();
   const int K = p.topk;
   Misc* m = s.misc;
   const uint64_t tf0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   const int lane = threadIdx.x & 31, ew = et >> 5;
-  named_sync(kEpiBarrier, kEpiThreads);
-  // A row held whole by this CTA is written from the buffer, cut to exactly
-  // k; a segment publishes its whole buffer (up to kCap entries, the slot's
-  // capacity), filtered by the row histogram's cutoff below.
+  epi_sync();
   const bool whole = rs >= t0 && re <= t1;
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-    if (whole && active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
-      compact<G>(s, g, K);  // cut to k (the regions stay the layout)
-  uint64_t tf1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  if (et == 0 && s.trace) s.trace[kTrFinPackNs] += tf1 - tf0;
   if (whole) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
+        compact<G>(s, g, K);  // cut to k (the regions stay the layout)
     write_rows<G>(p, s, wr, active);
     if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     return;
   }
   const int2 rc = p.row_ctas[w];
-  const int64_t c_first = rc.x, c_last = rc.y;
-  uint32_t* gh_base = p.row_hist + c_first * G * kRowHistBins;
-  const int64_t slot = static_cast<int64_t>(blockIdx.x) + w;
+  uint32_t* gh_base = p.row_hist + split_slot(p, w, rc.x) * G * kRowHistWords;
+  const int64_t slot = static_cast<int64_t>(v) + w;
+  uint64_t tf1 = tf0;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    uint32_t* gh = gh_base + g * kRowHistBins;
+    uint32_t* gh = gh_base + g * kRowHistWords;
     const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
-    // the segment's final buffer joins the row histogram: counted in shared
-    // memory, then the non-zero bins are added to the global one (and the
-    // shared bins zeroed again)
+    int off = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = active[g] ? m->wcnt[g][i] : 0;
+      off += i < ew ? c : 0;
+      tot += c;
+    }
     const int nw = active[g] ? m->wcnt[g][ew] : 0;
+    // the buffer's row-bin histogram: counted in shared memory, then its
+    // non-zero bins added to the row's (and the shared bins zeroed again)
     for (int j = lane; j < nw; j += 32) atomicAdd(&s.hist[row_bin(rk[j])], 1u);
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
     for (int b = et; b < kRowHistBins; b += kEpiThreads) {
       const uint32_t c = s.hist[b];
       if (c) {
@@ -1306,46 +792,14 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
       s.trace[kTrFinHistNs] += now - tf1;
       tf1 = now;
     }
-    // publish the candidates that can still make the row's top-k (bins at or
-    // above the histogram's current cutoff) and the threshold's bin
-    int cut = -1, above = 0;
-    if (active[g]) row_cutoff(gh, m, K, -1, &cut, &above);
-    if (et == 0 && s.trace) {
-      const uint64_t now = globaltimer_ns();
-      s.trace[kTrFinCutNs] += now - tf1;
-      tf1 = now;
+    // the whole buffer to the slot, each warp's region at its offset
+    const int64_t base = (slot * G + g) * p.slot_cap + off;
+    for (int j = lane; j < nw; j += 32) {
+      p.slot_key[base + j] = rk[j];
+      p.slot_idx[base + j] = rx[j];
     }
-    const int64_t base = (slot * G + g) * p.slot_cap;
-    int keep = 0;
-    for (int j = lane; j < nw; j += 32) keep += row_bin(rk[j]) >= cut ? 1 : 0;
-    keep = __reduce_add_sync(0xffffffffu, keep);
-    if (lane == 0) m->scan[ew] = keep;
-    named_sync(kEpiBarrier, kEpiThreads);
-    int pos = 0, tot = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      pos += i < ew ? m->scan[i] : 0;
-      tot += m->scan[i];
-    }
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int j0 = 0; j0 < nw; j0 += 32) {
-      const int j = j0 + lane;
-      const uint32_t u = j < nw ? rk[j] : 0u;
-      const bool kp = j < nw && row_bin(u) >= cut;
-      const uint32_t km = __ballot_sync(0xffffffffu, kp);
-      if (kp) {
-        p.slot_key[base + pos + __popc(km & lt)] = u;
-        p.slot_idx[base + pos + __popc(km & lt)] = rx[j];
-      }
-      pos += __popc(km);
-    }
-    named_sync(kEpiBarrier, kEpiThreads);
-    if (et == 0) {
-      p.slot_count[slot * G + g] = tot;
-      // a buffer that never filled dropped nothing: its histogram is exact
-      p.slot_thrbin[slot * G + g] = m->thr[g] ? row_bin(m->thr[g]) : -1;
-    }
-    named_sync(kEpiBarrier, kEpiThreads);
+    if (et == 0) p.slot_count[slot * G + g] = tot;
+    epi_sync();  // the shared histogram is reused for token g + 1
     if (et == 0 && s.trace) {
       const uint64_t now = globaltimer_ns();
       s.trace[kTrFinEmitNs] += now - tf1;
@@ -1353,43 +807,707 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int w, con
     }
   }
   __threadfence();
-  named_sync(kEpiBarrier, kEpiThreads);
+  epi_sync();
   if (et == 0) {
-    const int old = atomicAdd(&p.seg_counter[w], 1);
-    m->is_last = (old == static_cast<int>(c_last - c_first));
+    __threadfence();
+    atomicAdd(&p.seg_counter[w], 1);
+    if (m->npend < 2) m->pend[m->npend] = w;
+    ++m->npend;
+    if (s.trace) {
+      s.trace[kTrFinPublishNs] += globaltimer_ns() - tf1;
+      s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
+    }
   }
-  named_sync(kEpiBarrier, kEpiThreads);
-  if (et == 0 && s.trace) s.trace[kTrFinPublishNs] += globaltimer_ns() - tf1;
-  // The last segment to publish merges the row. A CTA with tiles still to
-  // stream defers the merge to its end, when its ring is idle for staging.
-  if (m->is_last && re < t1 && et == 0) m->pending_row = w;
-  if (m->is_last && re >= t1) merge_work_row<G>(p, s, w, wr, active, c_first, c_last);
-  if (et == 0 && s.trace) s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
 }
 
-template <int G, bool kLogits>
-__device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int64_t t0, int64_t t1,
-                         int64_t T, int64_t nC) {
-  using C = Cfg<G>;
-  volatile int* abort_flag = &s.misc->abort_flag;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int et = threadIdx.x - 64;
-  const int sub = warp & 3;                 // tensor-memory lanes [32*sub, 32*sub + 32)
-  const int mrow = sub * 32 + lane;         // key of the tile this thread scores
-  const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
-  int stage = 0, acc = 0;
-  uint32_t phase = 0, acc_phase = 0;
+// Warp-aggregated reservation of one position per lane with `take` set on a
+// shared-memory counter; returns the lane's position (counter base + rank
+// among the taking lanes). All lanes of the warp.
+__device__ __forceinline__ int warp_reserve(int* counter, bool take) {
+  const int lane = threadIdx.x & 31;
+  const unsigned tm = __ballot_sync(0xffffffffu, take);
+  if (!tm) return 0;
+  const int leader = __ffs(tm) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(tm));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  return base + __popc(tm & ((1u << lane) - 1u));
+}
 
-  int w = p.cta_row[blockIdx.x];
+// The `need` largest of the n keys staged at keys[0, n_r) (n_r = n rounded up
+// to 4, padding keys 0; every key shares its top 10 bits) with their indices
+// at idxs[], written to out[0, need) in no particular order. One pass
+// histograms bits 21..10 (4096 bins, in the group's idle candidate buffers)
+// and finds the bucket b1 of the need-th key; a second pass writes every key
+// above b1 and collects b1's keys in a short list, from which the missing
+// ones are taken by exact rank (equal keys in list order). A bucket too large
+// for the short list is resolved over bits 9..0 instead. Returns false when
+// the keys disagree with n. All threads of the group.
+template <int G>
+__device__ bool pick_from_list(const ScoreParams& p, const Smem& s, const uint32_t* keys,
+                               const int32_t* idxs, int n, int n_r, int need, int32_t* out) {
+  constexpr int kTieCap = 256;
+  static_assert(2 * G * Cfg<G>::kCap >= 4096 + 2 * kTieCap, "scratch fits the buffers");
+  const int et = epi_tid();
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  Misc* m = s.misc;
+  const bool tr = et == 0 && s.trace;
+  long long cy0 = tr ? clock64() : 0;
+  auto cyc = [&](int slot_id) {
+    if (tr) {
+      const long long now = clock64();
+      s.trace[slot_id] += static_cast<uint64_t>(now - cy0);
+      cy0 = now;
+    }
+  };
+  // scratch words over the candidate buffers: 4096 bins, then the short list
+  uint32_t* h = s.ckey;
+  uint32_t* tk = s.ckey + 4096;
+  int32_t* tx = reinterpret_cast<int32_t*>(s.ckey + 4096 + kTieCap);
+  for (int b = et; b < 4096; b += kEpiThreads) h[b] = 0u;
+  if (et == 0) {
+    m->cnt[0] = 0;  // keys written above b1
+    m->cnt[1] = 0;  // keys of b1 listed
+  }
+  epi_sync();
+  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
+  const int4* x4 = reinterpret_cast<const int4*>(idxs);
+  const int n4 = n_r >> 2;
+  for (int e = et; e < n4; e += kEpiThreads) {
+    const uint4 q = k4[e];
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (u[c] != 0u) atomicAdd(&h[(u[c] >> 10) & 4095u], 1u);
+  }
+  epi_sync();
+  cyc(kTrPickHistCyc);
+  // thread et holds bins [4095 - 32 et - 31, 4095 - 32 et], from the top
+  const int top = 4095 - 32 * et;
+  int grp[8];  // sums of its eight 4-bin groups, highest first
+  int local = 0;
+  {
+    const uint4* h4 = reinterpret_cast<const uint4*>(h + top - 31);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint4 c4 = h4[7 - b];
+      grp[b] = static_cast<int>(c4.x + c4.y + c4.z + c4.w);
+      local += grp[b];
+    }
+  }
+  int total;
+  const int excl = epi_exclusive_scan(m, local, &total);
+  if (et == 0) m->bcast[0] = -1;
+  epi_sync();
+  if (excl < need && need <= excl + local) {
+    int acc = excl, gsel = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (acc + grp[b] < need) {
+        acc += grp[b];
+        gsel = b + 1;
+      } else {
+        break;
+      }
+    }
+    for (int b = top - 4 * gsel; b > top - 4 * gsel - 4; --b) {
+      const int c = static_cast<int>(h[b]);
+      if (acc + c >= need) {
+        m->bcast[0] = b;
+        m->bcast[1] = acc;
+        m->bcast[2] = c;
+        break;
+      }
+      acc += c;
+    }
+  }
+  epi_sync();
+  const int b1 = m->bcast[0], above1 = m->bcast[1], cnt1 = m->bcast[2];
+  epi_sync();
+  cyc(kTrPickScanCyc);
+  if (total != n || b1 < 0) return false;
+  const int remaining = need - above1;  // keys of bucket b1 still to take
+  const bool short_list = cnt1 <= kTieCap;
+  // keys above b1 to the output; b1's keys to the short list
+  for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
+    const int e = e0 + lane;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    int4 xi = make_int4(0, 0, 0, 0);
+    if (e < n4) {
+      q = k4[e];
+      xi = x4[e];
+    }
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    const int32_t xv[4] = {xi.x, xi.y, xi.z, xi.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d1 = u[c] != 0u ? static_cast<int>((u[c] >> 10) & 4095u) : -1;
+      const int pos = warp_reserve(&m->cnt[0], d1 > b1);
+      if (d1 > b1 && pos < need) out[pos] = xv[c];
+      const int lp = warp_reserve(&m->cnt[1], short_list && d1 == b1);
+      if (short_list && d1 == b1 && lp < kTieCap) {
+        tk[lp] = u[c];
+        tx[lp] = xv[c];
+      }
+    }
+  }
+  epi_sync();
+  cyc(kTrPickSplitCyc);
+  if (m->cnt[0] != above1) return false;
+  if (short_list) {
+    // rank by key, then list position; the first `remaining` are in
+    const int nt = m->cnt[1];
+    for (int t = et; t < nt; t += kEpiThreads) {
+      const uint32_t ut = tk[t];
+      int rank = 0;
+      for (int jx = 0; jx < nt; ++jx) {
+        const uint32_t uj = tk[jx];
+        rank += (uj > ut || (uj == ut && jx < t)) ? 1 : 0;
+      }
+      if (rank < remaining) out[above1 + rank] = tx[t];
+    }
+  } else {
+    // a large bucket: its low 10 bits (the group's 1024-bin histogram, zero),
+    // then keys above the sub-bucket and the first tied ones
+    for (int e = et; e < n4; e += kEpiThreads) {
+      const uint4 q = k4[e];
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (u[c] != 0u && static_cast<int>((u[c] >> 10) & 4095u) == b1)
+          atomicAdd(&s.hist[u[c] & 1023u], 1u);
+    }
+    epi_sync();
+    int b2, above2, cnt2;
+    take_bucket(s.hist, m, 1024, remaining, &b2, &above2, &cnt2);
+    const int rem2 = remaining - above2;
+    if (et == 0) {
+      m->cnt[0] = 0;  // keys of b1 above b2
+      m->cnt[1] = 0;  // tie tickets
+    }
+    epi_sync();
+    for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
+      const int e = e0 + lane;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      int4 xi = make_int4(0, 0, 0, 0);
+      if (e < n4) {
+        q = k4[e];
+        xi = x4[e];
+      }
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+      const int32_t xv[4] = {xi.x, xi.y, xi.z, xi.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool in_b1 = u[c] != 0u && static_cast<int>((u[c] >> 10) & 4095u) == b1;
+        const int d2 = static_cast<int>(u[c] & 1023u);
+        const bool gt = in_b1 && d2 > b2, eq = in_b1 && d2 == b2;
+        const int pos = warp_reserve(&m->cnt[0], gt);
+        if (gt && above1 + pos < need) out[above1 + pos] = xv[c];
+        const int tkt = warp_reserve(&m->cnt[1], eq);
+        if (eq && tkt < rem2 && above1 + above2 + tkt < need) out[above1 + above2 + tkt] = xv[c];
+      }
+    }
+  }
+  epi_sync();
+  cyc(kTrPickOutCyc);
+  return true;
+}
+
+// The last `need` of token g's top k from the cutoff-bin list of split row w
+// (every entry of all segments in the resolved bucket; its count must equal
+// the histogram's `bc`; `cut` is the row bin all of them share), written to
+// out[0, need). The list is staged into this group's half of the idle stage
+// ring by two bulk copies. Returns false (having written nothing) when the
+// list disagrees with the histogram or a wait gave up.
+template <int G>
+__device__ bool select_from_list(const ScoreParams& p, const Smem& s, int w, int g, int64_t es,
+                                 int cut, int bc, int need, int32_t* out) {
+  using C = Cfg<G>;
+  constexpr int kCap = C::kListCap;
+  const int et = epi_tid();
+  const int lane = threadIdx.x & 31;
+  Misc* m = s.misc;
+  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  if (et == 0)
+    m->bcast[0] = static_cast<int>(__ldcg(&p.row_pos[static_cast<int64_t>(w) * G + g]) >> 32);
+  epi_sync();
+  const int n = m->bcast[0];
+  epi_sync();
+  if (n != bc || n <= 0 || n > kCap || p.elist_cap != kCap) return false;
+  const int n_r = (n + 3) & ~3;
+  uint8_t* half = s.kv + s.group * (C::kStages * 16384 / 2);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(half);
+  int32_t* idxs = reinterpret_cast<int32_t*>(half) + kCap;
+  const int64_t lo = (es * G + g) * static_cast<int64_t>(kCap);
+  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
+  fence_proxy_async_global();  // the list (acquired from other CTAs) precedes the copies' reads
+  epi_sync();
+  const int use = m->staged_uses;
+  if (et == 0) {
+    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(n_r) * 8u);
+    bulk_load(keys, p.elist_key + lo, static_cast<uint32_t>(n_r) * 4u, s.staged);
+    bulk_load(idxs, p.elist_idx + lo, static_cast<uint32_t>(n_r) * 4u, s.staged);
+  }
+  const bool ok = mbar_wait(s.staged, use & 1, &s.cs->abort_flag, p.dev_error, p.wait_ns);
+  if (!ok) {  // gave up: let the copies land before the ring is touched again
+    int dummy = 0;
+    mbar_wait(s.staged, use & 1, &dummy, p.dev_error);
+  }
+  // entries past the list's end become key 0, which no logit maps to
+  if (ok && et < n_r - n) keys[n + et] = 0u;
+  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
+  epi_sync();
+  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
+  if (et == 0) m->staged_uses = use + 1;
+  if (!all_ok) return false;
+  (void)cut;
+  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  const bool picked = pick_from_list<G>(p, s, keys, idxs, n, n_r, need, out);
+  if (et == 0 && s.trace) {
+    s.trace[kTrMergeLoadNs] += tq1 - tq0;
+    s.trace[kTrMergeRadixNs] += globaltimer_ns() - tq1;
+  }
+  return picked;
+}
+
+// Bucket of a level's complete histogram H (global, nb bins) that holds the
+// need-th largest of the keys it counts, the count in higher buckets and the
+// bucket's own count, for every thread of the group (cut = -1 when the
+// histogram holds fewer than `need` keys).
+__device__ __forceinline__ void level_cutoff(const uint32_t* H, int nb, int need, Misc* m, int* cut,
+                                             int* above, int* bc) {
+  if (nb == kRowHistBins) {
+    row_cutoff(H, m, need, -1, cut, above, bc);
+    return;
+  }
+  if (epi_tid() == 0) {
+    int acc = 0, c = -1, a = 0, b = 0;
+    for (int i = nb - 1; i >= 0; --i) {
+      const int h = static_cast<int>(__ldcg(&H[i]));
+      if (c < 0 && acc + h >= need) {
+        c = i;
+        a = acc;
+        b = h;
+      }
+      acc += h;
+    }
+    m->bcast[0] = c;
+    m->bcast[1] = a;
+    m->bcast[2] = b;
+  }
+  epi_sync();
+  *cut = m->bcast[0];
+  *above = m->bcast[1];
+  *bc = m->bcast[2];
+  epi_sync();
+}
+
+// Cutoff buckets with at most this many keys over all segments go to the
+// row's list and are resolved by one stream; larger ones take another digit
+// level first (every segment, one more round).
+constexpr int kListMax = 8192;
+
+// One split row's selection as this stream sees it (the same values in every
+// thread of the group).
+template <int G>
+struct RowSel {
+  int w, nseg, rounds;  // rounds this segment has counted in
+  int64_t es;           // histogram / list slot
+  int L[G], need[G], cut0[G], bcl[G];
+  uint32_t pre[G];
+  unsigned pending;  // bit g: token g takes another round
+  unsigned finals;   // bit g: this stream picks token g's list
+};
+
+template <int G>
+__device__ void sel_init(const ScoreParams& p, RowSel<G>& r, int w) {
+  const int2 rc = p.row_ctas[w];
+  const WorkRow wr = p.wr[w];
+  r.w = w;
+  r.nseg = rc.y - rc.x + 1;
+  r.rounds = 0;
+  r.es = split_slot(p, w, rc.x);
+  r.pending = 0u;
+  r.finals = 0u;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (g < wr.ntok && p.row_len[wr.row0 + g] > p.topk) r.pending |= 1u << g;
+    r.L[g] = 0;
+    r.need[g] = p.topk;
+    r.pre[g] = 0u;
+    r.cut0[g] = -1;
+    r.bcl[g] = 0;
+  }
+}
+
+// One round of split row r.w for this stream's segment (slot v + w), after
+// every segment has counted in for the previous round:
+//  - level L's histogram (complete) gives the bucket of the still-needed
+//    largest key, the count above it and its own count;
+//  - the segment writes the indices of its keys above that bucket to the
+//    output (positions from the row's counter);
+//  - a bucket with at most kListMax keys: the segment appends its keys in it
+//    to the row's list, and the stream that counts in last picks the missing
+//    keys from the list afterwards; all 32 bits resolved: the bucket's keys
+//    are equal and the segment takes its share by a ticket counter;
+//    otherwise the segment histograms the bucket's next digit for the next
+//    round.
+// Then the segment counts itself in. All threads of the group.
+template <int G>
+__device__ void sel_round(const ScoreParams& p, const Smem& s, int v, RowSel<G>& r) {
+  using C = Cfg<G>;
+  const int et = epi_tid();
+  const int lane = threadIdx.x & 31, ew = et >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int K = p.topk;
+  Misc* m = s.misc;
+  const int w = r.w;
+  const WorkRow wr = p.wr[w];
+  const int64_t slot = static_cast<int64_t>(v) + w;
+  const bool tr = et == 0 && s.trace;
+  uint64_t tq = tr ? globaltimer_ns() : 0;
+  auto lap = [&](int slot_id) {
+    if (tr) {
+      const uint64_t now = globaltimer_ns();
+      s.trace[slot_id] += now - tq;
+      tq = now;
+    }
+  };
+  unsigned listed = 0u;  // bit g: token g's list is complete after this round
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    if (!((r.pending >> g) & 1)) continue;
+    // this segment's candidates from its slot into the group's buffers,
+    // eight loads of each kind in flight per thread; key 0 pads the last chunk
+    const int64_t sg = slot * G + g;
+    const int n = __ldcg(&p.slot_count[sg]);
+    const uint32_t* sk = p.slot_key + sg * p.slot_cap;
+    const int32_t* si = p.slot_idx + sg * p.slot_cap;
+    uint32_t* ck = s.ckey + g * C::kCap;
+    int32_t* ci = s.cidx + g * C::kCap;
+    const int n32 = (n + 31) & ~31;
+    for (int b0 = 0; b0 < n32; b0 += 8 * kEpiThreads) {
+      uint32_t ub[8];
+      int32_t xb[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = b0 + q * kEpiThreads + et;
+        ub[q] = e < n ? __ldcg(&sk[e]) : 0u;
+        xb[q] = e < n ? __ldcg(&si[e]) : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int e = b0 + q * kEpiThreads + et;
+        if (e < n32) {
+          ck[e] = ub[q];
+          ci[e] = xb[q];
+        }
+      }
+    }
+    epi_sync();
+    const int nch = n32 >> 5;  // chunks; warp ew takes chunks ew, ew + 4, ...
+    lap(kTrRndLoadNs);
+    const int Lg = r.L[g];
+    uint32_t* hb = p.row_hist + (r.es * G + g) * kRowHistWords;
+    int cut, above, bc;
+    level_cutoff(hb + Lg * kRowHistBins, level_bins(Lg), r.need[g], m, &cut, &above, &bc);
+    lap(kTrRndCutNs);
+    if (tr) s.trace[kTrRndListSize] += static_cast<uint64_t>(bc);
+    if (cut < 0 || bc < 1) {  // the histograms disagree with the candidates
+      set_error(p.dev_error, IDX_DEV_INTERNAL);
+      r.pending &= ~(1u << g);
+      continue;
+    }
+    if (Lg == 0) r.cut0[g] = cut;
+    const bool to_list = bc <= min(kListMax, p.elist_cap);
+    const bool to_ties = !to_list && Lg == 3;
+    const uint32_t pg = r.pre[g], ucut = static_cast<uint32_t>(cut);
+    // class of an entry: 1 = above the bucket, 2 = in it, 0 = neither (key 0
+    // is no candidate)
+    auto klass = [&](uint32_t key) -> uint32_t {
+      if (key == 0u || !level_match(key, Lg, pg)) return 0u;
+      const uint32_t d = level_digit(key, Lg);
+      return d > ucut ? 1u : (d == ucut ? 2u : 0u);
+    };
+    // per-warp counts, then every warp's base in the group
+    long long cy0 = tr ? clock64() : 0;
+    auto cyc = [&](int slot_id) {
+      if (tr) {
+        const long long now = clock64();
+        s.trace[slot_id] += static_cast<uint64_t>(now - cy0);
+        cy0 = now;
+      }
+    };
+    int n_gt = 0, n_eq = 0;
+    for (int c0 = ew; c0 < nch; c0 += 16) {  // chunks c0, c0 + 4, c0 + 8, c0 + 12
+      uint32_t kk[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + 4 * q;
+        kk[q] = c < nch ? ck[c * 32 + lane] : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t k = klass(kk[q]);
+        n_gt += __popc(__ballot_sync(0xffffffffu, k == 1u));
+        n_eq += __popc(__ballot_sync(0xffffffffu, k == 2u));
+      }
+    }
+    cyc(kTrPassCountCyc);
+    if (lane == 0) {
+      m->scan[ew] = n_gt;
+      m->vote[1][ew] = n_eq;
+    }
+    epi_sync();
+    cyc(kTrPassScanCyc);
+    int gt_base = 0, eq_base = 0, tot_gt = 0, tot_eq = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      gt_base += i < ew ? m->scan[i] : 0;
+      eq_base += i < ew ? m->vote[1][i] : 0;
+      tot_gt += m->scan[i];
+      tot_eq += m->vote[1][i];
+    }
+    lap(kTrRndPassNs);
+    if (et == 0) {
+      int take = 0;
+      if (to_ties) {
+        const int tbase = atomicAdd(&p.tie_count[static_cast<int64_t>(w) * G + g], tot_eq);
+        take = min(max(r.need[g] - above - tbase, 0), tot_eq);
+      }
+      // output positions (low word) and list entries (high word) in one atomic
+      const unsigned long long add =
+          static_cast<unsigned long long>(tot_gt + take) |
+          (static_cast<unsigned long long>(to_list ? tot_eq : 0) << 32);
+      const unsigned long long old =
+          add ? atomicAdd(&p.row_pos[static_cast<int64_t>(w) * G + g], add) : 0ull;
+      m->bcast[0] = static_cast<int>(old & 0xffffffffull);
+      m->bcast[1] = static_cast<int>(old >> 32);
+      m->bcast[2] = take;
+    }
+    epi_sync();
+    const int obase = m->bcast[0], ebase = m->bcast[1], take = m->bcast[2];
+    epi_sync();
+    lap(kTrRndAtomicNs);
+    // write pass (ballot ranks, coalesced): keys above the bucket to the
+    // output, keys in it to the list or (ties) the first `take` to the output
+    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * K;
+    uint32_t* ek = p.elist_key + (r.es * G + g) * p.elist_cap;
+    int32_t* ei = p.elist_idx + (r.es * G + g) * p.elist_cap;
+    int og = obase + gt_base, oq = eq_base;
+    for (int c0 = ew; c0 < nch; c0 += 16) {  // chunks c0, c0 + 4, c0 + 8, c0 + 12
+      uint32_t kk[4];
+      int32_t xx[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + 4 * q;
+        kk[q] = c < nch ? ck[c * 32 + lane] : 0u;
+        xx[q] = c < nch ? ci[c * 32 + lane] : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t k = klass(kk[q]);
+        const unsigned gm = __ballot_sync(0xffffffffu, k == 1u);
+        const unsigned qm = __ballot_sync(0xffffffffu, k == 2u);
+        if (k == 1u) {
+          const int pos = og + __popc(gm & lt);
+          if (pos < K) out[pos] = xx[q];
+        } else if (k == 2u) {
+          const int rk = oq + __popc(qm & lt);
+          if (to_list) {
+            if (ebase + rk < p.elist_cap) {
+              ek[ebase + rk] = kk[q];
+              ei[ebase + rk] = xx[q];
+            }
+          } else if (to_ties) {
+            const int pos = obase + tot_gt + rk;
+            if (rk < take && pos < K) out[pos] = xx[q];
+          }
+        }
+        og += __popc(gm);
+        oq += __popc(qm);
+      }
+    }
+    cyc(kTrPassWriteCyc);
+    r.need[g] -= above;
+    r.pre[g] = Lg == 0 ? ucut : ((pg << (level_shift(Lg - 1) - level_shift(Lg))) | ucut);
+    if (to_list) {
+      listed |= 1u << g;
+      r.bcl[g] = bc;
+      r.pending &= ~(1u << g);
+    } else if (to_ties) {
+      r.pending &= ~(1u << g);
+    } else {
+      // the bucket's next digit, from every segment, for the next round
+      const int Ln = Lg + 1;
+      uint32_t* hn = hb + Ln * kRowHistBins;
+      for (int e = et; e < n; e += kEpiThreads) {
+        const uint32_t uu = ck[e];
+        if (uu != 0u && level_match(uu, Ln, r.pre[g])) atomicAdd(&s.hist[level_digit(uu, Ln)], 1u);
+      }
+      epi_sync();
+      for (int b = et; b < level_bins(Ln); b += kEpiThreads) {
+        const uint32_t c = s.hist[b];
+        if (c) {
+          atomicAdd(&hn[b], c);
+          s.hist[b] = 0u;
+        }
+      }
+      r.L[g] = Ln;
+    }
+    epi_sync();
+    cyc(kTrPassSyncCyc);
+    lap(kTrRndPassNs);
+  }
+  // count this segment in for the round
+  __threadfence();
+  epi_sync();
+  if (et == 0) {
+    __threadfence();
+    const int old = atomicAdd(&p.seg_counter[w], 1);
+    m->is_last = old == (r.rounds + 2) * r.nseg - 1;
+    __threadfence();
+  }
+  epi_sync();
+  lap(kTrRndArriveNs);
+  ++r.rounds;
+  if (m->is_last) r.finals |= listed;
+  epi_sync();
+}
+
+// Selection of this stream's split rows (at most two) once both of its
+// CTA's streams are done: the first round of each row runs as soon as all of
+// that row's segments have published (polling both rows, so that no row waits
+// on another), further rounds (cutoff buckets too large for a list) follow,
+// and the list picks this stream was left with come last.
+template <int G>
+__device__ void select_split_rows(const ScoreParams& p, const Smem& s, int v) {
+  const int et = epi_tid();
+  Misc* m = s.misc;
+  const uint64_t ts0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
+  const int np = min(m->npend, 2);
+  RowSel<G> r[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    if (i < np) sel_init<G>(p, r[i], m->pend[i]);
+  // first rounds, as the rows become ready
+  unsigned started = 0u;
+  const unsigned all = (1u << np) - 1u;
+  const uint64_t t_first = et == 0 ? globaltimer_ns() : 0;
+  for (uint32_t it = 0; started != all; ++it) {
+    if (et == 0) {
+      int ready = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        if (i < np && !((started >> i) & 1) &&
+            ld_acquire_gpu(&p.seg_counter[r[i].w]) >= r[i].nseg + p.wait_extra)
+          ready |= 1 << i;
+      if (!ready) {
+        if (s.cs->abort_flag) ready = -1;
+        else if (globaltimer_ns() - t_first > p.wait_ns) {
+          set_error(p.dev_error, IDX_DEV_TIMEOUT);
+          s.cs->abort_flag = 1;
+          ready = -1;
+        } else {
+          __nanosleep(32);
+        }
+      }
+      m->bcast[3] = ready;
+    }
+    epi_sync();
+    const int ready = m->bcast[3];
+    epi_sync();
+    if (ready < 0) return;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if ((ready >> i) & 1) {
+        sel_round<G>(p, s, v, r[i]);
+        started |= 1u << i;
+      }
+  }
+  uint64_t ts1 = 0;
+  if (et == 0 && s.trace) {
+    ts1 = globaltimer_ns();
+    s.trace[kTrSelWaitNs] += ts1 - ts0;
+    s.trace[kTrSelRows] += np;
+  }
+  // further rounds, row by row
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    while (i < np && r[i].pending) {
+      if (et == 0) {
+        if (s.trace) s.trace[kTrSelFallback] += 1;
+        m->sel_ok = !s.cs->abort_flag &&
+                    wait_count(&p.seg_counter[r[i].w], (r[i].rounds + 1) * r[i].nseg,
+                               &s.cs->abort_flag, p.dev_error, p.wait_ns);
+      }
+      epi_sync();
+      const bool ok = m->sel_ok != 0;
+      epi_sync();
+      if (!ok) return;
+      sel_round<G>(p, s, v, r[i]);
+    }
+  }
+  uint64_t ts2 = 0;
+  if (et == 0 && s.trace) {
+    ts2 = globaltimer_ns();
+    s.trace[kTrSelScanNs] += ts2 - ts1;
+  }
+  // the list picks
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (i >= np || !r[i].finals) continue;
+    const WorkRow wr = p.wr[r[i].w];
+    __threadfence();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (!((r[i].finals >> g) & 1)) continue;
+      const int K = p.topk, need = r[i].need[g];
+      int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * K;
+      if (select_from_list<G>(p, s, r[i].w, g, r[i].es, r[i].cut0[g], r[i].bcl[g], need,
+                              out + (K - need))) {
+        if (et == 0 && s.trace) s.trace[kTrSelList] += 1;
+      } else if (et == 0 && !s.cs->abort_flag) {
+        set_error(p.dev_error, IDX_DEV_INTERNAL);
+      }
+    }
+    if (et == 0 && s.trace) s.trace[kTrSelLast] += 1;
+  }
+  if (et == 0 && s.trace) s.trace[kTrSelFinalNs] += globaltimer_ns() - ts2;
+}
+
+// ---------------------------------------------------------------------------
+// epilogue group: one stream's tiles
+// ---------------------------------------------------------------------------
+
+// Streams epilogue group j's tiles (stream j of the CTA) through the score
+// and the streaming top-k, finalising each work row's segment as it ends.
+// Returns false when a pipeline wait gave up. All threads of the group.
+template <int G, bool kLogits>
+__device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, const Stream (&st)[2],
+                         int j) {
+  using C = Cfg<G>;
+  volatile int* abort_flag = &s.cs->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int et = epi_tid();
+  const int ew = et >> 5;
+  const int sub = warp & 3;          // tensor-memory lanes [32*sub, 32*sub + 32)
+  const int mrow = sub * 32 + lane;  // key of the tile this thread scores
+  const uint32_t lane_addr = static_cast<uint32_t>(sub * 32) << 16;
+  constexpr int S = C::kStreamStages;
+  const int64_t t0 = st[j].t0, t1 = st[j].t1;
+  const int v = st[j].v;
+
+  for (int b = et; b < C::kHistBins; b += kEpiThreads) s.hist[b] = 0u;  // zero between uses
+  if (t0 >= t1) return true;
+
+  int w = p.cta_row[v];
   int64_t rs = p.wr_tile_start[w], re = p.wr_tile_start[w + 1];
   WorkRow wr;
   int len[G];
   bool active[G];
-  int wcnt[G];        // entries in this warp's region of each token's buffer
-  uint32_t thr[G];    // each buffer's drop threshold
-  const int ew = et >> 5;
-
-  for (int b = et; b < C::kHistBins; b += kEpiThreads) s.hist[b] = 0u;  // zero between uses
+  int wcnt[G];      // entries in this warp's region of each token's buffer
+  uint32_t thr[G];  // each buffer's drop threshold
 
   auto begin_row = [&]() {
     wr = p.wr[w];
@@ -1400,7 +1518,8 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     }
     for (int i = et; i < G * kHeads; i += kEpiThreads) {
       const int g = i / kHeads;
-      s.wp[i] = g < wr.ntok ? p.wprime[static_cast<int64_t>(wr.row0 + g) * kHeads + i % kHeads] : 0.f;
+      s.wp[i] =
+          g < wr.ntok ? p.wprime[static_cast<int64_t>(wr.row0 + g) * kHeads + i % kHeads] : 0.f;
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -1414,7 +1533,7 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
         s.misc->thr[g] = 0u;
       }
     }
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
   };
   auto publish_counts = [&]() {
     if (lane == 0)
@@ -1425,32 +1544,37 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
 
   bool ok = true;
   long long cyc[5] = {0, 0, 0, 0, 0};  // per-phase clock totals (trace only)
-  for (int64_t t = t0; t < t1; ++t) {
+  for (int64_t k = 0; t0 + k < t1; ++k) {
+    const int64_t t = t0 + k;
     if (t >= re) {
       publish_counts();
-      if (!kLogits) finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
+      if (!kLogits) finalize_segment<G>(p, s, v, w, wr, active, rs, re, t0, t1);
       do {
         ++w;
         re = p.wr_tile_start[w + 1];
       } while (t >= re);
       rs = p.wr_tile_start[w];
-      named_sync(kEpiBarrier, kEpiThreads);
+      epi_sync();
       begin_row();
     }
     const int i = static_cast<int>(t - rs);
+    const int stage = j * S + static_cast<int>(k % S);
+    const uint32_t phase = static_cast<uint32_t>((k / S) & 1);
+    const int acc = 2 * j + static_cast<int>(k & 1);
+    const uint32_t acc_par = static_cast<uint32_t>((k >> 1) & 1);
     const bool tr = s.trace != nullptr;  // per-phase clocks only when tracing
     const long long c0 = tr ? clock64() : 0;
     // lane 0 of each warp waits for the stage (scales) and the accumulator
     bool wok = true;
     if (lane == 0)
-      wok = mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error) &&
-            mbar_wait(&s.tfull[acc], acc_phase, abort_flag, p.dev_error);
+      wok = mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error, p.wait_ns) &&
+            mbar_wait(&s.tfull[acc], acc_par, abort_flag, p.dev_error, p.wait_ns);
     wok = __shfl_sync(0xffffffffu, wok ? 1 : 0, 0) != 0;
     __syncwarp();
     const long long c1 = tr ? clock64() : 0;
     long long c2 = c1;
     float logit[G];
-    if (t == t0 && et == 0 && s.trace) s.trace[kTrFirstEpi] = globaltimer_ns();
+    if (k == 0 && et == 0 && s.trace) s.trace[kTrFirstEpi] = globaltimer_ns();
     if (wok) {
       tc_fence_after();
       const float scale = s.scales[stage * 128 + mrow];
@@ -1490,17 +1614,17 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       }
     }
     const long long c3 = tr ? clock64() : 0;
-    // Uniform decision across the four epilogue warps (double-buffered vote):
+    // Uniform decision across the group's four warps (double-buffered vote):
     // bit 0 = this warp's waits succeeded, bit 1 + g = its region of token g's
     // buffer has no room for another tile (then all warps compact it).
-    const int par = static_cast<int>(t & 1);
+    const int par = static_cast<int>(k & 1);
     int need = 0;
 #pragma unroll
     for (int g = 0; g < G; ++g)
       need |= (!kLogits && active[g] && wcnt[g] + 32 > C::kRegion) ? 2 << g : 0;
     publish_counts();
     if (lane == 0) s.misc->vote[par][ew] = (wok ? 1 : 0) | need;
-    named_sync(kEpiBarrier, kEpiThreads);
+    epi_sync();
     const long long c4 = tr ? clock64() : 0;
     const int v0 = s.misc->vote[par][0], v1 = s.misc->vote[par][1];
     const int v2 = s.misc->vote[par][2], v3 = s.misc->vote[par][3];
@@ -1526,12 +1650,13 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         // append to this warp's region: ballot + popc, no shared counter
-        const uint32_t k = float_key(logit[g]);
-        const bool pass = active[g] && key < len[g] && k > thr[g];
+        const uint32_t kk = float_key(logit[g]);
+        const bool pass = active[g] && key < len[g] && kk > thr[g];
         const unsigned pm = __ballot_sync(0xffffffffu, pass);
         if (pass) {
-          const int at = g * C::kCap + ew * C::kRegion + wcnt[g] + __popc(pm & ((1u << lane) - 1u));
-          s.ckey[at] = k;
+          const int at =
+              g * C::kCap + ew * C::kRegion + wcnt[g] + __popc(pm & ((1u << lane) - 1u));
+          s.ckey[at] = kk;
           s.cidx[at] = key;
         }
         wcnt[g] += __popc(pm);
@@ -1545,14 +1670,6 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
       cyc[3] += c4 - c3;
       cyc[4] += c5 - c4;
     }
-    if (++stage == C::kStages) {
-      stage = 0;
-      phase ^= 1;
-    }
-    if (++acc == 2) {
-      acc = 0;
-      acc_phase ^= 1;
-    }
   }
   if (et == 0 && s.trace) {
     s.trace[kTrLastEpi] = globaltimer_ns();
@@ -1563,105 +1680,103 @@ __device__ void epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, int
     s.trace[kTrEpiSelCyc] = cyc[4];
   }
   publish_counts();
-  if (!kLogits && ok) {
-    finalize_segment<G>(p, s, w, wr, active, rs, re, t0, t1, T, nC);
-    const int pw = s.misc->pending_row;  // set (by thread 0) before barriers all passed since
-    if (pw >= 0) {
-      const WorkRow pwr = p.wr[pw];
-      bool pact[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        pact[g] = g < pwr.ntok && p.row_len[pwr.row0 + g] > p.topk;
-      const int2 rc = p.row_ctas[pw];
-      merge_work_row<G>(p, s, pw, pwr, pact, rc.x, rc.y);
-    }
-  }
-  if (et == 0 && s.trace) s.trace[kTrFinal] = globaltimer_ns();
+  if (!kLogits && ok) finalize_segment<G>(p, s, v, w, wr, active, rs, re, t0, t1);
+  return ok;
 }
 
 template <int G, bool kLogits>
-__global__ void __launch_bounds__(kThreads, Cfg<G>::kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, 1)
     score_select_kernel(const __grid_constant__ ScoreParams p,
                         const __grid_constant__ CUtensorMap map) {
   using C = Cfg<G>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  Smem s = carve<G>(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the stream this thread serves: warps 2j, 2j + 1 and epilogue group j
+  const int group = warp < 4 ? (warp >> 1) : epi_group();
+  Smem s = carve<G>(base, group);
 
   // Shared-memory setup needs nothing from earlier kernels; everything after
   // pdl_wait() may read what they wrote.
   if (warp == 0 && lane == 0) prefetch_tensormap(&map);
   pdl_wait();
 
-  // With fewer tiles than CTAs only the first T CTAs take part, so that every
-  // participating CTA owns at least one tile (segment counts rely on it).
+  // With fewer tiles than virtual CTAs only the first T take part, so that
+  // every participating stream owns at least one tile (segment counts rely
+  // on it).
   const int64_t T = p.wr_tile_start[p.num_wr];
-  const int64_t nC = min(static_cast<int64_t>(gridDim.x), T);
-  const bool part = static_cast<int64_t>(blockIdx.x) < nC;
-  s.trace = (p.trace && part) ? reinterpret_cast<uint64_t*>(base + C::kTraceOff) : nullptr;
-  const int64_t t0 = part ? p.cta_tile[blockIdx.x] : 0;
-  const int64_t t1 = part ? p.cta_tile[blockIdx.x + 1] : 0;
+  const int64_t nV = min(static_cast<int64_t>(2 * gridDim.x), T);
+  Stream st[2];
+  bool part[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int v = 2 * static_cast<int>(blockIdx.x) + j;
+    part[j] = v < nV;
+    st[j].v = v;
+    st[j].t0 = part[j] ? p.cta_tile[v] : 0;
+    st[j].t1 = part[j] ? p.cta_tile[v + 1] : 0;
+  }
+  if (!(p.trace && part[group])) s.trace = nullptr;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1 + 4);
+      mbar_init(&s.empty[i], 1 + 4);  // the MMA's commit + the consuming group's warps
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 4);
-      mbar_init(&s.qfull[i], 1);
-      mbar_init(&s.qempty[i], 1);
+    for (int a = 0; a < 4; ++a) {
+      mbar_init(&s.tfull[a], 1);
+      mbar_init(&s.tempty[a], 4);
+      mbar_init(&s.qfull[a], 1);
+      mbar_init(&s.qempty[a], 1);
     }
-    mbar_init(s.done, 1);
-    mbar_init(s.staged, 1);
-    s.misc->abort_flag = 0;
-    s.misc->epi_done = 0;
-    s.misc->staged_uses = 0;
-    s.misc->pending_row = -1;
-    if (s.trace)
-      for (int i = 0; i < kTrSlots; ++i) s.trace[i] = 0;
+    for (int i = 0; i < 4; ++i) mbar_init(s.done + i, 1);  // done[2], staged[2]
+    s.cs->abort_flag = 0;
+    s.cs->epi_done = 0;
+    for (int gi = 0; gi < 2; ++gi) {
+      const Smem sg = carve<G>(base, gi);
+      sg.misc->staged_uses = 0;
+      sg.misc->npend = 0;
+      for (int i = 0; i < kTrSlots; ++i) sg.trace[i] = 0;
+    }
     fence_barrier_init();
   }
   __syncwarp();  // warp 0 reconverges before the block barrier (which counts whole warps)
-  if (warp == 1) tmem_alloc(&s.misc->tmem_base, C::kTmemCols);
+  if (warp == 1) tmem_alloc(&s.cs->tmem_base, C::kTmemCols);
   tc_fence_before();
   named_sync(kSetupBarrier, kThreads);
   tc_fence_after();
   pdl_trigger();
-  const uint32_t tmem = s.misc->tmem_base;
-  if (threadIdx.x == 0 && s.trace) {
+  const uint32_t tmem = s.cs->tmem_base;
+  if (warp >= 4 && epi_tid() == 0 && s.trace) {
     s.trace[kTrStart] = globaltimer_ns();
-    s.trace[kTrTiles] = static_cast<uint64_t>(t1 - t0);
+    s.trace[kTrTiles] = static_cast<uint64_t>(st[group].t1 - st[group].t0);
   }
 
-  if (t0 < t1) {
-    // One lane of each of warps 0 and 1 runs its role; the warp reconverges
-    // before the block barrier below (which counts whole warps).
-    if (warp == 0) {
-      if (lane == 0) producer<G>(p, &map, s, t0, t1);
-      __syncwarp();
-    } else if (warp == 1) {
-      if (lane == 0) mma_issuer<G>(p, s, tmem, t0, t1);
-      __syncwarp();
-    } else {
-      epilogue<G, kLogits>(p, s, tmem, t0, t1, T, nC);
+  if (warp < 4) {
+    // one lane runs the role; the warp reconverges before the block barrier
+    const bool has_tiles = st[group].t1 > st[group].t0;
+    if (lane == 0 && has_tiles) {
+      if (warp & 1) mma_issuer<G>(p, s, tmem, st[group]);
+      else producer<G>(p, &map, s, st[group]);
     }
+    __syncwarp();
+  } else {
+    const bool ok = epilogue<G, kLogits>(p, s, tmem, st, group);
+    // both streams are done with the stage ring before a selection stages
+    // lists in it
+    named_sync(kJointBarrier, 2 * kEpiThreads);
+    if (!kLogits && ok) select_split_rows<G>(p, s, st[group].v);
+    if (s.trace && epi_tid() == 0) s.trace[kTrFinal] = globaltimer_ns();
   }
-  if (threadIdx.x == 64) *reinterpret_cast<volatile int*>(&s.misc->epi_done) = 1;
+  if (threadIdx.x == kEpiBase) *reinterpret_cast<volatile int*>(&s.cs->epi_done) = 1;
   tc_fence_before();
   named_sync(kTeardownBarrier, kThreads);
-  if (threadIdx.x == 0 && s.trace) {
-    s.trace[kTrEnd] = globaltimer_ns();
-    s.trace[kTrSeen] = static_cast<uint64_t>(*reinterpret_cast<volatile int*>(&s.misc->epi_done));
-  }
-  if (threadIdx.x == 64 && s.trace) s.trace[kTrEndEpi] = globaltimer_ns();
-  if (s.trace) {
-    named_sync(kTeardownBarrier, kThreads);
-    if (threadIdx.x < kTrSlots)
-      p.trace[static_cast<int64_t>(blockIdx.x) * kTrSlots + threadIdx.x] = s.trace[threadIdx.x];
+  if (warp >= 4 && s.trace) {
+    if (epi_tid() == 0) s.trace[kTrEnd] = globaltimer_ns();
+    __syncwarp();
+    if (epi_tid() < kTrSlots)
+      p.trace[static_cast<int64_t>(st[group].v) * kTrSlots + epi_tid()] = s.trace[epi_tid()];
   }
   if (warp == 1) {
     tc_fence_after();
@@ -1676,30 +1791,21 @@ idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_cta
   // set once per device (any host thread; setting it twice is harmless)
   static std::atomic<bool> configured[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return IDX_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidDevice);
   if (dev >= kMaxDevices || !configured[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(score_select_kernel<G, kLogits>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes) != cudaSuccess)
-      return IDX_ERR_CUDA;
+    e = cudaFuncSetAttribute(score_select_kernel<G, kLogits>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return cuda_status(e);
     if (dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
   }
-  return launch_pdl(score_select_kernel<G, kLogits>, num_ctas, kThreads, C::kSmemBytes, s, p, map) ==
-                 cudaSuccess
-             ? IDX_OK
-             : IDX_ERR_CUDA;
+  // Top-k launches are cooperative: the streams sharing a split row wait for
+  // one another's segments before selecting.
+  return cuda_status(launch_pdl_ex(!kLogits, score_select_kernel<G, kLogits>, num_ctas, kThreads,
+                                   C::kSmemBytes, s, p, map));
 }
 
 }  // namespace
-
-int score_ctas_per_sm(int G) {
-  switch (G) {
-    case 1: return Cfg<1>::kCtasPerSm;
-    case 2: return Cfg<2>::kCtasPerSm;
-    case 4: return Cfg<4>::kCtasPerSm;
-    default: return 1;
-  }
-}
 
 idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s) {
@@ -1708,8 +1814,6 @@ idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensor
                           : launch_impl<1, false>(p, map, num_ctas, s);
     case 2: return logits ? launch_impl<2, true>(p, map, num_ctas, s)
                           : launch_impl<2, false>(p, map, num_ctas, s);
-    case 4: return logits ? launch_impl<4, true>(p, map, num_ctas, s)
-                          : launch_impl<4, false>(p, map, num_ctas, s);
     default: return IDX_ERR_UNSUPPORTED;
   }
 }

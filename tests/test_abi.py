@@ -42,7 +42,7 @@ def _declarations():
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     out = {}
     for m in re.finditer(r"\b(indexer_\w+)\s*\(([^)]*)\)\s*;", text):
-        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        params = [p.strip() for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
         out[m.group(1)] = [re.sub(r"\s*\b\w+$", "", p) if not p.endswith("*") else p
                            for p in params]
     return out
@@ -60,7 +60,7 @@ def _header_kind(t):
         return "ptr"
     base = t.replace("const", "").strip()
     return {"int32_t": "int32", "idx_status": "int32", "int64_t": "int64",
-            "size_t": "int64"}[base]
+            "uint64_t": "int64", "size_t": "int64"}[base]
 
 
 def test_binding_signatures_match_header_parameters():

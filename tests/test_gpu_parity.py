@@ -49,7 +49,29 @@ def _oracle_rows(d, lens, k, rows=None):
                               want_logits=True)
 
 
-def _check_decode(d, k, rows=None):
+def open_key_cap(k):
+    """Keys per row whose membership the tolerance band may leave open before
+    the set check is considered too loose to bite: 15% of k plus 4. With the
+    1e-3 relative band (1e-3 of A, the sum of |head terms|, which is several
+    times |logit|) the workloads leave at most ~6% of k open at k = 2048 and
+    ~14% at k = 64; a band grown by a factor of about three would exceed the
+    cap."""
+    return 4 + (3 * k) // 20
+
+
+def _check_rows(got, lens_h, lg, ta, tb, rows, k, bound_open=True):
+    worst = total = 0
+    for i, r in enumerate(rows):
+        n_open = check_topk_row(got[r], lg[i], ta[i], tb[i], k, int(lens_h[r]))
+        worst = max(worst, n_open)
+        total += n_open
+    print(f"rows {len(rows)}: keys left open by the tolerance: {total} (max {worst} per row)")
+    if bound_open:
+        assert worst <= open_key_cap(k), f"the tolerance leaves {worst} keys of a row open"
+    return worst
+
+
+def _check_decode(d, k, rows=None, bound_open=True):
     dd = _to(d) if d.q.device.type == "cpu" else d
     err = _err()
     lens = _expand(dd, err)
@@ -59,12 +81,7 @@ def _check_decode(d, k, rows=None):
     assert int(err.item()) == 0
     lens_h = lens.cpu().numpy()
     ref, lg, ta, tb, rows = _oracle_rows(d, lens_h, k, rows)
-    got = out.cpu().numpy()
-    open_keys = 0
-    for i, r in enumerate(rows):
-        open_keys += check_topk_row(got[r], lg[i], ta[i], tb[i], k, int(lens_h[r]))
-    print(f"rows {len(rows)}: keys left open by the tolerance: {open_keys}")
-    return open_keys
+    return _check_rows(out.cpu().numpy(), lens_h, lg, ta, tb, rows, k, bound_open)
 
 
 # ---------------------------------------------------------------------------
@@ -156,6 +173,13 @@ def test_logits_ragged_lengths_single_token():
     print("max |err| / (A + 1e-2 B):", _check_logits_case(d))
 
 
+def test_logits_long_rows_split_over_many_ctas():
+    """Rows of 40000 and 33000 keys: every CTA streams part of them, so the
+    logits of one row come from many CTAs' pipelines."""
+    d = synth.make_decode_from_lens([40000, 33000], [1, 1], 1, seed=14)
+    print("max |err| / (A + 1e-2 B):", _check_logits_case(d))
+
+
 def test_logits_two_token_rows():
     sl = [300, 129, 2000, 64, 5]
     dl = [2, 1, 2, 0, 2]
@@ -215,8 +239,14 @@ def test_topk_mtp_workload():
 
 
 def test_topk_long_context_sampled():
+    """32 of the 128 rows (the first, the last and a seeded sample), each
+    131072 keys with 1% heavy-tail keys."""
     d = synth.make_decode("long", device=DEV)
-    rows = np.array([0, 1, 17, 63, 64, 100, 126, 127])
+    rng = np.random.default_rng(7)
+    fixed = [0, 1, 63, 64, 126, 127]
+    rows = np.unique(np.concatenate([fixed, rng.choice(np.setdiff1d(np.arange(128), fixed), 26,
+                                                       replace=False)]))
+    assert rows.size == 32
     dh = synth.DecodeInputs(q=d.q.cpu(), w=d.w.cpu(), cache=d.cache.cpu(),
                             block_table=d.block_table.cpu(), seq_lens=d.seq_lens.cpu(),
                             decode_lens=d.decode_lens.cpu(), next_n=1, topk=2048)
@@ -228,9 +258,7 @@ def test_topk_long_context_sampled():
     assert int(err.item()) == 0
     lens_h = lens.cpu().numpy()
     _, lg, ta, tb, rows = _oracle_rows(dh, lens_h, 2048, rows)
-    got = out.cpu().numpy()
-    for i, r in enumerate(rows):
-        check_topk_row(got[r], lg[i], ta[i], tb[i], 2048, int(lens_h[r]))
+    _check_rows(out.cpu().numpy(), lens_h, lg, ta, tb, rows, 2048)
 
 
 def test_workspace_reuse_across_shapes():
@@ -249,8 +277,7 @@ def test_workspace_reuse_across_shapes():
     assert int(err.item()) == 0
     lens_h = lb.cpu().numpy()
     _, lg, ta, tb, rows = _oracle_rows(b, lens_h, 2048)
-    for i, r in enumerate(rows):
-        check_topk_row(out.cpu().numpy()[r], lg[i], ta[i], tb[i], 2048, int(lens_h[r]))
+    _check_rows(out.cpu().numpy(), lens_h, lg, ta, tb, rows, 2048)
 
 
 # ---------------------------------------------------------------------------
@@ -269,9 +296,7 @@ def _check_prefill(p, k, rows=None, budget=512 << 20, ws_tokens=40 * 8192):
         synth.bf16_bits(p.q), p.w.numpy(), p.cache.numpy(), p.block_table.numpy(),
         p.seq_lens.numpy(), p.query_start_loc.numpy(), k, rows=rows, want_logits=True)
     _, ln = oracle.prefill_rows(p.seq_lens.numpy(), p.query_start_loc.numpy())
-    got = out.cpu().numpy()
-    for i, r in enumerate(rows):
-        check_topk_row(got[r], lg[i], ta[i], tb[i], k, int(ln[r]))
+    _check_rows(out.cpu().numpy(), ln, lg, ta, tb, rows, k)
 
 
 def test_prefill_small_full():
@@ -282,16 +307,28 @@ def test_prefill_small_full():
 
 
 def test_prefill_few_queries_over_long_context():
-    """Chunked-prefill shape: 8 new queries over 100000 keys (two work rows of
-    four queries, each spread over many CTAs and merged from their slots)."""
+    """Chunked-prefill shape: 8 new queries over 100000 keys (four work rows of
+    two queries, each spread over many tile streams and selected together)."""
     p = synth.make_prefill(seed=53, seq_lens=[100000, 3000], query_lens=[8, 5])
     _check_prefill(p, 2048)
 
 
 def test_prefill_workload_sampled():
+    """A stratified sample of the 32768 query rows: 64 per request (one chunk
+    each under the 512 MiB budget): its edges, the rows around the causal-fill
+    boundary (2048 keys) and a seeded draw over the rest."""
     p = synth.make_prefill("prefill")
-    rows = np.array([0, 1, 2046, 2047, 2048, 2049, 5000, 8191, 8192, 8192 + 4095, 16383,
-                     24576 + 3000, 32767])
+    assert len(saib.indexer_plan_prefill_chunks(p.seq_lens, p.query_lens, 40 * 8192,
+                                                512 << 20)) == 4
+    rng = np.random.default_rng(5)
+    rows = []
+    for r in range(4):
+        base = 8192 * r
+        fixed = [0, 1, 2, 1000, 2045, 2046, 2047, 2048, 2049, 2050, 4095, 4096, 8190, 8191]
+        rest = rng.choice(np.setdiff1d(np.arange(8192), fixed), 64 - len(fixed), replace=False)
+        rows.extend(base + np.concatenate([fixed, rest]))
+    rows = np.unique(np.asarray(rows, np.int64))
+    assert rows.size == 256
     _check_prefill(p, 2048, rows=rows)
 
 
@@ -324,7 +361,7 @@ def test_topk_all_equal_logits_degenerate():
     c[:, :8192] = c[0, :128].repeat(64)            # one key row everywhere
     c[:, 8192:] = c[0, 8192:8196].repeat(64)       # and one scale
     d.cache = c
-    _check_decode(d, 2048)
+    _check_decode(d, 2048, bound_open=False)  # every key ties: the band leaves all open
 
 
 # ---------------------------------------------------------------------------
@@ -364,3 +401,100 @@ def test_insert_keys_out_of_range_slot_is_reported_and_skipped():
     assert int(err.item()) & 1  # IDX_DEV_BAD_BLOCK
     bits = k.view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(cache.cpu().numpy(), oracle.insert_keys(bits, slots, base))
+
+
+# ---------------------------------------------------------------------------
+# failure detection: a wait that gives up (no fault, no hang)
+# ---------------------------------------------------------------------------
+
+def test_wait_give_up_sets_timeout_then_next_call_is_clean():
+    """The split-row waits are made to wait for a segment that never comes,
+    with a 1 ms give-up time: the call returns, the error word carries
+    IDX_DEV_TIMEOUT, and a normal call right after is in parity."""
+    d = synth.make_decode_from_lens([9000, 3000, 2500, 40000], [1, 1, 1, 1], 1, seed=81)
+    dd = _to(d)
+    err = _err()
+    lens = _expand(dd, err)
+    torch.cuda.synchronize()
+    saib.indexer_debug_wait_limit(1_000_000, stall_split_rows=True)
+    try:
+        saib.indexer_decode_topk(dd.q, dd.w, dd.cache, dd.block_table, lens, 1, 2048,
+                                 dev_error=err)
+        torch.cuda.synchronize()
+    finally:
+        saib.indexer_debug_wait_limit(0)
+    assert int(err.item()) & saib.binding.DEV_TIMEOUT
+    _check_decode(d, 2048)
+
+
+# ---------------------------------------------------------------------------
+# the on-device work split itself
+# ---------------------------------------------------------------------------
+
+def _device_plan(d, k):
+    """Runs the decode top-k and reads the work split the prep kernel left in
+    the workspace, next to the expected split of test_schedule's restatement."""
+    from test_schedule import split
+    dd = _to(d)
+    R, G = d.num_reqs, d.next_n
+    err = _err()
+    lens = _expand(dd, err)
+    ws = saib.decode_workspace(R, G, k, DEV)
+    saib.indexer_decode_topk(dd.q, dd.w, dd.cache, dd.block_table, lens, G, k, workspace=ws,
+                             dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    offs, grid, (pen, div) = saib.indexer_debug_decode_plan(R, G, k)
+    lens_h = lens.cpu().numpy().reshape(R, G)
+
+    def arr(name, n):
+        o = offs[name]
+        return ws[o:o + 4 * n].view(torch.int32).cpu().numpy()
+
+    act = np.where(lens_h > k, lens_h, 0)
+    tiles = ((act.max(axis=1) + 127) // 128).astype(np.int64)
+    T = int(tiles.sum())
+    wts = arr("wr_tile_start", R + 1)
+    assert np.array_equal(wts, np.concatenate([[0], np.cumsum(tiles)]))
+    if T == 0:
+        return
+    nC = min(grid, T)
+    share = T // nC
+    penalty = pen + (share // div if div > 0 and share >= 64 else 0)
+    _, ranges = split(tiles.tolist(), grid, penalty)
+    cta_tile = arr("cta_tile", nC + 1)
+    assert np.array_equal(cta_tile, [a for a, _ in ranges] + [T]), "split differs"
+    # exact cover, every CTA at least one tile
+    assert cta_tile[0] == 0 and cta_tile[-1] == T and np.all(np.diff(cta_tile) >= 1)
+    row_ctas = arr("row_ctas", 2 * R).reshape(R, 2)
+    cta_row = arr("cta_row", grid)
+    slots = set()
+    for w in range(R):
+        if tiles[w] == 0:
+            assert tuple(row_ctas[w]) == (0, -1)
+            continue
+        rs, re = wts[w], wts[w + 1]
+        touching = [c for c in range(nC) if cta_tile[c] < re and cta_tile[c + 1] > rs]
+        assert touching == list(range(row_ctas[w][0], row_ctas[w][1] + 1))
+        for c in touching:                     # one candidate slot per (CTA, row)
+            assert c + w not in slots and c + w < grid + R
+            slots.add(c + w)
+    for c in range(nC):
+        w = int(np.searchsorted(wts[:-1], cta_tile[c], side="right")) - 1
+        assert cta_row[c] == w and wts[w] <= cta_tile[c] < wts[w + 1]
+    # split rows start in distinct CTAs (their histograms and lists)
+    firsts = [row_ctas[w][0] for w in range(R) if tiles[w] and row_ctas[w][1] > row_ctas[w][0]]
+    assert len(firsts) == len(set(firsts))
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "mtp", "long"])
+def test_device_plan_workloads(name):
+    d = synth.make_decode(name)
+    _device_plan(d, 2048)
+
+
+def test_device_plan_degenerate_shapes():
+    _device_plan(synth.make_decode_from_lens([2100], [1], 1, seed=90), 2048)      # one tile
+    _device_plan(synth.make_decode_from_lens([3000, 2049, 9000], [1, 1, 1], 1, seed=91), 2048)
+    _device_plan(synth.make_decode_from_lens([0, 100, 5000], [0, 1, 2], 2, seed=92), 64)
+    _device_plan(synth.make_decode_from_lens([131072, 5], [1, 1], 1, seed=93), 2048)
