@@ -49,6 +49,13 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-counters", metavar="NCU_REPORT",
+                    help="store the DRAM and tensor-pipe counters of the one score/select "
+                         "launch in this ncu report as --workload's entry of "
+                         "profiles/score_select_counters.json, then exit")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="measure only --workload (by default the decode-batch run also "
+                         "measures the long-context and MTP configurations)")
     ap.add_argument("--seed", type=int, default=0x5EED)
     return ap.parse_args()
 
@@ -186,24 +193,18 @@ def kernel_code_hash(root: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per score/select launch from the committed ncu summary of
-    the decode-batch workload, or None when that summary was taken on other
-    kernel sources (or another workload is being run)."""
-    if workload != "decode":
-        return None
-    fields = {}
+def profiled_counters(workload: str):
+    """The ncu counters of one score/select launch on `workload` (DRAM bytes
+    read + written, tensor-pipe activity), from profiles/score_select_counters.json,
+    or None when they were taken on other kernel sources (or not at all)."""
     try:
-        with open(os.path.join(ROOT, "profiles", "score_select_decode_batch.md")) as f:
-            for line in f:
-                k, _, v = line.strip().partition(":")
-                if k in ("source_sha256_16", "dram_bytes_per_launch"):
-                    fields[k] = v.strip()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "score_select_counters.json")) as f:
+            entry = json.load(f).get(workload)
+    except (OSError, ValueError):
         return None
-    if fields.get("source_sha256_16") != kernel_code_hash(ROOT):
+    if not entry or entry.get("source_sha256_16") != kernel_code_hash(ROOT):
         return None
-    return int(fields["dram_bytes_per_launch"])
+    return entry
 
 
 def measured_peak_fp8_tflops():
@@ -380,23 +381,19 @@ def run_insert(args, rank, world, local):
             "clocks": clk.summary(), "gpu_launches": K}), flush=True)
 
 
-def run_ours(args, rank, world, local):
+def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
+    """Device-timed decode steps on `workload` (expand + decode top-k through
+    the C ABI, CUDA graphs of the K steps, every step on its own copy of the
+    index cache so the copies together exceed L2 several times), the live mean
+    duration of the score/select kernel (CUDA events on the launch stream) and
+    the clocks sampled meanwhile. Returns a dict; the inputs for the end-to-end
+    leg are in it too."""
     import torch
 
     import synth
     import sparse_attention_indexer_block_gb300 as saib
-    from sparse_attention_indexer_block_gb300 import build as libbuild
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    libbuild.build()
-    saib.load()
-
-    seed = rank_seed(args.seed, rank)
-    d = synth.make_decode(args.workload, seed=seed, device=dev)
+    d = synth.make_decode(workload, seed=seed, device=dev)
     R, G, k = d.num_reqs, d.next_n, d.topk
     seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
     dl_h = d.decode_lens.cpu().numpy().astype(np.int64)
@@ -424,20 +421,19 @@ def run_ours(args, rank, world, local):
                                  out_idx=out, workspace=ws, dev_error=err, stream=stream)
 
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
+        for i in range(3):
             step(i)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())} during warm-up")
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up ({workload})")
 
     # CUDA graph of the K timed steps (replayed in pieces of at most 1000 steps)
-    K = args.steps
-    piece = min(K, 1000)
+    piece = min(steps, 1000)
     graphs = []
     done = 0
     with torch.cuda.stream(stream):
-        while done < K:
-            n = min(piece, K - done)
+        while done < steps:
+            n = min(piece, steps - done)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(done, done + n):
@@ -445,7 +441,6 @@ def run_ours(args, rank, world, local):
             graphs.append(g)
             done += n
     torch.cuda.synchronize()
-    launches = 3 * K  # expand, prep, score per step
 
     def barrier():
         if world > 1:
@@ -471,19 +466,17 @@ def run_ours(args, rank, world, local):
         barrier()
     ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
     if int(err.item()) != 0:
-        raise RuntimeError(f"device error word {int(err.item())} in the timed region")
-    value = whole_job_rate(keys_per_step, K, world, ms)
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region ({workload})")
 
     # live per-launch duration of the score/select kernel (eager, same rotation)
-    n_prof = min(K, 400)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_prof)]
+           for _ in range(prof_steps)]
     for a, b in evs:  # torch creates the event handles on first record
         a.record(stream)
         b.record(stream)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for i in range(n_prof):
+        for i in range(prof_steps):
             saib.indexer_profile_events(*evs[i])
             step(i)
         saib.indexer_profile_events(None, None)
@@ -492,15 +485,50 @@ def run_ours(args, rank, world, local):
     kern_avg = statistics.mean(kern_ms)
     peak, peak_kind = measured_peak_gbs()
     achieved = algo_bytes / (kern_avg / 1e3) / 1e9
+    counters = profiled_counters(workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload),
+                "frac": round(achieved / peak, 4),
+                "traffic": counters["dram_bytes_per_launch"] if counters else None,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                 "measured" else "fallback 6.8 TB/s",
-                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum, "
-                                   "profiles/score_select_decode_batch.md (same kernel sources)"),
+                "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                   "launch on the same kernel sources, "
+                                   "profiles/score_select_counters.json"),
                 "kernel": f"score_select_kernel<{G},false>", "kernel_ms_avg": round(kern_avg, 5),
                 "kernel_ms_median": round(statistics.median(kern_ms), 5),
+                "kernel_launches_timed": prof_steps,
                 "algorithmic_bytes_per_launch": algo_bytes}
+    if counters and counters.get("tensor_pipe_pct_of_active") is not None:
+        roofline["tensor_pipe_pct_of_active"] = counters["tensor_pipe_pct_of_active"]
+    return {"d": d, "R": R, "G": G, "k": k, "ms": ms, "steps": steps,
+            "keys_per_step": keys_per_step, "algo_bytes": algo_bytes, "roofline": roofline,
+            "clocks": clk.summary(), "n_copies": n_copies, "cache_bytes": cache_bytes, "l2": l2,
+            "ws": ws, "out": out, "lens": lens, "err": err, "stream": stream,
+            "row_lens_h": row_lens_h}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import sparse_attention_indexer_block_gb300 as saib
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    libbuild.build()
+    saib.load()
+
+    seed = rank_seed(args.seed, rank)
+    K = args.steps
+    res = measure_decode(args.workload, seed, dev, K, min(K, 400), world, local)
+    d, R, G, k = res["d"], res["R"], res["G"], res["k"]
+    ms, keys_per_step, algo_bytes = res["ms"], res["keys_per_step"], res["algo_bytes"]
+    value = whole_job_rate(keys_per_step, K, world, ms)
+    launches = 3 * K  # expand, prep, score per step
+    lens, out, ws, err, stream = res["lens"], res["out"], res["ws"], res["err"], res["stream"]
 
     # end to end: pinned host inputs in, indices out, every step
     host = {n: t.cpu().pin_memory() for n, t in
@@ -520,6 +548,12 @@ def run_ours(args, rank, world, local):
                                  out_idx=out, workspace=ws, dev_error=err, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
     n_e2e = max(3, min(K, 50))
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -537,9 +571,24 @@ def run_ours(args, rank, world, local):
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
 
+    # the other decode configurations the throughput target names (long
+    # context) or that share the kernel (MTP), measured the same way
+    extra = {}
+    if args.workload == WORKLOAD and not args.no_extra_configs:
+        host = dbuf = None
+        torch.cuda.empty_cache()
+        for wl, steps in (("long", 100), ("mtp", 300)):
+            r = measure_decode(wl, seed, dev, steps, min(steps, 100), world, local)
+            extra[wl] = {"workload": WORKLOAD_DESCS[wl], "metric_value": whole_job_rate(
+                r["keys_per_step"], steps, world, r["ms"]), "unit": "keys/s",
+                "ms_per_step": r["ms"] / steps, "steps": steps, "roofline": r["roofline"],
+                "clocks": r["clocks"], "gpu_launches": 3 * steps}
+            del r
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(d, row_lens_h)
+        cpu = cpu_baseline(d, res["row_lens_h"])
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": K,
@@ -550,14 +599,16 @@ def run_ours(args, rank, world, local):
                            "requests": R, "next_n": G, "topk": k,
                            "keys_per_step": keys_per_step,
                            "index_bytes_per_step": algo_bytes,
-                           "l2": f"cold: {n_copies} rotating index-cache copies "
-                                 f"({n_copies * cache_bytes / 2**20:.0f} MiB > 3 x L2 "
-                                 f"{l2 / 2**20:.0f} MiB)",
+                           "l2": f"cold: {res['n_copies']} rotating index-cache copies "
+                                 f"({res['n_copies'] * res['cache_bytes'] / 2**20:.0f} MiB > 3 x "
+                                 f"L2 {res['l2'] / 2**20:.0f} MiB)",
                            "timing": "CUDA events around CUDA-graph replays of K steps",
                            "parallelism": f"replicas x{world}"},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "clocks": clk.summary(), "gpu_launches": launches,
+                "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": res["clocks"], "gpu_launches": launches,
                 "hbm_gbs_index_stream": round(algo_bytes * K / (ms / 1e3) / 1e9, 1)}
+        if extra:
+            line["configs"] = extra
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -652,8 +703,59 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+COUNTER_METRICS = ("gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
+                   "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active")
+
+
+def record_counters(report: str, workload: str):
+    """Adds `workload`'s entry to profiles/score_select_counters.json from an
+    ncu report of one score/select launch on that workload (ncu -i ... --page
+    raw --csv), keyed by the current kernel-code hash."""
+    import csv
+    import io
+    raw = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], check=True,
+                         capture_output=True, text=True).stdout
+    rows = list(csv.reader(io.StringIO(raw)))
+    hdr, units = rows[0], rows[1]
+    found = [r for r in rows[2:] if any("score_select_kernel" in c for c in r)]
+    if len(found) != 1:
+        raise SystemExit(f"expected one score_select launch in {report}, found {len(found)}")
+    vals = dict(zip(hdr, found[0]))
+    unit = dict(zip(hdr, units))
+
+    def num(name, scale_to):
+        v = float(vals[name].replace(",", ""))
+        u = unit.get(name, "")
+        mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6,
+                "GB": 1e9, "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1,
+                "ns": 1e-9, "us": 1e-6, "ms": 1e-3, "%": 1, "": 1}[u]
+        return v * mult / scale_to
+    entry = {"source_sha256_16": kernel_code_hash(ROOT),
+             "kernel": next(c for c in found[0] if "score_select_kernel" in c),
+             "dram_bytes_read": int(num("dram__bytes_read.sum", 1)),
+             "dram_bytes_write": int(num("dram__bytes_write.sum", 1)),
+             "gpu_time_us_cold_serialised": round(num("gpu__time_duration.sum", 1e-6), 2)}
+    entry["dram_bytes_per_launch"] = entry["dram_bytes_read"] + entry["dram_bytes_write"]
+    tp = "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"
+    entry["tensor_pipe_pct_of_active"] = round(num(tp, 1), 2) if tp in vals else None
+    path = os.path.join(ROOT, "profiles", "score_select_counters.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data[workload] = entry
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({workload: entry}))
+
+
 def main():
     args = parse()
+    if args.record_counters:
+        record_counters(args.record_counters, args.workload)
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)

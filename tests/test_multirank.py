@@ -95,25 +95,26 @@ def test_reference_arm_line(capsys):
 
 
 def test_profiled_traffic_only_for_the_profiled_kernel_code(tmp_path, monkeypatch):
-    """bench.py reports the ncu DRAM bytes only while the kernel's code (not
-    its comments) hashes to the value recorded with the capture."""
+    """bench.py reports the ncu DRAM bytes of a workload only while the
+    kernel's code (not its comments) hashes to the value recorded with the
+    capture."""
     sys.path.insert(0, ROOT)
     import shutil
 
     import bench
-    assert bench.profiled_traffic("long") is None
     csrc = os.path.join(ROOT, "sparse_attention_indexer_block_gb300", "csrc")
     fake = tmp_path / "sparse_attention_indexer_block_gb300" / "csrc"
     shutil.copytree(csrc, fake)
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "score_select_decode_batch.md").write_text(
-        f"    source_sha256_16: {bench.kernel_code_hash(str(tmp_path))}\n"
-        "    dram_bytes_per_launch: 1234\n")
+    (tmp_path / "profiles" / "score_select_counters.json").write_text(json.dumps(
+        {"decode": {"source_sha256_16": bench.kernel_code_hash(str(tmp_path)),
+                    "dram_bytes_per_launch": 1234}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profiled_traffic("decode") == 1234
+    assert bench.profiled_counters("decode")["dram_bytes_per_launch"] == 1234
+    assert bench.profiled_counters("long") is None
     with open(fake / "common.cuh", "a") as f:
         f.write("\n// a comment only\n")
-    assert bench.profiled_traffic("decode") == 1234
+    assert bench.profiled_counters("decode")["dram_bytes_per_launch"] == 1234
     with open(fake / "common.cuh", "a") as f:
         f.write("\nconstexpr int kUnusedForTest = 1;\n")
-    assert bench.profiled_traffic("decode") is None
+    assert bench.profiled_counters("decode") is None
