@@ -178,13 +178,14 @@ def measured_peak_gbs():
 
 
 def kernel_code_hash(root: str) -> str:
-    """First 16 hex digits of the sha256 of the score/select kernel's code
-    (score_select.cu, common.cuh, internal.h without comments or whitespace)."""
+    """First 16 hex digits of the sha256 of the score/select and split-row
+    selection kernels' code (score_select.cu, row_select.cu, common.cuh,
+    internal.h without comments or whitespace)."""
     import hashlib
     import re
     csrc = os.path.join(root, "sparse_attention_indexer_block_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("score_select.cu", "common.cuh", "internal.h"):
+    for name in ("score_select.cu", "row_select.cu", "common.cuh", "internal.h"):
         with open(os.path.join(csrc, name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -194,9 +195,10 @@ def kernel_code_hash(root: str) -> str:
 
 
 def profiled_counters(workload: str):
-    """The ncu counters of one score/select launch on `workload` (DRAM bytes
-    read + written, tensor-pipe activity), from profiles/score_select_counters.json,
-    or None when they were taken on other kernel sources (or not at all)."""
+    """The ncu counters of one score/select launch and the split-row selection
+    launch after it on `workload` (DRAM bytes read + written, tensor-pipe
+    activity of the score kernel), from profiles/score_select_counters.json, or
+    None when they were taken on other kernel sources (or not at all)."""
     try:
         with open(os.path.join(ROOT, "profiles", "score_select_counters.json")) as f:
             entry = json.load(f).get(workload)
@@ -492,9 +494,12 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                 "measured" else "fallback 6.8 TB/s",
                 "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
-                                   "launch on the same kernel sources, "
+                                   "score/select launch and its split-row selection launch "
+                                   "on the same kernel sources, "
                                    "profiles/score_select_counters.json"),
-                "kernel": f"score_select_kernel<{G},false>", "kernel_ms_avg": round(kern_avg, 5),
+                "kernel": f"score_select_kernel<{G},false> + row_select_kernel (events "
+                          "around both launches)",
+                "kernel_ms_avg": round(kern_avg, 5),
                 "kernel_ms_median": round(statistics.median(kern_ms), 5),
                 "kernel_launches_timed": prof_steps,
                 "algorithmic_bytes_per_launch": algo_bytes}
@@ -527,7 +532,7 @@ def run_ours(args, rank, world, local):
     d, R, G, k = res["d"], res["R"], res["G"], res["k"]
     ms, keys_per_step, algo_bytes = res["ms"], res["keys_per_step"], res["algo_bytes"]
     value = whole_job_rate(keys_per_step, K, world, ms)
-    launches = 3 * K  # expand, prep, score per step
+    launches = 4 * K  # expand, prep, score/select, split-row selection per step
     lens, out, ws, err, stream = res["lens"], res["out"], res["ws"], res["err"], res["stream"]
 
     # end to end: pinned host inputs in, indices out, every step
@@ -582,7 +587,7 @@ def run_ours(args, rank, world, local):
             extra[wl] = {"workload": WORKLOAD_DESCS[wl], "metric_value": whole_job_rate(
                 r["keys_per_step"], steps, world, r["ms"]), "unit": "keys/s",
                 "ms_per_step": r["ms"] / steps, "steps": steps, "roofline": r["roofline"],
-                "clocks": r["clocks"], "gpu_launches": 3 * steps}
+                "clocks": r["clocks"], "gpu_launches": 4 * steps}
             del r
             torch.cuda.empty_cache()
 
@@ -709,35 +714,44 @@ COUNTER_METRICS = ("gpu__time_duration.sum", "dram__bytes_read.sum", "dram__byte
 
 def record_counters(report: str, workload: str):
     """Adds `workload`'s entry to profiles/score_select_counters.json from an
-    ncu report of one score/select launch on that workload (ncu -i ... --page
-    raw --csv), keyed by the current kernel-code hash."""
+    ncu report of one score/select launch and the split-row selection launch
+    after it on that workload (ncu -i ... --page raw --csv), keyed by the
+    current kernel-code hash. DRAM bytes and times are the two launches' sums."""
     import csv
     import io
     raw = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], check=True,
                          capture_output=True, text=True).stdout
     rows = list(csv.reader(io.StringIO(raw)))
     hdr, units = rows[0], rows[1]
-    found = [r for r in rows[2:] if any("score_select_kernel" in c for c in r)]
-    if len(found) != 1:
-        raise SystemExit(f"expected one score_select launch in {report}, found {len(found)}")
-    vals = dict(zip(hdr, found[0]))
     unit = dict(zip(hdr, units))
+    launches = {}
+    for name in ("score_select_kernel", "row_select_kernel"):
+        found = [r for r in rows[2:] if any(name in c for c in r)]
+        if len(found) != 1:
+            raise SystemExit(f"expected one {name} launch in {report}, found {len(found)}")
+        launches[name] = dict(zip(hdr, found[0]))
 
-    def num(name, scale_to):
+    def num(vals, name, scale_to):
         v = float(vals[name].replace(",", ""))
         u = unit.get(name, "")
         mult = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6,
                 "GB": 1e9, "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1,
                 "ns": 1e-9, "us": 1e-6, "ms": 1e-3, "%": 1, "": 1}[u]
         return v * mult / scale_to
+
+    def total(name, scale_to):
+        return sum(num(v, name, scale_to) for v in launches.values())
+    score = launches["score_select_kernel"]
     entry = {"source_sha256_16": kernel_code_hash(ROOT),
-             "kernel": next(c for c in found[0] if "score_select_kernel" in c),
-             "dram_bytes_read": int(num("dram__bytes_read.sum", 1)),
-             "dram_bytes_write": int(num("dram__bytes_write.sum", 1)),
-             "gpu_time_us_cold_serialised": round(num("gpu__time_duration.sum", 1e-6), 2)}
+             "kernel": next(c for c in score.values() if "score_select_kernel" in c),
+             "dram_bytes_read": int(total("dram__bytes_read.sum", 1)),
+             "dram_bytes_write": int(total("dram__bytes_write.sum", 1)),
+             "gpu_time_us_cold_serialised": round(total("gpu__time_duration.sum", 1e-6), 2),
+             "row_select_gpu_time_us_cold_serialised": round(
+                 num(launches["row_select_kernel"], "gpu__time_duration.sum", 1e-6), 2)}
     entry["dram_bytes_per_launch"] = entry["dram_bytes_read"] + entry["dram_bytes_write"]
     tp = "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active"
-    entry["tensor_pipe_pct_of_active"] = round(num(tp, 1), 2) if tp in vals else None
+    entry["tensor_pipe_pct_of_active"] = round(num(score, tp, 1), 2) if tp in score else None
     path = os.path.join(ROOT, "profiles", "score_select_counters.json")
     try:
         with open(path) as f:

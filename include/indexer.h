@@ -323,8 +323,8 @@ idx_status indexer_debug_wait_limit(uint64_t limit_ns, int32_t stall_split_rows)
  * library, held until the process exits); the call allocates nothing. Same
  * arguments and results as indexer_decode_topk without the workspace.
  *  - Limit: the batch must fit the scratch, i.e. indexer_decode_workspace_bytes
- *    (num_reqs, next_n, topk) <= 64 MiB (about 1050 requests at next_n = 1, 430
- *    at next_n = 2, top-2048, 152 SMs); a larger batch returns
+ *    (num_reqs, next_n, topk) <= 64 MiB (about 5700 requests at next_n = 1,
+ *    2050 at next_n = 2, top-2048, 152 SMs); a larger batch returns
  *    IDX_ERR_WORKSPACE before any work.
  *  - The first call on each device looks the scratch's device address up (this
  *    may load the library's device code); make that first call before any

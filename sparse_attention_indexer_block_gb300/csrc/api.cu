@@ -19,37 +19,59 @@ thread_local size_t g_trace_bytes = 0;
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 
-// Score/select launch bracketed by the profiling events when they are set.
-idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map, int nC,
+// Give-up time of the kernels' waits: 2 s, or the test setting of this thread;
+// with g_stall_rows the split-row selection waits for a segment that never
+// comes.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+thread_local uint64_t g_wait_ns = kDefaultWaitNs;
+thread_local int32_t g_stall_rows = 0;
+
+// The score/select launch and, in top-k mode, the split-row selection after
+// it, bracketed by the profiling events when they are set.
+idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                        cudaStream_t s) {
   if (g_prof_start) {
     const idx_status st = cuda_status(cudaEventRecord(g_prof_start, s));
     if (st != IDX_OK) return st;
   }
-  const idx_status st = launch_score(G, logits, p, map, nC, s);
+  const int streams = score_streams();
+  idx_status st = launch_score(G, logits, p, map, score_grid(), s);
+  if (st == IDX_OK && !logits) {
+    RowSelectParams r{};
+    r.wr = p.wr;
+    r.wr_tile_start = p.wr_tile_start;
+    r.cta_row = p.cta_row;
+    r.row_ctas = p.row_ctas;
+    r.row_len = p.row_len;
+    r.seg_counter = p.seg_counter;
+    r.slot_key = p.slot_key;
+    r.slot_idx = p.slot_idx;
+    r.seg_cum = p.seg_cum;
+    r.slot_cap = p.slot_cap;
+    r.row_hist = p.row_hist;
+    r.num_wr = p.num_wr;
+    r.streams = streams;
+    r.G = G;
+    r.topk = p.topk;
+    r.out_idx = p.out_idx;
+    r.out_row_base = p.out_row_base;
+    r.dev_error = p.dev_error;
+    r.wait_ns = g_wait_ns;
+    r.stall = g_stall_rows ? 1 : 0;
+    const int64_t grid = max_split_rows(p.num_wr, streams) * G;
+    // trace slots after the score kernel's (when the buffer holds both)
+    size_t tb = 0;
+    uint64_t* tbuf = trace_buffer(&tb);
+    const size_t score_slots = static_cast<size_t>(kTrSlots) * streams;
+    if (tbuf && tb >= 8 * (score_slots + static_cast<size_t>(kSelTrSlots) * grid))
+      r.trace = tbuf + score_slots;
+    st = launch_row_select(r, static_cast<int>(grid), s);
+  }
   if (st == IDX_OK && g_prof_stop) return cuda_status(cudaEventRecord(g_prof_stop, s));
   return st;
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-// Give-up time of the kernels' waits: 2 s, or the test setting of this thread;
-// with g_stall_rows the split-row waits wait for a segment that never comes.
-constexpr uint64_t kDefaultWaitNs = 2000000000ull;
-thread_local uint64_t g_wait_ns = kDefaultWaitNs;
-thread_local int32_t g_stall_rows = 0;
-
-// The split-row selection state of a launch: counters, cutoff-bin lists and
-// the wait limit.
-void set_split_lists(ScoreParams* p, uint8_t* ws, const WsLayout& L, int G) {
-  p->row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
-  p->tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
-  p->elist_key = reinterpret_cast<uint32_t*>(ws + L.elist_key);
-  p->elist_idx = reinterpret_cast<int32_t*>(ws + L.elist_idx);
-  p->elist_cap = elist_capacity(G);
-  p->wait_ns = g_wait_ns;
-  p->wait_extra = g_stall_rows ? 1 : 0;
-}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -71,32 +93,25 @@ WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas) 
     off += bytes;
     return o;
   };
-  const int64_t nslots = static_cast<int64_t>(num_ctas) + num_wr;
+  const int64_t nslots = 2 * static_cast<int64_t>(num_ctas);  // segment_slot
   const int64_t nsplit = max_split_rows(num_wr, num_ctas);
   L.wr = take(sizeof(WorkRow) * static_cast<size_t>(num_wr), 256);
   L.wr_tile_start = take(4 * static_cast<size_t>(num_wr + 1), 256);
   L.row_len = take(4 * static_cast<size_t>(rows), 256);
-  // per work row its segment counter, per token row its output / list
-  // position pair and tie counter (all zeroed by the prep kernel)
+  // per work row its segment counter (zeroed by the prep kernel)
   L.seg_counter = take(4 * static_cast<size_t>(num_wr), 256);
-  L.row_pos = take(8 * static_cast<size_t>(num_wr) * G, 256);
-  L.tie_count = take(4 * static_cast<size_t>(num_wr) * G, 256);
-  L.slot_count = take(4 * static_cast<size_t>(nslots * G), 256);
+  L.seg_cum = take(4 * static_cast<size_t>(nslots * G) * kRowHistBins, 256);
   L.q8 = take(static_cast<size_t>(rows) * kQRowBytes, 1024);
   L.wprime = take(4 * static_cast<size_t>(rows) * kHeads, 256);
   const size_t cap = static_cast<size_t>(candidate_capacity(G));
   L.slot_key = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
   L.slot_idx = take(4 * static_cast<size_t>(nslots * G) * cap, 256);
-  L.row_hist_words = static_cast<size_t>(nsplit) * G * 4096;  // four digit levels
+  L.row_hist_words = static_cast<size_t>(nsplit) * G * kRowHistBins;
   L.row_hist = take(4 * L.row_hist_words, 256);
   L.cta_row = take(4 * static_cast<size_t>(num_ctas), 256);
-  L.slot_thrbin = take(4 * static_cast<size_t>(nslots * G), 256);
   L.cta_tile = take(4 * static_cast<size_t>(num_ctas + 1), 256);
   L.row_vs = take(4 * static_cast<size_t>(num_wr + 1), 256);
   L.row_ctas = take(8 * static_cast<size_t>(num_wr), 256);
-  const size_t ecap = static_cast<size_t>(elist_capacity(G));
-  L.elist_key = take(4 * static_cast<size_t>(nsplit) * G * ecap, 256);
-  L.elist_idx = take(4 * static_cast<size_t>(nsplit) * G * ecap, 256);
   L.total = round_up(off, 256);
   return L;
 }
@@ -270,10 +285,9 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
   p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
   p.slot_cap = candidate_capacity(next_n);
-  p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+  p.seg_cum = reinterpret_cast<uint32_t*>(ws + L.seg_cum);
   p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
-  p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
-  set_split_lists(&p, ws, L, next_n);
+  p.wait_ns = g_wait_ns;
   p.out_idx = out_idx;
   p.out_row_base = 0;
   p.topk = topk;
@@ -283,7 +297,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   size_t tb = 0;
   p.trace = trace_buffer(&tb);
   if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-  return timed_score(next_n, logits, p, map, score_grid(), s);
+  return timed_score(next_n, logits, p, map, s);
 }
 
 }  // namespace
@@ -538,10 +552,9 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.slot_key = reinterpret_cast<uint32_t*>(ws + L.slot_key);
     p.slot_idx = reinterpret_cast<int32_t*>(ws + L.slot_idx);
     p.slot_cap = candidate_capacity(kPrefillG);
-    p.slot_count = reinterpret_cast<int32_t*>(ws + L.slot_count);
+    p.seg_cum = reinterpret_cast<uint32_t*>(ws + L.seg_cum);
     p.row_hist = reinterpret_cast<uint32_t*>(ws + L.row_hist);
-    p.slot_thrbin = reinterpret_cast<int32_t*>(ws + L.slot_thrbin);
-    set_split_lists(&p, ws, L, kPrefillG);
+    p.wait_ns = g_wait_ns;
     p.out_idx = out_idx;
     p.out_row_base = lo;
     p.topk = topk;
@@ -549,7 +562,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     size_t tb = 0;
     p.trace = trace_buffer(&tb);
     if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-    if ((st = timed_score(kPrefillG, false, p, map, score_grid(), s)) != IDX_OK) return st;
+    if ((st = timed_score(kPrefillG, false, p, map, s)) != IDX_OK) return st;
   }
   return IDX_OK;
 }

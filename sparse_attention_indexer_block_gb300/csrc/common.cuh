@@ -277,6 +277,29 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
 }
 
 // -------------------------------------------------------------------------
+// packed fp32 pairs: two independent round-to-nearest fp32 FMAs per instruction
+// -------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+// (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi), each an fp32 fmaf.
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// -------------------------------------------------------------------------
 // fp8 conversion of two fp32 values (round to nearest even, saturate to 448)
 // -------------------------------------------------------------------------
 

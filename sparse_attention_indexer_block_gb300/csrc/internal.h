@@ -22,32 +22,31 @@ inline idx_status cuda_status(cudaError_t e) {
 }
 
 // Launches `kernel` on `stream` with programmatic stream serialization (the
-// kernel calls pdl_wait() before it reads anything earlier work wrote). A
-// cooperative launch (all CTAs resident at once, or the launch fails) is for
-// kernels whose CTAs wait on one another.
+// kernel calls pdl_wait() before it reads anything earlier work wrote).
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl_ex(bool cooperative, void (*kernel)(KArgs...), unsigned grid,
-                                 unsigned block, size_t smem, cudaStream_t stream,
-                                 Args&&... args) {
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = cooperative ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
-                              cudaStream_t stream, Args&&... args) {
-  return launch_pdl_ex(false, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
+// Row histogram of a split row: counts of its candidates' top 10 key bits.
+constexpr int kRowHistBins = 1024;
+
+// Slot of the segment that stream v holds of a split work row: only a
+// stream's first and last work rows can be split, so two slots per stream
+// (the first row's, and the last one's when it differs).
+__host__ __device__ __forceinline__ int64_t segment_slot(int v, bool first_row) {
+  return 2 * static_cast<int64_t>(v) + (first_row ? 0 : 1);
 }
 
 
@@ -66,21 +65,14 @@ struct ScoreParams {
   const int32_t* row_len;        // [rows] validated key count per token row
   const uint8_t* q8;             // [rows, 8192] swizzled fp8 images of q
   const float* wprime;           // [rows, 64] w * sq
-  int32_t* seg_counter;          // [num_wr] finished segments per work row
-  uint32_t* slot_key;            // [nslots, G, slot_cap] candidate keys of finished segments
+  int32_t* seg_counter;          // [num_wr] published segments per work row (zeroed by prep)
+  uint32_t* slot_key;            // [nslots, G, slot_cap] candidate keys of split-row segments,
+                                 // sorted by row bin, highest first
   int32_t* slot_idx;             // [nslots, G, slot_cap] their token indices
-  int32_t* slot_count;           // [nslots, G]
-  int32_t* slot_thrbin;          // [nslots, G] row-histogram bin of the segment's final threshold
+  uint32_t* seg_cum;             // [nslots, G, 1024] entries of each slot at or above every row bin
   int32_t slot_cap;              // entries per slot (the candidate buffer's capacity)
   uint32_t* row_hist;            // [nsplit, G, 1024] histograms of split work rows (zeroed by prep)
-  unsigned long long* row_pos;   // [num_wr, G] output positions taken (low word) and cutoff-list
-                                 // entries (high word) so far (zeroed by prep)
-  uint32_t* elist_key;           // [nsplit, G, elist_cap] keys in a split row's cutoff bin
-  int32_t* elist_idx;            // [nsplit, G, elist_cap] their token indices
-  int32_t* tie_count;            // [num_wr, G] equal keys taken at the last digit (zeroed by prep)
-  int32_t elist_cap;             // entries per cutoff-bin list
-  uint64_t wait_ns;              // give-up time of every pipeline and row wait
-  int32_t wait_extra;            // added to the split-row wait target (test hook; 0)
+  uint64_t wait_ns;              // give-up time of every pipeline wait
   int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
   int64_t out_row_base;
   int32_t topk;
@@ -112,11 +104,6 @@ constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : 2560; }
 // Pipeline stages (128-key tiles in flight) of the score/select kernel.
 constexpr int score_stages(int G) { return G == 1 ? 8 : 4; }
 
-// Capacity of a split row's cutoff-bin list (entries per token row): each of
-// the kernel's two epilogue groups stages a list as key + index pairs in half
-// of the idle stage ring.
-constexpr int elist_capacity(int G) { return score_stages(G) * 16384 / 2 / 8; }
-
 // Split work rows (rows whose tiles several CTAs share) that one launch can
 // have: each starts in a different CTA, and there is at most one per work row.
 inline int64_t max_split_rows(int64_t num_wr, int num_ctas) {
@@ -125,9 +112,8 @@ inline int64_t max_split_rows(int64_t num_wr, int num_ctas) {
 
 // Workspace carve-up shared by decode and prefill.
 struct WsLayout {
-  size_t wr, wr_tile_start, row_len, seg_counter, slot_count, q8, wprime, slot_key, slot_idx;
-  size_t row_hist, row_hist_words, cta_row, slot_thrbin, cta_tile, row_vs, row_ctas;
-  size_t row_pos, elist_key, elist_idx, tie_count;
+  size_t wr, wr_tile_start, row_len, seg_counter, seg_cum, q8, wprime, slot_key, slot_idx;
+  size_t row_hist, row_hist_words, cta_row, cta_tile, row_vs, row_ctas;
   size_t total;
 };
 WsLayout ws_layout(int64_t num_wr, int64_t rows, int G, int topk, int num_ctas);
@@ -166,8 +152,6 @@ struct DecodePrepArgs {
   // a segment's drop threshold (more buffer cuts): the penalty grows by the
   // per-CTA tile share divided by this (0: no growth).
   int32_t row_penalty_div;
-  unsigned long long* row_pos = nullptr;  // [num_reqs, next_n], zeroed (set by the launcher)
-  int32_t* tie_count = nullptr;           // [num_reqs, next_n], zeroed (set by the launcher)
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -186,8 +170,6 @@ struct PrefillPrepArgs {
   uint32_t* err;
   int32_t num_ctas;     // grid of the score/select launch that follows
   int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
-  unsigned long long* row_pos = nullptr;  // [num_wr, 2], zeroed (set by the launcher)
-  int32_t* tie_count = nullptr;           // [num_wr, 2], zeroed (set by the launcher)
 };
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);
@@ -198,6 +180,40 @@ uint64_t* trace_buffer(size_t* bytes);
 
 idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s);
+
+// Everything the split-row selection kernel reads, for one launch (after the
+// score/select launch, on the same workspace).
+struct RowSelectParams {
+  const WorkRow* wr;
+  const int32_t* wr_tile_start;
+  const int32_t* cta_row;        // [streams] work row holding each stream's first tile
+  const int2* row_ctas;          // [num_wr] first and last stream of each work row
+  const int32_t* row_len;
+  const int32_t* seg_counter;
+  const uint32_t* slot_key;
+  const int32_t* slot_idx;
+  const uint32_t* seg_cum;
+  int32_t slot_cap;
+  const uint32_t* row_hist;
+  int32_t num_wr;
+  int32_t streams;               // tile streams the score/select launch was planned over
+  int32_t G;
+  int32_t topk;
+  int32_t* out_idx;
+  int64_t out_row_base;
+  uint32_t* dev_error;
+  uint64_t wait_ns;
+  int32_t stall;                 // test hook: wait for a segment that never comes (0)
+  uint64_t* trace;               // optional: kSelTrSlots per CTA
+};
+// Trace slots of one split-row selection CTA (ns from %globaltimer, or counts).
+enum SelTraceSlot {
+  kSelTrEntry = 0, kSelTrWaited, kSelTrPrefix, kSelTrCut0, kSelTrEmit0, kSelTrEnd, kSelTrCand,
+  kSelTrBin0, kSelTrBin1, kSelTrPath, kSelTrSegs, kSelTrSlots = 16
+};
+// One CTA per (possible split row, token row):
+// max_split_rows(num_wr, streams) * G CTAs.
+idx_status launch_row_select(const RowSelectParams& p, int grid, cudaStream_t s);
 
 // The score/select kernel runs one CTA per SM, each CTA two tile streams
 // ("virtual CTAs"): the work split is planned over score_streams() ranges and

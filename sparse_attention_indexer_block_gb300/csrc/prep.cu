@@ -252,18 +252,6 @@ __device__ void plan_ctas(const int32_t* wts, const int32_t* vs, int num_wr, int
   }
 }
 
-// Zeroes work row w's counters: its segment counter and, per token row, its
-// output / cutoff-list position pair and tie counter ([num_wr, G] each).
-__device__ __forceinline__ void zero_row_counters(int32_t* seg_counter,
-                                                  unsigned long long* row_pos,
-                                                  int32_t* tie_count, int G, int w) {
-  seg_counter[w] = 0;
-  for (int g = 0; g < G; ++g) {
-    row_pos[static_cast<int64_t>(w) * G + g] = 0ull;
-    tie_count[static_cast<int64_t>(w) * G + g] = 0;
-  }
-}
-
 // Zeroes n 32-bit words (16-byte aligned) with the blocks after block 0.
 __device__ __forceinline__ void zero_words(uint32_t* p, size_t n) {
   const size_t tid = static_cast<size_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x;
@@ -307,7 +295,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
         }
         tiles = (maxlen + kTileKeys - 1) / kTileKeys;
         wr[b] = WorkRow{b, b * G, G, maxlen};
-        zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, b);
+        seg_counter[b] = 0;
       }
       int total;
       const int excl = block_exclusive_scan(tiles, &total);
@@ -420,7 +408,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
         }
         wr[idx] = WorkRow{rq, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
         wts[idx] = (maxlen + kTileKeys - 1) / kTileKeys;  // tile count, scanned below
-        zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, idx);
+        seg_counter[idx] = 0;
       }
       carry += total;
       __syncthreads();
@@ -429,7 +417,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     for (int idx = carry + threadIdx.x; idx < a.num_wr; idx += kPrepThreads) {
       wr[idx] = WorkRow{a.req_begin, 0, 0, 0};
       wts[idx] = 0;
-      zero_row_counters(seg_counter, a.row_pos, a.tie_count, G, idx);
+      seg_counter[idx] = 0;
     }
     __syncthreads();
     int run = 0;
@@ -635,8 +623,6 @@ idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t
 idx_status launch_decode_prep(const DecodePrepArgs& args, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s) {
   DecodePrepArgs a = args;
-  a.row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
-  a.tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
   const int64_t rows = static_cast<int64_t>(a.num_reqs) * a.next_n;
   const int grid = 1 + prep_grid(rows * kHeads);
   const cudaError_t e = launch_pdl(
@@ -653,8 +639,6 @@ idx_status launch_decode_prep(const DecodePrepArgs& args, uint8_t* ws, const WsL
 idx_status launch_prefill_prep(const PrefillPrepArgs& args, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s) {
   PrefillPrepArgs a = args;
-  a.row_pos = reinterpret_cast<unsigned long long*>(ws + L.row_pos);
-  a.tie_count = reinterpret_cast<int32_t*>(ws + L.tie_count);
   const int64_t rows = a.row_hi - a.row_lo;
   const int grid = 1 + prep_grid(rows * kHeads);
   const cudaError_t e = launch_pdl(

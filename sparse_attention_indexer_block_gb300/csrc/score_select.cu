@@ -1,7 +1,7 @@
 // Score + select: the persistent kernel of the indexer.
 //
-// One CTA per SM (tensor-core kernels are scheduled one CTA per SM), launched
-// cooperatively so that all CTAs are resident at once. A CTA runs two
+// One CTA per SM (the occupancy of tensor-core kernels is one CTA per SM). A
+// CTA runs two
 // independent tile streams: the global sequence of 128-key tiles (work rows in
 // order, each work row cut into ceil(maxlen / 128) tiles) is split into
 // 2 x gridDim contiguous ranges ("virtual CTAs"), and CTA c streams ranges 2c
@@ -23,9 +23,9 @@
 //           select that shrinks the buffer back to k when it fills. No logits
 //           row leaves the SM.
 // A work row covered by several streams is a set of segments. Each segment
-// publishes its candidates and their row-bin histogram; once a stream has
-// finished all its tiles, the streams that share a split row select it
-// together (select_split_rows).
+// publishes the candidates it kept and adds their row-bin histogram to the
+// row's; the row's top k is selected from them by the split-row selection
+// kernel that runs after this one.
 //
 // Scoring (the method's statement; the pages name the kernel only):
 //   logit[t, s] = sum_h w[t, h] ReLU(scale_s (q[t, h] . k_s))
@@ -44,7 +44,6 @@ constexpr int kEpiBase = 128;        // first epilogue thread
 constexpr int kEpiThreads = 128;     // threads of one epilogue group
 constexpr int kTeardownBarrier = 2;  // used once, by all warps, before TMEM is freed
 constexpr int kSetupBarrier = 3;     // used once, by all warps, after barrier init and TMEM alloc
-constexpr int kJointBarrier = 5;     // both epilogue groups, once, after their streams
 // (named barrier 1 belongs to epilogue group 0, 4 to group 1)
 
 // Epilogue group of this thread (0: warps 4-7, 1: warps 8-11), its thread
@@ -81,12 +80,9 @@ struct Cfg {
   static constexpr int kGTrace = kGMisc + 256;
   static constexpr int kGroupBytes = kGTrace + kTrSlots * 8;
   static constexpr int kBarOff = kGroupOff + 2 * kGroupBytes;
-  static constexpr int kNumBars = 2 * kStages + 4 * 4 + 2 + 2;
+  static constexpr int kNumBars = 2 * kStages + 4 * 4 + 2;
   static constexpr int kSharedOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kSharedOff + 64 + 1024;  // + alignment slack
-  // the idle ring, halved, holds one cutoff-bin list per group (key + index)
-  static constexpr int kListCap = kStages * 16384 / 2 / 8;
-  static_assert(kListCap == elist_capacity(G), "cutoff-bin list capacity");
   static_assert(kCap % kEpiThreads == 0, "capacity");
   static_assert(kCap >= IDX_MAX_TOPK, "a slot must hold any k");
   static_assert(kTmemCols <= 512, "tensor memory");
@@ -111,11 +107,6 @@ struct Misc {
   int scan[4];
   uint32_t rmin[4], rmax[4];
   int wcnt[2][4];   // [token][epilogue warp] entries in the warp's region
-  int staged_uses;  // phases of `staged` used so far
-  int pend[2];      // split work rows this group published a segment of (at most two)
-  int npend;
-  int sel_ok;
-  int bcast[4];     // values one thread hands to the group
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
@@ -138,7 +129,6 @@ struct Smem {
   uint64_t* qfull;   // [4] q slot 2j + b of stream j
   uint64_t* qempty;  // [4]
   uint64_t* done;    // [2] each stream's MMAs complete
-  uint64_t* staged;  // this group's completion of the bulk copies that stage a list
   Misc* misc;
   CtaShared* cs;
   uint64_t* trace;   // this stream's trace slots (shared memory, copied out at exit), or nullptr
@@ -167,7 +157,6 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int group) {
   s.qfull = s.tempty + 4;
   s.qempty = s.qfull + 4;
   s.done = s.qempty + 4;
-  s.staged = s.done + 2 + group;
   s.cs = reinterpret_cast<CtaShared*>(base + C::kSharedOff);
   s.group = group;
   return s;
@@ -182,7 +171,6 @@ struct Stream {
 
 // Row histogram over the top 10 bits of the order-preserving key: sign, the
 // 8 exponent bits and the leading mantissa bit (bins of half a binade).
-constexpr int kRowHistBins = 1024;
 __device__ __forceinline__ int row_bin(uint32_t key) { return static_cast<int>(key >> 22); }
 
 // Index of split work row w (first virtual CTA v_first) among the launch's
@@ -641,103 +629,21 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
   }
 }
 
-// From a row histogram: cut = max(floor, the highest bin whose suffix count
-// (keys in bins >= it) reaches K) and above = the count in bins > cut; cut is
-// -1 when the histogram holds fewer than K keys and floor < 0.
-// Row-histogram bins held by epilogue thread et in the cutoff scans:
-// [hi - kCutPer + 1, hi] with hi = kRowHistBins - 1 - et * kCutPer, c[j] = bin hi - j.
-constexpr int kCutPer = kRowHistBins / kEpiThreads;
-__device__ __forceinline__ int cut_hi() { return kRowHistBins - 1 - epi_tid() * kCutPer; }
-
-__device__ __forceinline__ void load_row_bins(const uint32_t* gh, int (&c)[kCutPer]) {
-  const int hi = cut_hi();
-#pragma unroll
-  for (int j = 0; j < kCutPer; ++j) c[j] = static_cast<int>(__ldcg(&gh[hi - j]));
-}
-
-// row_cutoff over counts already held by the threads (c as in load_row_bins).
-// *bcount (nullable) gets the cutoff bin's count when the cutoff is the bin
-// holding the K-th key (not raised to `floor`), else -1.
-__device__ __forceinline__ void row_cutoff_vals(const int (&c)[kCutPer], Misc* m, int K, int floor,
-                                                int* cut, int* above, int* bcount = nullptr) {
-  const int et = epi_tid();
-  if (et == 0) {
-    m->bucket = -1;
-    m->above = 0;
-    m->bcount = -1;
-  }
-  const int hi = cut_hi();
-  int local = 0, local_above_floor = 0;
-#pragma unroll
-  for (int j = 0; j < kCutPer; ++j) {
-    local += c[j];
-    local_above_floor += hi - j > floor ? c[j] : 0;
-  }
-  int total;
-  const int excl = epi_exclusive_scan(m, local, &total);  // contains a barrier
-  if (excl < K && K <= excl + local) {
-    int acc = excl;
-#pragma unroll
-    for (int j = 0; j < kCutPer; ++j) {
-      if (acc + c[j] >= K) {
-        m->bucket = hi - j;
-        m->above = acc;
-        m->bcount = c[j];
-        break;
-      }
-      acc += c[j];
-    }
-  }
-  epi_sync();
-  int cb = m->bucket, ab = m->above, bc = m->bcount;
-  epi_sync();
-  if (bcount) *bcount = cb >= floor ? bc : -1;
-  if (cb < floor) {
-    int tot_above;
-    epi_exclusive_scan(m, local_above_floor, &tot_above);
-    epi_sync();
-    cb = floor;
-    ab = tot_above;
-  }
-  *cut = cb;
-  *above = ab;
-}
-
-__device__ __forceinline__ void row_cutoff(const uint32_t* gh, Misc* m, int K, int floor,
-                                           int* cut, int* above, int* bcount = nullptr) {
-  int c[kCutPer];
-  load_row_bins(gh, c);
-  row_cutoff_vals(c, m, K, floor, cut, above, bcount);
-}
-
 // ---------------------------------------------------------------------------
 // segments of split rows
 // ---------------------------------------------------------------------------
 
-// Words of one (split row, token row) histogram block: the row-bin histogram
-// of the candidates (level 0) and the finer levels the selection may need.
-constexpr int kRowHistWords = 4 * kRowHistBins;
-
-// The key digits the split-row selection resolves, most significant first:
-// level 0 is the row bin (bits 31..22), then bits 21..12, 11..2 and 1..0.
-__device__ __forceinline__ int level_shift(int L) {
-  return L == 0 ? 22 : (L == 1 ? 12 : (L == 2 ? 2 : 0));
-}
-__device__ __forceinline__ int level_bins(int L) { return L == 3 ? 4 : 1024; }
-// Key u has the resolved prefix `pre` of the levels above L.
-__device__ __forceinline__ bool level_match(uint32_t u, int L, uint32_t pre) {
-  return L == 0 || (u >> level_shift(L - 1)) == pre;
-}
-__device__ __forceinline__ uint32_t level_digit(uint32_t u, int L) {
-  return (u >> level_shift(L)) & static_cast<uint32_t>(level_bins(L) - 1);
-}
+// Row-histogram bins one epilogue thread holds in the segment's bin sort:
+// [hi - 7, hi] with hi = 1023 - 8 * et (highest bins first in thread order).
+constexpr int kBinsPerThread = kRowHistBins / kEpiThreads;
+static_assert(kBinsPerThread == 8, "bin split");
 
 // End of this stream's part of work row w. A row held whole by this stream
-// is cut to k and written out. A split row's segment publishes: its final
-// buffer is added to the row histogram (level 0) and copied whole to the
-// segment's slot (keys and token indices), then the segment counts itself in
-// the row's counter; the selection runs once this stream has all its tiles
-// done (select_split_rows).
+// is cut to k and written out. A split row's segment publishes, per token
+// row: its final buffer sorted by row bin, highest first, into the segment's
+// slot (keys and token indices), the number of its entries at or above every
+// row bin, and its counts added to the row histogram; then the segment
+// counts itself in on the row's counter (which the selection kernel checks).
 template <int G>
 __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int w,
                                  const WorkRow& wr, const bool (&active)[G], int64_t rs,
@@ -760,720 +666,71 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
     return;
   }
   const int2 rc = p.row_ctas[w];
-  uint32_t* gh_base = p.row_hist + split_slot(p, w, rc.x) * G * kRowHistWords;
-  const int64_t slot = static_cast<int64_t>(v) + w;
+  uint32_t* gh_base = p.row_hist + split_slot(p, w, rc.x) * G * kRowHistBins;
+  const int64_t slot = segment_slot(v, w == p.cta_row[v]);
   uint64_t tf1 = tf0;
+  const int hi = kRowHistBins - 1 - kBinsPerThread * et;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    uint32_t* gh = gh_base + g * kRowHistWords;
+    uint32_t* gh = gh_base + g * kRowHistBins;
     const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
-    int off = 0, tot = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = active[g] ? m->wcnt[g][i] : 0;
-      off += i < ew ? c : 0;
-      tot += c;
-    }
     const int nw = active[g] ? m->wcnt[g][ew] : 0;
-    // the buffer's row-bin histogram: counted in shared memory, then its
-    // non-zero bins added to the row's (and the shared bins zeroed again)
+    // the buffer's row-bin histogram in shared memory
     for (int j = lane; j < nw; j += 32) atomicAdd(&s.hist[row_bin(rk[j])], 1u);
     epi_sync();
-    for (int b = et; b < kRowHistBins; b += kEpiThreads) {
-      const uint32_t c = s.hist[b];
-      if (c) {
-        atomicAdd(&gh[b], c);
-        s.hist[b] = 0u;
-      }
+    int c[kBinsPerThread];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) {
+      c[i] = static_cast<int>(s.hist[hi - i]);
+      local += c[i];
     }
+    int tot;
+    int run = epi_exclusive_scan(m, local, &tot);  // entries in higher bins
+    // per bin: the row histogram, the entries at or above it, and (in the
+    // shared histogram) the first slot position of its entries
+    uint32_t* cum = p.seg_cum + (slot * G + g) * kRowHistBins;
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) {
+      if (c[i]) atomicAdd(&gh[hi - i], static_cast<uint32_t>(c[i]));
+      s.hist[hi - i] = static_cast<uint32_t>(run);
+      run += c[i];
+      cum[hi - i] = static_cast<uint32_t>(run);
+    }
+    epi_sync();
     if (et == 0 && s.trace) {
       const uint64_t now = globaltimer_ns();
       s.trace[kTrFinHistNs] += now - tf1;
       tf1 = now;
     }
-    // the whole buffer to the slot, each warp's region at its offset
-    const int64_t base = (slot * G + g) * p.slot_cap + off;
+    // the entries to their bins' positions
+    const int64_t base = (slot * G + g) * p.slot_cap;
     for (int j = lane; j < nw; j += 32) {
-      p.slot_key[base + j] = rk[j];
-      p.slot_idx[base + j] = rx[j];
+      const uint32_t key = rk[j];
+      const int64_t pos = base + atomicAdd(&s.hist[row_bin(key)], 1u);
+      p.slot_key[pos] = key;
+      p.slot_idx[pos] = rx[j];
     }
-    if (et == 0) p.slot_count[slot * G + g] = tot;
-    epi_sync();  // the shared histogram is reused for token g + 1
+    epi_sync();
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) s.hist[hi - i] = 0u;
+    epi_sync();  // the shared histogram is zero again (reused for token g + 1)
     if (et == 0 && s.trace) {
       const uint64_t now = globaltimer_ns();
       s.trace[kTrFinEmitNs] += now - tf1;
       tf1 = now;
     }
   }
-  __threadfence();
-  epi_sync();
+  // the selection kernel reads all this after this kernel has completed; the
+  // counter only lets it check that every segment published
   if (et == 0) {
-    __threadfence();
     atomicAdd(&p.seg_counter[w], 1);
-    if (m->npend < 2) m->pend[m->npend] = w;
-    ++m->npend;
     if (s.trace) {
       s.trace[kTrFinPublishNs] += globaltimer_ns() - tf1;
       s.trace[kTrFinalizeNs] += globaltimer_ns() - tf0;
     }
   }
-}
-
-// Warp-aggregated reservation of one position per lane with `take` set on a
-// shared-memory counter; returns the lane's position (counter base + rank
-// among the taking lanes). All lanes of the warp.
-__device__ __forceinline__ int warp_reserve(int* counter, bool take) {
-  const int lane = threadIdx.x & 31;
-  const unsigned tm = __ballot_sync(0xffffffffu, take);
-  if (!tm) return 0;
-  const int leader = __ffs(tm) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(tm));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  return base + __popc(tm & ((1u << lane) - 1u));
-}
-
-// The `need` largest of the n keys staged at keys[0, n_r) (n_r = n rounded up
-// to 4, padding keys 0; every key shares its top 10 bits) with their indices
-// at idxs[], written to out[0, need) in no particular order. One pass
-// histograms bits 21..10 (4096 bins, in the group's idle candidate buffers)
-// and finds the bucket b1 of the need-th key; a second pass writes every key
-// above b1 and collects b1's keys in a short list, from which the missing
-// ones are taken by exact rank (equal keys in list order). A bucket too large
-// for the short list is resolved over bits 9..0 instead. Returns false when
-// the keys disagree with n. All threads of the group.
-template <int G>
-__device__ bool pick_from_list(const ScoreParams& p, const Smem& s, const uint32_t* keys,
-                               const int32_t* idxs, int n, int n_r, int need, int32_t* out) {
-  constexpr int kTieCap = 256;
-  static_assert(2 * G * Cfg<G>::kCap >= 4096 + 2 * kTieCap, "scratch fits the buffers");
-  const int et = epi_tid();
-  const int lane = threadIdx.x & 31, ew = et >> 5;
-  Misc* m = s.misc;
-  const bool tr = et == 0 && s.trace;
-  long long cy0 = tr ? clock64() : 0;
-  auto cyc = [&](int slot_id) {
-    if (tr) {
-      const long long now = clock64();
-      s.trace[slot_id] += static_cast<uint64_t>(now - cy0);
-      cy0 = now;
-    }
-  };
-  // scratch words over the candidate buffers: 4096 bins, then the short list
-  uint32_t* h = s.ckey;
-  uint32_t* tk = s.ckey + 4096;
-  int32_t* tx = reinterpret_cast<int32_t*>(s.ckey + 4096 + kTieCap);
-  for (int b = et; b < 4096; b += kEpiThreads) h[b] = 0u;
-  if (et == 0) {
-    m->cnt[0] = 0;  // keys written above b1
-    m->cnt[1] = 0;  // keys of b1 listed
-  }
-  epi_sync();
-  const uint4* k4 = reinterpret_cast<const uint4*>(keys);
-  const int4* x4 = reinterpret_cast<const int4*>(idxs);
-  const int n4 = n_r >> 2;
-  for (int e = et; e < n4; e += kEpiThreads) {
-    const uint4 q = k4[e];
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (u[c] != 0u) atomicAdd(&h[(u[c] >> 10) & 4095u], 1u);
-  }
-  epi_sync();
-  cyc(kTrPickHistCyc);
-  // thread et holds bins [4095 - 32 et - 31, 4095 - 32 et], from the top
-  const int top = 4095 - 32 * et;
-  int grp[8];  // sums of its eight 4-bin groups, highest first
-  int local = 0;
-  {
-    const uint4* h4 = reinterpret_cast<const uint4*>(h + top - 31);
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const uint4 c4 = h4[7 - b];
-      grp[b] = static_cast<int>(c4.x + c4.y + c4.z + c4.w);
-      local += grp[b];
-    }
-  }
-  int total;
-  const int excl = epi_exclusive_scan(m, local, &total);
-  if (et == 0) m->bcast[0] = -1;
-  epi_sync();
-  if (excl < need && need <= excl + local) {
-    int acc = excl, gsel = 0;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (acc + grp[b] < need) {
-        acc += grp[b];
-        gsel = b + 1;
-      } else {
-        break;
-      }
-    }
-    for (int b = top - 4 * gsel; b > top - 4 * gsel - 4; --b) {
-      const int c = static_cast<int>(h[b]);
-      if (acc + c >= need) {
-        m->bcast[0] = b;
-        m->bcast[1] = acc;
-        m->bcast[2] = c;
-        break;
-      }
-      acc += c;
-    }
-  }
-  epi_sync();
-  const int b1 = m->bcast[0], above1 = m->bcast[1], cnt1 = m->bcast[2];
-  epi_sync();
-  cyc(kTrPickScanCyc);
-  if (total != n || b1 < 0) return false;
-  const int remaining = need - above1;  // keys of bucket b1 still to take
-  const bool short_list = cnt1 <= kTieCap;
-  // keys above b1 to the output; b1's keys to the short list
-  for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
-    const int e = e0 + lane;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    int4 xi = make_int4(0, 0, 0, 0);
-    if (e < n4) {
-      q = k4[e];
-      xi = x4[e];
-    }
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-    const int32_t xv[4] = {xi.x, xi.y, xi.z, xi.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int d1 = u[c] != 0u ? static_cast<int>((u[c] >> 10) & 4095u) : -1;
-      const int pos = warp_reserve(&m->cnt[0], d1 > b1);
-      if (d1 > b1 && pos < need) out[pos] = xv[c];
-      const int lp = warp_reserve(&m->cnt[1], short_list && d1 == b1);
-      if (short_list && d1 == b1 && lp < kTieCap) {
-        tk[lp] = u[c];
-        tx[lp] = xv[c];
-      }
-    }
-  }
-  epi_sync();
-  cyc(kTrPickSplitCyc);
-  if (m->cnt[0] != above1) return false;
-  if (short_list) {
-    // rank by key, then list position; the first `remaining` are in
-    const int nt = m->cnt[1];
-    for (int t = et; t < nt; t += kEpiThreads) {
-      const uint32_t ut = tk[t];
-      int rank = 0;
-      for (int jx = 0; jx < nt; ++jx) {
-        const uint32_t uj = tk[jx];
-        rank += (uj > ut || (uj == ut && jx < t)) ? 1 : 0;
-      }
-      if (rank < remaining) out[above1 + rank] = tx[t];
-    }
-  } else {
-    // a large bucket: its low 10 bits (the group's 1024-bin histogram, zero),
-    // then keys above the sub-bucket and the first tied ones
-    for (int e = et; e < n4; e += kEpiThreads) {
-      const uint4 q = k4[e];
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (u[c] != 0u && static_cast<int>((u[c] >> 10) & 4095u) == b1)
-          atomicAdd(&s.hist[u[c] & 1023u], 1u);
-    }
-    epi_sync();
-    int b2, above2, cnt2;
-    take_bucket(s.hist, m, 1024, remaining, &b2, &above2, &cnt2);
-    const int rem2 = remaining - above2;
-    if (et == 0) {
-      m->cnt[0] = 0;  // keys of b1 above b2
-      m->cnt[1] = 0;  // tie tickets
-    }
-    epi_sync();
-    for (int e0 = ew * 32; e0 < n4; e0 += kEpiThreads) {
-      const int e = e0 + lane;
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      int4 xi = make_int4(0, 0, 0, 0);
-      if (e < n4) {
-        q = k4[e];
-        xi = x4[e];
-      }
-      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-      const int32_t xv[4] = {xi.x, xi.y, xi.z, xi.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const bool in_b1 = u[c] != 0u && static_cast<int>((u[c] >> 10) & 4095u) == b1;
-        const int d2 = static_cast<int>(u[c] & 1023u);
-        const bool gt = in_b1 && d2 > b2, eq = in_b1 && d2 == b2;
-        const int pos = warp_reserve(&m->cnt[0], gt);
-        if (gt && above1 + pos < need) out[above1 + pos] = xv[c];
-        const int tkt = warp_reserve(&m->cnt[1], eq);
-        if (eq && tkt < rem2 && above1 + above2 + tkt < need) out[above1 + above2 + tkt] = xv[c];
-      }
-    }
-  }
-  epi_sync();
-  cyc(kTrPickOutCyc);
-  return true;
-}
-
-// The last `need` of token g's top k from the cutoff-bin list of split row w
-// (every entry of all segments in the resolved bucket; its count must equal
-// the histogram's `bc`; `cut` is the row bin all of them share), written to
-// out[0, need). The list is staged into this group's half of the idle stage
-// ring by two bulk copies. Returns false (having written nothing) when the
-// list disagrees with the histogram or a wait gave up.
-template <int G>
-__device__ bool select_from_list(const ScoreParams& p, const Smem& s, int w, int g, int64_t es,
-                                 int cut, int bc, int need, int32_t* out) {
-  using C = Cfg<G>;
-  constexpr int kCap = C::kListCap;
-  const int et = epi_tid();
-  const int lane = threadIdx.x & 31;
-  Misc* m = s.misc;
-  const uint64_t tq0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  if (et == 0)
-    m->bcast[0] = static_cast<int>(__ldcg(&p.row_pos[static_cast<int64_t>(w) * G + g]) >> 32);
-  epi_sync();
-  const int n = m->bcast[0];
-  epi_sync();
-  if (n != bc || n <= 0 || n > kCap || p.elist_cap != kCap) return false;
-  const int n_r = (n + 3) & ~3;
-  uint8_t* half = s.kv + s.group * (C::kStages * 16384 / 2);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(half);
-  int32_t* idxs = reinterpret_cast<int32_t*>(half) + kCap;
-  const int64_t lo = (es * G + g) * static_cast<int64_t>(kCap);
-  fence_proxy_async_shared();  // earlier generic accesses of the ring precede the copies
-  fence_proxy_async_global();  // the list (acquired from other CTAs) precedes the copies' reads
-  epi_sync();
-  const int use = m->staged_uses;
-  if (et == 0) {
-    mbar_arrive_expect_tx(s.staged, static_cast<uint32_t>(n_r) * 8u);
-    bulk_load(keys, p.elist_key + lo, static_cast<uint32_t>(n_r) * 4u, s.staged);
-    bulk_load(idxs, p.elist_idx + lo, static_cast<uint32_t>(n_r) * 4u, s.staged);
-  }
-  const bool ok = mbar_wait(s.staged, use & 1, &s.cs->abort_flag, p.dev_error, p.wait_ns);
-  if (!ok) {  // gave up: let the copies land before the ring is touched again
-    int dummy = 0;
-    mbar_wait(s.staged, use & 1, &dummy, p.dev_error);
-  }
-  // entries past the list's end become key 0, which no logit maps to
-  if (ok && et < n_r - n) keys[n + et] = 0u;
-  if (lane == 0) m->vote[0][et >> 5] = ok ? 1 : 0;
-  epi_sync();
-  const bool all_ok = m->vote[0][0] & m->vote[0][1] & m->vote[0][2] & m->vote[0][3];
-  if (et == 0) m->staged_uses = use + 1;
-  if (!all_ok) return false;
-  (void)cut;
-  const uint64_t tq1 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  const bool picked = pick_from_list<G>(p, s, keys, idxs, n, n_r, need, out);
-  if (et == 0 && s.trace) {
-    s.trace[kTrMergeLoadNs] += tq1 - tq0;
-    s.trace[kTrMergeRadixNs] += globaltimer_ns() - tq1;
-  }
-  return picked;
-}
-
-// Bucket of a level's complete histogram H (global, nb bins) that holds the
-// need-th largest of the keys it counts, the count in higher buckets and the
-// bucket's own count, for every thread of the group (cut = -1 when the
-// histogram holds fewer than `need` keys).
-__device__ __forceinline__ void level_cutoff(const uint32_t* H, int nb, int need, Misc* m, int* cut,
-                                             int* above, int* bc) {
-  if (nb == kRowHistBins) {
-    row_cutoff(H, m, need, -1, cut, above, bc);
-    return;
-  }
-  if (epi_tid() == 0) {
-    int acc = 0, c = -1, a = 0, b = 0;
-    for (int i = nb - 1; i >= 0; --i) {
-      const int h = static_cast<int>(__ldcg(&H[i]));
-      if (c < 0 && acc + h >= need) {
-        c = i;
-        a = acc;
-        b = h;
-      }
-      acc += h;
-    }
-    m->bcast[0] = c;
-    m->bcast[1] = a;
-    m->bcast[2] = b;
-  }
-  epi_sync();
-  *cut = m->bcast[0];
-  *above = m->bcast[1];
-  *bc = m->bcast[2];
-  epi_sync();
-}
-
-// Cutoff buckets with at most this many keys over all segments go to the
-// row's list and are resolved by one stream; larger ones take another digit
-// level first (every segment, one more round).
-constexpr int kListMax = 8192;
-
-// One split row's selection as this stream sees it (the same values in every
-// thread of the group).
-template <int G>
-struct RowSel {
-  int w, nseg, rounds;  // rounds this segment has counted in
-  int64_t es;           // histogram / list slot
-  int L[G], need[G], cut0[G], bcl[G];
-  uint32_t pre[G];
-  unsigned pending;  // bit g: token g takes another round
-  unsigned finals;   // bit g: this stream picks token g's list
-};
-
-template <int G>
-__device__ void sel_init(const ScoreParams& p, RowSel<G>& r, int w) {
-  const int2 rc = p.row_ctas[w];
-  const WorkRow wr = p.wr[w];
-  r.w = w;
-  r.nseg = rc.y - rc.x + 1;
-  r.rounds = 0;
-  r.es = split_slot(p, w, rc.x);
-  r.pending = 0u;
-  r.finals = 0u;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (g < wr.ntok && p.row_len[wr.row0 + g] > p.topk) r.pending |= 1u << g;
-    r.L[g] = 0;
-    r.need[g] = p.topk;
-    r.pre[g] = 0u;
-    r.cut0[g] = -1;
-    r.bcl[g] = 0;
-  }
-}
-
-// One round of split row r.w for this stream's segment (slot v + w), after
-// every segment has counted in for the previous round:
-//  - level L's histogram (complete) gives the bucket of the still-needed
-//    largest key, the count above it and its own count;
-//  - the segment writes the indices of its keys above that bucket to the
-//    output (positions from the row's counter);
-//  - a bucket with at most kListMax keys: the segment appends its keys in it
-//    to the row's list, and the stream that counts in last picks the missing
-//    keys from the list afterwards; all 32 bits resolved: the bucket's keys
-//    are equal and the segment takes its share by a ticket counter;
-//    otherwise the segment histograms the bucket's next digit for the next
-//    round.
-// Then the segment counts itself in. All threads of the group.
-template <int G>
-__device__ void sel_round(const ScoreParams& p, const Smem& s, int v, RowSel<G>& r) {
-  using C = Cfg<G>;
-  const int et = epi_tid();
-  const int lane = threadIdx.x & 31, ew = et >> 5;
-  const uint32_t lt = (1u << lane) - 1u;
-  const int K = p.topk;
-  Misc* m = s.misc;
-  const int w = r.w;
-  const WorkRow wr = p.wr[w];
-  const int64_t slot = static_cast<int64_t>(v) + w;
-  const bool tr = et == 0 && s.trace;
-  uint64_t tq = tr ? globaltimer_ns() : 0;
-  auto lap = [&](int slot_id) {
-    if (tr) {
-      const uint64_t now = globaltimer_ns();
-      s.trace[slot_id] += now - tq;
-      tq = now;
-    }
-  };
-  unsigned listed = 0u;  // bit g: token g's list is complete after this round
-#pragma unroll 1
-  for (int g = 0; g < G; ++g) {
-    if (!((r.pending >> g) & 1)) continue;
-    // this segment's candidates from its slot into the group's buffers,
-    // eight loads of each kind in flight per thread; key 0 pads the last chunk
-    const int64_t sg = slot * G + g;
-    const int n = __ldcg(&p.slot_count[sg]);
-    const uint32_t* sk = p.slot_key + sg * p.slot_cap;
-    const int32_t* si = p.slot_idx + sg * p.slot_cap;
-    uint32_t* ck = s.ckey + g * C::kCap;
-    int32_t* ci = s.cidx + g * C::kCap;
-    const int n32 = (n + 31) & ~31;
-    for (int b0 = 0; b0 < n32; b0 += 8 * kEpiThreads) {
-      uint32_t ub[8];
-      int32_t xb[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = b0 + q * kEpiThreads + et;
-        ub[q] = e < n ? __ldcg(&sk[e]) : 0u;
-        xb[q] = e < n ? __ldcg(&si[e]) : 0;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int e = b0 + q * kEpiThreads + et;
-        if (e < n32) {
-          ck[e] = ub[q];
-          ci[e] = xb[q];
-        }
-      }
-    }
-    epi_sync();
-    const int nch = n32 >> 5;  // chunks; warp ew takes chunks ew, ew + 4, ...
-    lap(kTrRndLoadNs);
-    const int Lg = r.L[g];
-    uint32_t* hb = p.row_hist + (r.es * G + g) * kRowHistWords;
-    int cut, above, bc;
-    level_cutoff(hb + Lg * kRowHistBins, level_bins(Lg), r.need[g], m, &cut, &above, &bc);
-    lap(kTrRndCutNs);
-    if (tr) s.trace[kTrRndListSize] += static_cast<uint64_t>(bc);
-    if (cut < 0 || bc < 1) {  // the histograms disagree with the candidates
-      set_error(p.dev_error, IDX_DEV_INTERNAL);
-      r.pending &= ~(1u << g);
-      continue;
-    }
-    if (Lg == 0) r.cut0[g] = cut;
-    const bool to_list = bc <= min(kListMax, p.elist_cap);
-    const bool to_ties = !to_list && Lg == 3;
-    const uint32_t pg = r.pre[g], ucut = static_cast<uint32_t>(cut);
-    // class of an entry: 1 = above the bucket, 2 = in it, 0 = neither (key 0
-    // is no candidate)
-    auto klass = [&](uint32_t key) -> uint32_t {
-      if (key == 0u || !level_match(key, Lg, pg)) return 0u;
-      const uint32_t d = level_digit(key, Lg);
-      return d > ucut ? 1u : (d == ucut ? 2u : 0u);
-    };
-    // per-warp counts, then every warp's base in the group
-    long long cy0 = tr ? clock64() : 0;
-    auto cyc = [&](int slot_id) {
-      if (tr) {
-        const long long now = clock64();
-        s.trace[slot_id] += static_cast<uint64_t>(now - cy0);
-        cy0 = now;
-      }
-    };
-    int n_gt = 0, n_eq = 0;
-    for (int c0 = ew; c0 < nch; c0 += 16) {  // chunks c0, c0 + 4, c0 + 8, c0 + 12
-      uint32_t kk[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = c0 + 4 * q;
-        kk[q] = c < nch ? ck[c * 32 + lane] : 0u;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t k = klass(kk[q]);
-        n_gt += __popc(__ballot_sync(0xffffffffu, k == 1u));
-        n_eq += __popc(__ballot_sync(0xffffffffu, k == 2u));
-      }
-    }
-    cyc(kTrPassCountCyc);
-    if (lane == 0) {
-      m->scan[ew] = n_gt;
-      m->vote[1][ew] = n_eq;
-    }
-    epi_sync();
-    cyc(kTrPassScanCyc);
-    int gt_base = 0, eq_base = 0, tot_gt = 0, tot_eq = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      gt_base += i < ew ? m->scan[i] : 0;
-      eq_base += i < ew ? m->vote[1][i] : 0;
-      tot_gt += m->scan[i];
-      tot_eq += m->vote[1][i];
-    }
-    lap(kTrRndPassNs);
-    if (et == 0) {
-      int take = 0;
-      if (to_ties) {
-        const int tbase = atomicAdd(&p.tie_count[static_cast<int64_t>(w) * G + g], tot_eq);
-        take = min(max(r.need[g] - above - tbase, 0), tot_eq);
-      }
-      // output positions (low word) and list entries (high word) in one atomic
-      const unsigned long long add =
-          static_cast<unsigned long long>(tot_gt + take) |
-          (static_cast<unsigned long long>(to_list ? tot_eq : 0) << 32);
-      const unsigned long long old =
-          add ? atomicAdd(&p.row_pos[static_cast<int64_t>(w) * G + g], add) : 0ull;
-      m->bcast[0] = static_cast<int>(old & 0xffffffffull);
-      m->bcast[1] = static_cast<int>(old >> 32);
-      m->bcast[2] = take;
-    }
-    epi_sync();
-    const int obase = m->bcast[0], ebase = m->bcast[1], take = m->bcast[2];
-    epi_sync();
-    lap(kTrRndAtomicNs);
-    // write pass (ballot ranks, coalesced): keys above the bucket to the
-    // output, keys in it to the list or (ties) the first `take` to the output
-    int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * K;
-    uint32_t* ek = p.elist_key + (r.es * G + g) * p.elist_cap;
-    int32_t* ei = p.elist_idx + (r.es * G + g) * p.elist_cap;
-    int og = obase + gt_base, oq = eq_base;
-    for (int c0 = ew; c0 < nch; c0 += 16) {  // chunks c0, c0 + 4, c0 + 8, c0 + 12
-      uint32_t kk[4];
-      int32_t xx[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = c0 + 4 * q;
-        kk[q] = c < nch ? ck[c * 32 + lane] : 0u;
-        xx[q] = c < nch ? ci[c * 32 + lane] : 0;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t k = klass(kk[q]);
-        const unsigned gm = __ballot_sync(0xffffffffu, k == 1u);
-        const unsigned qm = __ballot_sync(0xffffffffu, k == 2u);
-        if (k == 1u) {
-          const int pos = og + __popc(gm & lt);
-          if (pos < K) out[pos] = xx[q];
-        } else if (k == 2u) {
-          const int rk = oq + __popc(qm & lt);
-          if (to_list) {
-            if (ebase + rk < p.elist_cap) {
-              ek[ebase + rk] = kk[q];
-              ei[ebase + rk] = xx[q];
-            }
-          } else if (to_ties) {
-            const int pos = obase + tot_gt + rk;
-            if (rk < take && pos < K) out[pos] = xx[q];
-          }
-        }
-        og += __popc(gm);
-        oq += __popc(qm);
-      }
-    }
-    cyc(kTrPassWriteCyc);
-    r.need[g] -= above;
-    r.pre[g] = Lg == 0 ? ucut : ((pg << (level_shift(Lg - 1) - level_shift(Lg))) | ucut);
-    if (to_list) {
-      listed |= 1u << g;
-      r.bcl[g] = bc;
-      r.pending &= ~(1u << g);
-    } else if (to_ties) {
-      r.pending &= ~(1u << g);
-    } else {
-      // the bucket's next digit, from every segment, for the next round
-      const int Ln = Lg + 1;
-      uint32_t* hn = hb + Ln * kRowHistBins;
-      for (int e = et; e < n; e += kEpiThreads) {
-        const uint32_t uu = ck[e];
-        if (uu != 0u && level_match(uu, Ln, r.pre[g])) atomicAdd(&s.hist[level_digit(uu, Ln)], 1u);
-      }
-      epi_sync();
-      for (int b = et; b < level_bins(Ln); b += kEpiThreads) {
-        const uint32_t c = s.hist[b];
-        if (c) {
-          atomicAdd(&hn[b], c);
-          s.hist[b] = 0u;
-        }
-      }
-      r.L[g] = Ln;
-    }
-    epi_sync();
-    cyc(kTrPassSyncCyc);
-    lap(kTrRndPassNs);
-  }
-  // count this segment in for the round
-  __threadfence();
-  epi_sync();
-  if (et == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.seg_counter[w], 1);
-    m->is_last = old == (r.rounds + 2) * r.nseg - 1;
-    __threadfence();
-  }
-  epi_sync();
-  lap(kTrRndArriveNs);
-  ++r.rounds;
-  if (m->is_last) r.finals |= listed;
-  epi_sync();
-}
-
-// Selection of this stream's split rows (at most two) once both of its
-// CTA's streams are done: the first round of each row runs as soon as all of
-// that row's segments have published (polling both rows, so that no row waits
-// on another), further rounds (cutoff buckets too large for a list) follow,
-// and the list picks this stream was left with come last.
-template <int G>
-__device__ void select_split_rows(const ScoreParams& p, const Smem& s, int v) {
-  const int et = epi_tid();
-  Misc* m = s.misc;
-  const uint64_t ts0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-  const int np = min(m->npend, 2);
-  RowSel<G> r[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-    if (i < np) sel_init<G>(p, r[i], m->pend[i]);
-  // first rounds, as the rows become ready
-  unsigned started = 0u;
-  const unsigned all = (1u << np) - 1u;
-  const uint64_t t_first = et == 0 ? globaltimer_ns() : 0;
-  for (uint32_t it = 0; started != all; ++it) {
-    if (et == 0) {
-      int ready = 0;
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        if (i < np && !((started >> i) & 1) &&
-            ld_acquire_gpu(&p.seg_counter[r[i].w]) >= r[i].nseg + p.wait_extra)
-          ready |= 1 << i;
-      if (!ready) {
-        if (s.cs->abort_flag) ready = -1;
-        else if (globaltimer_ns() - t_first > p.wait_ns) {
-          set_error(p.dev_error, IDX_DEV_TIMEOUT);
-          s.cs->abort_flag = 1;
-          ready = -1;
-        } else {
-          __nanosleep(32);
-        }
-      }
-      m->bcast[3] = ready;
-    }
-    epi_sync();
-    const int ready = m->bcast[3];
-    epi_sync();
-    if (ready < 0) return;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if ((ready >> i) & 1) {
-        sel_round<G>(p, s, v, r[i]);
-        started |= 1u << i;
-      }
-  }
-  uint64_t ts1 = 0;
-  if (et == 0 && s.trace) {
-    ts1 = globaltimer_ns();
-    s.trace[kTrSelWaitNs] += ts1 - ts0;
-    s.trace[kTrSelRows] += np;
-  }
-  // further rounds, row by row
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    while (i < np && r[i].pending) {
-      if (et == 0) {
-        if (s.trace) s.trace[kTrSelFallback] += 1;
-        m->sel_ok = !s.cs->abort_flag &&
-                    wait_count(&p.seg_counter[r[i].w], (r[i].rounds + 1) * r[i].nseg,
-                               &s.cs->abort_flag, p.dev_error, p.wait_ns);
-      }
-      epi_sync();
-      const bool ok = m->sel_ok != 0;
-      epi_sync();
-      if (!ok) return;
-      sel_round<G>(p, s, v, r[i]);
-    }
-  }
-  uint64_t ts2 = 0;
-  if (et == 0 && s.trace) {
-    ts2 = globaltimer_ns();
-    s.trace[kTrSelScanNs] += ts2 - ts1;
-  }
-  // the list picks
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (i >= np || !r[i].finals) continue;
-    const WorkRow wr = p.wr[r[i].w];
-    __threadfence();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (!((r[i].finals >> g) & 1)) continue;
-      const int K = p.topk, need = r[i].need[g];
-      int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * K;
-      if (select_from_list<G>(p, s, r[i].w, g, r[i].es, r[i].cut0[g], r[i].bcl[g], need,
-                              out + (K - need))) {
-        if (et == 0 && s.trace) s.trace[kTrSelList] += 1;
-      } else if (et == 0 && !s.cs->abort_flag) {
-        set_error(p.dev_error, IDX_DEV_INTERNAL);
-      }
-    }
-    if (et == 0 && s.trace) s.trace[kTrSelLast] += 1;
-  }
-  if (et == 0 && s.trace) s.trace[kTrSelFinalNs] += globaltimer_ns() - ts2;
 }
 
 // ---------------------------------------------------------------------------
@@ -1587,24 +844,27 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
         tmem_ld_wait();
         if (g == 0 && tr) c2 = clock64();
         const float4* w4 = reinterpret_cast<const float4*>(s.wp + g * kHeads);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        // four chains (heads h = c mod 4) as two packed pairs (c = 0, 1 and
+        // c = 2, 3): the same fp32 FMAs in the same order
+        uint64_t a01 = 0ull, a23 = 0ull;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float4 x = w4[q];
-          a0 = fmaf(x.x, fmaxf(v0[4 * q + 0], 0.f), a0);
-          a1 = fmaf(x.y, fmaxf(v0[4 * q + 1], 0.f), a1);
-          a2 = fmaf(x.z, fmaxf(v0[4 * q + 2], 0.f), a2);
-          a3 = fmaf(x.w, fmaxf(v0[4 * q + 3], 0.f), a3);
+          a01 = fma_f32x2(pack_f32x2(x.x, x.y),
+                          pack_f32x2(fmaxf(v0[4 * q + 0], 0.f), fmaxf(v0[4 * q + 1], 0.f)), a01);
+          a23 = fma_f32x2(pack_f32x2(x.z, x.w),
+                          pack_f32x2(fmaxf(v0[4 * q + 2], 0.f), fmaxf(v0[4 * q + 3], 0.f)), a23);
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float4 x = w4[8 + q];
-          a0 = fmaf(x.x, fmaxf(v1[4 * q + 0], 0.f), a0);
-          a1 = fmaf(x.y, fmaxf(v1[4 * q + 1], 0.f), a1);
-          a2 = fmaf(x.z, fmaxf(v1[4 * q + 2], 0.f), a2);
-          a3 = fmaf(x.w, fmaxf(v1[4 * q + 3], 0.f), a3);
+          a01 = fma_f32x2(pack_f32x2(x.x, x.y),
+                          pack_f32x2(fmaxf(v1[4 * q + 0], 0.f), fmaxf(v1[4 * q + 1], 0.f)), a01);
+          a23 = fma_f32x2(pack_f32x2(x.z, x.w),
+                          pack_f32x2(fmaxf(v1[4 * q + 2], 0.f), fmaxf(v1[4 * q + 3], 0.f)), a23);
         }
-        logit[g] = ((a0 + a1) + (a2 + a3)) * scale;
+        const float2 s01 = unpack_f32x2(a01), s23 = unpack_f32x2(a23);
+        logit[g] = ((s01.x + s01.y) + (s23.x + s23.y)) * scale;
       }
       tc_fence_before();
       __syncwarp();
@@ -1730,13 +990,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.qfull[a], 1);
       mbar_init(&s.qempty[a], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(s.done + i, 1);  // done[2], staged[2]
+    for (int i = 0; i < 2; ++i) mbar_init(s.done + i, 1);
     s.cs->abort_flag = 0;
     s.cs->epi_done = 0;
     for (int gi = 0; gi < 2; ++gi) {
       const Smem sg = carve<G>(base, gi);
-      sg.misc->staged_uses = 0;
-      sg.misc->npend = 0;
       for (int i = 0; i < kTrSlots; ++i) sg.trace[i] = 0;
     }
     fence_barrier_init();
@@ -1762,11 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    const bool ok = epilogue<G, kLogits>(p, s, tmem, st, group);
-    // both streams are done with the stage ring before a selection stages
-    // lists in it
-    named_sync(kJointBarrier, 2 * kEpiThreads);
-    if (!kLogits && ok) select_split_rows<G>(p, s, st[group].v);
+    epilogue<G, kLogits>(p, s, tmem, st, group);
     if (s.trace && epi_tid() == 0) s.trace[kTrFinal] = globaltimer_ns();
   }
   if (threadIdx.x == kEpiBase) *reinterpret_cast<volatile int*>(&s.cs->epi_done) = 1;
@@ -1799,10 +1053,8 @@ idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_cta
     if (e != cudaSuccess) return cuda_status(e);
     if (dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
   }
-  // Top-k launches are cooperative: the streams sharing a split row wait for
-  // one another's segments before selecting.
-  return cuda_status(launch_pdl_ex(!kLogits, score_select_kernel<G, kLogits>, num_ctas, kThreads,
-                                   C::kSmemBytes, s, p, map));
+  return cuda_status(launch_pdl(score_select_kernel<G, kLogits>, num_ctas, kThreads, C::kSmemBytes,
+                                s, p, map));
 }
 
 }  // namespace

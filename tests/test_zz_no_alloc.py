@@ -68,7 +68,8 @@ def test_noalloc_matches_workspace_path_on_two_calls():
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():
-    R = 4096
+    R = 8192  # the fp8 q images alone (8 KB per token row) fill the 64 MiB scratch
+    assert saib.indexer_decode_workspace_bytes(R, 1, 2048) > 64 << 20
     q = torch.zeros((R, 64, 128), dtype=torch.bfloat16, device=DEV)
     w = torch.zeros((R, 64), dtype=torch.float32, device=DEV)
     cache = torch.zeros((1, 8448), dtype=torch.uint8, device=DEV)
