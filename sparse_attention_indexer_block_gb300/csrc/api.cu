@@ -34,7 +34,7 @@ idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorM
     const idx_status st = cuda_status(cudaEventRecord(g_prof_start, s));
     if (st != IDX_OK) return st;
   }
-  const int streams = score_streams();
+  const int streams = score_streams(G);
   idx_status st = launch_score(G, logits, p, map, score_grid(), s);
   if (st == IDX_OK && !logits) {
     RowSelectParams r{};
@@ -253,7 +253,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
     return IDX_ERR_INVALID_ARG;
   }
   if (num_reqs == 0) return IDX_OK;
-  const int nC = score_streams();
+  const int nC = score_streams(next_n);
   const int64_t rows = static_cast<int64_t>(num_reqs) * next_n;
   const WsLayout L = ws_layout(num_reqs, rows, next_n, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
@@ -392,7 +392,7 @@ idx_status indexer_decode_workspace_bytes(int32_t num_reqs, int32_t next_n, int3
   if (!bytes || num_reqs < 0) return IDX_ERR_INVALID_ARG;
   if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk,
-                               score_streams());
+                               score_streams(next_n));
   *bytes = L.total;
   return IDX_OK;
 }
@@ -401,7 +401,7 @@ idx_status indexer_debug_decode_plan(int32_t num_reqs, int32_t next_n, int32_t t
                                      int64_t* offsets, int32_t* grid, int32_t* penalty) {
   if (!offsets || !grid || !penalty || num_reqs < 0) return IDX_ERR_INVALID_ARG;
   if ((next_n != 1 && next_n != 2) || topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
-  const int nC = score_streams();
+  const int nC = score_streams(next_n);
   const WsLayout L = ws_layout(num_reqs, static_cast<int64_t>(num_reqs) * next_n, next_n, topk, nC);
   offsets[0] = static_cast<int64_t>(L.wr_tile_start);
   offsets[1] = static_cast<int64_t>(L.cta_tile);
@@ -494,7 +494,7 @@ idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
   const idx_status st = prefill_plan(seq_lens_host, query_lens_host, num_reqs, workspace_tokens,
                                      logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows);
   if (st != IDX_OK) return st;
-  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, score_streams()).total;
+  *bytes = ws_layout(max_wr, max_rows, kPrefillG, topk, score_streams(kPrefillG)).total;
   return IDX_OK;
 }
 
@@ -519,7 +519,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
                          logits_budget_bytes, &plan, &qsl, &max_wr, &max_rows)) != IDX_OK)
     return st;
   if (plan.empty()) return IDX_OK;
-  const int nC = score_streams();
+  const int nC = score_streams(kPrefillG);
   const WsLayout L = ws_layout(max_wr, max_rows, kPrefillG, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
   CUtensorMap map;

@@ -96,13 +96,18 @@ enum TraceSlot {
   kTrPickOutCyc, kTrSlots = 64
 };
 
-// Candidate-buffer capacity per token row of the score/select kernel for work
-// rows of G (1 or 2) tokens; a published segment slot holds up to this many
-// entries.
-constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : 2560; }
+// Tile streams one CTA of the score/select kernel runs for work rows of G (1
+// or 2) token rows: two for G = 1 (one epilogue group each), one for G = 2
+// (one epilogue group per token row).
+constexpr int score_streams_per_cta(int G) { return G == 1 ? 2 : 1; }
 
-// Pipeline stages (128-key tiles in flight) of the score/select kernel.
-constexpr int score_stages(int G) { return G == 1 ? 8 : 4; }
+// Candidate-buffer capacity of one epilogue group (one token row); a published
+// segment slot holds up to this many entries.
+constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : 4096; }
+
+// Pipeline stages (128-key tiles in flight) of one CTA of the score/select
+// kernel, over all its streams.
+constexpr int score_stages(int G) { return G == 1 ? 8 : 6; }
 
 // Split work rows (rows whose tiles several CTAs share) that one launch can
 // have: each starts in a different CTA, and there is at most one per work row.
@@ -215,10 +220,10 @@ enum SelTraceSlot {
 // max_split_rows(num_wr, streams) * G CTAs.
 idx_status launch_row_select(const RowSelectParams& p, int grid, cudaStream_t s);
 
-// The score/select kernel runs one CTA per SM, each CTA two tile streams
-// ("virtual CTAs"): the work split is planned over score_streams() ranges and
-// the launch has score_grid() CTAs.
+// The score/select kernel runs one CTA per SM, each CTA
+// score_streams_per_cta(G) tile streams: the work split is planned over
+// score_streams(G) ranges and the launch has score_grid() CTAs.
 inline int score_grid() { return device_sm_count(); }
-inline int score_streams() { return 2 * device_sm_count(); }
+inline int score_streams(int G) { return score_streams_per_cta(G) * device_sm_count(); }
 
 }  // namespace saib

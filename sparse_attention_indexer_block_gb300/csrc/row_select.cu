@@ -429,14 +429,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
   int c0[P0];
 #pragma unroll
   for (int j = 0; j < P0; ++j) c0[j] = static_cast<int>(__ldcg(&rh[top_bin<P0>() - j]));
-  // every segment has published (the wait is the test hook's: it asks for
-  // one segment more than there are and must give up)
+  // every segment has published: each of a segment's G epilogue groups (one
+  // per token row) counts in once (the wait is the test hook's: it asks for
+  // one more than there are and must give up)
   if (t == 0) {
     sh->abort_flag = 0;
     int ok = 1;
+    const int expected = nseg * p.G;
     if (p.stall) {
-      ok = wait_count(&p.seg_counter[w], nseg + 1, &sh->abort_flag, p.dev_error, p.wait_ns) ? 1 : 0;
-    } else if (__ldcg(&p.seg_counter[w]) != nseg) {
+      ok = wait_count(&p.seg_counter[w], expected + 1, &sh->abort_flag, p.dev_error, p.wait_ns) ? 1
+                                                                                               : 0;
+    } else if (__ldcg(&p.seg_counter[w]) != expected) {
       // a segment missing: the score/select kernel gave up (timeout), else a bug
       const uint32_t e = p.dev_error ? *reinterpret_cast<volatile uint32_t*>(p.dev_error) : 0u;
       if (!(e & IDX_DEV_TIMEOUT)) set_error(p.dev_error, IDX_DEV_INTERNAL);

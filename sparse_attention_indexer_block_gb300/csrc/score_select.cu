@@ -1,27 +1,27 @@
 // Score + select: the persistent kernel of the indexer.
 //
-// One CTA per SM (the occupancy of tensor-core kernels is one CTA per SM). A
-// CTA runs two
-// independent tile streams: the global sequence of 128-key tiles (work rows in
-// order, each work row cut into ceil(maxlen / 128) tiles) is split into
-// 2 x gridDim contiguous ranges ("virtual CTAs"), and CTA c streams ranges 2c
-// and 2c + 1 side by side, each with its own pipeline. Warp-specialised, per
-// stream j:
+// One CTA per SM (the occupancy of tensor-core kernels is one CTA per SM). The
+// global sequence of 128-key tiles (work rows in order, each work row cut into
+// ceil(maxlen / 128) tiles) is split into contiguous ranges ("streams"): for
+// work rows of one token row (G = 1) a CTA runs two independent streams side
+// by side, for work rows of two (G = 2) one stream whose two token rows are
+// scored by separate epilogue groups. Warp-specialised, per stream j:
 //   warp 2j      TMA producer: two 64-token pages per tile (8 KB of fp8 keys
 //                via a 3-D tensor map with the 128-byte swizzle, 256 B of fp32
-//                scales via a bulk copy each) into the stream's half of the
+//                scales via a bulk copy each) into the stream's part of the
 //                ring of shared-memory stages; the work row's fp8 q image
 //                (G x 8 KB) into one of the stream's two q slots.
 //   warp 2j + 1  MMA issuer: D[128 keys x 64G] = K_tile[128 x 128] .
 //                Q[64G x 128]^T as four tcgen05 kind::f8f6f4 MMAs (K = 32 each)
 //                into one of the stream's two tensor-memory accumulators.
-//   warps 4-7 (stream 0) and 8-11 (stream 1)  epilogue group: each thread owns
-//           one key (one TMEM lane), loads its 64 head dots per token, applies
-//           ReLU, the folded head weights w * sq and the key's scale, and feeds
-//           the logit to a streaming top-k: a shared-memory candidate buffer
-//           per token, a threshold below which keys are dropped, and a radix
-//           select that shrinks the buffer back to k when it fills. No logits
-//           row leaves the SM.
+//   warps 4-7 and 8-11: two epilogue groups (G = 1: one per stream; G = 2:
+//           one per token row of the single stream). Each thread owns one key
+//           (one TMEM lane), loads its group's 64 head dots, applies ReLU,
+//           the folded head weights w * sq and the key's scale, and feeds the
+//           logit to a streaming top-k: a shared-memory candidate buffer, a
+//           threshold below which keys are dropped, and a radix select that
+//           shrinks the buffer back to k when it fills. No logits row leaves
+//           the SM.
 // A work row covered by several streams is a set of segments. Each segment
 // publishes the candidates it kept and adds their row-bin histogram to the
 // row's; the row's top k is selected from them by the split-row selection
@@ -55,8 +55,11 @@ __device__ __forceinline__ void epi_sync() { named_sync(1 + 3 * epi_group(), kEp
 template <int G>
 struct Cfg {
   static constexpr int N = 64 * G;
-  static constexpr int kStages = score_stages(G);      // both streams
-  static constexpr int kStreamStages = kStages / 2;
+  static constexpr int kStreams = score_streams_per_cta(G);  // tile streams per CTA
+  static constexpr int kGroupsPerStream = 2 / kStreams;      // epilogue groups per stream
+  static constexpr int kTokens = G / kGroupsPerStream;       // token rows per group
+  static constexpr int kStages = score_stages(G);            // all streams
+  static constexpr int kStreamStages = kStages / kStreams;
   static constexpr int kCap = candidate_capacity(G);  // candidates per token row
   static constexpr int kRegion = kCap / 4;            // per-warp append region
   static constexpr int kPer = kRegion / 32;           // region entries per lane
@@ -64,18 +67,18 @@ struct Cfg {
   // boundary the radix search reaches first)
   static constexpr int kSlack = kCap / 24;
   static constexpr int kHistBins = 1024;
-  static constexpr uint32_t kTmemCols = 4 * N;  // four accumulators: two per stream
+  static constexpr uint32_t kTmemCols = 2 * kStreams * N;  // two accumulators per stream
   static constexpr uint32_t kIdesc = f8_idesc(128, N);
   // Shared memory: the stage ring, the q slots (2 streams x 2), the scales,
   // then one block per epilogue group, the mbarriers and the CTA-wide words.
   static constexpr int kKvOff = 0;
   static constexpr int kQOff = kKvOff + kStages * 16384;
-  static constexpr int kScaleOff = kQOff + 4 * G * kQRowBytes;
+  static constexpr int kScaleOff = kQOff + 2 * kStreams * G * kQRowBytes;
   static constexpr int kGroupOff = kScaleOff + kStages * 512;
   static constexpr int kGCandKey = 0;
-  static constexpr int kGCandIdx = kGCandKey + G * kCap * 4;
-  static constexpr int kGWp = kGCandIdx + G * kCap * 4;
-  static constexpr int kGHist = kGWp + G * 256;
+  static constexpr int kGCandIdx = kGCandKey + kTokens * kCap * 4;
+  static constexpr int kGWp = kGCandIdx + kTokens * kCap * 4;
+  static constexpr int kGHist = kGWp + kTokens * 256;
   static constexpr int kGMisc = kGHist + kHistBins * 4;
   static constexpr int kGTrace = kGMisc + 256;
   static constexpr int kGroupBytes = kGTrace + kTrSlots * 8;
@@ -85,7 +88,8 @@ struct Cfg {
   static constexpr int kSmemBytes = kSharedOff + 64 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
   static_assert(kCap >= IDX_MAX_TOPK, "a slot must hold any k");
-  static_assert(kTmemCols <= 512, "tensor memory");
+  static_assert(kTmemCols == 256, "tensor memory: a power of two the allocator takes");
+  static_assert(kStreams * kGroupsPerStream == 2 && kTokens == 1, "one token row per group");
   static_assert(kGroupBytes % 16 == 0 && kGTrace % 8 == 0, "alignment");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -162,7 +166,18 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int group) {
   return s;
 }
 
-// One of the CTA's two tile streams: virtual CTA v = 2 * blockIdx.x + j owns
+// The stream of the CTA a role serves and the first token row of the work
+// rows an epilogue group scores.
+template <int G>
+__device__ __forceinline__ int stream_of(const Smem& s) {
+  return Cfg<G>::kStreams == 2 ? s.group : 0;
+}
+template <int G>
+__device__ __forceinline__ int token_of(const Smem& s) {
+  return Cfg<G>::kStreams == 2 ? 0 : s.group * Cfg<G>::kTokens;
+}
+
+// One of the CTA's tile streams: stream v = kStreams * blockIdx.x + j owns
 // tiles [t0, t1) of the launch's tile sequence.
 struct Stream {
   int64_t t0, t1;
@@ -178,8 +193,9 @@ __device__ __forceinline__ int row_bin(uint32_t key) { return static_cast<int>(k
 // has no more work rows than virtual CTAs, else its first virtual CTA (split
 // rows start in different virtual CTAs). Either way below
 // max_split_rows(num_wr, 2 * gridDim.x).
+template <int G>
 __device__ __forceinline__ int64_t split_slot(const ScoreParams& p, int w, int v_first) {
-  return p.num_wr <= 2 * static_cast<int>(gridDim.x) ? w : v_first;
+  return p.num_wr <= Cfg<G>::kStreams * static_cast<int>(gridDim.x) ? w : v_first;
 }
 
 __device__ __forceinline__ void trace_set(const Smem& s, int slot, uint64_t v) {
@@ -217,7 +233,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
   using C = Cfg<G>;
   constexpr int S = C::kStreamStages;
   volatile int* abort_flag = &s.cs->abort_flag;
-  const int j = s.group;
+  const int j = stream_of<G>(s);
   uint64_t* full = s.full + j * S;
   uint64_t* empty = s.empty + j * S;
   uint8_t* kv = s.kv + j * S * 16384;
@@ -312,7 +328,7 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, c
   using C = Cfg<G>;
   constexpr int S = C::kStreamStages;
   volatile int* abort_flag = &s.cs->abort_flag;
-  const int j = s.group;
+  const int j = stream_of<G>(s);
   uint64_t* full = s.full + j * S;
   uint64_t* empty = s.empty + j * S;
   const uint8_t* kv = s.kv + j * S * 16384;
@@ -610,17 +626,17 @@ __device__ __forceinline__ int region_entries(const Smem& s, int g) {
 // Output of a row held entirely by this CTA (its buffer holds <= k entries).
 template <int G>
 __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& wr,
-                           const bool (&active)[G]) {
+                           const bool (&active)[Cfg<G>::kTokens]) {
   using C = Cfg<G>;
   const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int g = 0; g < C::kTokens; ++g) {
     if (!active[g]) continue;
     const int mine = region_entries<G>(s, g);
     int total;
     int pos = epi_exclusive_scan(s.misc, mine, &total);
-    int32_t* o = p.out_idx + (p.out_row_base + wr.row0 + g) * p.topk;
+    int32_t* o = p.out_idx + (p.out_row_base + wr.row0 + token_of<G>(s) + g) * p.topk;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
     for (int j = 0; j < mine; ++j)
       if (pos < p.topk) o[pos++] = rx[lane + 32 * j];
@@ -646,7 +662,7 @@ static_assert(kBinsPerThread == 8, "bin split");
 // counts itself in on the row's counter (which the selection kernel checks).
 template <int G>
 __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int w,
-                                 const WorkRow& wr, const bool (&active)[G], int64_t rs,
+                                 const WorkRow& wr, const bool (&active)[Cfg<G>::kTokens], int64_t rs,
                                  int64_t re, int64_t t0, int64_t t1) {
   using C = Cfg<G>;
   const int et = epi_tid();
@@ -658,7 +674,7 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
   const bool whole = rs >= t0 && re <= t1;
   if (whole) {
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < C::kTokens; ++g)
       if (active[g] && m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3] > K)
         compact<G>(s, g, K);  // cut to k (the regions stay the layout)
     write_rows<G>(p, s, wr, active);
@@ -666,13 +682,14 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
     return;
   }
   const int2 rc = p.row_ctas[w];
-  uint32_t* gh_base = p.row_hist + split_slot(p, w, rc.x) * G * kRowHistBins;
+  uint32_t* gh_base = p.row_hist + split_slot<G>(p, w, rc.x) * G * kRowHistBins;
   const int64_t slot = segment_slot(v, w == p.cta_row[v]);
   uint64_t tf1 = tf0;
   const int hi = kRowHistBins - 1 - kBinsPerThread * et;
+  const int g0 = token_of<G>(s);
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    uint32_t* gh = gh_base + g * kRowHistBins;
+  for (int g = 0; g < C::kTokens; ++g) {
+    uint32_t* gh = gh_base + (g0 + g) * kRowHistBins;
     const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
     const int nw = active[g] ? m->wcnt[g][ew] : 0;
@@ -690,7 +707,7 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
     int run = epi_exclusive_scan(m, local, &tot);  // entries in higher bins
     // per bin: the row histogram, the entries at or above it, and (in the
     // shared histogram) the first slot position of its entries
-    uint32_t* cum = p.seg_cum + (slot * G + g) * kRowHistBins;
+    uint32_t* cum = p.seg_cum + (slot * G + g0 + g) * kRowHistBins;
 #pragma unroll
     for (int i = 0; i < kBinsPerThread; ++i) {
       if (c[i]) atomicAdd(&gh[hi - i], static_cast<uint32_t>(c[i]));
@@ -705,7 +722,7 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
       tf1 = now;
     }
     // the entries to their bins' positions
-    const int64_t base = (slot * G + g) * p.slot_cap;
+    const int64_t base = (slot * G + g0 + g) * p.slot_cap;
     for (int j = lane; j < nw; j += 32) {
       const uint32_t key = rk[j];
       const int64_t pos = base + atomicAdd(&s.hist[row_bin(key)], 1u);
@@ -761,31 +778,33 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
   int w = p.cta_row[v];
   int64_t rs = p.wr_tile_start[w], re = p.wr_tile_start[w + 1];
   WorkRow wr;
-  int len[G];
-  bool active[G];
-  int wcnt[G];      // entries in this warp's region of each token's buffer
-  uint32_t thr[G];  // each buffer's drop threshold
+  constexpr int GT = C::kTokens;  // token rows g0, g0 + 1, ... of the group
+  const int g0 = token_of<G>(s);
+  int len[GT];
+  bool active[GT];
+  int wcnt[GT];      // entries in this warp's region of each token's buffer
+  uint32_t thr[GT];  // each buffer's drop threshold
 
   auto begin_row = [&]() {
     wr = p.wr[w];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      len[g] = g < wr.ntok ? p.row_len[wr.row0 + g] : 0;
-      active[g] = g < wr.ntok && (kLogits ? len[g] > 0 : len[g] > p.topk);
+    for (int g = 0; g < GT; ++g) {
+      len[g] = g0 + g < wr.ntok ? p.row_len[wr.row0 + g0 + g] : 0;
+      active[g] = g0 + g < wr.ntok && (kLogits ? len[g] > 0 : len[g] > p.topk);
     }
-    for (int i = et; i < G * kHeads; i += kEpiThreads) {
-      const int g = i / kHeads;
+    for (int i = et; i < GT * kHeads; i += kEpiThreads) {
+      const int g = g0 + i / kHeads;
       s.wp[i] =
           g < wr.ntok ? p.wprime[static_cast<int64_t>(wr.row0 + g) * kHeads + i % kHeads] : 0.f;
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int g = 0; g < GT; ++g) {
       wcnt[g] = 0;
       thr[g] = 0u;
     }
     if (et == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GT; ++g) {
         s.misc->cnt[g] = 0;
         s.misc->thr[g] = 0u;
       }
@@ -795,7 +814,7 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
   auto publish_counts = [&]() {
     if (lane == 0)
 #pragma unroll
-      for (int g = 0; g < G; ++g) s.misc->wcnt[g][ew] = wcnt[g];
+      for (int g = 0; g < GT; ++g) s.misc->wcnt[g][ew] = wcnt[g];
   };
   begin_row();
 
@@ -830,14 +849,14 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
     __syncwarp();
     const long long c1 = tr ? clock64() : 0;
     long long c2 = c1;
-    float logit[G];
+    float logit[GT];
     if (k == 0 && et == 0 && s.trace) s.trace[kTrFirstEpi] = globaltimer_ns();
     if (wok) {
       tc_fence_after();
       const float scale = s.scales[stage * 128 + mrow];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const uint32_t col = lane_addr + tmem + static_cast<uint32_t>(acc * C::N + g * 64);
+      for (int g = 0; g < GT; ++g) {
+        const uint32_t col = lane_addr + tmem + static_cast<uint32_t>(acc * C::N + (g0 + g) * 64);
         float v0[32], v1[32];
         tmem_ld32(col, v0);
         tmem_ld32(col + 32, v1);
@@ -880,7 +899,7 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
     const int par = static_cast<int>(k & 1);
     int need = 0;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < GT; ++g)
       need |= (!kLogits && active[g] && wcnt[g] + 32 > C::kRegion) ? 2 << g : 0;
     publish_counts();
     if (lane == 0) s.misc->vote[par][ew] = (wok ? 1 : 0) | need;
@@ -896,19 +915,19 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
     const int key = i * kTileKeys + mrow;
     if (kLogits) {
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+      for (int g = 0; g < GT; ++g)
         if (active[g] && key < len[g])
-          p.out_logits[static_cast<int64_t>(wr.row0 + g) * p.ld_logits + key] = logit[g];
+          p.out_logits[static_cast<int64_t>(wr.row0 + g0 + g) * p.ld_logits + key] = logit[g];
     } else {
 #pragma unroll
-      for (int g = 0; g < G; ++g)
+      for (int g = 0; g < GT; ++g)
         if ((needs >> g) & 1) {
           const int kept = compact<G>(s, g, p.topk, C::kSlack);
           wcnt[g] = (kept - ew + 3) >> 2;
           thr[g] = s.misc->thr[g];
         }
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
+      for (int g = 0; g < GT; ++g) {
         // append to this warp's region: ballot + popc, no shared counter
         const uint32_t kk = float_key(logit[g]);
         const bool pass = active[g] && key < len[g] && kk > thr[g];
@@ -966,27 +985,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every participating stream owns at least one tile (segment counts rely
   // on it).
   const int64_t T = p.wr_tile_start[p.num_wr];
-  const int64_t nV = min(static_cast<int64_t>(2 * gridDim.x), T);
+  const int64_t nV = min(static_cast<int64_t>(C::kStreams * gridDim.x), T);
   Stream st[2];
   bool part[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const int v = 2 * static_cast<int>(blockIdx.x) + j;
-    part[j] = v < nV;
+    const int v = C::kStreams * static_cast<int>(blockIdx.x) + j;
+    part[j] = j < C::kStreams && v < nV;
     st[j].v = v;
     st[j].t0 = part[j] ? p.cta_tile[v] : 0;
     st[j].t1 = part[j] ? p.cta_tile[v + 1] : 0;
   }
-  if (!(p.trace && part[group])) s.trace = nullptr;
+  // stream of this thread's role (warps 2 and 3 have none when kStreams == 1)
+  const int js = warp < 4 ? (warp >> 1) : stream_of<G>(s);
+  if (!(p.trace && part[js] && token_of<G>(s) == 0)) s.trace = nullptr;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1 + 4);  // the MMA's commit + the consuming group's warps
+      // the MMA's commit + the warps of the groups consuming the stage
+      mbar_init(&s.empty[i], 1 + 4 * C::kGroupsPerStream);
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(&s.tfull[a], 1);
-      mbar_init(&s.tempty[a], 4);
+      mbar_init(&s.tempty[a], 4 * C::kGroupsPerStream);
       mbar_init(&s.qfull[a], 1);
       mbar_init(&s.qempty[a], 1);
     }
@@ -1008,19 +1030,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s.cs->tmem_base;
   if (warp >= 4 && epi_tid() == 0 && s.trace) {
     s.trace[kTrStart] = globaltimer_ns();
-    s.trace[kTrTiles] = static_cast<uint64_t>(st[group].t1 - st[group].t0);
+    s.trace[kTrTiles] = static_cast<uint64_t>(st[js].t1 - st[js].t0);
   }
 
   if (warp < 4) {
     // one lane runs the role; the warp reconverges before the block barrier
-    const bool has_tiles = st[group].t1 > st[group].t0;
+    const bool has_tiles = part[js] && st[js].t1 > st[js].t0;
     if (lane == 0 && has_tiles) {
-      if (warp & 1) mma_issuer<G>(p, s, tmem, st[group]);
-      else producer<G>(p, &map, s, st[group]);
+      if (warp & 1) mma_issuer<G>(p, s, tmem, st[js]);
+      else producer<G>(p, &map, s, st[js]);
     }
     __syncwarp();
   } else {
-    epilogue<G, kLogits>(p, s, tmem, st, group);
+    epilogue<G, kLogits>(p, s, tmem, st, js);
     if (s.trace && epi_tid() == 0) s.trace[kTrFinal] = globaltimer_ns();
   }
   if (threadIdx.x == kEpiBase) *reinterpret_cast<volatile int*>(&s.cs->epi_done) = 1;
@@ -1030,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (epi_tid() == 0) s.trace[kTrEnd] = globaltimer_ns();
     __syncwarp();
     if (epi_tid() < kTrSlots)
-      p.trace[static_cast<int64_t>(st[group].v) * kTrSlots + epi_tid()] = s.trace[epi_tid()];
+      p.trace[static_cast<int64_t>(st[js].v) * kTrSlots + epi_tid()] = s.trace[epi_tid()];
   }
   if (warp == 1) {
     tc_fence_after();
