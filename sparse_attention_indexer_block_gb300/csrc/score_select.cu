@@ -62,7 +62,6 @@ struct Cfg {
   static constexpr int kStreamStages = kStages / kStreams;
   static constexpr int kCap = candidate_capacity(G);  // candidates per token row
   static constexpr int kRegion = kCap / 4;            // per-warp append region
-  static constexpr int kPer = kRegion / 32;           // region entries per lane
   // a full buffer is cut to at most k + kSlack entries (whichever bucket
   // boundary the radix search reaches first)
   static constexpr int kSlack = kCap / 24;
@@ -452,30 +451,32 @@ __device__ __forceinline__ void take_bucket(uint32_t* hist, Misc* m, int nb, int
   *bcount = m->bcount;
 }
 
-// The K-th largest among the member keys of all epilogue threads (member j of
-// this thread: key u[j] with bit j of `mem` set; K <= member count): an
+// The K-th largest key of token g's buffer (the group's four per-warp
+// regions in shared memory, counts in wcnt[g][*]; K <= their total): an
 // MSB-first radix select over v = key - min (10-bit digits below the top bit
 // of max - min, so the bins spread over the keys present) with one shared
-// histogram (zero on entry and on exit). Result: *mn (min member key), *hi and *pre (the member keys with
-// (key - mn) >> hi > pre are in, those equal to pre are tied) and *rem (how
-// many tied keys complete K). With slack > 0 the search may stop early at a
-// bucket that holds at most `slack` keys beyond K: the whole bucket is then
-// taken (*rem = its count), so up to K + slack keys are in. Contains epilogue
-// barriers; all epilogue threads.
-template <int N>
-__device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, int K,
-                          uint32_t* mn_out, int* hi_out, uint64_t* pre_out, int* rem_out,
-                          int slack = 0) {
+// histogram (zero on entry and on exit), reading the keys where they lie.
+// Result: *mn (min key), *hi and *pre (keys with (key - mn) >> hi > pre are
+// in, those equal to pre are tied) and *rem (how many tied keys complete K).
+// With slack > 0 the search may stop early at a bucket that holds at most
+// `slack` keys beyond K: the whole bucket is then taken (*rem = its count),
+// so up to K + slack keys are in. Contains epilogue barriers; all epilogue
+// threads.
+template <int G>
+__device__ void radix_kth(const Smem& s, int g, int K, uint32_t* mn_out, int* hi_out,
+                          uint64_t* pre_out, int* rem_out, int slack = 0) {
+  using C = Cfg<G>;
   const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
   Misc* m = s.misc;
+  const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
+  const int n_w = m->wcnt[g][ew];
   uint32_t mn = 0xffffffffu, mx = 0u;
-#pragma unroll
-  for (int j = 0; j < N; ++j)
-    if ((mem >> j) & 1) {
-      mn = min(mn, u[j]);
-      mx = max(mx, u[j]);
-    }
+  for (int r = lane; r < n_w; r += 32) {
+    const uint32_t u = rk[r];
+    mn = min(mn, u);
+    mx = max(mx, u);
+  }
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) {
@@ -493,11 +494,9 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
     const int lo = max(hi - 10, 0);
     const int nb = 1 << (hi - lo);
     const uint64_t ta = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const uint64_t v = u[j] - mn;
-      if (((mem >> j) & 1) && (v >> hi) == pre)
-        atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
+    for (int r = lane; r < n_w; r += 32) {
+      const uint64_t v = rk[r] - mn;
+      if ((v >> hi) == pre) atomicAdd(&s.hist[(v >> lo) & static_cast<uint64_t>(nb - 1)], 1u);
     }
     epi_sync();
     const uint64_t tb = (et == 0 && s.trace) ? globaltimer_ns() : 0;
@@ -522,94 +521,75 @@ __device__ void radix_kth(const Smem& s, const uint32_t (&u)[N], uint64_t mem, i
   *rem_out = remaining;
 }
 
-// Position p of a packed candidate buffer: buffers are split into four
-// per-warp regions (appends need no shared counter); packed entries are dealt
-// round-robin over the regions so every region has the same room afterwards.
-template <int G>
-__device__ __forceinline__ int buf_at(int g, int p) {
-  return g * Cfg<G>::kCap + (p & 3) * Cfg<G>::kRegion + (p >> 2);
-}
-
-// Packs candidate buffer g (the four regions, counts in wcnt[g][*]) into its
-// K largest keys (all of them when there are <= K; ties at the K-th value
-// broken arbitrarily): the entries go to registers, radix_kth finds the K-th
-// key, one scan gives every kept entry its packed position. The drop
-// threshold becomes min + (resolved prefix of the K-th key): keys at or below
-// it cannot displace the K kept ones. Sets cnt[g] to the entries kept and
-// returns it; all epilogue threads.
+// Cuts token g's buffer to its K largest keys (all of them when there are
+// <= K; up to K + slack when the radix search stops early; ties at the K-th
+// value broken arbitrarily): radix_kth finds the cut, then every warp packs
+// the kept entries of its own region to the region's front, in place (a
+// kept entry never moves past one not yet read). The drop threshold becomes
+// min + (resolved prefix of the K-th key): keys at or below it cannot
+// displace the kept ones. Leaves each warp's count in wcnt[g][*], sets
+// cnt[g] to the entries kept and returns it; all epilogue threads.
 template <int G>
 __device__ int compact(const Smem& s, int g, int K, int slack = 0) {
   using C = Cfg<G>;
-  static_assert(C::kPer <= 64, "member mask");
   const int et = epi_tid();
   const int lane = threadIdx.x & 31, ew = et >> 5;
-  uint32_t* ck = s.ckey;
-  int32_t* ci = s.cidx;
   Misc* m = s.misc;
+  uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
+  int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
   const uint64_t tc0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
   const int n_w = m->wcnt[g][ew];
   const int n = m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3];
-  uint32_t ku[C::kPer];
-  int32_t ki[C::kPer];
-  uint64_t mem = 0;
-  const int rbase = g * C::kCap + ew * C::kRegion;
-#pragma unroll
-  for (int j = 0; j < C::kPer; ++j) {
-    const int r = j * 32 + lane;
-    ku[j] = r < n_w ? ck[rbase + r] : 0u;
-    ki[j] = r < n_w ? ci[rbase + r] : 0;
-    if (r < n_w) mem |= 1ull << j;
-  }
+  if (n <= K) return n;  // uniform: nothing to cut
   uint32_t mn = 0;
   int hi = 0, remaining = 0;
   uint64_t pre = 0;
-  const bool select = n > K;
-  if (select) {
+  {
     const uint64_t tr0 = (et == 0 && s.trace) ? globaltimer_ns() : 0;
-    radix_kth(s, ku, mem, K, &mn, &hi, &pre, &remaining, slack);
+    radix_kth<G>(s, g, K, &mn, &hi, &pre, &remaining, slack);
     if (et == 0 && s.trace) s.trace[kTrCompactRadixNs] += globaltimer_ns() - tr0;
   }
-  // One scan of (tied << 16 | greater) gives every thread the counts before it;
-  // tied keys are taken in thread order until `remaining` of them are in.
-  int n_gt = 0, n_eq = 0;
-#pragma unroll
-  for (int j = 0; j < C::kPer; ++j) {
-    const bool in = (mem >> j) & 1;
-    const uint64_t top = static_cast<uint64_t>(ku[j] - mn) >> hi;
-    n_gt += (in && (!select || top > pre)) ? 1 : 0;
-    n_eq += (in && select && top == pre) ? 1 : 0;
-  }
-  int tot;
-  const int before = epi_exclusive_scan(m, (n_eq << 16) | n_gt, &tot);
-  const int eq_before = before >> 16;
-  int take_eq = min(max(remaining - eq_before, 0), n_eq);
-  int pos = (before & 0xffff) + min(eq_before, remaining);
-  const int kept = (tot & 0xffff) + min(tot >> 16, remaining);
-#pragma unroll
-  for (int j = 0; j < C::kPer; ++j) {
-    const bool in = (mem >> j) & 1;
-    const uint64_t top = static_cast<uint64_t>(ku[j] - mn) >> hi;
-    bool take = in && (!select || top > pre);
-    if (in && select && top == pre && take_eq > 0) {
-      take = true;
-      --take_eq;
-    }
-    if (take) {
-      ck[buf_at<G>(g, pos)] = ku[j];
-      ci[buf_at<G>(g, pos)] = ki[j];
-      ++pos;
-    }
-  }
+  // tied keys are taken in warp order, then region order, until `remaining`
+  int n_eq = 0;
+  for (int r = lane; r < n_w; r += 32) n_eq += ((rk[r] - mn) >> hi) == pre ? 1 : 0;
+  n_eq = __reduce_add_sync(0xffffffffu, n_eq);
+  if (lane == 0) m->scan[ew] = n_eq;
   epi_sync();
+  int eq_seen = 0;  // tied keys of the warps before this one, then of this warp so far
+  for (int i = 0; i < ew; ++i) eq_seen += m->scan[i];
+  const unsigned below = (1u << lane) - 1u;
+  int kept_w = 0;
+  for (int c0 = 0; c0 < n_w; c0 += 32) {
+    const int r = c0 + lane;
+    const bool in = r < n_w;
+    const uint32_t key = in ? rk[r] : 0u;
+    const int32_t idx = in ? rx[r] : 0;
+    const uint64_t top = static_cast<uint64_t>(key - mn) >> hi;
+    const bool eq = in && top == pre;
+    const unsigned em = __ballot_sync(0xffffffffu, eq);
+    const bool keep = (in && top > pre) || (eq && eq_seen + __popc(em & below) < remaining);
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();  // every lane has read its entry before any is overwritten
+    if (keep) {
+      const int d = kept_w + __popc(km & below);
+      rk[d] = key;
+      rx[d] = idx;
+    }
+    __syncwarp();
+    kept_w += __popc(km);
+    eq_seen += __popc(em);
+  }
+  if (lane == 0) m->wcnt[g][ew] = kept_w;
+  epi_sync();
+  const int kept = m->wcnt[g][0] + m->wcnt[g][1] + m->wcnt[g][2] + m->wcnt[g][3];
   if (et == 0) {
     m->cnt[g] = kept;
-    if (select) m->thr[g] = max(m->thr[g], mn + static_cast<uint32_t>(pre << hi));
+    m->thr[g] = max(m->thr[g], mn + static_cast<uint32_t>(pre << hi));
     if (s.trace) {
       s.trace[kTrCompactNs] += globaltimer_ns() - tc0;
       s.trace[kTrCompactN] += 1;
     }
   }
-  if (lane == 0) m->wcnt[g][ew] = (kept - ew + 3) >> 2;
   epi_sync();
   return kept;
 }
@@ -922,8 +902,8 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
 #pragma unroll
       for (int g = 0; g < GT; ++g)
         if ((needs >> g) & 1) {
-          const int kept = compact<G>(s, g, p.topk, C::kSlack);
-          wcnt[g] = (kept - ew + 3) >> 2;
+          compact<G>(s, g, p.topk, C::kSlack);
+          wcnt[g] = s.misc->wcnt[g][ew];
           thr[g] = s.misc->thr[g];
         }
 #pragma unroll
