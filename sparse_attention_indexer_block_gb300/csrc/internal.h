@@ -103,11 +103,11 @@ constexpr int score_streams_per_cta(int G) { return G == 1 ? 2 : 1; }
 
 // Candidate-buffer capacity of one epilogue group (one token row); a published
 // segment slot holds up to this many entries.
-constexpr int candidate_capacity(int G) { return G == 1 ? 3072 : 4096; }
+constexpr int candidate_capacity(int G) { return G == 1 ? 5120 : 6144; }
 
 // Pipeline stages (128-key tiles in flight) of one CTA of the score/select
 // kernel, over all its streams.
-constexpr int score_stages(int G) { return G == 1 ? 8 : 6; }
+constexpr int score_stages(int G) { return G == 1 ? 6 : 4; }
 
 // Split work rows (rows whose tiles several CTAs share) that one launch can
 // have: each starts in a different CTA, and there is at most one per work row.
