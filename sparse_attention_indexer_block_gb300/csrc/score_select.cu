@@ -205,20 +205,35 @@ __device__ __forceinline__ void trace_set(const Smem& s, int slot, uint64_t v) {
 // producer (one thread per stream)
 // ---------------------------------------------------------------------------
 
-// The pages of tile `tile` of a work row (-1: none, or outside the cache).
+// The block-table entries of a tile's two pages as read (kNoPage past the
+// work row's pages), and the pages they name once checked (-1: none, or
+// outside the cache, which is reported). Reading and checking are apart so
+// that the producer can read one tile ahead without waiting for the load.
+constexpr int32_t kNoPage = INT32_MIN;
+struct TileRaw {
+  int32_t v[2];
+};
 struct TilePages {
   int pid[2];
 };
 
-__device__ __forceinline__ TilePages tile_pages(const ScoreParams& p, const int32_t* bt_row,
-                                                int npages, int tile) {
+__device__ __forceinline__ TileRaw tile_raw(const int32_t* bt_row, int npages, int tile) {
+  TileRaw r;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int pg = 2 * tile + h;
+    r.v[h] = pg < npages ? bt_row[pg] : kNoPage;
+  }
+  return r;
+}
+
+__device__ __forceinline__ TilePages tile_check(const ScoreParams& p, const TileRaw& r) {
   TilePages tp;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     tp.pid[h] = -1;
-    const int pg = 2 * tile + h;
-    if (pg < npages) {
-      const int32_t pv = bt_row[pg];
+    const int32_t pv = r.v[h];
+    if (pv != kNoPage) {
       if (pv >= 0 && static_cast<int64_t>(pv) < p.num_pages) tp.pid[h] = pv;
       else set_error(p.dev_error, IDX_DEV_BAD_BLOCK);
     }
@@ -267,7 +282,9 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
   int npages = (wr.maxlen + kPageTokens - 1) / kPageTokens;
   // the page ids of the next tile are read one tile ahead (their load latency
   // overlaps the wait for a free stage)
-  TilePages next = tile_pages(p, bt_row, npages, static_cast<int>(st.t0 - rs));
+  TileRaw next = tile_raw(bt_row, npages, static_cast<int>(st.t0 - rs));
+  // the index pages are read once: first out of L2
+  const uint64_t stream_policy = l2_evict_first_policy();
 
   int stage = 0;
   uint32_t phase = 0;
@@ -284,11 +301,12 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
       if (!load_q()) break;
       bt_row = p.block_table + static_cast<int64_t>(wr.req) * p.bt_stride;
       npages = (wr.maxlen + kPageTokens - 1) / kPageTokens;
-      next = tile_pages(p, bt_row, npages, static_cast<int>(t - rs));
+      next = tile_raw(bt_row, npages, static_cast<int>(t - rs));
     }
-    const TilePages cur = next;
-    if (t + 1 < st.t1 && t + 1 < re) next = tile_pages(p, bt_row, npages, static_cast<int>(t + 1 - rs));
-    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
+    const TilePages cur = tile_check(p, next);
+    // (a stage's first use needs no wait: nothing has used it yet)
+    if (t - st.t0 >= S && !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_error, p.wait_ns))
+      break;
     uint32_t bytes = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) bytes += cur.pid[h] >= 0 ? kPageValueBytes + 256 : 0;
@@ -297,11 +315,15 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (cur.pid[h] < 0) continue;
-      tma_load_3d(kv + stage * 16384 + h * kPageValueBytes, map, 0, 0, cur.pid[h], &full[stage]);
-      bulk_load(scales + stage * 128 + h * 64,
-                p.cache + static_cast<int64_t>(cur.pid[h]) * kPageBytes + kPageValueBytes, 256,
-                &full[stage]);
+      tma_load_3d_hint(kv + stage * 16384 + h * kPageValueBytes, map, 0, 0, cur.pid[h],
+                       &full[stage], stream_policy);
+      bulk_load_hint(scales + stage * 128 + h * 64,
+                     p.cache + static_cast<int64_t>(cur.pid[h]) * kPageBytes + kPageValueBytes,
+                     256, &full[stage], stream_policy);
     }
+    // the next tile's block-table entries, read after this tile's copies are
+    // issued (checked when that tile is issued)
+    if (t + 1 < st.t1 && t + 1 < re) next = tile_raw(bt_row, npages, static_cast<int>(t + 1 - rs));
     last_par[stage] = static_cast<int>(phase);
     if (++stage == S) {
       stage = 0;
@@ -355,7 +377,8 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, c
     const int acc = 2 * j + static_cast<int>(k & 1);
     const uint32_t acc_par = static_cast<uint32_t>((k >> 1) & 1);
     if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_error, p.wait_ns)) break;
-    if (!mbar_wait(&s.tempty[acc], acc_par ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
+    // (an accumulator's first use needs no wait)
+    if (k >= 2 && !mbar_wait(&s.tempty[acc], acc_par ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
     tc_fence_after();
     if (k == 0) trace_set(s, kTrFirstMma, globaltimer_ns());
     const uint32_t a_base = smem_u32(kv + stage * 16384);
