@@ -412,15 +412,15 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     caches = [d.cache] + [d.cache.clone() for _ in range(n_copies - 1)]
     ws = saib.decode_workspace(R, G, k, dev)
     out = torch.empty((R * G, k), dtype=torch.int32, device=dev)
-    lens = torch.empty(R * G, dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
 
+    # one step: the whole hot path from the requests' (seq_lens, decode_lens),
+    # the row expansion (S1) done by the launch's first kernel
     def step(i):
-        saib.indexer_expand_decode_rows(d.seq_lens, d.decode_lens, G, row_seq_lens=lens,
-                                        dev_error=err, stream=stream)
-        saib.indexer_decode_topk(d.q, d.w, caches[i % n_copies], d.block_table, lens, G, k,
-                                 out_idx=out, workspace=ws, dev_error=err, stream=stream)
+        saib.indexer_decode_topk_from_lens(d.q, d.w, caches[i % n_copies], d.block_table,
+                                           d.seq_lens, d.decode_lens, G, k, out_idx=out,
+                                           workspace=ws, dev_error=err, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(3):
@@ -508,7 +508,7 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     return {"d": d, "R": R, "G": G, "k": k, "ms": ms, "steps": steps,
             "keys_per_step": keys_per_step, "algo_bytes": algo_bytes, "roofline": roofline,
             "clocks": clk.summary(), "n_copies": n_copies, "cache_bytes": cache_bytes, "l2": l2,
-            "ws": ws, "out": out, "lens": lens, "err": err, "stream": stream,
+            "ws": ws, "out": out, "err": err, "stream": stream,
             "row_lens_h": row_lens_h}
 
 
@@ -532,8 +532,8 @@ def run_ours(args, rank, world, local):
     d, R, G, k = res["d"], res["R"], res["G"], res["k"]
     ms, keys_per_step, algo_bytes = res["ms"], res["keys_per_step"], res["algo_bytes"]
     value = whole_job_rate(keys_per_step, K, world, ms)
-    launches = 4 * K  # expand, prep, score/select, split-row selection per step
-    lens, out, ws, err, stream = res["lens"], res["out"], res["ws"], res["err"], res["stream"]
+    launches = 3 * K  # prep (with the row expansion), score/select, split-row selection
+    out, ws, err, stream = res["out"], res["ws"], res["err"], res["stream"]
 
     # end to end: pinned host inputs in, indices out, every step
     host = {n: t.cpu().pin_memory() for n, t in
@@ -547,10 +547,9 @@ def run_ours(args, rank, world, local):
     def e2e_step():
         for n in host:
             dbuf[n].copy_(host[n], non_blocking=True)
-        saib.indexer_expand_decode_rows(dbuf["seq"], dbuf["dl"], G, row_seq_lens=lens,
-                                        dev_error=err, stream=stream)
-        saib.indexer_decode_topk(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"], lens, G, k,
-                                 out_idx=out, workspace=ws, dev_error=err, stream=stream)
+        saib.indexer_decode_topk_from_lens(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"],
+                                           dbuf["seq"], dbuf["dl"], G, k, out_idx=out,
+                                           workspace=ws, dev_error=err, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
     def barrier():
@@ -587,7 +586,7 @@ def run_ours(args, rank, world, local):
             extra[wl] = {"workload": WORKLOAD_DESCS[wl], "metric_value": whole_job_rate(
                 r["keys_per_step"], steps, world, r["ms"]), "unit": "keys/s",
                 "ms_per_step": r["ms"] / steps, "steps": steps, "roofline": r["roofline"],
-                "clocks": r["clocks"], "gpu_launches": 4 * steps}
+                "clocks": r["clocks"], "gpu_launches": 3 * steps}
             del r
             torch.cuda.empty_cache()
 

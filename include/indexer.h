@@ -194,6 +194,26 @@ idx_status indexer_decode_topk(const void* q, const float* weights, const uint8_
                                uint32_t* dev_error, void* stream);
 
 /*
+ * indexer_decode_topk with the row expansion folded in ([RUNNER] token_rows,
+ * [INDEXER] DeepSeekV32IndexerDecodeMetadata: token j of a request with
+ * d = decode_lens[b] new tokens and L = seq_lens[b] keys sees L - d + j + 1
+ * keys; rows j >= d of the [num_reqs, next_n] grid are padding, length 0).
+ * The same lengths indexer_expand_decode_rows (mode 0) writes, computed by
+ * the launch's first kernel instead of a separate one. seq_lens, decode_lens
+ * int32 [num_reqs] on the device; other arguments, the workspace size and the
+ * results as indexer_decode_topk.
+ */
+idx_status indexer_decode_topk_from_lens(const void* q, const float* weights,
+                                         const uint8_t* index_cache, int64_t num_pages,
+                                         const int32_t* block_table, int64_t bt_stride,
+                                         int32_t bt_width, const int32_t* seq_lens,
+                                         const int32_t* decode_lens, int32_t num_reqs,
+                                         int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                         int32_t topk, int32_t* out_idx, void* workspace,
+                                         size_t workspace_bytes, uint32_t* dev_error,
+                                         void* stream);
+
+/*
  * Introspection of the on-device work split (for tests): where, inside a
  * decode workspace for (num_reqs, next_n, topk) on the current device, the
  * prep kernel leaves the plan the score/select kernel follows, as byte

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     decode_workspace,
     indexer_decode_logits,
     indexer_decode_topk,
+    indexer_decode_topk_from_lens,
     indexer_decode_topk_noalloc,
     indexer_decode_workspace_bytes,
     indexer_expand_decode_rows,

@@ -35,6 +35,8 @@ SIGNATURES = {
     "indexer_decode_workspace_bytes": (C.c_int, [_I32, _I32, _I32, C.POINTER(_SZ)]),
     "indexer_decode_topk": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
                                       _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "indexer_decode_topk_from_lens": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _I32,
+                                                _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "indexer_decode_logits": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32, _I32,
                                         _I32, _I32, _P, _I64, _P, _SZ, _P, _P]),
     "indexer_plan_prefill_chunks": (C.c_int, [_P, _P, _I32, _I64, _I64, _P, _I32,
@@ -190,6 +192,26 @@ def indexer_decode_topk(q, weights, index_cache, block_table, row_seq_lens, next
         int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_idx), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
     _check("indexer_decode_topk", st)
+    return out_idx
+
+
+def indexer_decode_topk_from_lens(q, weights, index_cache, block_table, seq_lens, decode_lens,
+                                  next_n: int, topk: int = MAX_TOPK, out_idx=None,
+                                  workspace=None, dev_error=None, stream=None):
+    """indexer_decode_topk with the row expansion done on the device by the
+    launch itself: seq_lens, decode_lens int32 [num_reqs]."""
+    R = int(block_table.shape[0])
+    rows = R * next_n
+    if out_idx is None:
+        out_idx = torch.empty((rows, topk), dtype=torch.int32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, next_n, topk, q.device)
+    st = load().indexer_decode_topk_from_lens(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(seq_lens), _ptr(decode_lens),
+        R, next_n, int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_idx), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_topk_from_lens", st)
     return out_idx
 
 

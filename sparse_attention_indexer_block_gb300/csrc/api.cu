@@ -233,9 +233,17 @@ void decode_row_penalty(bool logits, int next_n, int32_t* penalty, int32_t* div)
   *div = logits ? 0 : (next_n == 1 ? 25 : 24);
 }
 
+// Token rows' key counts: given per row, or expanded from the requests'
+// (seq_lens, decode_lens) by the prep kernel.
+struct RowLens {
+  const int32_t* row_seq_lens;
+  const int32_t* seq_lens;
+  const int32_t* decode_lens;
+};
+
 idx_status decode_common(bool logits, const void* q, const float* weights,
                          const uint8_t* index_cache, int64_t num_pages, const int32_t* block_table,
-                         int64_t bt_stride, int32_t bt_width, const int32_t* row_seq_lens,
+                         int64_t bt_stride, int32_t bt_width, const RowLens& lens,
                          int32_t num_reqs, int32_t next_n, int32_t num_heads, int32_t head_dim,
                          int32_t topk, int32_t* out_idx, float* out_logits, int64_t ld_logits,
                          void* workspace, size_t workspace_bytes, uint32_t* dev_error,
@@ -245,7 +253,8 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
                                num_heads, head_dim, topk);
   if (st != IDX_OK) return st;
-  if (!row_seq_lens || !workspace || !aligned(workspace, 256)) return IDX_ERR_INVALID_ARG;
+  if (!lens.row_seq_lens && (!lens.seq_lens || !lens.decode_lens)) return IDX_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return IDX_ERR_INVALID_ARG;
   if (logits) {
     if (!out_logits || ld_logits < static_cast<int64_t>(bt_width) * kPageTokens)
       return IDX_ERR_INVALID_ARG;
@@ -263,9 +272,9 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t row_penalty, row_penalty_div;
   decode_row_penalty(logits, next_n, &row_penalty, &row_penalty_div);
-  DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, row_seq_lens, num_reqs, next_n,
-                   topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty,
-                   row_penalty_div};
+  DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, lens.row_seq_lens, num_reqs,
+                   next_n, topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty,
+                   row_penalty_div, lens.seq_lens, lens.decode_lens};
   if ((st = launch_decode_prep(a, ws, L, s)) != IDX_OK) return st;
   ScoreParams p{};
   p.cache = index_cache;
@@ -419,8 +428,25 @@ idx_status indexer_decode_topk(const void* q, const float* weights, const uint8_
                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
                                uint32_t* dev_error, void* stream) {
   return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
-                       row_seq_lens, num_reqs, next_n, num_heads, head_dim, topk, out_idx, nullptr,
-                       0, workspace, workspace_bytes, dev_error, stream);
+                       RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
+                       head_dim, topk, out_idx, nullptr, 0, workspace, workspace_bytes, dev_error,
+                       stream);
+}
+
+idx_status indexer_decode_topk_from_lens(const void* q, const float* weights,
+                                         const uint8_t* index_cache, int64_t num_pages,
+                                         const int32_t* block_table, int64_t bt_stride,
+                                         int32_t bt_width, const int32_t* seq_lens,
+                                         const int32_t* decode_lens, int32_t num_reqs,
+                                         int32_t next_n, int32_t num_heads, int32_t head_dim,
+                                         int32_t topk, int32_t* out_idx, void* workspace,
+                                         size_t workspace_bytes, uint32_t* dev_error,
+                                         void* stream) {
+  if (!seq_lens || !decode_lens) return IDX_ERR_INVALID_ARG;
+  return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       RowLens{nullptr, seq_lens, decode_lens}, num_reqs, next_n, num_heads,
+                       head_dim, topk, out_idx, nullptr, 0, workspace, workspace_bytes, dev_error,
+                       stream);
 }
 
 idx_status indexer_decode_logits(const void* q, const float* weights, const uint8_t* index_cache,
@@ -431,8 +457,9 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                                  void* workspace, size_t workspace_bytes, uint32_t* dev_error,
                                  void* stream) {
   return decode_common(true, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
-                       row_seq_lens, num_reqs, next_n, num_heads, head_dim, topk, nullptr,
-                       out_logits, ld_logits, workspace, workspace_bytes, dev_error, stream);
+                       RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
+                       head_dim, topk, nullptr, out_logits, ld_logits, workspace, workspace_bytes,
+                       dev_error, stream);
 }
 
 idx_status indexer_plan_prefill_chunks(const int32_t* seq_lens_host,

@@ -143,7 +143,7 @@ idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t
 struct DecodePrepArgs {
   const __nv_bfloat16* q;
   const float* w;
-  const int32_t* row_seq_lens;
+  const int32_t* row_seq_lens;  // per token row, or nullptr: from seq_lens / decode_lens below
   int32_t num_reqs;
   int32_t next_n;
   int32_t topk;
@@ -157,6 +157,8 @@ struct DecodePrepArgs {
   // a segment's drop threshold (more buffer cuts): the penalty grows by the
   // per-CTA tile share divided by this (0: no growth).
   int32_t row_penalty_div;
+  const int32_t* seq_lens = nullptr;     // [num_reqs] (when row_seq_lens is nullptr)
+  const int32_t* decode_lens = nullptr;  // [num_reqs]
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);

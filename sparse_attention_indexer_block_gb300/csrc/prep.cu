@@ -261,6 +261,16 @@ __device__ __forceinline__ void zero_words(uint32_t* p, size_t n) {
   for (size_t i = (n / 4) * 4 + tid; i < n; i += nt) p[i] = 0;
 }
 
+// Key count of token row r = b * next_n + j before validation: the given
+// per-row length, or the row expansion's (token j of a request of d tokens
+// and L keys sees L - d + j + 1 keys; rows j >= d are padding, 0).
+__device__ __forceinline__ int64_t raw_row_len(const DecodePrepArgs& a, int64_t r) {
+  if (a.row_seq_lens) return a.row_seq_lens[r];
+  const int64_t b = r / a.next_n, j = r % a.next_n;
+  const int64_t L = a.seq_lens[b], d = a.decode_lens[b];
+  return j < d ? L - d + j + 1 : 0;
+}
+
 // Block 0: work-row schedule (tile counts and their exclusive prefix), validated
 // row lengths and zeroed segment counters. Other blocks: zeroed row histograms,
 // q quantisation into the swizzled images and the exact causal rows of short
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
         int maxlen = 0;
         for (int g = 0; g < G; ++g) {
           const int64_t r = static_cast<int64_t>(b) * G + g;
-          const int len = static_cast<int>(clamp_len(a.row_seq_lens[r], a.bt_width, a.err, true));
+          const int len = static_cast<int>(clamp_len(raw_row_len(a, r), a.bt_width, a.err, true));
           row_len[r] = len;
           const bool active = a.score_all ? len > 0 : len > a.topk;
           if (active) maxlen = max(maxlen, len);
@@ -325,7 +335,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
   quantize_tasks<true>(a.q, a.w, 0, rows * kHeads, q8img, wprime, gw, nw);
   if (!a.score_all) {
     for (int64_t r = gw; r < rows; r += nw) {
-      const int64_t len = clamp_len(a.row_seq_lens[r], a.bt_width, a.err, false);
+      const int64_t len = clamp_len(raw_row_len(a, r), a.bt_width, a.err, false);
       if (len > a.topk) continue;
       int32_t* o = a.out_idx + r * a.topk;
       for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;

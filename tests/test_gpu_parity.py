@@ -238,6 +238,30 @@ def test_topk_mtp_workload():
     _check_decode(synth.make_decode("mtp"), 2048)
 
 
+def test_topk_from_lens_matches_expand_then_topk():
+    """The entry point that expands the rows itself (prep kernel), on the MTP
+    workload (two-token requests and padded rows): its output passes the same
+    oracle checks as expansion + top-k on the expansion's lengths, and the
+    rows with len <= k (causal fill, padding) are identical."""
+    d = synth.make_decode("mtp")
+    dd = _to(d)
+    err = _err()
+    lens = _expand(dd, err)
+    out_a = saib.indexer_decode_topk(dd.q, dd.w, dd.cache, dd.block_table, lens, d.next_n, 2048,
+                                     dev_error=err)
+    out_b = saib.indexer_decode_topk_from_lens(dd.q, dd.w, dd.cache, dd.block_table, dd.seq_lens,
+                                               dd.decode_lens, d.next_n, 2048, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    lens_h = lens.cpu().numpy()
+    a, b = out_a.cpu().numpy(), out_b.cpu().numpy()
+    short = lens_h <= 2048
+    assert short.any() and (~short).any()
+    assert np.array_equal(a[short], b[short])
+    ref, lg, ta, tb, rows = _oracle_rows(d, lens_h, 2048, None)
+    _check_rows(b, lens_h, lg, ta, tb, rows, 2048, True)
+
+
 def test_topk_long_context_sampled():
     """32 of the 128 rows (the first, the last and a seeded sample), each
     131072 keys with 1% heavy-tail keys."""
