@@ -224,13 +224,18 @@ idx_status check_common(const void* q, const float* w, const uint8_t* cache, int
   return IDX_OK;
 }
 
-// A work row that ends inside a CTA's range costs that CTA a segment
-// finalisation (publication, sometimes a buffer cut) worth about `penalty`
-// tiles of streaming; the split gives such CTAs correspondingly fewer tiles.
-// When each CTA streams >= 64 tiles the penalty grows by the share / `div`.
+// A work row that ends inside a stream's range costs that stream a segment
+// finalisation (publication, and a fresh buffer for the next row that fills
+// and is cut again) worth about `penalty` tiles of streaming; the split gives
+// such streams correspondingly fewer tiles. When each stream streams >= 64
+// tiles the penalty grows by the share / `div` (the fresh buffer's cuts grow
+// with the row's length). One-token rows: fitted to per-stream end times on
+// GB300 (end = a + b * tiles + c * row ends; c = 0.6 tiles on the decode
+// batch, 23.5 on long context, share 431). Two-token rows: 12 + share / 24
+// measured faster on MTP than the fit there (2 + share / 43).
 void decode_row_penalty(bool logits, int next_n, int32_t* penalty, int32_t* div) {
-  *penalty = logits ? 0 : (next_n == 1 ? 6 : 12);
-  *div = logits ? 0 : (next_n == 1 ? 25 : 24);
+  *penalty = logits ? 0 : (next_n == 1 ? 1 : 12);
+  *div = logits ? 0 : (next_n == 1 ? 19 : 24);
 }
 
 // Token rows' key counts: given per row, or expanded from the requests'

@@ -72,7 +72,7 @@ def test_schedule_small_and_ragged():
         tiles = rng.integers(0, 30, R)
         tiles[rng.random(R) < 0.3] = 0
         for grid in (1, 2, 7, 152, 500):
-            for penalty in (0, 6, 12):
+            for penalty in (0, 1, 2, 6, 12):
                 check(tiles.tolist(), grid, penalty)
 
 
