@@ -31,7 +31,7 @@ namespace saib {
 
 namespace {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kListCap = 16384;  // keys of the cutoff bin kept in shared memory
 constexpr int kTieCap = 512;     // keys of the second-level bin ranked pairwise
