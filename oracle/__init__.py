@@ -77,6 +77,16 @@ def _load():
         lib.ora_plan_prefill_chunks.argtypes = [P, P, i32, i64, i64, P, i64]
         lib.ora_prefill_rows.restype = None
         lib.ora_prefill_rows.argtypes = [P, P, i32, P, P]
+        lib.ora_e2m1_decode.restype = C.c_double
+        lib.ora_e2m1_decode.argtypes = [u8]
+        lib.ora_ue8m0_decode.restype = C.c_double
+        lib.ora_ue8m0_decode.argtypes = [u8]
+        lib.ora_e2m1_encode.restype = u8
+        lib.ora_e2m1_encode.argtypes = [C.c_double]
+        lib.ora_mxfp4_quantize_token.restype = None
+        lib.ora_mxfp4_quantize_token.argtypes = [P, P]
+        lib.ora_row_logits_mxfp4.restype = C.c_int
+        lib.ora_row_logits_mxfp4.argtypes = [P, P, i32, i32, P, i64, P, i64, P, P, P]
         _lib = lib
         return lib
 
@@ -197,6 +207,91 @@ def row_logits(q8_row, wprime_row, cache, bt_row, length: int):
     if rc != 0:
         raise ValueError(f"oracle: bad page id in block table (rc={rc})")
     return lg[:length], ta[:length], tb[:length]
+
+
+# --------------------------------------------------------------------------
+# MXFP4 index keys (e2m1 values in blocks of 32 sharing a ue8m0 scale)
+# --------------------------------------------------------------------------
+
+MX_TOKEN_BYTES = 68    # 64 bytes of packed e2m1 values + 4 ue8m0 block scales
+MX_PAGE_BYTES = 64 * MX_TOKEN_BYTES
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """e2m1 value of each 4-bit code (closed form; no infinities, max 6)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.ora_e2m1_decode(int(x)) for x in c], dtype=np.float64).reshape(
+        np.shape(codes))
+
+
+def ue8m0_decode(codes) -> np.ndarray:
+    """2^(E - 127) for each exponent byte (255: NaN)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.ora_ue8m0_decode(int(x)) for x in c], dtype=np.float64).reshape(
+        np.shape(codes))
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Round-to-nearest-even onto the e2m1 grid, saturating at +-6."""
+    lib = _load()
+    v = np.asarray(x, dtype=np.float64).ravel()
+    return np.array([lib.ora_e2m1_encode(float(f)) for f in v], dtype=np.uint8).reshape(
+        np.shape(x))
+
+
+def mxfp4_quantize(keys) -> np.ndarray:
+    """MXFP4 entries uint8 [T, 68] of keys float32 [T, 128] (the MX
+    shared-exponent rule per block of 32)."""
+    k = np.ascontiguousarray(keys, dtype=np.float32)
+    out = np.zeros((k.shape[0], MX_TOKEN_BYTES), np.uint8)
+    lib = _load()
+    for t in range(k.shape[0]):
+        lib.ora_mxfp4_quantize_token(_p(k[t]), _p(out[t]))
+    return out
+
+
+def mxfp4_values(entries) -> np.ndarray:
+    """float64 [T, 128] key values of MXFP4 entries uint8 [T, 68]."""
+    e = np.asarray(entries, dtype=np.uint8)
+    codes = np.empty(e.shape[:-1] + (128,), np.uint8)
+    codes[..., 0::2] = e[..., :64] & 0xF
+    codes[..., 1::2] = e[..., :64] >> 4
+    table = e2m1_decode(np.arange(16, dtype=np.uint8))
+    scales = ue8m0_decode(e[..., 64:68])
+    return table[codes] * np.repeat(scales, 32, axis=-1)
+
+
+def row_logits_mxfp4(q8_row, wprime_row, cache, bt_row, length: int):
+    """Logits and tolerance magnitudes (A, B) of one token row over an MXFP4
+    cache uint8 [pages, 4352], fp64."""
+    q8_row = np.ascontiguousarray(q8_row, dtype=np.uint8)
+    wp = np.ascontiguousarray(wprime_row, dtype=np.float64)
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    bt_row = np.ascontiguousarray(bt_row, dtype=np.int32)
+    H, D = q8_row.shape
+    lg = np.empty(max(length, 1), np.float64)
+    ta = np.empty_like(lg)
+    tb = np.empty_like(lg)
+    rc = _load().ora_row_logits_mxfp4(_p(q8_row), _p(wp), H, D, _p(cache), cache.shape[0],
+                                      _p(bt_row), length, _p(lg), _p(ta), _p(tb))
+    if rc != 0:
+        raise ValueError(f"oracle: bad page id in block table (rc={rc})")
+    return lg[:length], ta[:length], tb[:length]
+
+
+def decode_topk_mxfp4(q_bf16_bits, w, cache, block_table, row_lens, next_n: int, k: int):
+    """Decode top-k over an MXFP4 cache: row r = b * next_n + j reads
+    block-table row b; rows with len <= k give the causal row."""
+    q8, _, wp = quantize_q(q_bf16_bits, w)
+    rows = np.asarray(row_lens).shape[0]
+    out = np.empty((rows, k), np.int32)
+    for r in range(rows):
+        L = int(row_lens[r])
+        lg, _, _ = row_logits_mxfp4(q8[r], wp[r], cache, block_table[r // next_n], L)
+        out[r] = topk_row(lg, L, k)
+    return out
 
 
 def topk_row(logits, length: int, k: int) -> np.ndarray:

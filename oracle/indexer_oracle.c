@@ -21,7 +21,10 @@
  *  - "vllm.models.glm5next.common.sparse_indexer": _decode_topk_seq_lens
  *    (padded rows get seq_len 0), _fill_short_decode_causal_indices (exact
  *    causal rows when every key would be selected), _gather_workspace_shapes
- *    (fp8 values + 4-byte fp32 scale per token).
+ *    (fp8 values + 4-byte fp32 scale per token; the MXFP4 path: head_dim / 2
+ *    bytes of packed mxfp4 values + head_dim / MXFP4_BLOCK_SIZE ue8m0 scale
+ *    bytes per token) and kv_cache_as_quant_view (the MXFP4 cache view: token
+ *    stride head_dim / 2 + head_dim / MXFP4_BLOCK_SIZE bytes inside a page).
  *  - The scoring rule logit[t,s] = sum_h w[t,h] * ReLU(scale_s * (q[t,h] . k_s))
  *    and top-k = 2048 come from the statement of the method; the pages only name
  *    the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
@@ -38,6 +41,20 @@
  *    s % 64 (negative = padding); scale = amax / 448 and codes e4m3(x / scale),
  *    fp32 steps like the q quantisation; amax == 0 gives zero codes, scale 0.
  *  - Since scale_s >= 0, ReLU(scale_s * x) = scale_s * ReLU(x).
+ *  - MXFP4 index keys (the cache format the INDEXER page gates behind
+ *    use_fp4_indexer_cache): MXFP4_BLOCK_SIZE = 32 (so 4 scale bytes and a
+ *    68-byte token entry); a page is 64 token entries back to back (4352
+ *    bytes, the quant view's token stride with no padding); inside an entry
+ *    the 64 value bytes come first (element 2i in the low nibble of byte i,
+ *    2i + 1 in the high nibble), then the 4 scale bytes (block b covers
+ *    elements 32b .. 32b + 31), in the order the gather workspace lists them.
+ *    e2m1: 1 sign, 2 exponent (bias 1), 1 mantissa bit, no infinities or NaN,
+ *    largest magnitude 6; ue8m0: 2^(E - 127), E = 255 is NaN. A key's value
+ *    d is e2m1(code_d) * 2^(E_{d/32} - 127); there is no per-token fp32 scale.
+ *    The cache writer is not shown: the oracle quantises a block of 32 by the
+ *    shared-exponent rule of the MX format: E = floor(log2(amax)) - 2 + 127
+ *    (2 = the largest e2m1 exponent; clamped to [0, 254]; amax = 0 gives
+ *    E = 0 and zero codes), codes = e2m1_rne_satfinite(x / 2^(E - 127)).
  *  - Rows with len <= k output [0, 1, ..., len-1, -1, ...]; rows with len > k
  *    output the k indices of the largest logits; ties are broken here by the
  *    smaller index (any k-subset that agrees within the tolerance is accepted
@@ -278,6 +295,132 @@ int ora_row_logits(const uint8_t* q8_row, const double* wprime_row, int32_t head
     logits[s] = scale * acc;
     if (tol_a) tol_a[s] = scale * acc_a;
     if (tol_b) tol_b[s] = scale * acc_b;
+  }
+  free(qd);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP4 index keys                                                           */
+/* ------------------------------------------------------------------------ */
+
+#define ORA_MX_BLOCK 32
+#define ORA_MX_TOKEN_BYTES (ORA_DIM / 2 + ORA_DIM / ORA_MX_BLOCK) /* 68 */
+#define ORA_MX_PAGE_BYTES (ORA_PAGE_TOKENS * ORA_MX_TOKEN_BYTES) /* 4352 */
+
+/* e2m1 (the low 4 bits of code): e == 0 gives m * 0.5 (0 or 0.5), else
+ * 2^(e - 1) * (1 + m / 2); the sign bit negates. */
+double ora_e2m1_decode(uint8_t code) {
+  int s = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
+/* ue8m0: 2^(E - 127); E = 255 is NaN. */
+double ora_ue8m0_decode(uint8_t e) {
+  if (e == 255) return NAN;
+  return ldexp(1.0, (int)e - 127);
+}
+
+/* Round-to-nearest-even onto the e2m1 grid, saturating to +-6: a search over
+ * the 8 non-negative codes, which increase with the code. */
+uint8_t ora_e2m1_encode(double x) {
+  uint8_t sign = signbit(x) ? 0x8 : 0x0;
+  double a = fabs(x);
+  if (isnan(x)) return 0; /* never produced by the writer below */
+  if (a >= 6.0) return sign | 0x7;
+  int lo = 0;
+  for (int c = 0; c <= 7; ++c) {
+    if (ora_e2m1_decode((uint8_t)c) <= a) lo = c;
+    else break;
+  }
+  double vlo = ora_e2m1_decode((uint8_t)lo);
+  if (vlo == a) return sign | (uint8_t)lo;
+  int hi = lo + 1;
+  double vhi = ora_e2m1_decode((uint8_t)hi);
+  double dlo = a - vlo, dhi = vhi - a;
+  int pick;
+  if (dlo < dhi) pick = lo;
+  else if (dhi < dlo) pick = hi;
+  else pick = (lo & 1) ? hi : lo; /* tie: even mantissa */
+  return sign | (uint8_t)pick;
+}
+
+/* One token's MXFP4 entry (68 bytes) from its 128 values, by the MX
+ * shared-exponent rule (see the readings above). */
+void ora_mxfp4_quantize_token(const float* x, uint8_t* out) {
+  memset(out, 0, ORA_MX_TOKEN_BYTES);
+  for (int b = 0; b < ORA_DIM / ORA_MX_BLOCK; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < ORA_MX_BLOCK; ++i) {
+      double a = fabs((double)x[b * ORA_MX_BLOCK + i]);
+      if (a > amax) amax = a;
+    }
+    int E = 0;
+    if (amax > 0.0) {
+      int ex;
+      frexp(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+      E = (ex - 1) - 2 + 127;
+      if (E < 0) E = 0;
+      if (E > 254) E = 254;
+    }
+    out[ORA_DIM / 2 + b] = (uint8_t)E;
+    if (amax == 0.0) continue;
+    double X = ldexp(1.0, E - 127);
+    for (int i = 0; i < ORA_MX_BLOCK; ++i) {
+      int d = b * ORA_MX_BLOCK + i;
+      uint8_t c = ora_e2m1_encode((double)x[d] / X);
+      out[d / 2] |= (uint8_t)((d & 1) ? (c << 4) : c);
+    }
+  }
+}
+
+/* Value d of an MXFP4 entry. */
+static double mx_value(const uint8_t* entry, int d) {
+  uint8_t byte = entry[d / 2];
+  uint8_t code = (d & 1) ? (byte >> 4) : (byte & 0xF);
+  return ora_e2m1_decode(code) * ora_ue8m0_decode(entry[ORA_DIM / 2 + d / ORA_MX_BLOCK]);
+}
+
+/* Logits of one token row over keys [0, len) with an MXFP4 cache:
+ *   logit[s] = sum_h wprime[h] * max(dot_h(s), 0),
+ *   dot_h(s) = sum_d q8[h][d] * k_s[d],  k_s[d] = e2m1(code) * 2^(E - 127)
+ * (each block's 32 products are exact in fp64 and share one power of two).
+ * tol_a / tol_b as ora_row_logits with scale 1 (either may be NULL).
+ * Returns -1 when a page id is outside [0, num_pages), else 0. */
+int ora_row_logits_mxfp4(const uint8_t* q8_row, const double* wprime_row, int32_t heads,
+                         int32_t dim, const uint8_t* cache, int64_t num_pages,
+                         const int32_t* bt_row, int64_t len, double* logits, double* tol_a,
+                         double* tol_b) {
+  pthread_once(&g_dec_once, init_dec);
+  double* qd = (double*)malloc(sizeof(double) * (size_t)heads * dim);
+  double kd[ORA_DIM];
+  if (!qd || dim != ORA_DIM) { free(qd); return -2; }
+  for (int64_t i = 0; i < (int64_t)heads * dim; ++i) qd[i] = g_dec[q8_row[i]];
+  for (int64_t s = 0; s < len; ++s) {
+    int64_t page = bt_row[s / ORA_PAGE_TOKENS];
+    if (page < 0 || page >= num_pages) { free(qd); return -1; }
+    const uint8_t* entry = cache + page * ORA_MX_PAGE_BYTES + (s % ORA_PAGE_TOKENS) * ORA_MX_TOKEN_BYTES;
+    for (int d = 0; d < ORA_DIM; ++d) kd[d] = mx_value(entry, d);
+    double acc = 0.0, acc_a = 0.0, acc_b = 0.0;
+    for (int32_t h = 0; h < heads; ++h) {
+      const double* qh = qd + (int64_t)h * dim;
+      double dot = 0.0, adot = 0.0;
+      for (int d = 0; d < ORA_DIM; ++d) {
+        double p = qh[d] * kd[d];
+        dot += p;
+        adot += fabs(p);
+      }
+      double relu = dot > 0.0 ? dot : 0.0;
+      acc += wprime_row[h] * relu;
+      acc_a += fabs(wprime_row[h]) * relu;
+      acc_b += fabs(wprime_row[h]) * adot;
+    }
+    logits[s] = acc;
+    if (tol_a) tol_a[s] = acc_a;
+    if (tol_b) tol_b[s] = acc_b;
   }
   free(qd);
   return 0;

@@ -504,3 +504,149 @@ def test_fraction_exactness_of_score_scale():
         dot = sum(a * b for a, b in zip(qd, kd))
         tot += Fraction(float(wp[0, h])) * max(Fraction(0.375) * dot, Fraction(0))
     assert abs(Fraction(float(lg[0])) - tot) <= abs(tot) * Fraction(1, 10 ** 15)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 index keys (GLM5 page: _gather_workspace_shapes, kv_cache_as_quant_view;
+# INDEXER page: the use_fp4_indexer_cache gate)
+# ---------------------------------------------------------------------------
+
+def _golden_e2m1():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_codes.txt"))
+            if l.strip() and not l.startswith("#")]
+    return {int(c): float(v) for c, v in rows}
+
+
+def test_e2m1_decode_matches_golden_table():
+    g = _golden_e2m1()
+    got = oracle.e2m1_decode(np.arange(16, dtype=np.uint8))
+    for c in range(16):
+        assert got[c] == g[c] and np.signbit(got[c]) == np.signbit(g[c]), c
+
+
+def test_e2m1_encode_round_trips_and_rounds_to_nearest_even():
+    g = _golden_e2m1()
+    for c in range(16):
+        want = c if c != 8 else 8  # -0 keeps its sign bit
+        assert int(oracle.e2m1_encode(g[c])) == want, c
+    # midpoints (worked by hand): ties go to the even mantissa
+    cases = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6,
+             -0.75: 10, -5.0: 14,
+             0.26: 1, 0.74: 1, 1.26: 3, 4.9: 6, 5.1: 7,
+             6.0: 7, 7.9: 7, 1e9: 7, -100.0: 15}
+    for x, c in cases.items():
+        assert int(oracle.e2m1_encode(x)) == c, (x, c)
+
+
+def test_ue8m0_decode_matches_torch_for_every_code():
+    tvals = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64)
+    got = oracle.ue8m0_decode(np.arange(256, dtype=np.uint8))
+    t = tvals.numpy()
+    assert np.isnan(got[255]) and np.isnan(t[255])
+    assert np.array_equal(got[:255], t[:255])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+
+
+def test_mxfp4_quantize_hand_worked_blocks():
+    x = np.zeros((1, 128), np.float32)
+    x[0, :6] = [6.0, -3.0, 1.5, 0.75, 0.2, 0.0]     # block 0: amax 6 -> E = 2 - 2 + 127
+    x[0, 32] = 0.3                                   # block 1: amax 0.3 -> E = -2 - 2 + 127
+    x[0, 33] = -0.1                                  #   0.1 / 2^-4 = 1.6 -> 1.5
+    # block 2: all zero -> E = 0, zero codes
+    x[0, 96] = 7.9                                   # block 3: amax 7.9 -> E = 127, saturates
+    e = oracle.mxfp4_quantize(x)[0]
+    assert e[0] == 0xD7 and e[1] == 0x23 and e[2] == 0x00   # (6, -3), (1.5, 1.0), (0, 0)
+    assert e[16] == (0xB << 4 | 0x6)                       # (0.3 -> 4.0 * 2^-4, -0.1 -> -1.5 * 2^-4)
+    assert list(e[64:68]) == [127, 123, 0, 127]
+    assert e[48] == 0x07                                   # 7.9 -> 6 (saturated)
+    v = oracle.mxfp4_values(e[None])[0]
+    assert v[:6].tolist() == [6.0, -3.0, 1.5, 1.0, 0.0, 0.0]
+    assert v[32] == 0.25 and v[33] == -0.09375 and v[96] == 6.0
+
+
+def test_mxfp4_quantize_error_bound_and_scale_rule():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((64, 128)) * np.exp2(rng.integers(-20, 20, (64, 1)))).astype(np.float32)
+    e = oracle.mxfp4_quantize(x)
+    v = oracle.mxfp4_values(e)
+    for b in range(4):
+        blk = x[:, 32 * b:32 * (b + 1)].astype(np.float64)
+        amax = np.abs(blk).max(axis=1)
+        E = np.floor(np.log2(amax)).astype(int) - 2 + 127
+        assert np.array_equal(e[:, 64 + b].astype(int), E)
+        X = np.exp2(E - 127.0)[:, None]
+        # the block's largest value lands in [4X, 8X): at most 2X from the grid
+        # (saturation at 6X), every other value within half a step (<= X)
+        assert (np.abs(v[:, 32 * b:32 * (b + 1)] - blk) <= 2 * X).all()
+        inside = np.abs(blk) <= 6 * X
+        assert (np.abs(v[:, 32 * b:32 * (b + 1)] - blk)[inside] <= X.repeat(32, 1)[inside]).all()
+
+
+def _mx_cache(rng, pages):
+    keys = rng.standard_normal((pages * 64, 128)).astype(np.float32)
+    return oracle.mxfp4_quantize(keys).reshape(pages, oracle.MX_PAGE_BYTES), keys
+
+
+def test_mxfp4_row_logits_hand_computed_key():
+    # one head; q8 = code 0x38 (1.0) on d = 0 and 40, 0xB8 (-1.0) on d = 100
+    q8 = np.zeros((1, 128), np.uint8)
+    q8[0, 0] = 0x38
+    q8[0, 40] = 0x38
+    q8[0, 100] = 0xB8
+    entry = np.zeros(68, np.uint8)
+    entry[0] = 0x07            # d = 0: 6.0
+    entry[20] = 0x05           # d = 40: 3.0
+    entry[50] = 0x0C           # d = 100: -2.0
+    entry[64:68] = [126, 128, 127, 125]   # block scales 0.5, 2, 1, 0.25
+    cache = np.zeros((2, oracle.MX_PAGE_BYTES), np.uint8)
+    slot = 5
+    cache[1, slot * 68:(slot + 1) * 68] = entry
+    bt = np.array([1], np.int32)
+    lg, ta, tb = oracle.row_logits_mxfp4(q8, np.array([0.5]), cache, bt, slot + 1)
+    dot = 1.0 * 6.0 * 0.5 + 1.0 * 3.0 * 2.0 + (-1.0) * (-2.0) * 0.25   # 3 + 6 + 0.5
+    assert lg[slot] == 0.5 * dot and ta[slot] == 0.5 * dot and tb[slot] == 0.5 * dot
+    assert (lg[:slot] == 0.0).all()
+
+
+def test_mxfp4_row_logits_match_dense_restatement_on_permuted_pages():
+    rng = np.random.default_rng(11)
+    pages = 6
+    cache, _ = _mx_cache(rng, pages)
+    q = rng.standard_normal((4, 128)).astype(np.float32)
+    q8 = oracle.e4m3_encode(q * 16)
+    wp = rng.standard_normal(4)
+    bt = rng.permutation(pages).astype(np.int32)
+    L = pages * 64 - 17
+    lg, ta, tb = oracle.row_logits_mxfp4(q8, wp, cache, bt, L)
+    # dense restatement: gather the pages by fancy indexing, decode, matmul
+    ent = cache.reshape(pages, 64, 68)[bt].reshape(-1, 68)[:L]
+    k = oracle.mxfp4_values(ent)
+    dots = oracle.e4m3_decode(q8) @ k.T                   # [H, L]
+    want = (wp[:, None] * np.maximum(dots, 0)).sum(0)
+    assert np.allclose(lg, want, rtol=1e-12, atol=1e-12)
+    # the dot of one head is exact: scaled by 2^(10 - (E_min - 127)) it is an integer
+    e_min = int(ent[:, 64:68].min())
+    scaled = dots * np.exp2(9 + 1 - (e_min - 127))
+    assert np.array_equal(scaled, np.round(scaled))
+
+
+def test_mxfp4_decode_topk_matches_brute_force():
+    rng = np.random.default_rng(12)
+    pages = 5
+    cache, _ = _mx_cache(rng, pages)
+    R, next_n, k = 2, 2, 40
+    q = torch.randn(R * next_n, 64, 128, generator=torch.Generator().manual_seed(3))
+    qbits = q.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w = (rng.standard_normal((R * next_n, 64)) / 8).astype(np.float32)
+    bt = np.stack([rng.permutation(pages), rng.permutation(pages)]).astype(np.int32)
+    lens = np.array([300, 301, 30, 0], np.int32)
+    out = oracle.decode_topk_mxfp4(qbits, w, cache, bt, lens, next_n, k)
+    q8, _, wp = oracle.quantize_q(qbits, w)
+    for r in range(R * next_n):
+        L = int(lens[r])
+        if L <= k:
+            assert out[r].tolist() == list(range(L)) + [-1] * (k - L)
+            continue
+        lg, _, _ = oracle.row_logits_mxfp4(q8[r], wp[r], cache, bt[r // next_n], L)
+        order = sorted(range(L), key=lambda i: (-lg[i], i))
+        assert sorted(out[r].tolist()) == sorted(order[:k])
