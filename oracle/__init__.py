@@ -87,6 +87,14 @@ def _load():
         lib.ora_mxfp4_quantize_token.argtypes = [P, P]
         lib.ora_row_logits_mxfp4.restype = C.c_int
         lib.ora_row_logits_mxfp4.argtypes = [P, P, i32, i32, P, i64, P, i64, P, P, P]
+        lib.ora_topk_row_values.restype = None
+        lib.ora_topk_row_values.argtypes = [P, i64, i32, P, P]
+        lib.ora_dcp_local_len.restype = i64
+        lib.ora_dcp_local_len.argtypes = [i64, i32, i32, i32]
+        lib.ora_dcp_global_index.restype = i64
+        lib.ora_dcp_global_index.argtypes = [i64, i32, i32, i32]
+        lib.ora_merge_candidates.restype = None
+        lib.ora_merge_candidates.argtypes = [P, P, i64, i32, P, P]
         _lib = lib
         return lib
 
@@ -353,6 +361,90 @@ def decode_topk(q_bf16_bits, w, cache, block_table, row_lens, next_n: int, k: in
     out, lg, ta, tb = score_select_rows(q8, wp, cache, block_table, rows, rows // next_n,
                                         row_lens[rows], k, want_logits, threads)
     return out, lg, ta, tb, rows
+
+
+# --------------------------------------------------------------------------
+# key-sharded (decode context parallel) decode
+# --------------------------------------------------------------------------
+
+def topk_row_values(logits, length: int, k: int):
+    """(indices int32 [k], logits float64 [k]) of a row: all keys when
+    length <= k (-1 / -inf past length), else the k best."""
+    lg = np.ascontiguousarray(logits, dtype=np.float64)
+    out = np.empty(k, np.int32)
+    val = np.empty(k, np.float64)
+    _load().ora_topk_row_values(_p(lg), length, k, _p(out), _p(val))
+    return out, val
+
+
+def dcp_local_lens(lens, rank: int, world: int, interleave: int) -> np.ndarray:
+    """Rank `rank`'s key count of each length (the INDEXER page's DCP rule)."""
+    lib = _load()
+    a = np.asarray(lens, dtype=np.int64).ravel()
+    return np.array([lib.ora_dcp_local_len(int(L), rank, world, interleave) for L in a],
+                    dtype=np.int64).reshape(np.shape(lens))
+
+
+def dcp_global_index(local, rank: int, world: int, interleave: int) -> np.ndarray:
+    """Global token of each of rank `rank`'s local keys (negative stays -1)."""
+    lib = _load()
+    a = np.asarray(local, dtype=np.int64).ravel()
+    return np.array([lib.ora_dcp_global_index(int(j), rank, world, interleave) if j >= 0 else -1
+                     for j in a], dtype=np.int64).reshape(np.shape(local))
+
+
+def merge_candidates(vals, idx, k: int):
+    """Per row: the k best (logit desc, index asc) of candidates vals / idx
+    [..., rows, n] flattened over the leading axes per row (idx < 0 empty)."""
+    v = np.asarray(vals, dtype=np.float64)
+    x = np.asarray(idx, dtype=np.int32)
+    rows = v.shape[-2]
+    v = np.ascontiguousarray(np.moveaxis(v, -2, 0).reshape(rows, -1))
+    x = np.ascontiguousarray(np.moveaxis(x, -2, 0).reshape(rows, -1))
+    out = np.empty((rows, k), np.int32)
+    ov = np.empty((rows, k), np.float64)
+    lib = _load()
+    for r in range(rows):
+        lib.ora_merge_candidates(_p(v[r]), _p(x[r]), v.shape[1], k, _p(out[r]), _p(ov[r]))
+    return out, ov
+
+
+def dcp_rank_topk_values(q_bf16_bits, w, cache, block_table, row_lens, next_n: int, k: int,
+                         rank: int, world: int, interleave: int):
+    """One rank's part: for token row r (block-table row r // next_n of the
+    rank's local cache) the top k of its local keys with their logits, the
+    indices in global token positions. Returns (idx [rows, k], val [rows, k],
+    local lens, logits list, tol_a list, tol_b list) (logits over local keys)."""
+    q8, _, wp = quantize_q(q_bf16_bits, w)
+    local = dcp_local_lens(np.asarray(row_lens, dtype=np.int64), rank, world, interleave)
+    rows = local.shape[0]
+    out = np.empty((rows, k), np.int32)
+    val = np.empty((rows, k), np.float64)
+    lgs, tas, tbs = [], [], []
+    for r in range(rows):
+        L = int(local[r])
+        lg, ta, tb = row_logits(q8[r], wp[r], cache, block_table[r // next_n], L)
+        o, v = topk_row_values(lg, L, k)
+        out[r] = dcp_global_index(o, rank, world, interleave)
+        val[r] = v
+        lgs.append(lg)
+        tas.append(ta)
+        tbs.append(tb)
+    return out, val, local, lgs, tas, tbs
+
+
+def dcp_decode_topk(q_bf16_bits, w, shards, row_lens, next_n: int, k: int, interleave: int):
+    """Key-sharded decode top-k: shards[r] = (cache, block_table) of rank r
+    (its local keys in order); each rank's candidates, then their merge.
+    Returns (idx [rows, k] by (logit desc, index asc), val [rows, k])."""
+    world = len(shards)
+    vals, idxs = [], []
+    for rank, (cache, bt) in enumerate(shards):
+        o, v, *_ = dcp_rank_topk_values(q_bf16_bits, w, cache, bt, row_lens, next_n, k, rank,
+                                        world, interleave)
+        vals.append(v)
+        idxs.append(o)
+    return merge_candidates(np.stack(vals), np.stack(idxs), k)
 
 
 # --------------------------------------------------------------------------

@@ -25,6 +25,8 @@
  *    bytes of packed mxfp4 values + head_dim / MXFP4_BLOCK_SIZE ue8m0 scale
  *    bytes per token) and kv_cache_as_quant_view (the MXFP4 cache view: token
  *    stride head_dim / 2 + head_dim / MXFP4_BLOCK_SIZE bytes inside a page).
+ *    _build_prefill_chunk_metadata_kernel's DCP branch also gives the key
+ *    count of one rank of a key-sharded (decode context parallel) cache.
  *  - The scoring rule logit[t,s] = sum_h w[t,h] * ReLU(scale_s * (q[t,h] . k_s))
  *    and top-k = 2048 come from the statement of the method; the pages only name
  *    the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
@@ -55,6 +57,13 @@
  *    shared-exponent rule of the MX format: E = floor(log2(amax)) - 2 + 127
  *    (2 = the largest e2m1 exponent; clamped to [0, 254]; amax = 0 gives
  *    E = 0 and zero codes), codes = e2m1_rne_satfinite(x / 2^(E - 127)).
+ *  - Key-sharded decode (the pages give only the local key count): each rank
+ *    scores the keys it holds for a row (its local count of the row's
+ *    length, dealt in runs of I tokens) and keeps its top k with their
+ *    logits (a row of <= k local keys keeps them all); the ranks' candidates,
+ *    in global token positions, are merged by the same rule as one row's
+ *    top k. The merged set equals the unsharded row's top k, since every
+ *    key of the global top k is in its own rank's top k.
  *  - Rows with len <= k output [0, 1, ..., len-1, -1, ...]; rows with len > k
  *    output the k indices of the largest logits; ties are broken here by the
  *    smaller index (any k-subset that agrees within the tolerance is accepted
@@ -452,6 +461,61 @@ void ora_topk_row(const double* logits, int64_t len, int32_t k, int32_t* out) {
   for (int64_t s = 0; s < len; ++s) { p[s].v = logits[s]; p[s].i = (int32_t)s; }
   qsort(p, (size_t)len, sizeof(ora_pair), cmp_pair);
   for (int32_t i = 0; i < k; ++i) out[i] = p[i].i;
+  free(p);
+}
+
+/* len <= k: every key, out = [0, ..., len-1, -1, ...] with its logit (-inf
+ * past len); len > k: as ora_topk_row, with the logit of each index. The
+ * form a key-sharded rank hands to the merge: its row of len <= k keys
+ * still needs the logits. */
+void ora_topk_row_values(const double* logits, int64_t len, int32_t k, int32_t* out,
+                         double* out_val) {
+  ora_topk_row(logits, len, k, out);
+  for (int32_t i = 0; i < k; ++i) out_val[i] = out[i] >= 0 ? logits[out[i]] : -INFINITY;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Key-sharded decode (decode context parallelism)                           */
+/* ------------------------------------------------------------------------ */
+/* INDEXER page, _build_prefill_chunk_metadata_kernel, the DCP_WORLD_SIZE > 1
+ * branch: a sequence's keys are dealt to the W ranks in runs of I tokens
+ * (token t goes to rank (t / I) % W, after the rank's earlier tokens), so
+ * rank r holds, of L keys,
+ *   base + min(max(rem - r * I, 0), I),  base = L / I / W * I,  rem = L - base * W
+ * (floor divisions, in the kernel's order). W <= 1: all L. */
+int64_t ora_dcp_local_len(int64_t L, int32_t rank, int32_t world, int32_t interleave) {
+  if (world <= 1) return L;
+  const int64_t base = L / interleave / world * interleave;
+  const int64_t rem = L - base * world;
+  int64_t r = rem - (int64_t)rank * interleave;
+  if (r < 0) r = 0;
+  if (r > interleave) r = interleave;
+  return base + r;
+}
+
+/* Token of the whole sequence that rank `rank` holds as its local key j: its
+ * (j / I)-th run, which comes after (j / I) full rounds of W runs and `rank`
+ * runs of the current round; offset j % I inside the run. */
+int64_t ora_dcp_global_index(int64_t j, int32_t rank, int32_t world, int32_t interleave) {
+  if (world <= 1) return j;
+  return (j / interleave) * (int64_t)interleave * world + (int64_t)rank * interleave +
+         j % interleave;
+}
+
+/* One row's merge of the ranks' candidates: n (logit, global index) pairs,
+ * index < 0 = an empty slot. out = the k best by (logit desc, index asc) in
+ * that order, -1 (and -inf) past the candidates. */
+void ora_merge_candidates(const double* val, const int32_t* idx, int64_t n, int32_t k,
+                          int32_t* out, double* out_val) {
+  ora_pair* p = (ora_pair*)malloc(sizeof(ora_pair) * (size_t)(n > 0 ? n : 1));
+  int64_t m = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (idx[i] >= 0) { p[m].v = val[i]; p[m].i = idx[i]; ++m; }
+  qsort(p, (size_t)m, sizeof(ora_pair), cmp_pair);
+  for (int32_t i = 0; i < k; ++i) {
+    out[i] = i < m ? p[i].i : -1;
+    out_val[i] = i < m ? p[i].v : -INFINITY;
+  }
   free(p);
 }
 

@@ -210,6 +210,40 @@ def make_decode_from_lens(seq_lens, decode_lens, next_n: int, seed: int = MASTER
                         next_n=next_n, topk=topk)
 
 
+def shard_decode(inp: DecodeInputs, world: int, interleave: int, seed: int = MASTER_SEED):
+    """Key-sharded copies of a decode cache: a list over ranks of (cache uint8
+    [P_r, 8448], block_table int32 [R, W_r]) on the inputs' device.
+
+    Token t of request b is dealt to rank (t // interleave) % world; a rank
+    stores the tokens it is dealt in their order as its local tokens 0, 1, ...
+    (the same fp8 codes and scale bytes), on pages of its own seeded random
+    permutation. Data placement only: the bytes of each token are copied."""
+    dev = inp.cache.device
+    cache = inp.cache.cpu().numpy()
+    bt = inp.block_table.cpu().numpy()
+    lens = inp.seq_lens.cpu().numpy().astype(np.int64)
+    shards = []
+    for r in range(world):
+        toks = [np.nonzero((np.arange(L) // interleave) % world == r)[0] for L in lens]
+        local_lens = np.array([len(t) for t in toks], np.int32)
+        lbt, P, _, _ = page_table(local_lens, seed + 101 * (r + 1))
+        out = np.zeros((P, PAGE_BYTES), np.uint8)
+        for b, t in enumerate(toks):
+            if len(t) == 0:
+                continue
+            j = np.arange(len(t))
+            src_pg, src_sl = bt[b, t // PAGE_TOKENS], t % PAGE_TOKENS
+            dst_pg, dst_sl = lbt[b, j // PAGE_TOKENS], j % PAGE_TOKENS
+            vals = cache[:, :SCALE_OFFSET].reshape(-1, PAGE_TOKENS, HEAD_DIM)
+            scl = cache[:, SCALE_OFFSET:].reshape(-1, PAGE_TOKENS, 4)
+            ov = out[:, :SCALE_OFFSET].reshape(-1, PAGE_TOKENS, HEAD_DIM)
+            os_ = out[:, SCALE_OFFSET:].reshape(-1, PAGE_TOKENS, 4)
+            ov[dst_pg, dst_sl] = vals[src_pg, src_sl]
+            os_[dst_pg, dst_sl] = scl[src_pg, src_sl]
+        shards.append((torch.from_numpy(out).to(dev), torch.from_numpy(lbt).to(dev)))
+    return shards
+
+
 def make_prefill(name_or_wl="prefill", seed: int = MASTER_SEED, device="cpu",
                  seq_lens=None, query_lens=None) -> PrefillInputs:
     wl = WORKLOADS[name_or_wl] if isinstance(name_or_wl, str) else name_or_wl

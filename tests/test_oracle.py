@@ -650,3 +650,98 @@ def test_mxfp4_decode_topk_matches_brute_force():
         lg, _, _ = oracle.row_logits_mxfp4(q8[r], wp[r], cache, bt[r // next_n], L)
         order = sorted(range(L), key=lambda i: (-lg[i], i))
         assert sorted(out[r].tolist()) == sorted(order[:k])
+
+
+# --------------------------------------------------------------------------
+# key-sharded (decode context parallel) decode
+# --------------------------------------------------------------------------
+
+def test_dcp_local_len_matches_counting_the_dealt_tokens():
+    # INDEXER page, _build_prefill_chunk_metadata_kernel (DCP branch): token t
+    # goes to rank (t // I) % W; the closed form must count exactly those.
+    for world in (1, 2, 3, 4, 8):
+        for inter in (1, 2, 3, 5, 64):
+            lens = np.arange(0, 700, 7 if inter > 5 else 1)
+            tot = np.zeros_like(lens)
+            for r in range(world):
+                got = oracle.dcp_local_lens(lens, r, world, inter)
+                ref = np.array([int(((np.arange(L) // inter) % world == r).sum()) for L in lens])
+                assert np.array_equal(got, ref), (world, inter, r)
+                tot += got
+            assert np.array_equal(tot, lens)
+
+
+def test_dcp_local_len_hand_cases():
+    # 130 keys, runs of 64 over 2 ranks: rank 0 holds 0..63 and 128..129
+    assert oracle.dcp_local_lens([130], 0, 2, 64)[0] == 66
+    assert oracle.dcp_local_lens([130], 1, 2, 64)[0] == 64
+    # 10 keys, runs of 1 over 4 ranks: 3, 3, 2, 2
+    assert [int(oracle.dcp_local_lens([10], r, 4, 1)[0]) for r in range(4)] == [3, 3, 2, 2]
+
+
+def test_dcp_global_index_inverts_the_dealing():
+    for world, inter, L in ((2, 1, 37), (3, 5, 101), (4, 64, 1000), (1, 7, 20)):
+        t = np.arange(L)
+        owner = (t // inter) % world
+        seen = []
+        for r in range(world):
+            n = int(oracle.dcp_local_lens([L], r, world, inter)[0])
+            g = oracle.dcp_global_index(np.arange(n), r, world, inter)
+            assert np.array_equal(g, t[owner == r])   # rank r's tokens, in order
+            seen.append(g)
+        assert np.array_equal(np.sort(np.concatenate(seen)), t)
+    assert oracle.dcp_global_index([-1], 1, 2, 64)[0] == -1
+
+
+def test_topk_row_values_keeps_short_rows_whole():
+    rng = np.random.default_rng(11)
+    lg = rng.standard_normal(50)
+    o, v = oracle.topk_row_values(lg, 50, 64)
+    assert np.array_equal(o[:50], np.arange(50)) and np.all(o[50:] == -1)
+    assert np.array_equal(v[:50], lg) and np.all(np.isneginf(v[50:]))
+    lg = rng.standard_normal(300)
+    o, v = oracle.topk_row_values(lg, 300, 64)
+    assert np.array_equal(o, np.argsort(-lg, kind="stable")[:64])
+    assert np.array_equal(v, lg[o])
+
+
+def test_merge_candidates_brute_force():
+    rng = np.random.default_rng(12)
+    for n_per, world, k in ((64, 2, 64), (30, 3, 64), (100, 4, 37)):
+        vals = np.round(rng.standard_normal((world, 5, n_per)), 1)   # many ties
+        idx = rng.permutation(world * 5 * n_per).reshape(world, 5, n_per).astype(np.int32)
+        idx[rng.random(idx.shape) < 0.2] = -1
+        vals[idx < 0] = -np.inf
+        out, ov = oracle.merge_candidates(vals, idx, k)
+        for r in range(5):
+            cand = sorted((-vals[w, r, i], idx[w, r, i]) for w in range(world)
+                          for i in range(n_per) if idx[w, r, i] >= 0)
+            ref = [c[1] for c in cand[:k]] + [-1] * max(0, k - len(cand))
+            assert list(out[r]) == ref
+            assert np.array_equal(ov[r][:len(cand)], [-c[0] for c in cand[:k]])
+
+
+@pytest.mark.parametrize("world,inter,next_n", [(1, 1, 1), (2, 1, 1), (3, 64, 2), (4, 5, 1)])
+def test_dcp_decode_topk_equals_the_unsharded_topk(world, inter, next_n):
+    # every key of a row's top k is in its own rank's top k, so the merge of
+    # the ranks' candidates is the unsharded row's top k (same logits)
+    k = 96
+    seq = np.array([40, 96, 97, 400, 1000, 333], np.int32)
+    dl = np.array([1, 2, 1, 2, 2, 1], np.int32) if next_n == 2 else np.ones(6, np.int32)
+    inp = synth.make_decode_from_lens(seq, dl, next_n, seed=31 + world)
+    qb = synth.bf16_bits(inp.q)
+    w = inp.w.numpy()
+    rl, _, _ = oracle.expand_rows(seq, dl, next_n)
+    shards = [(c.numpy(), b.numpy()) for c, b in synth.shard_decode(inp, world, inter, seed=5)]
+    got, gv = oracle.dcp_decode_topk(qb, w, shards, rl, next_n, k, inter)
+    ref, lg, _, _, _ = oracle.decode_topk(qb, w, inp.cache.numpy(), inp.block_table.numpy(), rl,
+                                          next_n, k, want_logits=True)
+    for r in range(rl.shape[0]):
+        L = int(rl[r])
+        n = min(L, k)
+        assert np.all(got[r, n:] == -1) and np.all(np.isneginf(gv[r, n:]))
+        assert np.array_equal(gv[r, :n], lg[r][got[r, :n]])        # the unsharded logits
+        order = np.lexsort((np.arange(L), -lg[r]))[:n]              # (logit desc, index asc)
+        assert np.array_equal(got[r, :n], order)
+        assert set(got[r, :n]) == set(ref[r][ref[r] >= 0])
+

@@ -78,3 +78,20 @@ def test_heavy_tail_shifts_the_stated_fraction_of_tokens():
 
     gain = mean_projection(tail) - mean_projection(plain)
     assert abs(gain - 0.05 * 4.0) < 0.05
+
+
+def test_shard_decode_places_each_token_once():
+    seq = np.array([130, 5], np.int32)
+    inp = synth.make_decode_from_lens(seq, np.ones(2, np.int32), 1, seed=3)
+    shards = synth.shard_decode(inp, 2, 64, seed=9)
+    c, bt = inp.cache.numpy(), inp.block_table.numpy()
+    def entry(cache, btab, b, t):
+        pg, sl = btab[b, t // 64], t % 64
+        return (bytes(cache[pg, sl * 128:(sl + 1) * 128]),
+                bytes(cache[pg, 8192 + 4 * sl:8192 + 4 * sl + 4]))
+    for b, L in enumerate(seq):
+        for t in range(L):
+            r = (t // 64) % 2
+            j = (t // 128) * 64 + t % 64
+            sc, sbt = shards[r]
+            assert entry(c, bt, b, t) == entry(sc.numpy(), sbt.numpy(), b, j)
