@@ -97,6 +97,10 @@ WORKLOAD_DESCS = {
              "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
     "tiny": ("tiny decode: 4 requests, next_n 1, seq_lens {1000, 2048, 3000, 4096}, "
              "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
+    "dcp_long": ("long context (128 x 131072 keys, 1% heavy-tail) key-sharded over 2 decode-"
+                 "context-parallel ranks in runs of 1 token, the ranks run one after the other "
+                 "on one GPU: per rank top-2048 with logits over its 65536 keys per row, then "
+                 "the merge of the ranks' candidates"),
 }
 
 
@@ -512,6 +516,81 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
             "row_lens_h": row_lens_h}
 
 
+def measure_dcp(workload, dcp_world, interleave, seed, dev, steps, world):
+    """Device-timed key-sharded decode steps: every rank's top k with logits
+    on its own shard of the cache (the ranks one after the other on this GPU),
+    then the merge of their candidates, all through the C ABI, in CUDA graphs.
+    The shards together are the workload's cache (well above L2)."""
+    import torch
+
+    import synth
+    import sparse_attention_indexer_block_gb300 as saib
+
+    d = synth.make_decode(workload, seed=seed, device=dev)
+    R, G, k = d.num_reqs, d.next_n, d.topk
+    assert G == 1
+    shards = synth.shard_decode(d, dcp_world, interleave, seed=seed)
+    seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
+    keys_per_step = int(seq_h.sum())
+    algo_bytes = keys_per_step * PAGE_KEY_BYTES
+    ws = saib.decode_workspace(R, G, k, dev)
+    cv = torch.empty((dcp_world, R, k), dtype=torch.float32, device=dev)
+    ci = torch.empty((dcp_world, R, k), dtype=torch.int32, device=dev)
+    out = torch.empty((R, k), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        for r, (cache, bt) in enumerate(shards):
+            saib.indexer_decode_topk_values(d.q, d.w, cache, bt, d.seq_lens, G, k, dcp_rank=r,
+                                            dcp_world=dcp_world, dcp_interleave=interleave,
+                                            out_idx=ci[r], out_val=cv[r], workspace=ws,
+                                            dev_error=err, stream=stream)
+        saib.indexer_dcp_merge(cv, ci, k, out_idx=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up (dcp)")
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                step()
+    torch.cuda.synchronize()
+    t_soak = time.time()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        with torch.cuda.stream(stream):
+            while time.time() - t_soak < 1.0:
+                g.replay()
+                stream.synchronize()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the timed region (dcp)")
+    peak, peak_kind = measured_peak_gbs()
+    gbs = algo_bytes * steps / (ms / 1e3) / 1e9
+    return {"workload": WORKLOAD_DESCS["dcp_long"],
+            "metric_value": whole_job_rate(keys_per_step, steps, world, ms), "unit": "keys/s",
+            "ms_per_step": ms / steps, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "peak_source": peak_kind,
+                         "kernel": "the whole step (every rank's prep, score/select, split-row "
+                                   "selection and index map, then the merge), CUDA events "
+                                   "around graph replays",
+                         "algorithmic_bytes_per_step": algo_bytes},
+            "clocks": clk.summary(), "gpu_launches": (4 * dcp_world + 1) * steps}
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -589,6 +668,8 @@ def run_ours(args, rank, world, local):
                 "clocks": r["clocks"], "gpu_launches": 3 * steps}
             del r
             torch.cuda.empty_cache()
+        extra["dcp_long"] = measure_dcp("long", 2, 1, seed, dev, 50, world)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

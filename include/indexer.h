@@ -63,11 +63,14 @@
  *    scheduled while the previous work in the stream finishes, but it waits
  *    for that work to complete before it reads or writes any memory, so the
  *    stream's ordering is what the caller sees.
- *  - The top-k score/select kernel is a cooperative launch (one or two CTAs
- *    per SM, all resident at once): the CTAs that share a request's keys wait
- *    for one another's candidates before selecting (each wait gives up after
- *    2 s and sets IDX_DEV_TIMEOUT). It fails with IDX_ERR_CUDA rather than
- *    run partly resident.
+ *  - A top-k call is three launches: the prep kernel (row lengths, q
+ *    quantisation, the work split), the score/select kernel (one CTA per SM)
+ *    and the selection of rows whose keys several CTAs scored (one CTA per
+ *    such row and token, after the score/select kernel has completed). No CTA
+ *    waits on another; a CTA's own pipeline waits give up after 2 s and set
+ *    IDX_DEV_TIMEOUT.
+ *  - [INDEXER] _build_prefill_chunk_metadata_kernel's DCP branch also defines
+ *    the key-sharded (decode context parallel) calls below.
  */
 #ifndef SAIB_INDEXER_H
 #define SAIB_INDEXER_H
@@ -100,6 +103,7 @@ typedef enum {
 #define IDX_PAGE_TOKENS 64
 #define IDX_PAGE_BYTES 8448
 #define IDX_MAX_TOPK 2048
+#define IDX_DCP_MAX_CANDIDATES 16384 /* dcp_world * topk of indexer_dcp_merge */
 
 /* Human-readable name of a status code (static string). */
 const char* indexer_status_string(idx_status status);
@@ -117,7 +121,8 @@ const char* indexer_last_cuda_error(void);
  * tokens), decode_lens int32 [num_reqs] (new tokens, 0 <= d <= next_n for
  * mode 0), block_table as above.
  * mode 0 (padded grid): row b*next_n + j gets len = L_b - d_b + j + 1 for
- *   j < d_b and 0 otherwise; num_out_rows must be >= num_reqs*next_n.
+ *   j < d_b and 0 otherwise; num_out_rows must be >= num_reqs*next_n, and
+ *   rows past num_reqs*next_n are left as they are.
  * mode 1 (flatten): the d_b tokens of request b take consecutive rows starting
  *   at sum_{b' < b} d_b' with the same len; rows from sum d_b up to
  *   num_out_rows get len 0; more tokens than num_out_rows sets
@@ -250,6 +255,72 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                                  int32_t topk, float* out_logits, int64_t ld_logits,
                                  void* workspace, size_t workspace_bytes, uint32_t* dev_error,
                                  void* stream);
+
+/*
+ * Key-sharded (decode context parallel) decode ([INDEXER]
+ * _build_prefill_chunk_metadata_kernel, its DCP_WORLD_SIZE > 1 branch): the
+ * keys of a sequence are dealt to dcp_world ranks in runs of dcp_interleave
+ * tokens (token t to rank (t / I) % W, as that rank's next local key), so rank
+ * r holds, of L keys, base + min(max(rem - r * I, 0), I) with
+ * base = L / I / W * I and rem = L - base * W (integer division; I =
+ * dcp_interleave, W = dcp_world). A rank's cache holds its local keys 0, 1, ...
+ * in its own pages. A decode row then takes the top k over every rank's
+ * candidates: each rank runs indexer_decode_topk_values on its cache, the
+ * ranks' outputs are gathered ([W, rows, topk] each, rank-major: what an
+ * all-gather of them holds) and indexer_dcp_merge picks the k best.
+ */
+
+/*
+ * Local key counts: local_lens[i] = rank dcp_rank's count of row_seq_lens[i]
+ * keys by the rule above (int32 [num_rows] each, device; negative lengths are
+ * copied as they are). 1 <= dcp_world, 0 <= dcp_rank < dcp_world,
+ * dcp_interleave >= 1, else IDX_ERR_INVALID_ARG.
+ */
+idx_status indexer_dcp_local_lens(const int32_t* row_seq_lens, int64_t num_rows, int32_t dcp_rank,
+                                  int32_t dcp_world, int32_t dcp_interleave, int32_t* local_lens,
+                                  void* stream);
+
+/*
+ * Decode top-k with the selected logits, on one rank of a key-sharded cache
+ * (dcp_world = 1: the whole cache, dcp_rank 0). Arguments as
+ * indexer_decode_topk (same workspace size), except:
+ *  - row_seq_lens are the rows' key counts over the whole sequence; each row
+ *    scores the rank's local count of them (the rule above) from index_cache /
+ *    block_table, the rank's own cache;
+ *  - every row with at least one local key is scored and selected: a row of
+ *    n <= topk local keys outputs all n (no causal shortcut: a merge needs
+ *    their logits);
+ *  - out_val float [num_reqs * next_n, topk] gets the logit of each output
+ *    index (the indexer's score, as indexer_decode_logits computes it) and
+ *    -inf where out_idx is -1;
+ *  - out_idx holds global token positions: local key j of rank r is
+ *    (j / I) * I * W + r * I + j % I. Entries are in no particular order.
+ * IDX_ERR_INVALID_ARG for a null out_val or rank / world / interleave outside
+ * the ranges of indexer_dcp_local_lens.
+ */
+idx_status indexer_decode_topk_values(const void* q, const float* weights,
+                                      const uint8_t* index_cache, int64_t num_pages,
+                                      const int32_t* block_table, int64_t bt_stride,
+                                      int32_t bt_width, const int32_t* row_seq_lens,
+                                      int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                      int32_t head_dim, int32_t topk, int32_t dcp_rank,
+                                      int32_t dcp_world, int32_t dcp_interleave, int32_t* out_idx,
+                                      float* out_val, void* workspace, size_t workspace_bytes,
+                                      uint32_t* dev_error, void* stream);
+
+/*
+ * Merge of the ranks' candidates: cand_val float / cand_idx int32
+ * [dcp_world, num_rows, topk] (slab w = rank w's indexer_decode_topk_values
+ * output; idx < 0 = empty). out_idx int32 [num_rows, topk] gets, per row, the
+ * topk candidates with the largest values (any of several equal to the k-th),
+ * in no particular order, -1 past the candidates when there are fewer;
+ * out_val (nullable) float [num_rows, topk] their values (-inf past them).
+ * dcp_world * topk <= IDX_DCP_MAX_CANDIDATES, else IDX_ERR_UNSUPPORTED. One
+ * 1024-thread CTA per row; the candidates are read once.
+ */
+idx_status indexer_dcp_merge(const float* cand_val, const int32_t* cand_idx, int32_t dcp_world,
+                             int64_t num_rows, int32_t topk, int32_t* out_idx, float* out_val,
+                             void* stream);
 
 /*
  * Host-only prefill chunk plan ([INDEXER] split_indexer_prefill_chunks): pack

@@ -8,10 +8,13 @@ first call does, and raises if it has not been built.
 from .binding import (  # noqa: F401
     IndexerError,
     decode_workspace,
+    indexer_dcp_local_lens,
+    indexer_dcp_merge,
     indexer_decode_logits,
     indexer_decode_topk,
     indexer_decode_topk_from_lens,
     indexer_decode_topk_noalloc,
+    indexer_decode_topk_values,
     indexer_decode_workspace_bytes,
     indexer_expand_decode_rows,
     indexer_insert_keys,

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "IDX_OK", 1: "IDX_ERR_INVALID_ARG", 2: "IDX_ERR_UNSUPPORTED",
                 3: "IDX_ERR_WORKSPACE", 4: "IDX_ERR_CUDA", 5: "IDX_ERR_CAPACITY"}
 DEV_BAD_BLOCK, DEV_BAD_LEN, DEV_TIMEOUT, DEV_OVERFLOW = 1, 2, 4, 8
 NUM_HEADS, HEAD_DIM, PAGE_TOKENS, PAGE_BYTES, MAX_TOPK = 64, 128, 64, 8448, 2048
+DCP_MAX_CANDIDATES = 16384
 
 # exported symbols and their ctypes signatures (kept in step with indexer.h)
 _P, _I32, _I64, _SZ = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
@@ -52,6 +53,11 @@ SIGNATURES = {
                                             C.POINTER(_I32), C.POINTER(_I32)]),
     "indexer_decode_topk_noalloc": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
                                               _I32, _I32, _I32, _P, _P, _P]),
+    "indexer_dcp_local_lens": (C.c_int, [_P, _I64, _I32, _I32, _I32, _P, _P]),
+    "indexer_decode_topk_values": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
+                                             _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ,
+                                             _P, _P]),
+    "indexer_dcp_merge": (C.c_int, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -213,6 +219,56 @@ def indexer_decode_topk_from_lens(q, weights, index_cache, block_table, seq_lens
         int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
     _check("indexer_decode_topk_from_lens", st)
     return out_idx
+
+
+def indexer_dcp_local_lens(row_seq_lens, dcp_rank: int, dcp_world: int, dcp_interleave: int,
+                           local_lens=None, stream=None):
+    """Rank dcp_rank's key count of each length (int32 tensors)."""
+    n = int(row_seq_lens.numel())
+    if local_lens is None:
+        local_lens = torch.empty_like(row_seq_lens)
+    st = load().indexer_dcp_local_lens(_ptr(row_seq_lens), n, dcp_rank, dcp_world,
+                                       dcp_interleave, _ptr(local_lens), _stream(stream))
+    _check("indexer_dcp_local_lens", st)
+    return local_lens
+
+
+def indexer_decode_topk_values(q, weights, index_cache, block_table, row_seq_lens, next_n: int,
+                               topk: int = MAX_TOPK, dcp_rank: int = 0, dcp_world: int = 1,
+                               dcp_interleave: int = 1, out_idx=None, out_val=None,
+                               workspace=None, dev_error=None, stream=None):
+    """Top-k with the selected logits on one rank of a key-sharded cache
+    (the whole cache when dcp_world == 1); indices in global positions.
+    Returns (out_idx int32, out_val float32), both [rows, topk]."""
+    R = int(block_table.shape[0])
+    rows = R * next_n
+    if out_idx is None:
+        out_idx = torch.empty((rows, topk), dtype=torch.int32, device=q.device)
+    if out_val is None:
+        out_val = torch.empty((rows, topk), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, next_n, topk, q.device)
+    st = load().indexer_decode_topk_values(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, next_n,
+        int(q.shape[1]), int(q.shape[2]), topk, dcp_rank, dcp_world, dcp_interleave,
+        _ptr(out_idx), _ptr(out_val), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_topk_values", st)
+    return out_idx, out_val
+
+
+def indexer_dcp_merge(cand_val, cand_idx, topk: int = MAX_TOPK, out_idx=None, out_val=None,
+                      stream=None):
+    """The top k of the ranks' candidates cand_val float32 / cand_idx int32
+    [world, rows, topk]. Returns (out_idx, out_val) [rows, topk]."""
+    world, rows = int(cand_idx.shape[0]), int(cand_idx.shape[1])
+    if out_idx is None:
+        out_idx = torch.empty((rows, topk), dtype=torch.int32, device=cand_idx.device)
+    st = load().indexer_dcp_merge(_ptr(cand_val), _ptr(cand_idx), world, rows, topk,
+                                  _ptr(out_idx), _ptr(out_val), _stream(stream))
+    _check("indexer_dcp_merge", st)
+    return out_idx, out_val
 
 
 def indexer_decode_logits(q, weights, index_cache, block_table, row_seq_lens, next_n: int,

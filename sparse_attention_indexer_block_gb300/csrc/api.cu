@@ -54,6 +54,7 @@ idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorM
     r.G = G;
     r.topk = p.topk;
     r.out_idx = p.out_idx;
+    r.out_val = p.out_val;
     r.out_row_base = p.out_row_base;
     r.dev_error = p.dev_error;
     r.wait_ns = g_wait_ns;
@@ -246,14 +247,26 @@ struct RowLens {
   const int32_t* decode_lens;
 };
 
+// Values mode: the selected keys' logits beside their indices, every row of
+// > 0 keys selected; on one rank of a key-sharded cache (world > 1) the rows
+// score the rank's share of their keys and the indices go out global.
+struct ValuesOut {
+  float* out_val;
+  int32_t rank, world, interleave;
+};
+
 idx_status decode_common(bool logits, const void* q, const float* weights,
                          const uint8_t* index_cache, int64_t num_pages, const int32_t* block_table,
                          int64_t bt_stride, int32_t bt_width, const RowLens& lens,
                          int32_t num_reqs, int32_t next_n, int32_t num_heads, int32_t head_dim,
                          int32_t topk, int32_t* out_idx, float* out_logits, int64_t ld_logits,
                          void* workspace, size_t workspace_bytes, uint32_t* dev_error,
-                         void* stream) {
+                         void* stream, const ValuesOut* vo = nullptr) {
   if (num_reqs < 0) return IDX_ERR_INVALID_ARG;
+  const bool values = vo != nullptr;
+  if (values && (!vo->out_val || vo->world < 1 || vo->rank < 0 || vo->rank >= vo->world ||
+                 vo->interleave < 1))
+    return IDX_ERR_INVALID_ARG;
   if (next_n != 1 && next_n != 2) return IDX_ERR_UNSUPPORTED;
   idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
                                num_heads, head_dim, topk);
@@ -278,8 +291,14 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   int32_t row_penalty, row_penalty_div;
   decode_row_penalty(logits, next_n, &row_penalty, &row_penalty_div);
   DecodePrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, lens.row_seq_lens, num_reqs,
-                   next_n, topk, bt_width, logits ? 1 : 0, out_idx, dev_error, nC, row_penalty,
-                   row_penalty_div, lens.seq_lens, lens.decode_lens};
+                   next_n, topk, bt_width, (logits || values) ? 1 : 0, out_idx, dev_error, nC,
+                   row_penalty, row_penalty_div, lens.seq_lens, lens.decode_lens};
+  if (values) {
+    a.out_val = vo->out_val;
+    a.dcp_rank = vo->rank;
+    a.dcp_world = vo->world;
+    a.dcp_interleave = vo->interleave;
+  }
   if ((st = launch_decode_prep(a, ws, L, s)) != IDX_OK) return st;
   ScoreParams p{};
   p.cache = index_cache;
@@ -305,13 +324,18 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   p.out_idx = out_idx;
   p.out_row_base = 0;
   p.topk = topk;
+  p.short_len = values ? 0 : topk;
+  p.out_val = values ? vo->out_val : nullptr;
   p.out_logits = out_logits;
   p.ld_logits = ld_logits;
   p.dev_error = dev_error;
   size_t tb = 0;
   p.trace = trace_buffer(&tb);
   if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-  return timed_score(next_n, logits, p, map, s);
+  st = timed_score(next_n, logits, p, map, s);
+  if (st == IDX_OK && values && vo->world > 1)
+    st = launch_dcp_globalise(out_idx, rows * topk, vo->rank, vo->world, vo->interleave, s);
+  return st;
 }
 
 }  // namespace
@@ -467,6 +491,47 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                        dev_error, stream);
 }
 
+idx_status indexer_decode_topk_values(const void* q, const float* weights,
+                                      const uint8_t* index_cache, int64_t num_pages,
+                                      const int32_t* block_table, int64_t bt_stride,
+                                      int32_t bt_width, const int32_t* row_seq_lens,
+                                      int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                      int32_t head_dim, int32_t topk, int32_t dcp_rank,
+                                      int32_t dcp_world, int32_t dcp_interleave, int32_t* out_idx,
+                                      float* out_val, void* workspace, size_t workspace_bytes,
+                                      uint32_t* dev_error, void* stream) {
+  if (!out_val) return IDX_ERR_INVALID_ARG;
+  const ValuesOut vo{out_val, dcp_rank, dcp_world, dcp_interleave};
+  return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
+                       head_dim, topk, out_idx, nullptr, 0, workspace, workspace_bytes, dev_error,
+                       stream, &vo);
+}
+
+idx_status indexer_dcp_local_lens(const int32_t* row_seq_lens, int64_t num_rows, int32_t dcp_rank,
+                                  int32_t dcp_world, int32_t dcp_interleave, int32_t* local_lens,
+                                  void* stream) {
+  if (num_rows < 0 || dcp_world < 1 || dcp_rank < 0 || dcp_rank >= dcp_world ||
+      dcp_interleave < 1)
+    return IDX_ERR_INVALID_ARG;
+  if (num_rows == 0) return IDX_OK;
+  if (!row_seq_lens || !local_lens) return IDX_ERR_INVALID_ARG;
+  return launch_dcp_local_lens(row_seq_lens, num_rows, dcp_rank, dcp_world, dcp_interleave,
+                               local_lens, static_cast<cudaStream_t>(stream));
+}
+
+idx_status indexer_dcp_merge(const float* cand_val, const int32_t* cand_idx, int32_t dcp_world,
+                             int64_t num_rows, int32_t topk, int32_t* out_idx, float* out_val,
+                             void* stream) {
+  if (num_rows < 0 || dcp_world < 1) return IDX_ERR_INVALID_ARG;
+  if (topk < 1 || topk > IDX_MAX_TOPK) return IDX_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(dcp_world) * topk > IDX_DCP_MAX_CANDIDATES) return IDX_ERR_UNSUPPORTED;
+  if (num_rows == 0) return IDX_OK;
+  if (!cand_val || !cand_idx || !out_idx) return IDX_ERR_INVALID_ARG;
+  return launch_dcp_merge(cand_val, cand_idx, dcp_world, num_rows, topk, out_idx, out_val,
+                          static_cast<cudaStream_t>(stream));
+}
+
 idx_status indexer_plan_prefill_chunks(const int32_t* seq_lens_host,
                                        const int32_t* query_lens_host, int32_t num_reqs,
                                        int64_t workspace_tokens, int64_t logits_budget_bytes,
@@ -590,6 +655,7 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.out_idx = out_idx;
     p.out_row_base = lo;
     p.topk = topk;
+    p.short_len = topk;
     p.dev_error = dev_error;
     size_t tb = 0;
     p.trace = trace_buffer(&tb);

@@ -49,6 +49,22 @@ __host__ __device__ __forceinline__ int64_t segment_slot(int v, bool first_row) 
   return 2 * static_cast<int64_t>(v) + (first_row ? 0 : 1);
 }
 
+// Keys a rank of a key-sharded (decode context parallel) cache holds of a
+// sequence of L keys, when the sequence is dealt to `world` ranks in runs of
+// `interleave` tokens (token t on rank (t / interleave) % world): base +
+// min(max(rem - rank * interleave, 0), interleave), base = L / interleave /
+// world * interleave, rem = L - base * world (INDEXER page,
+// _build_prefill_chunk_metadata_kernel, DCP branch). Negative L is returned
+// as it is (the caller's validation reports it).
+__host__ __device__ __forceinline__ int64_t dcp_local_len(int64_t L, int rank, int world,
+                                                          int interleave) {
+  if (world <= 1 || L < 0) return L;
+  const int64_t base = L / interleave / world * interleave;
+  const int64_t rem = L - base * world;
+  const int64_t r = rem - static_cast<int64_t>(rank) * interleave;
+  return base + (r < 0 ? 0 : (r > interleave ? interleave : r));
+}
+
 
 // Everything the score/select kernel reads, for one launch.
 struct ScoreParams {
@@ -76,6 +92,10 @@ struct ScoreParams {
   int32_t* out_idx;              // [*, topk] (row = out_row_base + token row)
   int64_t out_row_base;
   int32_t topk;
+  // Top-k mode selects rows of more than short_len keys: topk (shorter rows
+  // are written by the prep kernel), or 0 when out_val is set.
+  int32_t short_len;
+  float* out_val;                // nullable: [*, topk] logit of each output index, -inf if none
   float* out_logits;             // logits mode only
   int64_t ld_logits;
   uint32_t* dev_error;
@@ -159,6 +179,10 @@ struct DecodePrepArgs {
   int32_t row_penalty_div;
   const int32_t* seq_lens = nullptr;     // [num_reqs] (when row_seq_lens is nullptr)
   const int32_t* decode_lens = nullptr;  // [num_reqs]
+  // Values mode (score_all set, top-k output): rows of 0 keys get -1 / -inf.
+  float* out_val = nullptr;
+  // Key-sharded cache: every row scores dcp_local_len(its length) keys.
+  int32_t dcp_rank = 0, dcp_world = 1, dcp_interleave = 1;
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -207,6 +231,8 @@ struct RowSelectParams {
   int32_t G;
   int32_t topk;
   int32_t* out_idx;
+  float* out_val;                // nullable: the selected keys' logits; rows of <= k keys are
+                                 // then selected here too (all their keys)
   int64_t out_row_base;
   uint32_t* dev_error;
   uint64_t wait_ns;
@@ -221,6 +247,15 @@ enum SelTraceSlot {
 // One CTA per (possible split row, token row):
 // max_split_rows(num_wr, streams) * G CTAs.
 idx_status launch_row_select(const RowSelectParams& p, int grid, cudaStream_t s);
+
+// Key-sharded decode: rank-local key counts, local-to-global output indices,
+// and the merge of the ranks' (logit, index) candidates.
+idx_status launch_dcp_local_lens(const int32_t* lens, int64_t n, int rank, int world,
+                                 int interleave, int32_t* out, cudaStream_t s);
+idx_status launch_dcp_globalise(int32_t* idx, int64_t n, int rank, int world, int interleave,
+                                cudaStream_t s);
+idx_status launch_dcp_merge(const float* val, const int32_t* idx, int world, int64_t rows,
+                            int topk, int32_t* out_idx, float* out_val, cudaStream_t s);
 
 // The score/select kernel runs one CTA per SM, each CTA
 // score_streams_per_cta(G) tile streams: the work split is planned over

@@ -263,12 +263,18 @@ __device__ __forceinline__ void zero_words(uint32_t* p, size_t n) {
 
 // Key count of token row r = b * next_n + j before validation: the given
 // per-row length, or the row expansion's (token j of a request of d tokens
-// and L keys sees L - d + j + 1 keys; rows j >= d are padding, 0).
+// and L keys sees L - d + j + 1 keys; rows j >= d are padding, 0); on a
+// key-sharded cache, this rank's share of it.
 __device__ __forceinline__ int64_t raw_row_len(const DecodePrepArgs& a, int64_t r) {
-  if (a.row_seq_lens) return a.row_seq_lens[r];
-  const int64_t b = r / a.next_n, j = r % a.next_n;
-  const int64_t L = a.seq_lens[b], d = a.decode_lens[b];
-  return j < d ? L - d + j + 1 : 0;
+  int64_t len;
+  if (a.row_seq_lens) {
+    len = a.row_seq_lens[r];
+  } else {
+    const int64_t b = r / a.next_n, j = r % a.next_n;
+    const int64_t L = a.seq_lens[b], d = a.decode_lens[b];
+    len = j < d ? L - d + j + 1 : 0;
+  }
+  return dcp_local_len(len, a.dcp_rank, a.dcp_world, a.dcp_interleave);
 }
 
 // Block 0: work-row schedule (tile counts and their exclusive prefix), validated
@@ -333,12 +339,17 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(
   const int64_t gw = (static_cast<int64_t>(blockIdx.x - 1) * kPrepThreads + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x - 1) * kPrepThreads) >> 5;
   quantize_tasks<true>(a.q, a.w, 0, rows * kHeads, q8img, wprime, gw, nw);
-  if (!a.score_all) {
+  if (!a.score_all || a.out_val) {
+    // top k: rows of <= k keys are the causal row; values: rows of no keys
+    // are empty (the others are all scored)
+    const int64_t short_len = a.score_all ? 0 : a.topk;
     for (int64_t r = gw; r < rows; r += nw) {
       const int64_t len = clamp_len(raw_row_len(a, r), a.bt_width, a.err, false);
-      if (len > a.topk) continue;
+      if (len > short_len) continue;
       int32_t* o = a.out_idx + r * a.topk;
       for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;
+      if (a.out_val)
+        for (int i = lane; i < a.topk; i += 32) a.out_val[r * a.topk + i] = -INFINITY;
     }
   }
 }

@@ -23,6 +23,8 @@
 // rank over bits 9..0 with tie tickets for keys equal in all 32 bits. Which of
 // several equal keys at the k-th value are taken is arbitrary (the method
 // leaves it open). The output row holds its k indices in no particular order.
+// With values asked for, each index's logit goes out beside it, and rows of
+// <= k keys (not causal-filled then) take all their keys, padded with -1.
 #include <atomic>
 
 #include "internal.h"
@@ -154,7 +156,7 @@ __device__ __forceinline__ int top_bin() {
 // The bin holding the need-th largest key of a kSelThreads * PER-bin
 // histogram whose counts thread t holds as c[j] = bin top_bin<PER>() - j, the
 // count in higher bins and the bin's own count, in sh->cut for every thread
-// (bin -1 when fewer than `need` keys are counted).
+// (bin -1 and the total count when fewer than `need` keys are counted).
 template <int PER>
 __device__ void find_cut(const int (&c)[PER], int need, SelShared* sh) {
   int local = 0;
@@ -165,6 +167,7 @@ __device__ void find_cut(const int (&c)[PER], int need, SelShared* sh) {
   int ex[3], tot[3];
   block_scan3(v, ex, tot, sh->scan);  // its barriers order the write above
   claim_cut<PER>(c, top_bin<PER>(), ex[0], need, sh);
+  if (threadIdx.x == 0 && tot[0] < need) sh->cut = Cut{-1, tot[0], 0};  // no claim then
   __syncthreads();
 }
 
@@ -267,9 +270,11 @@ __device__ __forceinline__ void for_each_bin_batch(const BinRanges& r, F&& f) {
 // Selects `need` keys of the bin b0 from the source `visit` hands out (the
 // list, or the slots' b0 ranges) into out[0, need): bits 21..10 (4096 bins;
 // s.hist is zero on entry), then either an exact rank of the last bin's keys
-// or bits 9..0 and tie tickets. Returns false when the counts disagree.
-template <class Visit>
-__device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t* out) {
+// or bits 9..0 and tie tickets; with kVals each key's logit goes to ov at
+// its index's position. Returns false when the counts disagree.
+template <bool kVals, class Visit>
+__device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t* out,
+                              float* ov) {
   constexpr int P1 = 4096 / kSelThreads, P2 = 1024 / kSelThreads;
   SelShared* sh = s.sh;
   const int t = threadIdx.x;
@@ -306,7 +311,10 @@ __device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t
       eq |= (rank && in && d1 == b1) ? 1u << j : 0u;
     }
     emit8(&sh->nout, gt, [&](int j, int pos) {
-      if (pos < cut1.above) out[pos] = b.x[j];
+      if (pos < cut1.above) {
+        out[pos] = b.x[j];
+        if (kVals) ov[pos] = key_float(b.k[j]);
+      }
     });
     emit8(&sh->nlist, eq, [&](int j, int pos) {
       if (pos < kTieCap) {
@@ -318,6 +326,7 @@ __device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t
   __syncthreads();
   if (sh->nout != cut1.above || (rank && sh->nlist != cut1.count)) return false;
   int32_t* out1 = out + cut1.above;
+  float* ov1 = kVals ? ov + cut1.above : nullptr;
   if (rank) {
     // rank by key, then list position: the first need1 are in
     const int m = cut1.count;
@@ -328,7 +337,10 @@ __device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t
         const uint32_t kj = s.tkey[j];
         r += (kj > ki || (kj == ki && j < i)) ? 1 : 0;
       }
-      if (r < need1) out1[r] = s.tidx[i];
+      if (r < need1) {
+        out1[r] = s.tidx[i];
+        if (kVals) ov1[r] = key_float(ki);
+      }
     }
     return true;
   }
@@ -364,16 +376,23 @@ __device__ bool select_in_bin(const SelSmem& s, Visit&& visit, int need, int32_t
       eq |= (in && (b.k[j] & 1023u) == b2) ? 1u << j : 0u;
     }
     emit8(&sh->nout, gt, [&](int j, int pos) {
-      if (pos < cut2.above) out1[pos] = b.x[j];
+      if (pos < cut2.above) {
+        out1[pos] = b.x[j];
+        if (kVals) ov1[pos] = key_float(b.k[j]);
+      }
     });
     emit8(&sh->nticket, eq, [&](int j, int pos) {
-      if (pos < need2) out1[cut2.above + pos] = b.x[j];
+      if (pos < need2) {
+        out1[cut2.above + pos] = b.x[j];
+        if (kVals) ov1[cut2.above + pos] = key_float(b.k[j]);
+      }
     });
   });
   __syncthreads();
   return sh->nout == cut2.above && sh->nticket >= need2;
 }
 
+template <bool kVals>
 __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSelectParams p) {
   constexpr int P0 = kRowHistBins / kSelThreads;
   extern __shared__ uint8_t smem_raw[];
@@ -412,13 +431,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
   const WorkRow wr = p.wr[w];
   if (g >= wr.ntok) return;
   const int K = p.topk;
-  if (p.row_len[wr.row0 + g] <= K) return;  // written by the prep kernel
+  // a row of <= k keys: causal-filled by the prep kernel, or (values) all
+  // its keys taken here
+  const bool take_all = p.row_len[wr.row0 + g] <= K;
+  if (!kVals && take_all) return;
   const int nseg = rc.y - rc.x + 1;
   if (nseg > kMaxSegs) {
     if (t == 0) set_error(p.dev_error, IDX_DEV_INTERNAL);
     return;
   }
   int32_t* out = p.out_idx + (p.out_row_base + wr.row0 + g) * static_cast<int64_t>(K);
+  float* ov = kVals ? p.out_val + (p.out_row_base + wr.row0 + g) * static_cast<int64_t>(K)
+                    : nullptr;
   // the first segment is the first stream's first row's only when the row
   // starts at that stream's first tile; later segments always are
   const bool first_is_first_row = p.cta_row[rc.x] == w;
@@ -454,11 +478,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
   if (tr) tr[kSelTrPrefix] = globaltimer_ns();
   if (sh->bad) return;
   const Cut cut0 = sh->cut;
-  if (cut0.bin < 0) {
+  if (cut0.bin < 0 && !(kVals && take_all)) {
     if (t == 0) set_error(p.dev_error, IDX_DEV_INTERNAL);
     return;
   }
-  const int b0 = cut0.bin;
+  const int b0 = cut0.bin;  // -1: fewer than k keys (values mode), all of them go out
   // each segment's entries above b0 and in b0 (prefixes of its sorted slot),
   // and their prefixes over the segments
   int ngt = 0, neq = 0;
@@ -468,7 +492,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
     if (i < nseg) {
       const int64_t slot = segment_slot(rc.x + i, i > 0 || first_is_first_row);
       const uint32_t* cum = p.seg_cum + (slot * p.G + g) * kRowHistBins;
-      const int at = min(static_cast<int>(__ldcg(&cum[b0])), p.slot_cap);
+      const int at = min(static_cast<int>(__ldcg(&cum[kVals ? max(b0, 0) : b0])), p.slot_cap);
       gt = b0 + 1 < kRowHistBins ? min(static_cast<int>(__ldcg(&cum[b0 + 1])), at) : 0;
       eq = at - gt;
       sh->seg_base[i] = (slot * p.G + g) * p.slot_cap;
@@ -524,13 +548,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       x[u] = dst[u] >= 0 ? __ldcg(p.slot_idx + src[u]) : 0;
-      k[u] = dst[u] >= ngt ? __ldcg(p.slot_key + src[u]) : 0u;
+      k[u] = (kVals ? dst[u] >= 0 : dst[u] >= ngt) ? __ldcg(p.slot_key + src[u]) : 0u;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (dst[u] < 0) continue;
       if (dst[u] < ngt) {
         out[dst[u]] = x[u];
+        if (kVals) ov[dst[u]] = key_float(k[u]);
       } else {
         s.lkey[dst[u] - ngt] = k[u];
         s.lidx[dst[u] - ngt] = x[u];
@@ -540,13 +565,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
   __syncthreads();
   if (tr) tr[kSelTrEmit0] = globaltimer_ns();
   const int need0 = K - ngt;
+  if (kVals && b0 < 0) {  // every key is out: pad
+    for (int e = ngt + t; e < K; e += kSelThreads) {
+      out[e] = -1;
+      ov[e] = -INFINITY;
+    }
+    return;
+  }
   bool ok;
   if (list) {
-    ok = select_in_bin(
-        s, [&](auto&& f) { for_each_list_batch(s.lkey, s.lidx, neq, f); }, need0, out + ngt);
+    ok = select_in_bin<kVals>(
+        s, [&](auto&& f) { for_each_list_batch(s.lkey, s.lidx, neq, f); }, need0, out + ngt,
+        kVals ? ov + ngt : nullptr);
   } else {
     const BinRanges r{p.slot_key, p.slot_idx, sh, nseg, neq};
-    ok = select_in_bin(s, [&](auto&& f) { for_each_bin_batch(r, f); }, need0, out + ngt);
+    ok = select_in_bin<kVals>(s, [&](auto&& f) { for_each_bin_batch(r, f); }, need0, out + ngt,
+                              kVals ? ov + ngt : nullptr);
   }
   if (!ok && t == 0) set_error(p.dev_error, IDX_DEV_INTERNAL);
   if (tr) {
@@ -560,18 +594,20 @@ __global__ void __launch_bounds__(kSelThreads, 1) row_select_kernel(const RowSel
 
 idx_status launch_row_select(const RowSelectParams& p, int grid, cudaStream_t s) {
   if (grid <= 0) return IDX_OK;
-  static std::atomic<bool> configured[kMaxDevices];
+  static std::atomic<bool> configured[2][kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidDevice);
   const size_t smem = kSelSmemBytes + 16;
-  if (dev >= kMaxDevices || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(row_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int vals = p.out_val ? 1 : 0;
+  auto kernel = vals ? row_select_kernel<true> : row_select_kernel<false>;
+  if (dev >= kMaxDevices || !configured[vals][dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_status(e);
-    if (dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
+    if (dev < kMaxDevices) configured[vals][dev].store(true, std::memory_order_release);
   }
-  return cuda_status(launch_pdl(row_select_kernel, grid, kSelThreads, smem, s, p));
+  return cuda_status(launch_pdl(kernel, grid, kSelThreads, smem, s, p));
 }
 
 }  // namespace saib

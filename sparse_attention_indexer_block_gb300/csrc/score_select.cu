@@ -626,7 +626,8 @@ __device__ __forceinline__ int region_entries(const Smem& s, int g) {
   return lane < nw ? (nw - lane + 31) / 32 : 0;
 }
 
-// Output of a row held entirely by this CTA (its buffer holds <= k entries).
+// Output of a row held entirely by this CTA (its buffer holds <= k entries),
+// with each index's logit when values are asked for.
 template <int G>
 __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& wr,
                            const bool (&active)[Cfg<G>::kTokens]) {
@@ -639,11 +640,20 @@ __device__ void write_rows(const ScoreParams& p, const Smem& s, const WorkRow& w
     const int mine = region_entries<G>(s, g);
     int total;
     int pos = epi_exclusive_scan(s.misc, mine, &total);
-    int32_t* o = p.out_idx + (p.out_row_base + wr.row0 + token_of<G>(s) + g) * p.topk;
+    const int64_t row = p.out_row_base + wr.row0 + token_of<G>(s) + g;
+    int32_t* o = p.out_idx + row * p.topk;
+    float* ov = p.out_val ? p.out_val + row * p.topk : nullptr;
     const int32_t* rx = s.cidx + g * C::kCap + ew * C::kRegion;
+    const uint32_t* rk = s.ckey + g * C::kCap + ew * C::kRegion;
     for (int j = 0; j < mine; ++j)
-      if (pos < p.topk) o[pos++] = rx[lane + 32 * j];
-    for (int e = total + et; e < p.topk; e += kEpiThreads) o[e] = -1;
+      if (pos < p.topk) {
+        if (ov) ov[pos] = key_float(rk[lane + 32 * j]);
+        o[pos++] = rx[lane + 32 * j];
+      }
+    for (int e = total + et; e < p.topk; e += kEpiThreads) {
+      o[e] = -1;
+      if (ov) ov[e] = -INFINITY;
+    }
     epi_sync();
   }
 }
@@ -793,7 +803,7 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
 #pragma unroll
     for (int g = 0; g < GT; ++g) {
       len[g] = g0 + g < wr.ntok ? p.row_len[wr.row0 + g0 + g] : 0;
-      active[g] = g0 + g < wr.ntok && (kLogits ? len[g] > 0 : len[g] > p.topk);
+      active[g] = g0 + g < wr.ntok && (kLogits ? len[g] > 0 : len[g] > p.short_len);
     }
     for (int i = et; i < GT * kHeads; i += kEpiThreads) {
       const int g = g0 + i / kHeads;

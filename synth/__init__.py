@@ -219,28 +219,29 @@ def shard_decode(inp: DecodeInputs, world: int, interleave: int, seed: int = MAS
     (the same fp8 codes and scale bytes), on pages of its own seeded random
     permutation. Data placement only: the bytes of each token are copied."""
     dev = inp.cache.device
-    cache = inp.cache.cpu().numpy()
-    bt = inp.block_table.cpu().numpy()
     lens = inp.seq_lens.cpu().numpy().astype(np.int64)
+    bt = inp.block_table.long()
+    P0 = inp.cache.shape[0]
+    src_v = inp.cache.view(P0, PAGE_BYTES)[:, :SCALE_OFFSET].view(P0, PAGE_TOKENS, HEAD_DIM)
+    src_s = inp.cache.view(P0, PAGE_BYTES)[:, SCALE_OFFSET:].view(P0, PAGE_TOKENS, 4)
     shards = []
     for r in range(world):
         toks = [np.nonzero((np.arange(L) // interleave) % world == r)[0] for L in lens]
-        local_lens = np.array([len(t) for t in toks], np.int32)
-        lbt, P, _, _ = page_table(local_lens, seed + 101 * (r + 1))
-        out = np.zeros((P, PAGE_BYTES), np.uint8)
-        for b, t in enumerate(toks):
-            if len(t) == 0:
-                continue
-            j = np.arange(len(t))
-            src_pg, src_sl = bt[b, t // PAGE_TOKENS], t % PAGE_TOKENS
-            dst_pg, dst_sl = lbt[b, j // PAGE_TOKENS], j % PAGE_TOKENS
-            vals = cache[:, :SCALE_OFFSET].reshape(-1, PAGE_TOKENS, HEAD_DIM)
-            scl = cache[:, SCALE_OFFSET:].reshape(-1, PAGE_TOKENS, 4)
-            ov = out[:, :SCALE_OFFSET].reshape(-1, PAGE_TOKENS, HEAD_DIM)
-            os_ = out[:, SCALE_OFFSET:].reshape(-1, PAGE_TOKENS, 4)
-            ov[dst_pg, dst_sl] = vals[src_pg, src_sl]
-            os_[dst_pg, dst_sl] = scl[src_pg, src_sl]
-        shards.append((torch.from_numpy(out).to(dev), torch.from_numpy(lbt).to(dev)))
+        local_lens = np.array([len(t) for t in toks], np.int64)
+        lbt, P, _, _ = page_table(local_lens.astype(np.int32), seed + 101 * (r + 1))
+        out = torch.zeros((P, PAGE_BYTES), dtype=torch.uint8, device=dev)
+        dst_v = out[:, :SCALE_OFFSET].view(P, PAGE_TOKENS, HEAD_DIM)
+        dst_s = out[:, SCALE_OFFSET:].view(P, PAGE_TOKENS, 4)
+        lbt_t = torch.from_numpy(lbt).to(dev).long()
+        if local_lens.sum() > 0:
+            b = torch.from_numpy(np.repeat(np.arange(len(lens)), local_lens)).to(dev)
+            t = torch.from_numpy(np.concatenate(toks)).to(dev)
+            j = torch.from_numpy(np.concatenate([np.arange(n) for n in local_lens])).to(dev)
+            sp, ss = bt[b, t // PAGE_TOKENS], t % PAGE_TOKENS
+            dp, ds = lbt_t[b, j // PAGE_TOKENS], j % PAGE_TOKENS
+            dst_v[dp, ds] = src_v[sp, ss]
+            dst_s[dp, ds] = src_s[sp, ss]
+        shards.append((out, lbt_t.int()))
     return shards
 
 

@@ -170,3 +170,41 @@ def test_prefill_validation(lib):
     st = lib.indexer_prefill_workspace_bytes(sl.ctypes.data, ql.ctypes.data, 2, 2048, 1000,
                                              1 << 20, C.byref(out))
     assert st == 1
+
+
+def _values(lib, **over):
+    a = dict(q=FAKE, w=FAKE, cache=FAKE, pages=10, bt=FAKE, bt_stride=4, bt_width=4, lens=FAKE,
+             R=2, next_n=1, H=64, D=128, k=2048, rank=0, world=2, inter=64, out=FAKE, val=FAKE,
+             ws=FAKE, ws_bytes=16, err=None)
+    a.update(over)
+    return lib.indexer_decode_topk_values(
+        a["q"], a["w"], a["cache"], a["pages"], a["bt"], a["bt_stride"], a["bt_width"], a["lens"],
+        a["R"], a["next_n"], a["H"], a["D"], a["k"], a["rank"], a["world"], a["inter"], a["out"],
+        a["val"], a["ws"], a["ws_bytes"], a["err"], None)
+
+
+def test_key_sharded_argument_validation(lib):
+    # the checks come before any device work (ws_bytes = 16 ends a valid call
+    # at the workspace check)
+    assert _values(lib) == 3
+    assert _values(lib, val=None) == 1
+    assert _values(lib, world=0) == 1
+    assert _values(lib, rank=2) == 1
+    assert _values(lib, rank=-1) == 1
+    assert _values(lib, inter=0) == 1
+    assert _values(lib, H=32) == 2
+    assert _values(lib, R=0) == 0
+    f = lib.indexer_dcp_local_lens
+    assert f(FAKE, 4, 0, 0, 1, FAKE, None) == 1      # world < 1
+    assert f(FAKE, 4, 2, 2, 1, FAKE, None) == 1      # rank >= world
+    assert f(FAKE, 4, 0, 2, 0, FAKE, None) == 1      # interleave < 1
+    assert f(None, 4, 0, 2, 1, FAKE, None) == 1
+    assert f(FAKE, -1, 0, 2, 1, FAKE, None) == 1
+    assert f(FAKE, 0, 0, 2, 1, FAKE, None) == 0      # nothing to do
+    m = lib.indexer_dcp_merge
+    assert m(FAKE, FAKE, 9, 4, 2048, FAKE, None, None) == 2   # 9 * 2048 > 16384 candidates
+    assert m(FAKE, FAKE, 2, 4, 0, FAKE, None, None) == 2
+    assert m(FAKE, FAKE, 2, 4, 2049, FAKE, None, None) == 2
+    assert m(FAKE, FAKE, 0, 4, 64, FAKE, None, None) == 1
+    assert m(None, FAKE, 2, 4, 64, FAKE, None, None) == 1
+    assert m(FAKE, FAKE, 2, 0, 64, FAKE, None, None) == 0

@@ -112,13 +112,20 @@ def test_expand_rows_bit_exact():
         btr = rng.integers(0, 1000, (R, W)).astype(np.int32)
         for mode in (0, 1):
             out_rows = R * nn + 3
+            # mode 0 writes the R * nn grid rows only: the rows past it keep
+            # their sentinel; mode 1 writes every row (zero tail)
+            sentinel = torch.full((out_rows,), -7, dtype=torch.int32, device=DEV)
             l, b = saib.indexer_expand_decode_rows(
                 torch.from_numpy(sl).to(DEV), torch.from_numpy(dlr).to(DEV), nn, mode=mode,
-                block_table=torch.from_numpy(btr).to(DEV), num_out_rows=out_rows,
-                want_block_table=True, dev_error=err)
+                block_table=torch.from_numpy(btr).to(DEV), row_seq_lens=sentinel,
+                num_out_rows=out_rows, want_block_table=True, dev_error=err)
             rl, rb, n = oracle.expand_rows(sl, dlr, nn, mode, btr, out_rows)
             torch.cuda.synchronize()
-            assert np.array_equal(l.cpu().numpy(), rl)
+            if mode == 0:
+                assert np.array_equal(l.cpu().numpy()[:R * nn], rl[:R * nn])
+                assert np.all(l.cpu().numpy()[R * nn:] == -7)
+            else:
+                assert np.array_equal(l.cpu().numpy(), rl)
             bb = b.cpu().numpy()
             assert np.array_equal(bb[:n], rb[:n])
             if mode == 0:
