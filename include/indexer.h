@@ -69,8 +69,8 @@
  *    such row and token, after the score/select kernel has completed). No CTA
  *    waits on another; a CTA's own pipeline waits give up after 2 s and set
  *    IDX_DEV_TIMEOUT.
- *  - [INDEXER] _build_prefill_chunk_metadata_kernel's DCP branch also defines
- *    the key-sharded (decode context parallel) calls below.
+ *  - [INDEXER] _build_prefill_chunk_metadata_kernel (COMPRESS_RATIO, its DCP branch) also defines
+ *    the compressed and key-sharded (decode context parallel) calls below.
  */
 #ifndef SAIB_INDEXER_H
 #define SAIB_INDEXER_H
@@ -257,56 +257,81 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                                  void* stream);
 
 /*
- * Key-sharded (decode context parallel) decode ([INDEXER]
- * _build_prefill_chunk_metadata_kernel, its DCP_WORLD_SIZE > 1 branch): the
- * keys of a sequence are dealt to dcp_world ranks in runs of dcp_interleave
- * tokens (token t to rank (t / I) % W, as that rank's next local key), so rank
- * r holds, of L keys, base + min(max(rem - r * I, 0), I) with
- * base = L / I / W * I and rem = L - base * W (integer division; I =
- * dcp_interleave, W = dcp_world). A rank's cache holds its local keys 0, 1, ...
- * in its own pages. A decode row then takes the top k over every rank's
- * candidates: each rank runs indexer_decode_topk_values on its cache, the
- * ranks' outputs are gathered ([W, rows, topk] each, rank-major: what an
+ * Compressed and key-sharded caches ([INDEXER] _build_prefill_chunk_metadata_kernel
+ * with COMPRESS_RATIO and its DCP_WORLD_SIZE > 1 branch; the DeepseekV4
+ * decode metadata divides the per-token seq_lens by compress_ratio):
+ *  - a compressed cache holds one entry per compress_ratio tokens C, so a
+ *    row of L tokens sees L / C entries (integer division);
+ *  - a key-sharded (decode context parallel) cache deals the entries of a
+ *    sequence to dcp_world ranks in runs of dcp_interleave (entry e to rank
+ *    (e / I) % W, as that rank's next local entry), so rank r holds, of n
+ *    entries, base + min(max(rem - r * I, 0), I) with base = n / I / W * I
+ *    and rem = n - base * W (I = dcp_interleave, W = dcp_world).
+ * A rank's cache holds its local entries 0, 1, ... in its own pages. A row
+ * then takes the top k over every rank's candidates: each rank runs
+ * indexer_decode_topk_values (or indexer_prefill_topk_values) on its cache,
+ * the ranks' outputs are gathered ([W, rows, topk] each, rank-major: what an
  * all-gather of them holds) and indexer_dcp_merge picks the k best.
  */
 
 /*
- * Local key counts: local_lens[i] = rank dcp_rank's count of row_seq_lens[i]
- * keys by the rule above (int32 [num_rows] each, device; negative lengths are
- * copied as they are). 1 <= dcp_world, 0 <= dcp_rank < dcp_world,
- * dcp_interleave >= 1, else IDX_ERR_INVALID_ARG.
+ * Entry counts: key_counts[i] = rank dcp_rank's count of the entries a row of
+ * row_seq_lens[i] tokens sees by the rules above (int32 [num_rows] each,
+ * device; negative lengths are copied as they are). Rows of a plain
+ * indexer_decode_topk over a compressed cache take these counts as their
+ * row_seq_lens. compress_ratio >= 1, 1 <= dcp_world, 0 <= dcp_rank <
+ * dcp_world, dcp_interleave >= 1, else IDX_ERR_INVALID_ARG.
  */
-idx_status indexer_dcp_local_lens(const int32_t* row_seq_lens, int64_t num_rows, int32_t dcp_rank,
-                                  int32_t dcp_world, int32_t dcp_interleave, int32_t* local_lens,
-                                  void* stream);
+idx_status indexer_index_key_counts(const int32_t* row_seq_lens, int64_t num_rows,
+                                   int32_t compress_ratio, int32_t dcp_rank, int32_t dcp_world,
+                                   int32_t dcp_interleave, int32_t* key_counts, void* stream);
 
 /*
- * Decode top-k with the selected logits, on one rank of a key-sharded cache
- * (dcp_world = 1: the whole cache, dcp_rank 0). Arguments as
- * indexer_decode_topk (same workspace size), except:
- *  - row_seq_lens are the rows' key counts over the whole sequence; each row
- *    scores the rank's local count of them (the rule above) from index_cache /
- *    block_table, the rank's own cache;
+ * Decode top-k with the selected logits, on one rank of a compressed and / or
+ * key-sharded cache (compress_ratio = dcp_world = 1, dcp_rank 0: the plain
+ * cache). Arguments as indexer_decode_topk (same workspace size), except:
+ *  - row_seq_lens are the rows' token counts over the whole sequence; each row
+ *    scores the rank's count of its entries (the rules above) from
+ *    index_cache / block_table, the rank's own cache;
  *  - every row with at least one local key is scored and selected: a row of
  *    n <= topk local keys outputs all n (no causal shortcut: a merge needs
  *    their logits);
  *  - out_val float [num_reqs * next_n, topk] gets the logit of each output
  *    index (the indexer's score, as indexer_decode_logits computes it) and
  *    -inf where out_idx is -1;
- *  - out_idx holds global token positions: local key j of rank r is
+ *  - out_idx holds global entry positions: local entry j of rank r is
  *    (j / I) * I * W + r * I + j % I. Entries are in no particular order.
- * IDX_ERR_INVALID_ARG for a null out_val or rank / world / interleave outside
- * the ranges of indexer_dcp_local_lens.
+ * IDX_ERR_INVALID_ARG for a null out_val or a ratio / rank / world /
+ * interleave outside the ranges of indexer_index_key_counts.
  */
 idx_status indexer_decode_topk_values(const void* q, const float* weights,
                                       const uint8_t* index_cache, int64_t num_pages,
                                       const int32_t* block_table, int64_t bt_stride,
                                       int32_t bt_width, const int32_t* row_seq_lens,
                                       int32_t num_reqs, int32_t next_n, int32_t num_heads,
-                                      int32_t head_dim, int32_t topk, int32_t dcp_rank,
-                                      int32_t dcp_world, int32_t dcp_interleave, int32_t* out_idx,
-                                      float* out_val, void* workspace, size_t workspace_bytes,
-                                      uint32_t* dev_error, void* stream);
+                                      int32_t head_dim, int32_t topk, int32_t compress_ratio,
+                                      int32_t dcp_rank, int32_t dcp_world, int32_t dcp_interleave,
+                                      int32_t* out_idx, float* out_val, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_error, void* stream);
+
+/*
+ * Prefill top-k with the selected logits on one rank of a compressed and / or
+ * key-sharded cache ([INDEXER] _build_prefill_chunk_metadata_kernel: query i
+ * of a request of L tokens and Q queries sees (L - Q + 1 + i) / C entries,
+ * then the rank's count of them). Arguments as indexer_prefill_topk (same
+ * workspace size) plus compress_ratio / dcp_* (as indexer_decode_topk_values)
+ * and out_val float [sum of query_lens, topk]; every query with at least one
+ * entry is scored and selected (no causal shortcut), out_idx holds global
+ * entry positions in no particular order, -1 / -inf in empty slots.
+ */
+idx_status indexer_prefill_topk_values(
+    const void* q, const float* weights, const uint8_t* index_cache, int64_t num_pages,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width, const int32_t* seq_lens,
+    const int32_t* query_start_loc, const int32_t* seq_lens_host, const int32_t* query_lens_host,
+    int32_t num_reqs, int32_t num_heads, int32_t head_dim, int32_t topk, int32_t compress_ratio,
+    int32_t dcp_rank, int32_t dcp_world, int32_t dcp_interleave, int64_t workspace_tokens,
+    int64_t logits_budget_bytes, int32_t* out_idx, float* out_val, void* workspace,
+    size_t workspace_bytes, uint32_t* dev_error, void* stream);
 
 /*
  * Merge of the ranks' candidates: cand_val float / cand_idx int32

@@ -93,6 +93,8 @@ def _load():
         lib.ora_dcp_local_len.argtypes = [i64, i32, i32, i32]
         lib.ora_dcp_global_index.restype = i64
         lib.ora_dcp_global_index.argtypes = [i64, i32, i32, i32]
+        lib.ora_index_key_count.restype = i64
+        lib.ora_index_key_count.argtypes = [i64, i32, i32, i32, i32]
         lib.ora_merge_candidates.restype = None
         lib.ora_merge_candidates.argtypes = [P, P, i64, i32, P, P]
         _lib = lib
@@ -385,6 +387,16 @@ def dcp_local_lens(lens, rank: int, world: int, interleave: int) -> np.ndarray:
                     dtype=np.int64).reshape(np.shape(lens))
 
 
+def index_key_counts(lens, ratio: int = 1, rank: int = 0, world: int = 1,
+                     interleave: int = 1) -> np.ndarray:
+    """Cache entries a row of each length sees: one per `ratio` tokens (a
+    compressed cache), then rank `rank`'s local count of them."""
+    lib = _load()
+    a = np.asarray(lens, dtype=np.int64).ravel()
+    return np.array([lib.ora_index_key_count(int(L), ratio, rank, world, interleave) for L in a],
+                    dtype=np.int64).reshape(np.shape(lens))
+
+
 def dcp_global_index(local, rank: int, world: int, interleave: int) -> np.ndarray:
     """Global token of each of rank `rank`'s local keys (negative stays -1)."""
     lib = _load()
@@ -410,20 +422,25 @@ def merge_candidates(vals, idx, k: int):
 
 
 def dcp_rank_topk_values(q_bf16_bits, w, cache, block_table, row_lens, next_n: int, k: int,
-                         rank: int, world: int, interleave: int):
+                         rank: int, world: int, interleave: int, ratio: int = 1,
+                         bt_rows=None):
     """One rank's part: for token row r (block-table row r // next_n of the
-    rank's local cache) the top k of its local keys with their logits, the
-    indices in global token positions. Returns (idx [rows, k], val [rows, k],
+    rank's local cache, or bt_rows[r]) the top k of its local keys (the
+    rank's count of row_lens[r] // ratio entries) with their logits, the
+    indices in global entry positions. Returns (idx [rows, k], val [rows, k],
     local lens, logits list, tol_a list, tol_b list) (logits over local keys)."""
     q8, _, wp = quantize_q(q_bf16_bits, w)
-    local = dcp_local_lens(np.asarray(row_lens, dtype=np.int64), rank, world, interleave)
+    local = index_key_counts(np.asarray(row_lens, dtype=np.int64), ratio, rank, world,
+                             interleave)
     rows = local.shape[0]
+    if bt_rows is None:
+        bt_rows = np.arange(rows) // next_n
     out = np.empty((rows, k), np.int32)
     val = np.empty((rows, k), np.float64)
     lgs, tas, tbs = [], [], []
     for r in range(rows):
         L = int(local[r])
-        lg, ta, tb = row_logits(q8[r], wp[r], cache, block_table[r // next_n], L)
+        lg, ta, tb = row_logits(q8[r], wp[r], cache, block_table[bt_rows[r]], L)
         o, v = topk_row_values(lg, L, k)
         out[r] = dcp_global_index(o, rank, world, interleave)
         val[r] = v
@@ -433,7 +450,8 @@ def dcp_rank_topk_values(q_bf16_bits, w, cache, block_table, row_lens, next_n: i
     return out, val, local, lgs, tas, tbs
 
 
-def dcp_decode_topk(q_bf16_bits, w, shards, row_lens, next_n: int, k: int, interleave: int):
+def dcp_decode_topk(q_bf16_bits, w, shards, row_lens, next_n: int, k: int, interleave: int,
+                    ratio: int = 1, bt_rows=None):
     """Key-sharded decode top-k: shards[r] = (cache, block_table) of rank r
     (its local keys in order); each rank's candidates, then their merge.
     Returns (idx [rows, k] by (logit desc, index asc), val [rows, k])."""
@@ -441,10 +459,21 @@ def dcp_decode_topk(q_bf16_bits, w, shards, row_lens, next_n: int, k: int, inter
     vals, idxs = [], []
     for rank, (cache, bt) in enumerate(shards):
         o, v, *_ = dcp_rank_topk_values(q_bf16_bits, w, cache, bt, row_lens, next_n, k, rank,
-                                        world, interleave)
+                                        world, interleave, ratio, bt_rows)
         vals.append(v)
         idxs.append(o)
     return merge_candidates(np.stack(vals), np.stack(idxs), k)
+
+
+def dcp_prefill_topk(q_bf16_bits, w, shards, seq_lens, query_start_loc, k: int,
+                     interleave: int, ratio: int = 1):
+    """Key-sharded (and compressed) prefill top-k: query i of request r sees
+    the rank's local count of (L - Q + 1 + i) // ratio cache entries on each
+    rank (INDEXER page, _build_prefill_chunk_metadata_kernel with
+    COMPRESS_RATIO and the DCP branch); the ranks' candidates are merged.
+    Returns (idx [rows, k] by (logit desc, index asc), val [rows, k])."""
+    req, ln = prefill_rows(seq_lens, query_start_loc)
+    return dcp_decode_topk(q_bf16_bits, w, shards, ln, 1, k, interleave, ratio, bt_rows=req)
 
 
 # --------------------------------------------------------------------------

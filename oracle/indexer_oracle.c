@@ -26,7 +26,10 @@
  *    bytes per token) and kv_cache_as_quant_view (the MXFP4 cache view: token
  *    stride head_dim / 2 + head_dim / MXFP4_BLOCK_SIZE bytes inside a page).
  *    _build_prefill_chunk_metadata_kernel's DCP branch also gives the key
- *    count of one rank of a key-sharded (decode context parallel) cache.
+ *    count of one rank of a key-sharded (decode context parallel) cache, and
+ *    its COMPRESS_RATIO the key count of a compressed cache (DeepseekV4: one
+ *    cache entry per compress_ratio tokens; the decode metadata divides the
+ *    per-token seq_lens by the same ratio).
  *  - The scoring rule logit[t,s] = sum_h w[t,h] * ReLU(scale_s * (q[t,h] . k_s))
  *    and top-k = 2048 come from the statement of the method; the pages only name
  *    the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
@@ -491,6 +494,16 @@ int64_t ora_dcp_local_len(int64_t L, int32_t rank, int32_t world, int32_t interl
   if (r < 0) r = 0;
   if (r > interleave) r = interleave;
   return base + r;
+}
+
+/* Index keys a row sees when the cache holds one entry per `ratio` tokens
+ * (INDEXER page: DeepseekV4's compress_ratio; the decode path divides the
+ * per-token seq_lens by it, _build_prefill_chunk_metadata_kernel computes
+ * (start_pos + 1 + i) / COMPRESS_RATIO), then, on a key-sharded cache, the
+ * rank's local count of those entries (the same kernel's DCP branch). */
+int64_t ora_index_key_count(int64_t L, int32_t ratio, int32_t rank, int32_t world,
+                            int32_t interleave) {
+  return ora_dcp_local_len(L / ratio, rank, world, interleave);
 }
 
 /* Token of the whole sequence that rank `rank` holds as its local key j: its

@@ -8,8 +8,8 @@ first call does, and raises if it has not been built.
 from .binding import (  # noqa: F401
     IndexerError,
     decode_workspace,
-    indexer_dcp_local_lens,
     indexer_dcp_merge,
+    indexer_index_key_counts,
     indexer_decode_logits,
     indexer_decode_topk,
     indexer_decode_topk_from_lens,
@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     indexer_insert_keys,
     indexer_plan_prefill_chunks,
     indexer_prefill_topk,
+    indexer_prefill_topk_values,
     indexer_prefill_workspace_bytes,
     indexer_profile_events,
     indexer_trace_buffer,

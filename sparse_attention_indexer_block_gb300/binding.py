@@ -53,10 +53,13 @@ SIGNATURES = {
                                             C.POINTER(_I32), C.POINTER(_I32)]),
     "indexer_decode_topk_noalloc": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
                                               _I32, _I32, _I32, _P, _P, _P]),
-    "indexer_dcp_local_lens": (C.c_int, [_P, _I64, _I32, _I32, _I32, _P, _P]),
+    "indexer_index_key_counts": (C.c_int, [_P, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "indexer_decode_topk_values": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
-                                             _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _SZ,
-                                             _P, _P]),
+                                             _I32, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P,
+                                             _SZ, _P, _P]),
+    "indexer_prefill_topk_values": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _P, _P, _P,
+                                              _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
+                                              _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "indexer_dcp_merge": (C.c_int, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
 }
 
@@ -221,22 +224,25 @@ def indexer_decode_topk_from_lens(q, weights, index_cache, block_table, seq_lens
     return out_idx
 
 
-def indexer_dcp_local_lens(row_seq_lens, dcp_rank: int, dcp_world: int, dcp_interleave: int,
-                           local_lens=None, stream=None):
-    """Rank dcp_rank's key count of each length (int32 tensors)."""
+def indexer_index_key_counts(row_seq_lens, compress_ratio: int = 1, dcp_rank: int = 0,
+                             dcp_world: int = 1, dcp_interleave: int = 1, key_counts=None,
+                             stream=None):
+    """Cache entries each row sees on rank dcp_rank of a compressed and / or
+    key-sharded cache (int32 tensors)."""
     n = int(row_seq_lens.numel())
-    if local_lens is None:
-        local_lens = torch.empty_like(row_seq_lens)
-    st = load().indexer_dcp_local_lens(_ptr(row_seq_lens), n, dcp_rank, dcp_world,
-                                       dcp_interleave, _ptr(local_lens), _stream(stream))
-    _check("indexer_dcp_local_lens", st)
-    return local_lens
+    if key_counts is None:
+        key_counts = torch.empty_like(row_seq_lens)
+    st = load().indexer_index_key_counts(_ptr(row_seq_lens), n, compress_ratio, dcp_rank,
+                                         dcp_world, dcp_interleave, _ptr(key_counts),
+                                         _stream(stream))
+    _check("indexer_index_key_counts", st)
+    return key_counts
 
 
 def indexer_decode_topk_values(q, weights, index_cache, block_table, row_seq_lens, next_n: int,
-                               topk: int = MAX_TOPK, dcp_rank: int = 0, dcp_world: int = 1,
-                               dcp_interleave: int = 1, out_idx=None, out_val=None,
-                               workspace=None, dev_error=None, stream=None):
+                               topk: int = MAX_TOPK, compress_ratio: int = 1, dcp_rank: int = 0,
+                               dcp_world: int = 1, dcp_interleave: int = 1, out_idx=None,
+                               out_val=None, workspace=None, dev_error=None, stream=None):
     """Top-k with the selected logits on one rank of a key-sharded cache
     (the whole cache when dcp_world == 1); indices in global positions.
     Returns (out_idx int32, out_val float32), both [rows, topk]."""
@@ -251,8 +257,8 @@ def indexer_decode_topk_values(q, weights, index_cache, block_table, row_seq_len
     st = load().indexer_decode_topk_values(
         _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
         int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, next_n,
-        int(q.shape[1]), int(q.shape[2]), topk, dcp_rank, dcp_world, dcp_interleave,
-        _ptr(out_idx), _ptr(out_val), _ptr(workspace),
+        int(q.shape[1]), int(q.shape[2]), topk, compress_ratio, dcp_rank, dcp_world,
+        dcp_interleave, _ptr(out_idx), _ptr(out_val), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
     _check("indexer_decode_topk_values", st)
     return out_idx, out_val
@@ -341,6 +347,34 @@ def indexer_prefill_topk(q, weights, index_cache, block_table, seq_lens, query_s
         _stream(stream))
     _check("indexer_prefill_topk", st)
     return out_idx
+
+
+def indexer_prefill_topk_values(q, weights, index_cache, block_table, seq_lens, query_start_loc,
+                                seq_lens_host, query_lens_host, topk: int = MAX_TOPK,
+                                compress_ratio: int = 1, dcp_rank: int = 0, dcp_world: int = 1,
+                                dcp_interleave: int = 1, workspace_tokens: int = 40 * 8192,
+                                logits_budget_bytes: int = 512 << 20, out_idx=None, out_val=None,
+                                workspace=None, dev_error=None, stream=None):
+    """Prefill top-k with the selected logits on one rank of a compressed and
+    / or key-sharded cache. Returns (out_idx int32, out_val float32)."""
+    sl, ql = _host_i32(seq_lens_host), _host_i32(query_lens_host)
+    total_q = int(q.shape[0])
+    if out_idx is None:
+        out_idx = torch.empty((total_q, topk), dtype=torch.int32, device=q.device)
+    if out_val is None:
+        out_val = torch.empty((total_q, topk), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = indexer_prefill_workspace_bytes(sl, ql, topk, workspace_tokens, logits_budget_bytes)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    st = load().indexer_prefill_topk_values(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(seq_lens),
+        _ptr(query_start_loc), sl.ctypes.data, ql.ctypes.data, sl.shape[0], int(q.shape[1]),
+        int(q.shape[2]), topk, compress_ratio, dcp_rank, dcp_world, dcp_interleave,
+        workspace_tokens, logits_budget_bytes, _ptr(out_idx), _ptr(out_val), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_prefill_topk_values", st)
+    return out_idx, out_val
 
 
 def indexer_profile_events(start_event=None, stop_event=None):

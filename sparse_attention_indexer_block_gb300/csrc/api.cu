@@ -252,8 +252,13 @@ struct RowLens {
 // score the rank's share of their keys and the indices go out global.
 struct ValuesOut {
   float* out_val;
-  int32_t rank, world, interleave;
+  int32_t compress_ratio, rank, world, interleave;
 };
+
+bool valid_values(const ValuesOut* vo) {
+  return vo->out_val && vo->compress_ratio >= 1 && vo->world >= 1 && vo->rank >= 0 &&
+         vo->rank < vo->world && vo->interleave >= 1;
+}
 
 idx_status decode_common(bool logits, const void* q, const float* weights,
                          const uint8_t* index_cache, int64_t num_pages, const int32_t* block_table,
@@ -264,9 +269,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
                          void* stream, const ValuesOut* vo = nullptr) {
   if (num_reqs < 0) return IDX_ERR_INVALID_ARG;
   const bool values = vo != nullptr;
-  if (values && (!vo->out_val || vo->world < 1 || vo->rank < 0 || vo->rank >= vo->world ||
-                 vo->interleave < 1))
-    return IDX_ERR_INVALID_ARG;
+  if (values && !valid_values(vo)) return IDX_ERR_INVALID_ARG;
   if (next_n != 1 && next_n != 2) return IDX_ERR_UNSUPPORTED;
   idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
                                num_heads, head_dim, topk);
@@ -295,6 +298,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
                    row_penalty, row_penalty_div, lens.seq_lens, lens.decode_lens};
   if (values) {
     a.out_val = vo->out_val;
+    a.compress_ratio = vo->compress_ratio;
     a.dcp_rank = vo->rank;
     a.dcp_world = vo->world;
     a.dcp_interleave = vo->interleave;
@@ -496,28 +500,28 @@ idx_status indexer_decode_topk_values(const void* q, const float* weights,
                                       const int32_t* block_table, int64_t bt_stride,
                                       int32_t bt_width, const int32_t* row_seq_lens,
                                       int32_t num_reqs, int32_t next_n, int32_t num_heads,
-                                      int32_t head_dim, int32_t topk, int32_t dcp_rank,
-                                      int32_t dcp_world, int32_t dcp_interleave, int32_t* out_idx,
-                                      float* out_val, void* workspace, size_t workspace_bytes,
-                                      uint32_t* dev_error, void* stream) {
+                                      int32_t head_dim, int32_t topk, int32_t compress_ratio,
+                                      int32_t dcp_rank, int32_t dcp_world, int32_t dcp_interleave,
+                                      int32_t* out_idx, float* out_val, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_error, void* stream) {
   if (!out_val) return IDX_ERR_INVALID_ARG;
-  const ValuesOut vo{out_val, dcp_rank, dcp_world, dcp_interleave};
+  const ValuesOut vo{out_val, compress_ratio, dcp_rank, dcp_world, dcp_interleave};
   return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
                        RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
                        head_dim, topk, out_idx, nullptr, 0, workspace, workspace_bytes, dev_error,
                        stream, &vo);
 }
 
-idx_status indexer_dcp_local_lens(const int32_t* row_seq_lens, int64_t num_rows, int32_t dcp_rank,
-                                  int32_t dcp_world, int32_t dcp_interleave, int32_t* local_lens,
-                                  void* stream) {
-  if (num_rows < 0 || dcp_world < 1 || dcp_rank < 0 || dcp_rank >= dcp_world ||
-      dcp_interleave < 1)
+idx_status indexer_index_key_counts(const int32_t* row_seq_lens, int64_t num_rows,
+                                   int32_t compress_ratio, int32_t dcp_rank, int32_t dcp_world,
+                                   int32_t dcp_interleave, int32_t* key_counts, void* stream) {
+  if (num_rows < 0 || compress_ratio < 1 || dcp_world < 1 || dcp_rank < 0 ||
+      dcp_rank >= dcp_world || dcp_interleave < 1)
     return IDX_ERR_INVALID_ARG;
   if (num_rows == 0) return IDX_OK;
-  if (!row_seq_lens || !local_lens) return IDX_ERR_INVALID_ARG;
-  return launch_dcp_local_lens(row_seq_lens, num_rows, dcp_rank, dcp_world, dcp_interleave,
-                               local_lens, static_cast<cudaStream_t>(stream));
+  if (!row_seq_lens || !key_counts) return IDX_ERR_INVALID_ARG;
+  return launch_key_counts(row_seq_lens, num_rows, compress_ratio, dcp_rank, dcp_world,
+                           dcp_interleave, key_counts, static_cast<cudaStream_t>(stream));
 }
 
 idx_status indexer_dcp_merge(const float* cand_val, const int32_t* cand_idx, int32_t dcp_world,
@@ -595,15 +599,21 @@ idx_status indexer_prefill_workspace_bytes(const int32_t* seq_lens_host,
   return IDX_OK;
 }
 
-idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8_t* index_cache,
-                                int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
-                                int32_t bt_width, const int32_t* seq_lens,
-                                const int32_t* query_start_loc, const int32_t* seq_lens_host,
-                                const int32_t* query_lens_host, int32_t num_reqs,
-                                int32_t num_heads, int32_t head_dim, int32_t topk,
-                                int64_t workspace_tokens, int64_t logits_budget_bytes,
-                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
-                                uint32_t* dev_error, void* stream) {
+}  // extern "C"
+
+namespace {
+
+idx_status prefill_common(const void* q, const float* weights, const uint8_t* index_cache,
+                          int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                          int32_t bt_width, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, const int32_t* seq_lens_host,
+                          const int32_t* query_lens_host, int32_t num_reqs, int32_t num_heads,
+                          int32_t head_dim, int32_t topk, int64_t workspace_tokens,
+                          int64_t logits_budget_bytes, int32_t* out_idx, void* workspace,
+                          size_t workspace_bytes, uint32_t* dev_error, void* stream,
+                          const ValuesOut* vo) {
+  const bool values = vo != nullptr;
+  if (values && !valid_values(vo)) return IDX_ERR_INVALID_ARG;
   idx_status st = check_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
                                num_heads, head_dim, topk);
   if (st != IDX_OK) return st;
@@ -630,6 +640,13 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     PrefillPrepArgs a{static_cast<const __nv_bfloat16*>(q), weights, seq_lens, query_start_loc,
                       c.r0, c.r1, lo, hi, static_cast<int32_t>(nw), topk, bt_width, out_idx,
                       dev_error, nC, 0};
+    if (values) {
+      a.out_val = vo->out_val;
+      a.compress_ratio = vo->compress_ratio;
+      a.dcp_rank = vo->rank;
+      a.dcp_world = vo->world;
+      a.dcp_interleave = vo->interleave;
+    }
     if ((st = launch_prefill_prep(a, ws, L, s)) != IDX_OK) return st;
     ScoreParams p{};
     p.cache = index_cache;
@@ -655,14 +672,54 @@ idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8
     p.out_idx = out_idx;
     p.out_row_base = lo;
     p.topk = topk;
-    p.short_len = topk;
+    p.short_len = values ? 0 : topk;
+    p.out_val = values ? vo->out_val : nullptr;
     p.dev_error = dev_error;
     size_t tb = 0;
     p.trace = trace_buffer(&tb);
     if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
     if ((st = timed_score(kPrefillG, false, p, map, s)) != IDX_OK) return st;
+    if (values && vo->world > 1 &&
+        (st = launch_dcp_globalise(out_idx + lo * topk, (hi - lo) * topk, vo->rank, vo->world,
+                                   vo->interleave, s)) != IDX_OK)
+      return st;
   }
   return IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+idx_status indexer_prefill_topk(const void* q, const float* weights, const uint8_t* index_cache,
+                                int64_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                                int32_t bt_width, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, const int32_t* seq_lens_host,
+                                const int32_t* query_lens_host, int32_t num_reqs,
+                                int32_t num_heads, int32_t head_dim, int32_t topk,
+                                int64_t workspace_tokens, int64_t logits_budget_bytes,
+                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_error, void* stream) {
+  return prefill_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                        seq_lens, query_start_loc, seq_lens_host, query_lens_host, num_reqs,
+                        num_heads, head_dim, topk, workspace_tokens, logits_budget_bytes, out_idx,
+                        workspace, workspace_bytes, dev_error, stream, nullptr);
+}
+
+idx_status indexer_prefill_topk_values(
+    const void* q, const float* weights, const uint8_t* index_cache, int64_t num_pages,
+    const int32_t* block_table, int64_t bt_stride, int32_t bt_width, const int32_t* seq_lens,
+    const int32_t* query_start_loc, const int32_t* seq_lens_host, const int32_t* query_lens_host,
+    int32_t num_reqs, int32_t num_heads, int32_t head_dim, int32_t topk, int32_t compress_ratio,
+    int32_t dcp_rank, int32_t dcp_world, int32_t dcp_interleave, int64_t workspace_tokens,
+    int64_t logits_budget_bytes, int32_t* out_idx, float* out_val, void* workspace,
+    size_t workspace_bytes, uint32_t* dev_error, void* stream) {
+  if (!out_val) return IDX_ERR_INVALID_ARG;
+  const ValuesOut vo{out_val, compress_ratio, dcp_rank, dcp_world, dcp_interleave};
+  return prefill_common(q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                        seq_lens, query_start_loc, seq_lens_host, query_lens_host, num_reqs,
+                        num_heads, head_dim, topk, workspace_tokens, logits_budget_bytes, out_idx,
+                        workspace, workspace_bytes, dev_error, stream, &vo);
 }
 
 }  // extern "C"

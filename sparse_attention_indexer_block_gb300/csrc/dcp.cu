@@ -17,14 +17,13 @@ constexpr int kMergeThreads = 1024;
 constexpr int kMergeWarps = kMergeThreads / 32;
 constexpr int kMergeCap = IDX_DCP_MAX_CANDIDATES;  // candidates of a row in shared memory
 
-__global__ void __launch_bounds__(kMapThreads) dcp_local_lens_kernel(const int32_t* lens,
-                                                                     int64_t n, int rank,
-                                                                     int world, int interleave,
-                                                                     int32_t* out) {
+__global__ void __launch_bounds__(kMapThreads) key_counts_kernel(const int32_t* lens, int64_t n,
+                                                                 int ratio, int rank, int world,
+                                                                 int interleave, int32_t* out) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kMapThreads;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kMapThreads + threadIdx.x; i < n;
        i += stride)
-    out[i] = static_cast<int32_t>(dcp_local_len(lens[i], rank, world, interleave));
+    out[i] = static_cast<int32_t>(index_key_count(lens[i], ratio, rank, world, interleave));
 }
 
 // Rank-local key j is global token (j / I) * I * W + rank * I + j % I: its
@@ -194,11 +193,11 @@ unsigned map_grid(int64_t n) {
 
 }  // namespace
 
-idx_status launch_dcp_local_lens(const int32_t* lens, int64_t n, int rank, int world,
-                                 int interleave, int32_t* out, cudaStream_t s) {
+idx_status launch_key_counts(const int32_t* lens, int64_t n, int ratio, int rank, int world,
+                             int interleave, int32_t* out, cudaStream_t s) {
   if (n <= 0) return IDX_OK;
-  dcp_local_lens_kernel<<<map_grid(n), kMapThreads, 0, s>>>(lens, n, rank, world, interleave,
-                                                            out);
+  key_counts_kernel<<<map_grid(n), kMapThreads, 0, s>>>(lens, n, ratio, rank, world, interleave,
+                                                        out);
   return cuda_status(cudaGetLastError());
 }
 

@@ -65,6 +65,16 @@ __host__ __device__ __forceinline__ int64_t dcp_local_len(int64_t L, int rank, i
   return base + (r < 0 ? 0 : (r > interleave ? interleave : r));
 }
 
+// Cache entries a row of L tokens sees when the cache holds one entry per
+// `ratio` tokens (INDEXER page: DeepseekV4's compress_ratio divides the
+// per-token seq_lens; _build_prefill_chunk_metadata_kernel divides each
+// query's key count by COMPRESS_RATIO), then this rank's share of them.
+__host__ __device__ __forceinline__ int64_t index_key_count(int64_t L, int ratio, int rank,
+                                                            int world, int interleave) {
+  if (L < 0) return L;
+  return dcp_local_len(ratio > 1 ? L / ratio : L, rank, world, interleave);
+}
+
 
 // Everything the score/select kernel reads, for one launch.
 struct ScoreParams {
@@ -181,8 +191,9 @@ struct DecodePrepArgs {
   const int32_t* decode_lens = nullptr;  // [num_reqs]
   // Values mode (score_all set, top-k output): rows of 0 keys get -1 / -inf.
   float* out_val = nullptr;
-  // Key-sharded cache: every row scores dcp_local_len(its length) keys.
-  int32_t dcp_rank = 0, dcp_world = 1, dcp_interleave = 1;
+  // Compressed and / or key-sharded cache: every row scores
+  // index_key_count(its length) keys.
+  int32_t compress_ratio = 1, dcp_rank = 0, dcp_world = 1, dcp_interleave = 1;
 };
 idx_status launch_decode_prep(const DecodePrepArgs& a, uint8_t* ws, const WsLayout& L,
                               cudaStream_t s);
@@ -201,6 +212,10 @@ struct PrefillPrepArgs {
   uint32_t* err;
   int32_t num_ctas;     // grid of the score/select launch that follows
   int32_t row_penalty;  // tiles of streaming time one work row's end costs its CTA
+  // Values mode: every query with > 0 keys is scored, queries of 0 keys get
+  // -1 / -inf; compressed and / or key-sharded cache as in DecodePrepArgs.
+  float* out_val = nullptr;
+  int32_t compress_ratio = 1, dcp_rank = 0, dcp_world = 1, dcp_interleave = 1;
 };
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);
@@ -250,8 +265,8 @@ idx_status launch_row_select(const RowSelectParams& p, int grid, cudaStream_t s)
 
 // Key-sharded decode: rank-local key counts, local-to-global output indices,
 // and the merge of the ranks' (logit, index) candidates.
-idx_status launch_dcp_local_lens(const int32_t* lens, int64_t n, int rank, int world,
-                                 int interleave, int32_t* out, cudaStream_t s);
+idx_status launch_key_counts(const int32_t* lens, int64_t n, int ratio, int rank, int world,
+                             int interleave, int32_t* out, cudaStream_t s);
 idx_status launch_dcp_globalise(int32_t* idx, int64_t n, int rank, int world, int interleave,
                                 cudaStream_t s);
 idx_status launch_dcp_merge(const float* val, const int32_t* idx, int world, int64_t rows,

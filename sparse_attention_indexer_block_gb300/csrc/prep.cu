@@ -274,7 +274,7 @@ __device__ __forceinline__ int64_t raw_row_len(const DecodePrepArgs& a, int64_t 
     const int64_t L = a.seq_lens[b], d = a.decode_lens[b];
     len = j < d ? L - d + j + 1 : 0;
   }
-  return dcp_local_len(len, a.dcp_rank, a.dcp_world, a.dcp_interleave);
+  return index_key_count(len, a.compress_ratio, a.dcp_rank, a.dcp_world, a.dcp_interleave);
 }
 
 // Block 0: work-row schedule (tile counts and their exclusive prefix), validated
@@ -369,7 +369,8 @@ __device__ __forceinline__ int64_t prefill_len(const PrefillPrepArgs& a, int r, 
                                                bool report) {
   const int64_t qs = a.qsl[r], qe = a.qsl[r + 1];
   const int64_t v = static_cast<int64_t>(a.seq_lens[r]) - (qe - qs) + 1 + (row - qs);
-  return clamp_len(v, a.bt_width, a.err, report);
+  return clamp_len(index_key_count(v, a.compress_ratio, a.dcp_rank, a.dcp_world, a.dcp_interleave),
+                   a.bt_width, a.err, report);
 }
 
 // Block 0: work rows of the chunk (up to two consecutive queries of one
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
         int maxlen = 0;
         for (int g = 0; g < ntok; ++g) {
           const int len = static_cast<int>(prefill_len(a, rq, first + g, true));
-          if (len > a.topk) maxlen = max(maxlen, len);
+          if (len > (a.out_val ? 0 : a.topk)) maxlen = max(maxlen, len);
         }
         wr[idx] = WorkRow{rq, static_cast<int32_t>(first - a.row_lo), ntok, maxlen};
         wts[idx] = (maxlen + kTileKeys - 1) / kTileKeys;  // tile count, scanned below
@@ -464,9 +465,13 @@ __global__ void __launch_bounds__(kPrepThreads) prefill_prep_kernel(
     const int r = find_request(a.qsl, a.req_begin, a.req_end, row);
     const int64_t len = prefill_len(a, r, row, false);
     if (lane == 0) row_len[lr] = static_cast<int32_t>(len);
-    if (len <= a.topk) {
+    // top k: queries of <= k keys are the causal row; values: queries of no
+    // keys are empty (the others are all scored)
+    if (len <= (a.out_val ? 0 : a.topk)) {
       int32_t* o = a.out_idx + row * a.topk;
       for (int i = lane; i < a.topk; i += 32) o[i] = i < len ? i : -1;
+      if (a.out_val)
+        for (int i = lane; i < a.topk; i += 32) a.out_val[row * a.topk + i] = -INFINITY;
     }
   }
   quantize_tasks<true>(a.q, a.w, a.row_lo * kHeads, rows * kHeads, q8img, wprime, gw, nw);

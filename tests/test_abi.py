@@ -174,13 +174,13 @@ def test_prefill_validation(lib):
 
 def _values(lib, **over):
     a = dict(q=FAKE, w=FAKE, cache=FAKE, pages=10, bt=FAKE, bt_stride=4, bt_width=4, lens=FAKE,
-             R=2, next_n=1, H=64, D=128, k=2048, rank=0, world=2, inter=64, out=FAKE, val=FAKE,
-             ws=FAKE, ws_bytes=16, err=None)
+             R=2, next_n=1, H=64, D=128, k=2048, ratio=1, rank=0, world=2, inter=64, out=FAKE,
+             val=FAKE, ws=FAKE, ws_bytes=16, err=None)
     a.update(over)
     return lib.indexer_decode_topk_values(
         a["q"], a["w"], a["cache"], a["pages"], a["bt"], a["bt_stride"], a["bt_width"], a["lens"],
-        a["R"], a["next_n"], a["H"], a["D"], a["k"], a["rank"], a["world"], a["inter"], a["out"],
-        a["val"], a["ws"], a["ws_bytes"], a["err"], None)
+        a["R"], a["next_n"], a["H"], a["D"], a["k"], a["ratio"], a["rank"], a["world"],
+        a["inter"], a["out"], a["val"], a["ws"], a["ws_bytes"], a["err"], None)
 
 
 def test_key_sharded_argument_validation(lib):
@@ -192,15 +192,27 @@ def test_key_sharded_argument_validation(lib):
     assert _values(lib, rank=2) == 1
     assert _values(lib, rank=-1) == 1
     assert _values(lib, inter=0) == 1
+    assert _values(lib, ratio=0) == 1
     assert _values(lib, H=32) == 2
     assert _values(lib, R=0) == 0
-    f = lib.indexer_dcp_local_lens
-    assert f(FAKE, 4, 0, 0, 1, FAKE, None) == 1      # world < 1
-    assert f(FAKE, 4, 2, 2, 1, FAKE, None) == 1      # rank >= world
-    assert f(FAKE, 4, 0, 2, 0, FAKE, None) == 1      # interleave < 1
-    assert f(None, 4, 0, 2, 1, FAKE, None) == 1
-    assert f(FAKE, -1, 0, 2, 1, FAKE, None) == 1
-    assert f(FAKE, 0, 0, 2, 1, FAKE, None) == 0      # nothing to do
+    f = lib.indexer_index_key_counts
+    assert f(FAKE, 4, 1, 0, 0, 1, FAKE, None) == 1      # world < 1
+    assert f(FAKE, 4, 1, 2, 2, 1, FAKE, None) == 1      # rank >= world
+    assert f(FAKE, 4, 1, 0, 2, 0, FAKE, None) == 1      # interleave < 1
+    assert f(FAKE, 4, 0, 0, 2, 1, FAKE, None) == 1      # ratio < 1
+    assert f(None, 4, 1, 0, 2, 1, FAKE, None) == 1
+    assert f(FAKE, -1, 1, 0, 2, 1, FAKE, None) == 1
+    assert f(FAKE, 0, 1, 0, 2, 1, FAKE, None) == 0      # nothing to do
+    sl = np.array([10, 5], np.int32)
+    ql = np.array([4, 5], np.int32)
+    p = lib.indexer_prefill_topk_values
+    base = [FAKE, FAKE, FAKE, 10, FAKE, 4, 4, FAKE, FAKE, sl.ctypes.data, ql.ctypes.data, 2, 64,
+            128, 2048]
+    tail = [1000, 1 << 20, FAKE, FAKE, FAKE, 16, None, None]
+    assert p(*base, 1, 0, 2, 64, *tail) == 3             # valid up to the workspace size
+    assert p(*base, 0, 0, 2, 64, *tail) == 1             # ratio < 1
+    assert p(*base, 1, 2, 2, 64, *tail) == 1             # rank >= world
+    assert p(*base, 4, 0, 1, 1, *tail[:3], None, *tail[4:]) == 1   # no out_val
     m = lib.indexer_dcp_merge
     assert m(FAKE, FAKE, 9, 4, 2048, FAKE, None, None) == 2   # 9 * 2048 > 16384 candidates
     assert m(FAKE, FAKE, 2, 4, 0, FAKE, None, None) == 2

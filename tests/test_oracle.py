@@ -745,3 +745,45 @@ def test_dcp_decode_topk_equals_the_unsharded_topk(world, inter, next_n):
         assert np.array_equal(got[r, :n], order)
         assert set(got[r, :n]) == set(ref[r][ref[r] >= 0])
 
+
+
+def test_index_key_counts_compress_then_deal():
+    # a compressed cache holds entry e for tokens [e * C, e * C + C) once they
+    # are all present (L // C entries: the INDEXER page's seq_lens //
+    # compress_ratio); the entries are then dealt to ranks like tokens
+    for C in (1, 2, 4, 7):
+        for world, inter in ((1, 1), (2, 1), (3, 64), (4, 5)):
+            lens = np.arange(0, 900)
+            for r in range(world):
+                got = oracle.index_key_counts(lens, C, r, world, inter)
+                ref = np.array([int(((np.arange(L // C) // inter) % world == r).sum())
+                                for L in lens])
+                assert np.array_equal(got, ref), (C, world, inter, r)
+    assert oracle.index_key_counts([10], 4)[0] == 2 and oracle.index_key_counts([3], 4)[0] == 0
+
+
+@pytest.mark.parametrize("world,inter,ratio", [(1, 1, 4), (2, 1, 1), (2, 64, 4), (3, 5, 2)])
+def test_sharded_prefill_equals_the_unsharded_prefill(world, inter, ratio):
+    # query i of request r sees (L - Q + 1 + i) // ratio entries; the merge of
+    # the ranks' candidates is the unsharded top k over them
+    k = 48
+    seq = np.array([300, 90, 517], np.int32)
+    ql = np.array([5, 90, 7], np.int32)
+    ent = seq // ratio                           # entries of the compressed cache
+    inp = synth.make_decode_from_lens(ent, np.ones(3, np.int32), 1, seed=44 + ratio)
+    qsl = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    pre = synth.make_prefill(seq_lens=seq, query_lens=ql, seed=45)
+    qb, w = synth.bf16_bits(pre.q), pre.w.numpy()
+    shards = [(c.numpy(), b.numpy()) for c, b in synth.shard_decode(inp, world, inter, seed=6)]
+    got, gv = oracle.dcp_prefill_topk(qb, w, shards, seq, qsl, k, inter, ratio)
+    req, ln = oracle.prefill_rows(seq, qsl)
+    n_ent = ln // ratio
+    q8, _, wp = oracle.quantize_q(qb, w)
+    for i in range(ln.shape[0]):
+        L = int(n_ent[i])
+        lg, _, _ = oracle.row_logits(q8[i], wp[i], inp.cache.numpy(),
+                                     inp.block_table.numpy()[req[i]], L)
+        n = min(L, k)
+        order = np.lexsort((np.arange(L), -lg))[:n]
+        assert np.array_equal(got[i, :n], order) and np.all(got[i, n:] == -1)
+        assert np.array_equal(gv[i, :n], lg[order])
