@@ -39,6 +39,7 @@ WORKLOAD_DESC = ("decode batch: 32 requests, next_n 1, seq_lens uniform in [2048
                  "64 index heads x head_dim 128, bf16 q, fp8 e4m3 paged index-K (page 64, "
                  "fp32 per-token scale), random block table, top-2048")
 PAGE_KEY_BYTES = 132  # 128 fp8 values + 4-byte scale per key
+MX_KEY_BYTES = 68     # 64 bytes of packed e2m1 values + 4 ue8m0 block scales per key
 
 
 def parse():
@@ -97,6 +98,11 @@ WORKLOAD_DESCS = {
              "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
     "tiny": ("tiny decode: 4 requests, next_n 1, seq_lens {1000, 2048, 3000, 4096}, "
              "64 index heads x 128, fp8 e4m3 paged index-K, top-2048"),
+    "decode_mxfp4": ("decode batch with MXFP4 index keys: 32 requests, next_n 1, seq_lens "
+                     "uniform in [2048, 32768], 64 index heads x 128, 68-byte e2m1 + ue8m0 keys, "
+                     "top-2048"),
+    "long_mxfp4": ("long context with MXFP4 index keys: 128 requests, next_n 1, seq_len 131072, "
+                   "64 index heads x 128, 68-byte e2m1 + ue8m0 keys, top-2048"),
     "dcp_long": ("long context (128 x 131072 keys, 1% heavy-tail) key-sharded over 2 decode-"
                  "context-parallel ranks in runs of 1 token, the ranks run one after the other "
                  "on one GPU: per rank top-2048 with logits over its 65536 keys per row, then "
@@ -387,7 +393,7 @@ def run_insert(args, rank, world, local):
             "clocks": clk.summary(), "gpu_launches": K}), flush=True)
 
 
-def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
+def measure_decode(workload, seed, dev, steps, prof_steps, world, local, mx=False):
     """Device-timed decode steps on `workload` (expand + decode top-k through
     the C ABI, CUDA graphs of the K steps, every step on its own copy of the
     index cache so the copies together exceed L2 several times), the live mean
@@ -399,7 +405,13 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     import synth
     import sparse_attention_indexer_block_gb300 as saib
 
-    d = synth.make_decode(workload, seed=seed, device=dev)
+    if mx:  # the workload's lengths over MXFP4 keys (next_n 1)
+        wl = synth.WORKLOADS[workload]
+        sl = synth.draw_seq_lens(wl, seed)
+        d = synth.make_decode_mxfp4_from_lens(sl, np.ones(len(sl), np.int32), 1, seed=seed,
+                                              device=dev)
+    else:
+        d = synth.make_decode(workload, seed=seed, device=dev)
     R, G, k = d.num_reqs, d.next_n, d.topk
     seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
     dl_h = d.decode_lens.cpu().numpy().astype(np.int64)
@@ -407,7 +419,7 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     row_lens_h = np.concatenate([[L - dd + j + 1 if j < dd else 0 for j in range(G)]
                                  for L, dd in zip(seq_h, dl_h)])
     keys_per_step = int(row_lens_h.sum())
-    algo_bytes = int(seq_h.sum()) * PAGE_KEY_BYTES
+    algo_bytes = int(seq_h.sum()) * (MX_KEY_BYTES if mx else PAGE_KEY_BYTES)
 
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
@@ -422,6 +434,11 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     # one step: the whole hot path from the requests' (seq_lens, decode_lens),
     # the row expansion (S1) done by the launch's first kernel
     def step(i):
+        if mx:
+            saib.indexer_decode_topk_mxfp4(d.q, d.w, caches[i % n_copies], d.block_table,
+                                           d.seq_lens, k, out_idx=out, workspace=ws,
+                                           dev_error=err, stream=stream)
+            return
         saib.indexer_decode_topk_from_lens(d.q, d.w, caches[i % n_copies], d.block_table,
                                            d.seq_lens, d.decode_lens, G, k, out_idx=out,
                                            workspace=ws, dev_error=err, stream=stream)
@@ -491,7 +508,7 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
     kern_avg = statistics.mean(kern_ms)
     peak, peak_kind = measured_peak_gbs()
     achieved = algo_bytes / (kern_avg / 1e3) / 1e9
-    counters = profiled_counters(workload)
+    counters = profiled_counters(workload + ("_mxfp4" if mx else ""))
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": counters["dram_bytes_per_launch"] if counters else None,
@@ -501,8 +518,8 @@ def measure_decode(workload, seed, dev, steps, prof_steps, world, local):
                                    "score/select launch and its split-row selection launch "
                                    "on the same kernel sources, "
                                    "profiles/score_select_counters.json"),
-                "kernel": f"score_select_kernel<{G},false> + row_select_kernel (events "
-                          "around both launches)",
+                "kernel": f"score_select_kernel<{G},false,{'true' if mx else 'false'}> + "
+                          "row_select_kernel (events around both launches)",
                 "kernel_ms_avg": round(kern_avg, 5),
                 "kernel_ms_median": round(statistics.median(kern_ms), 5),
                 "kernel_launches_timed": prof_steps,
@@ -607,7 +624,9 @@ def run_ours(args, rank, world, local):
 
     seed = rank_seed(args.seed, rank)
     K = args.steps
-    res = measure_decode(args.workload, seed, dev, K, min(K, 400), world, local)
+    mx = args.workload.endswith("_mxfp4")
+    base_wl = args.workload[:-len("_mxfp4")] if mx else args.workload
+    res = measure_decode(base_wl, seed, dev, K, min(K, 400), world, local, mx=mx)
     d, R, G, k = res["d"], res["R"], res["G"], res["k"]
     ms, keys_per_step, algo_bytes = res["ms"], res["keys_per_step"], res["algo_bytes"]
     value = whole_job_rate(keys_per_step, K, world, ms)
@@ -626,9 +645,14 @@ def run_ours(args, rank, world, local):
     def e2e_step():
         for n in host:
             dbuf[n].copy_(host[n], non_blocking=True)
-        saib.indexer_decode_topk_from_lens(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"],
-                                           dbuf["seq"], dbuf["dl"], G, k, out_idx=out,
-                                           workspace=ws, dev_error=err, stream=stream)
+        if mx:
+            saib.indexer_decode_topk_mxfp4(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"],
+                                           dbuf["seq"], k, out_idx=out, workspace=ws,
+                                           dev_error=err, stream=stream)
+        else:
+            saib.indexer_decode_topk_from_lens(dbuf["q"], dbuf["w"], dbuf["cache"], dbuf["bt"],
+                                               dbuf["seq"], dbuf["dl"], G, k, out_idx=out,
+                                               workspace=ws, dev_error=err, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
     def barrier():
@@ -670,9 +694,18 @@ def run_ours(args, rank, world, local):
             torch.cuda.empty_cache()
         extra["dcp_long"] = measure_dcp("long", 2, 1, seed, dev, 50, world)
         torch.cuda.empty_cache()
+        for wl, steps in (("decode", 400), ("long", 100)):
+            r = measure_decode(wl, seed, dev, steps, min(steps, 100), world, local, mx=True)
+            extra[wl + "_mxfp4"] = {
+                "workload": WORKLOAD_DESCS[wl + "_mxfp4"], "metric_value": whole_job_rate(
+                    r["keys_per_step"], steps, world, r["ms"]), "unit": "keys/s",
+                "ms_per_step": r["ms"] / steps, "steps": steps, "roofline": r["roofline"],
+                "clocks": r["clocks"], "gpu_launches": 3 * steps}
+            del r
+            torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not mx:
         cpu = cpu_baseline(d, res["row_lens_h"])
 
     if rank == 0:

@@ -104,6 +104,7 @@ typedef enum {
 #define IDX_PAGE_BYTES 8448
 #define IDX_MAX_TOPK 2048
 #define IDX_DCP_MAX_CANDIDATES 16384 /* dcp_world * topk of indexer_dcp_merge */
+#define IDX_MXFP4_PAGE_BYTES 4352    /* 64 entries x (64 B packed e2m1 + 4 ue8m0 scales) */
 
 /* Human-readable name of a status code (static string). */
 const char* indexer_status_string(idx_status status);
@@ -255,6 +256,43 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                                  int32_t topk, float* out_logits, int64_t ld_logits,
                                  void* workspace, size_t workspace_bytes, uint32_t* dev_error,
                                  void* stream);
+
+/*
+ * Decode top-k over an MXFP4 index cache ([GLM5] _gather_workspace_shapes, its
+ * MXFP4 branch: head_dim / 2 bytes of packed mxfp4 values and head_dim /
+ * MXFP4_BLOCK_SIZE ue8m0 scale bytes per token; kv_cache_as_quant_view: that
+ * 68-byte token stride inside a page; [INDEXER] the use_fp4_indexer_cache
+ * switch of the metadata builder).
+ * index_cache uint8 [num_pages, 4352]: page p holds 64 token entries back to
+ * back; an entry is 64 bytes of e2m1 codes (element 2i in the low nibble of
+ * byte i, 2i + 1 in the high one) then 4 ue8m0 bytes (block b scales elements
+ * 32b .. 32b + 31 by 2^(E_b - 127)); the key value of element d is
+ * e2m1(code_d) * 2^(E_{d/32} - 127) (E = 255, NaN, must not occur). Base
+ * address 16-byte aligned. Other arguments, the workspace size and the
+ * results as indexer_decode_topk; next_n must be 1 (IDX_ERR_UNSUPPORTED
+ * otherwise). The keys are re-encoded on chip for the fp8 tensor cores with
+ * one power-of-two scale per key: exact for every block within 2^11 of the
+ * key's largest block, smaller blocks rounded to e4m3.
+ */
+idx_status indexer_decode_topk_mxfp4(const void* q, const float* weights,
+                                     const uint8_t* index_cache, int64_t num_pages,
+                                     const int32_t* block_table, int64_t bt_stride,
+                                     int32_t bt_width, const int32_t* row_seq_lens,
+                                     int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                     int32_t head_dim, int32_t topk, int32_t* out_idx,
+                                     void* workspace, size_t workspace_bytes, uint32_t* dev_error,
+                                     void* stream);
+
+/* The logits of indexer_decode_topk_mxfp4 (for parity checks), written like
+ * indexer_decode_logits's. */
+idx_status indexer_decode_logits_mxfp4(const void* q, const float* weights,
+                                       const uint8_t* index_cache, int64_t num_pages,
+                                       const int32_t* block_table, int64_t bt_stride,
+                                       int32_t bt_width, const int32_t* row_seq_lens,
+                                       int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                       int32_t head_dim, int32_t topk, float* out_logits,
+                                       int64_t ld_logits, void* workspace, size_t workspace_bytes,
+                                       uint32_t* dev_error, void* stream);
 
 /*
  * Compressed and key-sharded caches ([INDEXER] _build_prefill_chunk_metadata_kernel

@@ -11,8 +11,10 @@ from .binding import (  # noqa: F401
     indexer_dcp_merge,
     indexer_index_key_counts,
     indexer_decode_logits,
+    indexer_decode_logits_mxfp4,
     indexer_decode_topk,
     indexer_decode_topk_from_lens,
+    indexer_decode_topk_mxfp4,
     indexer_decode_topk_noalloc,
     indexer_decode_topk_values,
     indexer_decode_workspace_bytes,

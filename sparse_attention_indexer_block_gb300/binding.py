@@ -61,6 +61,10 @@ SIGNATURES = {
                                               _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                               _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "indexer_dcp_merge": (C.c_int, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
+    "indexer_decode_topk_mxfp4": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
+                                            _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "indexer_decode_logits_mxfp4": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
+                                              _I32, _I32, _I32, _P, _I64, _P, _SZ, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -275,6 +279,42 @@ def indexer_dcp_merge(cand_val, cand_idx, topk: int = MAX_TOPK, out_idx=None, ou
                                   _ptr(out_idx), _ptr(out_val), _stream(stream))
     _check("indexer_dcp_merge", st)
     return out_idx, out_val
+
+
+def indexer_decode_topk_mxfp4(q, weights, index_cache, block_table, row_seq_lens,
+                              topk: int = MAX_TOPK, out_idx=None, workspace=None, dev_error=None,
+                              stream=None):
+    """Decode top-k (next_n = 1) over an MXFP4 cache uint8 [pages, 4352]."""
+    R = int(block_table.shape[0])
+    if out_idx is None:
+        out_idx = torch.empty((R, topk), dtype=torch.int32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, 1, topk, q.device)
+    st = load().indexer_decode_topk_mxfp4(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, 1,
+        int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_idx), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_topk_mxfp4", st)
+    return out_idx
+
+
+def indexer_decode_logits_mxfp4(q, weights, index_cache, block_table, row_seq_lens,
+                                topk: int = MAX_TOPK, out_logits=None, workspace=None,
+                                dev_error=None, stream=None):
+    R = int(block_table.shape[0])
+    ld = int(block_table.shape[1]) * PAGE_TOKENS
+    if out_logits is None:
+        out_logits = torch.full((R, ld), float("nan"), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(R, 1, topk, q.device)
+    st = load().indexer_decode_logits_mxfp4(
+        _ptr(q), _ptr(weights), _ptr(index_cache), int(index_cache.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), int(block_table.shape[1]), _ptr(row_seq_lens), R, 1,
+        int(q.shape[1]), int(q.shape[2]), topk, _ptr(out_logits), ld, _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
+    _check("indexer_decode_logits_mxfp4", st)
+    return out_logits
 
 
 def indexer_decode_logits(q, weights, index_cache, block_table, row_seq_lens, next_n: int,

@@ -29,13 +29,13 @@ thread_local int32_t g_stall_rows = 0;
 // The score/select launch and, in top-k mode, the split-row selection after
 // it, bracketed by the profiling events when they are set.
 idx_status timed_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool mx = false) {
   if (g_prof_start) {
     const idx_status st = cuda_status(cudaEventRecord(g_prof_start, s));
     if (st != IDX_OK) return st;
   }
   const int streams = score_streams(G);
-  idx_status st = launch_score(G, logits, p, map, score_grid(), s);
+  idx_status st = launch_score(G, logits, mx, p, map, score_grid(), s);
   if (st == IDX_OK && !logits) {
     RowSelectParams r{};
     r.wr = p.wr;
@@ -266,8 +266,9 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
                          int32_t num_reqs, int32_t next_n, int32_t num_heads, int32_t head_dim,
                          int32_t topk, int32_t* out_idx, float* out_logits, int64_t ld_logits,
                          void* workspace, size_t workspace_bytes, uint32_t* dev_error,
-                         void* stream, const ValuesOut* vo = nullptr) {
+                         void* stream, const ValuesOut* vo = nullptr, bool mx = false) {
   if (num_reqs < 0) return IDX_ERR_INVALID_ARG;
+  if (mx && next_n != 1) return IDX_ERR_UNSUPPORTED;
   const bool values = vo != nullptr;
   if (values && !valid_values(vo)) return IDX_ERR_INVALID_ARG;
   if (next_n != 1 && next_n != 2) return IDX_ERR_UNSUPPORTED;
@@ -287,8 +288,8 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   const int64_t rows = static_cast<int64_t>(num_reqs) * next_n;
   const WsLayout L = ws_layout(num_reqs, rows, next_n, topk, nC);
   if (workspace_bytes < L.total) return IDX_ERR_WORKSPACE;
-  CUtensorMap map;
-  if ((st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
+  CUtensorMap map{};  // (MXFP4 pages are read with bulk copies)
+  if (!mx && (st = encode_cache_map(&map, index_cache, num_pages)) != IDX_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t row_penalty, row_penalty_div;
@@ -336,7 +337,7 @@ idx_status decode_common(bool logits, const void* q, const float* weights,
   size_t tb = 0;
   p.trace = trace_buffer(&tb);
   if (tb < sizeof(uint64_t) * kTrSlots * static_cast<size_t>(nC)) p.trace = nullptr;
-  st = timed_score(next_n, logits, p, map, s);
+  st = timed_score(next_n, logits, p, map, s, mx);
   if (st == IDX_OK && values && vo->world > 1)
     st = launch_dcp_globalise(out_idx, rows * topk, vo->rank, vo->world, vo->interleave, s);
   return st;
@@ -493,6 +494,34 @@ idx_status indexer_decode_logits(const void* q, const float* weights, const uint
                        RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
                        head_dim, topk, nullptr, out_logits, ld_logits, workspace, workspace_bytes,
                        dev_error, stream);
+}
+
+idx_status indexer_decode_topk_mxfp4(const void* q, const float* weights,
+                                     const uint8_t* index_cache, int64_t num_pages,
+                                     const int32_t* block_table, int64_t bt_stride,
+                                     int32_t bt_width, const int32_t* row_seq_lens,
+                                     int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                     int32_t head_dim, int32_t topk, int32_t* out_idx,
+                                     void* workspace, size_t workspace_bytes, uint32_t* dev_error,
+                                     void* stream) {
+  return decode_common(false, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
+                       head_dim, topk, out_idx, nullptr, 0, workspace, workspace_bytes, dev_error,
+                       stream, nullptr, true);
+}
+
+idx_status indexer_decode_logits_mxfp4(const void* q, const float* weights,
+                                       const uint8_t* index_cache, int64_t num_pages,
+                                       const int32_t* block_table, int64_t bt_stride,
+                                       int32_t bt_width, const int32_t* row_seq_lens,
+                                       int32_t num_reqs, int32_t next_n, int32_t num_heads,
+                                       int32_t head_dim, int32_t topk, float* out_logits,
+                                       int64_t ld_logits, void* workspace, size_t workspace_bytes,
+                                       uint32_t* dev_error, void* stream) {
+  return decode_common(true, q, weights, index_cache, num_pages, block_table, bt_stride, bt_width,
+                       RowLens{row_seq_lens, nullptr, nullptr}, num_reqs, next_n, num_heads,
+                       head_dim, topk, nullptr, out_logits, ld_logits, workspace, workspace_bytes,
+                       dev_error, stream, nullptr, true);
 }
 
 idx_status indexer_decode_topk_values(const void* q, const float* weights,

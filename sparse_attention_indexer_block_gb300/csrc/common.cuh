@@ -18,6 +18,11 @@ constexpr int kPageValueBytes = kPageTokens * kDim;           // 8192
 constexpr int kPageBytes = kPageTokens * (kDim + 4);          // 8448
 constexpr int kTileKeys = 128;                                // MMA M: two pages
 constexpr int kQRowBytes = kHeads * kDim;                     // 8192 fp8 bytes per token row
+// MXFP4 index keys: 64 bytes of packed e2m1 (element 2i in the low nibble of
+// byte i) then 4 ue8m0 block scales (block b = elements 32b .. 32b + 31) per
+// token, 64 tokens per page back to back.
+constexpr int kMxTokenBytes = kDim / 2 + kDim / 32;             // 68
+constexpr int kMxPageBytes = kPageTokens * kMxTokenBytes;       // 4352
 
 // A "work row" is a group of up to G token rows that read the same request's
 // keys and are scored by one MMA (N = 64*G): the next_n tokens of a decode

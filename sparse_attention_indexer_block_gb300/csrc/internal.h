@@ -220,11 +220,12 @@ struct PrefillPrepArgs {
 idx_status launch_prefill_prep(const PrefillPrepArgs& a, uint8_t* ws, const WsLayout& L,
                                cudaStream_t s);
 
-// G = token rows per work row (1 or 2); logits = write logits instead of selecting.
+// G = token rows per work row (1 or 2); logits = write logits instead of selecting;
+// mx = the cache holds MXFP4 keys (4352-byte pages; G = 1 only).
 // Thread-local trace buffer set by indexer_trace_buffer (nullptr = off).
 uint64_t* trace_buffer(size_t* bytes);
 
-idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
+idx_status launch_score(int G, bool logits, bool mx, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s);
 
 // Everything the split-row selection kernel reads, for one launch (after the

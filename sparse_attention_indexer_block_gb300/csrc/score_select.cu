@@ -27,6 +27,18 @@
 // row's; the row's top k is selected from them by the split-row selection
 // kernel that runs after this one.
 //
+// MXFP4 keys (kMx): the stage area holds one 16 KB tile per stream for the
+// MMA and, behind them, a ring of raw slots (a tile's two 4352-byte pages,
+// three per stream). The producer copies raw pages into the ring; one tile
+// ahead of its scoring, the epilogue group re-encodes a raw slot into its
+// stream's tile as 128 e4m3 codes per key in the swizzled layout the MMA
+// reads, with one power-of-two scale per key, and frees the raw slot; the
+// MMA waits for that and frees the tile when it completes. An e2m1 value v of a block
+// with exponent E_b becomes the e4m3 code of v * 2^(6 + E_b - E_max), E_max
+// the key's largest block exponent, and the key's scale is 2^(E_max - 133):
+// exact for every block within 2^11 of the key's largest (e4m3 normals;
+// blocks further below are rounded to e4m3).
+//
 // Scoring (the method's statement; the pages name the kernel only):
 //   logit[t, s] = sum_h w[t, h] ReLU(scale_s (q[t, h] . k_s))
 //               = scale_s * sum_h (w[t, h] sq[t, h]) ReLU(q8[t, h] . k8_s),
@@ -82,7 +94,7 @@ struct Cfg {
   static constexpr int kGTrace = kGMisc + 256;
   static constexpr int kGroupBytes = kGTrace + kTrSlots * 8;
   static constexpr int kBarOff = kGroupOff + 2 * kGroupBytes;
-  static constexpr int kNumBars = 2 * kStages + 4 * 4 + 2;
+  static constexpr int kNumBars = 2 * kStages + 4 * 4 + 2 + 4;
   static constexpr int kSharedOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kSharedOff + 64 + 1024;  // + alignment slack
   static_assert(kCap % kEpiThreads == 0, "capacity");
@@ -110,6 +122,7 @@ struct Misc {
   int scan[4];
   uint32_t rmin[4], rmax[4];
   int wcnt[2][4];   // [token][epilogue warp] entries in the warp's region
+  int mx_ok;        // the raw pages of the stage being re-encoded arrived
 };
 static_assert(sizeof(Misc) <= 256, "misc block");
 
@@ -132,6 +145,7 @@ struct Smem {
   uint64_t* qfull;   // [4] q slot 2j + b of stream j
   uint64_t* qempty;  // [4]
   uint64_t* done;    // [2] each stream's MMAs complete
+  uint64_t* conv;    // [4] (MXFP4 keys) stream j's tile written (j), consumed (2 + j)
   Misc* misc;
   CtaShared* cs;
   uint64_t* trace;   // this stream's trace slots (shared memory, copied out at exit), or nullptr
@@ -160,6 +174,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, int group) {
   s.qfull = s.tempty + 4;
   s.qempty = s.qfull + 4;
   s.done = s.qempty + 4;
+  s.conv = s.done + 2;
   s.cs = reinterpret_cast<CtaShared*>(base + C::kSharedOff);
   s.group = group;
   return s;
@@ -241,10 +256,20 @@ __device__ __forceinline__ TilePages tile_check(const ScoreParams& p, const Tile
   return tp;
 }
 
-template <int G>
+// MXFP4 keys: stream j's MMA tile at kv + 16384 j, its raw slots (stage
+// index of the ring, as for fp8 stages) from kv + kMxRawOff on.
+constexpr int kMxRawOff = 2 * 16384;
+constexpr int kMxRawSlot = 2 * kMxPageBytes;  // 8704
+__device__ __forceinline__ uint8_t* mx_raw_slot(const Smem& s, int stage) {
+  return s.kv + kMxRawOff + stage * kMxRawSlot;
+}
+
+template <int G, bool kMx>
 __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Smem& s,
                          const Stream& st) {
   using C = Cfg<G>;
+  static_assert(!kMx || (G == 1 && kMxRawOff + C::kStages * kMxRawSlot <= C::kStages * 16384),
+                "MXFP4 tiles and raw slots fit the stage area");
   constexpr int S = C::kStreamStages;
   volatile int* abort_flag = &s.cs->abort_flag;
   const int j = stream_of<G>(s);
@@ -309,17 +334,24 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
       break;
     uint32_t bytes = 0;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) bytes += cur.pid[h] >= 0 ? kPageValueBytes + 256 : 0;
+    for (int h = 0; h < 2; ++h)
+      bytes += cur.pid[h] >= 0 ? (kMx ? kMxPageBytes : kPageValueBytes + 256) : 0;
     if (t == st.t0) trace_set(s, kTrFirstTma, globaltimer_ns());
     mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (cur.pid[h] < 0) continue;
-      tma_load_3d_hint(kv + stage * 16384 + h * kPageValueBytes, map, 0, 0, cur.pid[h],
+      if constexpr (kMx) {
+        bulk_load_hint(mx_raw_slot(s, j * S + stage) + h * kMxPageBytes,
+                       p.cache + static_cast<int64_t>(cur.pid[h]) * kMxPageBytes, kMxPageBytes,
                        &full[stage], stream_policy);
-      bulk_load_hint(scales + stage * 128 + h * 64,
-                     p.cache + static_cast<int64_t>(cur.pid[h]) * kPageBytes + kPageValueBytes,
-                     256, &full[stage], stream_policy);
+      } else {
+        tma_load_3d_hint(kv + stage * 16384 + h * kPageValueBytes, map, 0, 0, cur.pid[h],
+                         &full[stage], stream_policy);
+        bulk_load_hint(scales + stage * 128 + h * 64,
+                       p.cache + static_cast<int64_t>(cur.pid[h]) * kPageBytes + kPageValueBytes,
+                       256, &full[stage], stream_policy);
+      }
     }
     // the next tile's block-table entries, read after this tile's copies are
     // issued (checked when that tile is issued)
@@ -344,7 +376,7 @@ __device__ void producer(const ScoreParams& p, const CUtensorMap* map, const Sme
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread per stream)
 // ---------------------------------------------------------------------------
-template <int G>
+template <int G, bool kMx>
 __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, const Stream& st) {
   using C = Cfg<G>;
   constexpr int S = C::kStreamStages;
@@ -376,19 +408,23 @@ __device__ void mma_issuer(const ScoreParams& p, const Smem& s, uint32_t tmem, c
     }
     const int acc = 2 * j + static_cast<int>(k & 1);
     const uint32_t acc_par = static_cast<uint32_t>((k >> 1) & 1);
-    if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_error, p.wait_ns)) break;
+    // the keys are in shared memory: copied (fp8), or re-encoded into the
+    // stream's tile (MXFP4)
+    if (!mbar_wait(kMx ? &s.conv[j] : &full[stage], kMx ? static_cast<uint32_t>(k & 1) : phase,
+                   abort_flag, p.dev_error, p.wait_ns))
+      break;
     // (an accumulator's first use needs no wait)
     if (k >= 2 && !mbar_wait(&s.tempty[acc], acc_par ^ 1, abort_flag, p.dev_error, p.wait_ns)) break;
     tc_fence_after();
     if (k == 0) trace_set(s, kTrFirstMma, globaltimer_ns());
-    const uint32_t a_base = smem_u32(kv + stage * 16384);
+    const uint32_t a_base = smem_u32(kMx ? s.kv + j * 16384 : kv + stage * 16384);
     const uint32_t b_base = smem_u32(s.q + (2 * j + qslot) * G * kQRowBytes);
     const uint32_t d = tmem + static_cast<uint32_t>(acc * C::N);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       mma_f8(d, sw128_kmajor_desc(a_base + kk * 32), sw128_kmajor_desc(b_base + kk * 32),
              C::kIdesc, kk > 0 ? 1u : 0u);
-    mma_commit(&empty[stage]);
+    mma_commit(kMx ? &s.conv[2 + j] : &empty[stage]);  // (MXFP4: the stream's tile is free)
     mma_commit(&s.tfull[acc]);
     issued = true;
     if (++stage == S) {
@@ -764,13 +800,107 @@ __device__ void finalize_segment(const ScoreParams& p, const Smem& s, int v, int
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4 keys: re-encoding a stage for the fp8 MMA
+// ---------------------------------------------------------------------------
+
+// 2^e as fp32 (0 below the subnormal range), built from its bits.
+__device__ __forceinline__ float pow2f(int e) {
+  if (e >= -126) return __int_as_float((e + 127) << 23);
+  if (e >= -149) return __int_as_float(1 << (e + 149));
+  return 0.f;
+}
+
+// e4m3 codes of the e2m1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 scaled by
+// 2^t, as two words (codes of magnitudes 0-3, 4-7) for byte permutes. For
+// t >= -5 every scaled magnitude is an e4m3 normal (or 0) and its code is the
+// unscaled code with t added to the exponent field; below, the scaled values
+// are rounded to e4m3.
+__device__ __forceinline__ uint2 mx_lut(int t) {
+  constexpr uint32_t kLo = 0x3C383000u;  // 1.5, 1, 0.5, 0
+  constexpr uint32_t kHi = 0x4C484440u;  // 6, 4, 3, 2
+  if (t >= -5) {
+    const uint32_t d = static_cast<uint32_t>(t * 8);  // per-byte exponent step, no carries
+    return make_uint2(kLo + d * 0x01010100u, kHi + d * 0x01010101u);
+  }
+  const float u = pow2f(t);
+  const uint32_t lo = static_cast<uint32_t>(cvt_e4m3x2(0.f, 0.5f * u)) |
+                      (static_cast<uint32_t>(cvt_e4m3x2(u, 1.5f * u)) << 16);
+  const uint32_t hi = static_cast<uint32_t>(cvt_e4m3x2(2.f * u, 3.f * u)) |
+                      (static_cast<uint32_t>(cvt_e4m3x2(4.f * u, 6.f * u)) << 16);
+  return make_uint2(lo, hi);
+}
+
+// The epilogue group re-encodes tile c of stream j (raw slot `stage`, whose
+// pages landed with phase `phase`) into the stream's MMA tile once the MMA
+// of tile c - 1 has released it: thread et writes key et's 128 e4m3 codes
+// as row et of the swizzled tile (16-byte chunk c at c ^ (et mod 8)) and the
+// key's scale, makes them visible to the tensor cores, and its warp counts
+// in on the tile and on the raw slot. Returns false (in every thread of the
+// group alike) when a wait gave up.
+template <int G>
+__device__ bool mx_convert(const ScoreParams& p, const Smem& s, int j, int64_t c, int stage,
+                           uint32_t phase, volatile int* abort_flag) {
+  const int et = epi_tid();
+  const int lane = threadIdx.x & 31;
+  if (et == 0)
+    s.misc->mx_ok =
+        mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error, p.wait_ns) &&
+                (c == 0 || mbar_wait(&s.conv[2 + j], static_cast<uint32_t>((c - 1) & 1),
+                                     abort_flag, p.dev_error, p.wait_ns))
+            ? 1
+            : 0;
+  epi_sync();
+  const bool wok = s.misc->mx_ok != 0;
+  uint8_t* tile = s.kv + j * 16384;
+  const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+      mx_raw_slot(s, stage) + (et >> 6) * kMxPageBytes + (et & 63) * kMxTokenBytes);
+  uint32_t w[17];
+#pragma unroll
+  for (int i = 0; i < 17; ++i) w[i] = wok ? raw[i] : 0u;
+  if (wok) {
+    const uint32_t e = w[16];
+    const int eb[4] = {static_cast<int>(e & 255u), static_cast<int>((e >> 8) & 255u),
+                       static_cast<int>((e >> 16) & 255u), static_cast<int>(e >> 24)};
+    const int emax = max(max(eb[0], eb[1]), max(eb[2], eb[3]));
+    s.scales[stage * 128 + et] = pow2f(emax - 133);
+    uint2 lut[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) lut[b] = mx_lut(6 + eb[b] - emax);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t x = w[2 * c + h];
+        const uint2 l = lut[c >> 1];
+        // magnitudes (bits 0-2 of each nibble) through the table, signs
+        // (bit 3) to bit 7 of each byte
+        o[2 * h] = __byte_perm(l.x, l.y, x & 0x7777u) |
+                   __byte_perm(0x8000u, 0u, (x >> 3) & 0x1111u);
+        o[2 * h + 1] = __byte_perm(l.x, l.y, (x >> 16) & 0x7777u) |
+                       __byte_perm(0x8000u, 0u, (x >> 19) & 0x1111u);
+      }
+      *reinterpret_cast<uint4*>(tile + et * 128 + ((c ^ (et & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    fence_proxy_async_shared();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    mbar_arrive(&s.conv[j]);       // the tile is ready for the MMA
+    mbar_arrive(&s.empty[stage]);  // the raw slot is free
+  }
+  return wok;
+}
+
+// ---------------------------------------------------------------------------
 // epilogue group: one stream's tiles
 // ---------------------------------------------------------------------------
 
 // Streams epilogue group j's tiles (stream j of the CTA) through the score
 // and the streaming top-k, finalising each work row's segment as it ends.
 // Returns false when a pipeline wait gave up. All threads of the group.
-template <int G, bool kLogits>
+template <int G, bool kLogits, bool kMx>
 __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, const Stream (&st)[2],
                          int j) {
   using C = Cfg<G>;
@@ -832,9 +962,23 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
   begin_row();
 
   bool ok = true;
+  // MXFP4 keys: tile k + 1 is re-encoded before tile k is scored (the MMA
+  // of tile k, which it waits for, was enabled one iteration earlier)
+  if constexpr (kMx) {
+    if (t0 < t1)
+      ok = mx_convert<G>(p, s, j, 0, j * S, 0u, abort_flag);
+  }
   long long cyc[5] = {0, 0, 0, 0, 0};  // per-phase clock totals (trace only)
-  for (int64_t k = 0; t0 + k < t1; ++k) {
+  for (int64_t k = 0; (kMx ? ok : true) && t0 + k < t1; ++k) {
     const int64_t t = t0 + k;
+    if constexpr (kMx) {
+      const int64_t c = k + 1;
+      if (t0 + c < t1 && !mx_convert<G>(p, s, j, c, j * S + static_cast<int>(c % S),
+                                        static_cast<uint32_t>((c / S) & 1), abort_flag)) {
+        ok = false;
+        break;
+      }
+    }
     if (t >= re) {
       publish_counts();
       if (!kLogits) finalize_segment<G>(p, s, v, w, wr, active, rs, re, t0, t1);
@@ -856,7 +1000,9 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
     // lane 0 of each warp waits for the stage (scales) and the accumulator
     bool wok = true;
     if (lane == 0)
-      wok = mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error, p.wait_ns) &&
+      // (MXFP4: the group wrote the scales itself; the raw slot may be
+      // holding a later tile already)
+      wok = (kMx || mbar_wait(&s.full[stage], phase, abort_flag, p.dev_error, p.wait_ns)) &&
             mbar_wait(&s.tfull[acc], acc_par, abort_flag, p.dev_error, p.wait_ns);
     wok = __shfl_sync(0xffffffffu, wok ? 1 : 0, 0) != 0;
     __syncwarp();
@@ -902,7 +1048,7 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&s.tempty[acc]);
-        mbar_arrive(&s.empty[stage]);
+        if (!kMx) mbar_arrive(&s.empty[stage]);
       }
     }
     const long long c3 = tr ? clock64() : 0;
@@ -976,7 +1122,7 @@ __device__ bool epilogue(const ScoreParams& p, const Smem& s, uint32_t tmem, con
   return ok;
 }
 
-template <int G, bool kLogits>
+template <int G, bool kLogits, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     score_select_kernel(const __grid_constant__ ScoreParams p,
                         const __grid_constant__ CUtensorMap map) {
@@ -991,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Shared-memory setup needs nothing from earlier kernels; everything after
   // pdl_wait() may read what they wrote.
-  if (warp == 0 && lane == 0) prefetch_tensormap(&map);
+  if (!kMx && warp == 0 && lane == 0) prefetch_tensormap(&map);  // (MXFP4 pages: bulk copies)
   pdl_wait();
 
   // With fewer tiles than virtual CTAs only the first T take part, so that
@@ -1016,8 +1162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
-      // the MMA's commit + the warps of the groups consuming the stage
-      mbar_init(&s.empty[i], 1 + 4 * C::kGroupsPerStream);
+      // the MMA's commit + the warps of the groups consuming the stage (MXFP4
+      // raw slots: the converting group's warps)
+      mbar_init(&s.empty[i], kMx ? 4 : 1 + 4 * C::kGroupsPerStream);
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(&s.tfull[a], 1);
@@ -1026,6 +1173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s.qempty[a], 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(s.done + i, 1);
+    if constexpr (kMx) {
+      for (int i = 0; i < 2; ++i) mbar_init(&s.conv[i], 4);      // stream i's tile written
+      for (int i = 2; i < 4; ++i) mbar_init(&s.conv[i], 1);      // ... and consumed (MMA)
+    }
     s.cs->abort_flag = 0;
     s.cs->epi_done = 0;
     for (int gi = 0; gi < 2; ++gi) {
@@ -1050,12 +1201,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one lane runs the role; the warp reconverges before the block barrier
     const bool has_tiles = part[js] && st[js].t1 > st[js].t0;
     if (lane == 0 && has_tiles) {
-      if (warp & 1) mma_issuer<G>(p, s, tmem, st[js]);
-      else producer<G>(p, &map, s, st[js]);
+      if (warp & 1) mma_issuer<G, kMx>(p, s, tmem, st[js]);
+      else producer<G, kMx>(p, &map, s, st[js]);
     }
     __syncwarp();
   } else {
-    epilogue<G, kLogits>(p, s, tmem, st, js);
+    epilogue<G, kLogits, kMx>(p, s, tmem, st, js);
     if (s.trace && epi_tid() == 0) s.trace[kTrFinal] = globaltimer_ns();
   }
   if (threadIdx.x == kEpiBase) *reinterpret_cast<volatile int*>(&s.cs->epi_done) = 1;
@@ -1073,7 +1224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int G, bool kLogits>
+template <int G, bool kLogits, bool kMx>
 idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_ctas, cudaStream_t s) {
   using C = Cfg<G>;
   // the dynamic shared-memory limit is a per-device attribute of the kernel:
@@ -1083,24 +1234,29 @@ idx_status launch_impl(const ScoreParams& p, const CUtensorMap& map, int num_cta
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0) return cuda_status(e != cudaSuccess ? e : cudaErrorInvalidDevice);
   if (dev >= kMaxDevices || !configured[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(score_select_kernel<G, kLogits>,
+    e = cudaFuncSetAttribute(score_select_kernel<G, kLogits, kMx>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return cuda_status(e);
     if (dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
   }
-  return cuda_status(launch_pdl(score_select_kernel<G, kLogits>, num_ctas, kThreads, C::kSmemBytes,
+  return cuda_status(launch_pdl(score_select_kernel<G, kLogits, kMx>, num_ctas, kThreads, C::kSmemBytes,
                                 s, p, map));
 }
 
 }  // namespace
 
-idx_status launch_score(int G, bool logits, const ScoreParams& p, const CUtensorMap& map,
+idx_status launch_score(int G, bool logits, bool mx, const ScoreParams& p, const CUtensorMap& map,
                         int num_ctas, cudaStream_t s) {
+  if (mx) {  // MXFP4 keys: one-token work rows
+    if (G != 1) return IDX_ERR_UNSUPPORTED;
+    return logits ? launch_impl<1, true, true>(p, map, num_ctas, s)
+                  : launch_impl<1, false, true>(p, map, num_ctas, s);
+  }
   switch (G) {
-    case 1: return logits ? launch_impl<1, true>(p, map, num_ctas, s)
-                          : launch_impl<1, false>(p, map, num_ctas, s);
-    case 2: return logits ? launch_impl<2, true>(p, map, num_ctas, s)
-                          : launch_impl<2, false>(p, map, num_ctas, s);
+    case 1: return logits ? launch_impl<1, true, false>(p, map, num_ctas, s)
+                          : launch_impl<1, false, false>(p, map, num_ctas, s);
+    case 2: return logits ? launch_impl<2, true, false>(p, map, num_ctas, s)
+                          : launch_impl<2, false, false>(p, map, num_ctas, s);
     default: return IDX_ERR_UNSUPPORTED;
   }
 }

@@ -37,6 +37,8 @@ NUM_HEADS = 64
 HEAD_DIM = 128
 PAGE_TOKENS = 64
 PAGE_BYTES = PAGE_TOKENS * (HEAD_DIM + 4)
+MX_TOKEN_BYTES = HEAD_DIM // 2 + HEAD_DIM // 32   # packed e2m1 values + ue8m0 block scales
+MX_PAGE_BYTES = PAGE_TOKENS * MX_TOKEN_BYTES
 SCALE_OFFSET = PAGE_TOKENS * HEAD_DIM
 TOPK = 2048
 MASTER_SEED = 0x5EED
@@ -204,6 +206,40 @@ def make_decode_from_lens(seq_lens, decode_lens, next_n: int, seed: int = MASTER
 
     fill_cache(cache, g, bias)
     return DecodeInputs(q=q, w=w, cache=cache,
+                        block_table=torch.from_numpy(bt).to(device),
+                        seq_lens=torch.from_numpy(seq_lens).to(device),
+                        decode_lens=torch.from_numpy(decode_lens).to(device),
+                        next_n=next_n, topk=topk)
+
+
+def make_decode_mxfp4_from_lens(seq_lens, decode_lens, next_n: int, seed: int = MASTER_SEED,
+                                device="cpu", topk: int = TOPK,
+                                scale_exponents=(124, 127)) -> DecodeInputs:
+    """Decode inputs whose cache holds MXFP4 index keys: pages of 64 entries
+    of 68 bytes (64 bytes of packed e2m1 codes, element 2i in the low nibble of
+    byte i, then 4 ue8m0 block scales), uint8 [P, 4352]. Every value byte is
+    uniform (each e2m1 code equally likely) and every block scale exponent is
+    uniform in the inclusive range `scale_exponents`. q, weights and the page
+    table are drawn as for the fp8 cache."""
+    device = torch.device(device)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    decode_lens = np.asarray(decode_lens, dtype=np.int32)
+    rows = len(seq_lens) * next_n
+    g = _gen(device, seed * 7919 + 23)
+    q = torch.randn((rows, NUM_HEADS, HEAD_DIM), generator=g, device=device).to(torch.bfloat16)
+    w = torch.randn((rows, NUM_HEADS), generator=g, device=device) / 8.0
+    bt, P, _, _ = page_table(seq_lens, seed)
+    cache = torch.empty((P, PAGE_TOKENS, MX_TOKEN_BYTES), dtype=torch.uint8, device=device)
+    lo, hi = scale_exponents
+    for p0 in range(0, P, 8192):
+        p1 = min(P, p0 + 8192)
+        cache[p0:p1, :, :HEAD_DIM // 2] = torch.randint(
+            0, 256, (p1 - p0, PAGE_TOKENS, HEAD_DIM // 2), generator=g, device=device,
+            dtype=torch.int32).to(torch.uint8)
+        cache[p0:p1, :, HEAD_DIM // 2:] = torch.randint(
+            lo, hi + 1, (p1 - p0, PAGE_TOKENS, HEAD_DIM // 32), generator=g, device=device,
+            dtype=torch.int32).to(torch.uint8)
+    return DecodeInputs(q=q, w=w, cache=cache.view(P, MX_PAGE_BYTES),
                         block_table=torch.from_numpy(bt).to(device),
                         seq_lens=torch.from_numpy(seq_lens).to(device),
                         decode_lens=torch.from_numpy(decode_lens).to(device),

@@ -220,3 +220,12 @@ def test_key_sharded_argument_validation(lib):
     assert m(FAKE, FAKE, 0, 4, 64, FAKE, None, None) == 1
     assert m(None, FAKE, 2, 4, 64, FAKE, None, None) == 1
     assert m(FAKE, FAKE, 2, 0, 64, FAKE, None, None) == 0
+
+
+def test_mxfp4_argument_validation(lib):
+    f = lib.indexer_decode_topk_mxfp4
+    args = [FAKE, FAKE, FAKE, 10, FAKE, 4, 4, FAKE, 2]
+    tail = [64, 128, 2048, FAKE, FAKE, 16, None, None]
+    assert f(*args, 2, *tail) == 2                    # next_n must be 1
+    assert f(*args, 1, *tail) == 3                    # valid up to the workspace size
+    assert f(FAKE, FAKE, FAKE + 8, 10, FAKE, 4, 4, FAKE, 2, 1, *tail) == 1   # cache alignment
