@@ -813,15 +813,16 @@ __device__ __forceinline__ float pow2f(int e) {
 // e4m3 codes of the e2m1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 scaled by
 // 2^t, as two words (codes of magnitudes 0-3, 4-7) for byte permutes. For
 // t >= -5 every scaled magnitude is an e4m3 normal (or 0) and its code is the
-// unscaled code with t added to the exponent field; below, the scaled values
-// are rounded to e4m3.
+// unscaled code with t added to the exponent field (mx_lut); below, the
+// scaled values are rounded to e4m3 (mx_lut_small, out of line: rare).
 __device__ __forceinline__ uint2 mx_lut(int t) {
   constexpr uint32_t kLo = 0x3C383000u;  // 1.5, 1, 0.5, 0
   constexpr uint32_t kHi = 0x4C484440u;  // 6, 4, 3, 2
-  if (t >= -5) {
-    const uint32_t d = static_cast<uint32_t>(t * 8);  // per-byte exponent step, no carries
-    return make_uint2(kLo + d * 0x01010100u, kHi + d * 0x01010101u);
-  }
+  const uint32_t d = static_cast<uint32_t>(t * 8);  // per-byte exponent step, no carries
+  return make_uint2(kLo + d * 0x01010100u, kHi + d * 0x01010101u);
+}
+
+__device__ __noinline__ uint2 mx_lut_small(int t) {
   const float u = pow2f(t);
   const uint32_t lo = static_cast<uint32_t>(cvt_e4m3x2(0.f, 0.5f * u)) |
                       (static_cast<uint32_t>(cvt_e4m3x2(u, 1.5f * u)) << 16);
@@ -864,8 +865,16 @@ __device__ bool mx_convert(const ScoreParams& p, const Smem& s, int j, int64_t c
     const int emax = max(max(eb[0], eb[1]), max(eb[2], eb[3]));
     s.scales[stage * 128 + et] = pow2f(emax - 133);
     uint2 lut[4];
+    const int emin = min(min(eb[0], eb[1]), min(eb[2], eb[3]));
+    if (6 + emin - emax >= -5) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) lut[b] = mx_lut(6 + eb[b] - emax);
+      for (int b = 0; b < 4; ++b) lut[b] = mx_lut(6 + eb[b] - emax);
+    } else {
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        lut[b] = 6 + eb[b] - emax >= -5 ? mx_lut(6 + eb[b] - emax)
+                                        : mx_lut_small(6 + eb[b] - emax);
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       uint32_t o[4];
@@ -874,11 +883,11 @@ __device__ bool mx_convert(const ScoreParams& p, const Smem& s, int j, int64_t c
         const uint32_t x = w[2 * c + h];
         const uint2 l = lut[c >> 1];
         // magnitudes (bits 0-2 of each nibble) through the table, signs
-        // (bit 3) to bit 7 of each byte
-        o[2 * h] = __byte_perm(l.x, l.y, x & 0x7777u) |
-                   __byte_perm(0x8000u, 0u, (x >> 3) & 0x1111u);
-        o[2 * h + 1] = __byte_perm(l.x, l.y, (x >> 16) & 0x7777u) |
-                       __byte_perm(0x8000u, 0u, (x >> 19) & 0x1111u);
+        // (bit 3) to bit 7 of each byte (a permute reads the low 16 bits of
+        // its selector)
+        const uint32_t mag = x & 0x77777777u, sgn = (x >> 3) & 0x11111111u;
+        o[2 * h] = __byte_perm(l.x, l.y, mag) | __byte_perm(0x8000u, 0u, sgn);
+        o[2 * h + 1] = __byte_perm(l.x, l.y, mag >> 16) | __byte_perm(0x8000u, 0u, sgn >> 16);
       }
       *reinterpret_cast<uint4*>(tile + et * 128 + ((c ^ (et & 7)) << 4)) =
           make_uint4(o[0], o[1], o[2], o[3]);
