@@ -41,6 +41,19 @@ def check_topk_row(sel, logits, tol_a, tol_b, k, length):
     return int((~must & ~never).sum())
 
 
+def relative_error_where_uncancelled(gpu, logits, tol_a):
+    """max |gpu - oracle| / |logit| over keys whose |logit| >= A / 2 (head
+    terms of one sign dominate, so A is within 2x of |logit| and the band's
+    1e-3 of A is the stated 1e-3 relative to the logit), and how many keys
+    that covers."""
+    gpu = np.asarray(gpu, np.float64)
+    o = np.asarray(logits, np.float64)
+    sel = (np.abs(o) >= 0.5 * np.asarray(tol_a)) & (o != 0)
+    if not sel.any():
+        return 0.0, 0
+    return float((np.abs(gpu[sel] - o[sel]) / np.abs(o[sel])).max()), int(sel.sum())
+
+
 def check_logits(gpu, logits, tol_a, tol_b):
     gpu = np.asarray(gpu, np.float64)
     err = np.abs(gpu - logits)

@@ -12,7 +12,7 @@ import torch
 import oracle
 import synth
 import sparse_attention_indexer_block_gb300 as saib
-from _util import check_logits, check_topk_row
+from _util import check_logits, check_topk_row, relative_error_where_uncancelled
 
 pytestmark = pytest.mark.gpu
 
@@ -51,10 +51,13 @@ def test_mxfp4_logits_match_oracle(exps):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     lg = lg.cpu().numpy()
-    worst = 0.0
+    worst = rel = 0.0
     for r, (o, a, b) in enumerate(_oracle(d, seq, range(len(seq)))):
         worst = max(worst, check_logits(lg[r, :seq[r]], o, a, b))
-    print(f"max |gpu - oracle| / (A + 0.01 B): {worst:.3g}")
+        rel = max(rel, relative_error_where_uncancelled(lg[r, :seq[r]], o, a)[0])
+    print(f"max |gpu - oracle| / (A + 0.01 B): {worst:.3g}; / |logit| where |logit| >= A/2: "
+          f"{rel:.3g}")
+    assert rel <= 1e-3
 
 
 def test_mxfp4_topk_matches_oracle():

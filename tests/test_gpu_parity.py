@@ -12,7 +12,7 @@ import torch
 import oracle
 import synth
 import sparse_attention_indexer_block_gb300 as saib
-from _util import check_logits, check_topk_row
+from _util import check_logits, check_topk_row, relative_error_where_uncancelled
 
 pytestmark = pytest.mark.gpu
 
@@ -163,10 +163,16 @@ def _check_logits_case(d):
     lens_h = lens.cpu().numpy()
     _, lg, ta, tb, rows = _oracle_rows(d, lens_h, 2048)
     g = lg_gpu.cpu().numpy()
-    worst = 0.0
+    worst = rel = 0.0
+    n_rel = 0
     for i, r in enumerate(rows):
         L = int(lens_h[r])
         worst = max(worst, check_logits(g[r, :L], lg[i], ta[i], tb[i]))
+        e, n = relative_error_where_uncancelled(g[r, :L], lg[i], ta[i])
+        rel, n_rel = max(rel, e), n_rel + n
+    # the method's "1e-3 relative", shown directly where |logit| is close to A
+    print(f"max |err| / |logit| over {n_rel} keys with |logit| >= A / 2: {rel:.3g}")
+    assert rel <= 1e-3
     return worst
 
 
