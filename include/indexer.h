@@ -466,6 +466,16 @@ idx_status indexer_trace_buffer(void* buffer, size_t bytes);
 idx_status indexer_debug_wait_limit(uint64_t limit_ns, int32_t stall_split_rows);
 
 /*
+ * Test hook for indexer_insert_keys's division: for n pairs (a[i], b[i])
+ * (float, device) writes the quotient the insert computes (the correctly
+ * rounded reciprocal of b and two correction steps when b >= 2^-100, else
+ * the IEEE division) to quotient[i] and the IEEE round-to-nearest quotient
+ * to quotient_ieee[i], so that tests can compare them.
+ */
+idx_status indexer_debug_divide(const float* a, const float* b, int64_t n, float* quotient,
+                                float* quotient_ieee, void* stream);
+
+/*
  * indexer_decode_topk without a caller workspace. The pages have no
  * counterpart: this is a convenience of this library.
  *

@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     indexer_prefill_workspace_bytes,
     indexer_profile_events,
     indexer_trace_buffer,
+    indexer_debug_divide,
     indexer_debug_wait_limit,
     indexer_debug_decode_plan,
     indexer_quantize_q,

@@ -49,6 +49,7 @@ SIGNATURES = {
     "indexer_profile_events": (C.c_int, [_P, _P]),
     "indexer_trace_buffer": (C.c_int, [_P, _SZ]),
     "indexer_debug_wait_limit": (C.c_int, [C.c_uint64, _I32]),
+    "indexer_debug_divide": (C.c_int, [_P, _P, _I64, _P, _P, _P]),
     "indexer_debug_decode_plan": (C.c_int, [_I32, _I32, _I32, C.POINTER(_I64),
                                             C.POINTER(_I32), C.POINTER(_I32)]),
     "indexer_decode_topk_noalloc": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
@@ -446,6 +447,16 @@ def indexer_debug_decode_plan(num_reqs: int, next_n: int, topk: int = MAX_TOPK):
            load().indexer_debug_decode_plan(num_reqs, next_n, topk, offs, C.byref(grid), pen))
     names = ("wr_tile_start", "cta_tile", "row_ctas", "cta_row")
     return dict(zip(names, [int(v) for v in offs])), int(grid.value), (int(pen[0]), int(pen[1]))
+
+
+def indexer_debug_divide(a, b, stream=None):
+    """(the insert's quotient, the IEEE quotient) of float32 tensors a / b."""
+    q = torch.empty_like(a)
+    qi = torch.empty_like(a)
+    st = load().indexer_debug_divide(_ptr(a), _ptr(b), int(a.numel()), _ptr(q), _ptr(qi),
+                                     _stream(stream))
+    _check("indexer_debug_divide", st)
+    return q, qi
 
 
 def indexer_debug_wait_limit(limit_ns: int = 0, stall_split_rows: bool = False):

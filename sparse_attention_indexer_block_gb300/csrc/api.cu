@@ -362,6 +362,14 @@ idx_status indexer_debug_wait_limit(uint64_t limit_ns, int32_t stall_split_rows)
   return IDX_OK;
 }
 
+idx_status indexer_debug_divide(const float* a, const float* b, int64_t n, float* quotient,
+                                float* quotient_ieee, void* stream) {
+  if (n < 0) return IDX_ERR_INVALID_ARG;
+  if (n == 0) return IDX_OK;
+  if (!a || !b || !quotient || !quotient_ieee) return IDX_ERR_INVALID_ARG;
+  return launch_divide_check(a, b, n, quotient, quotient_ieee, static_cast<cudaStream_t>(stream));
+}
+
 idx_status indexer_profile_events(void* start_event, void* stop_event) {
   g_prof_start = static_cast<cudaEvent_t>(start_event);
   g_prof_stop = static_cast<cudaEvent_t>(stop_event);

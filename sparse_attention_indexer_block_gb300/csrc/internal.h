@@ -167,6 +167,10 @@ idx_status launch_expand(const int32_t* seq_lens, const int32_t* decode_lens, in
 idx_status launch_insert_keys(const __nv_bfloat16* k, const int64_t* slots, int64_t n,
                               uint8_t* cache, int64_t num_pages, uint32_t* err, cudaStream_t s);
 
+// Test hook: the insert's quotient and the IEEE quotient of n pairs.
+idx_status launch_divide_check(const float* a, const float* b, int64_t n, float* fast, float* ieee,
+                               cudaStream_t s);
+
 idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows,
                                  uint8_t* q8, float* wprime, cudaStream_t s);
 

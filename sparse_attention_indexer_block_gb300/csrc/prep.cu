@@ -555,6 +555,24 @@ __global__ void __launch_bounds__(kPrepThreads) expand_kernel(
   }
 }
 
+// Correctly rounded a / b from the correctly rounded reciprocal y = RN(1 / b)
+// by Markstein's correction (IBM J. Res. Dev. 34(1), 1990): when q is within
+// one ulp of a / b, r = a - b q is exact as one fused multiply-add and
+// RN(q + r y) is the correctly rounded quotient. q0 = RN(a y) can be up to
+// about 1.5 ulp off (a / b just below a power of two), so one correction
+// first brings it within one ulp (its residual is still exact: |q0 - a / b|
+// stays within 2 ulp) and a second one rounds it correctly. The residuals
+// are exact only without underflow. In the cache insert |a| <= 448 b, so
+// nothing overflows; with b >= 2^-100 every quotient of magnitude >= 2^-10
+// (the ones an e4m3 code depends on: smaller ones are code 0) has a normal
+// a and exact residuals; a smaller b takes the IEEE division.
+__device__ __forceinline__ float div_rn_recip(float a, float b, float y) {
+  const float q0 = __fmul_rn(a, y);
+  const float q1 = __fmaf_rn(__fmaf_rn(-b, q0, a), y, q0);
+  return __fmaf_rn(__fmaf_rn(-b, q1, a), y, q1);
+}
+constexpr float kRecipDivMin = 0x1p-100f;  // smallest divisor of the reciprocal path
+
 // Index-key cache insert: token i's 128 bf16 values are quantised with their
 // own fp32 scale amax / 448 (correctly rounded) into e4m3 codes of x / scale
 // (correctly rounded quotient, round-to-nearest-even, saturating) and written
@@ -603,15 +621,40 @@ __global__ void __launch_bounds__(kPrepThreads) insert_keys_kernel(
       uint32_t codes = 0u;
       if (amax > 0.0f) {
         scale = __fdiv_rn(amax, 448.0f);
-        codes = static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale))) |
-                (static_cast<uint32_t>(cvt_e4m3x2(__fdiv_rn(x2, scale), __fdiv_rn(x3, scale)))
-                 << 16);
+        float q0, q1, q2, q3;
+        if (scale >= kRecipDivMin) {  // warp-uniform (one scale per token)
+          const float y = __frcp_rn(scale);
+          q0 = div_rn_recip(x0, scale, y);
+          q1 = div_rn_recip(x1, scale, y);
+          q2 = div_rn_recip(x2, scale, y);
+          q3 = div_rn_recip(x3, scale, y);
+        } else {
+          q0 = __fdiv_rn(x0, scale);
+          q1 = __fdiv_rn(x1, scale);
+          q2 = __fdiv_rn(x2, scale);
+          q3 = __fdiv_rn(x3, scale);
+        }
+        codes = static_cast<uint32_t>(cvt_e4m3x2(q0, q1)) |
+                (static_cast<uint32_t>(cvt_e4m3x2(q2, q3)) << 16);
       }
       uint8_t* page = cache + (sl[u] / kPageTokens) * kPageBytes;
       const int tok = static_cast<int>(sl[u] % kPageTokens);
       *reinterpret_cast<uint32_t*>(page + tok * kDim + 4 * lane) = codes;
       if (lane == 0) *reinterpret_cast<float*>(page + kPageValueBytes + tok * 4) = scale;
     }
+  }
+}
+
+// Test hook: both quotients of each pair (the insert's and the IEEE one).
+__global__ void __launch_bounds__(kPrepThreads) divide_check_kernel(const float* a, const float* b,
+                                                                    int64_t n, float* fast,
+                                                                    float* ieee) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kPrepThreads;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x; i < n;
+       i += stride) {
+    fast[i] = b[i] >= kRecipDivMin ? div_rn_recip(a[i], b[i], __frcp_rn(b[i]))
+                                   : __fdiv_rn(a[i], b[i]);
+    ieee[i] = __fdiv_rn(a[i], b[i]);
   }
 }
 
@@ -638,6 +681,13 @@ idx_status launch_insert_keys(const __nv_bfloat16* k, const int64_t* slots, int6
                               uint8_t* cache, int64_t num_pages, uint32_t* err, cudaStream_t s) {
   return cuda_status(launch_pdl(insert_keys_kernel, prep_grid((n + 3) / 4), kPrepThreads, 0, s, k, slots, n,
                     cache, num_pages, err));
+}
+
+idx_status launch_divide_check(const float* a, const float* b, int64_t n, float* fast, float* ieee,
+                               cudaStream_t s) {
+  if (n <= 0) return IDX_OK;
+  divide_check_kernel<<<prep_grid((n + 31) / 32), kPrepThreads, 0, s>>>(a, b, n, fast, ieee);
+  return cuda_status(cudaGetLastError());
 }
 
 idx_status launch_quantize_plain(const __nv_bfloat16* q, const float* w, int64_t rows, uint8_t* q8,

@@ -405,6 +405,43 @@ def test_topk_all_equal_logits_degenerate():
 # index-key cache insert: bit-exact
 # ---------------------------------------------------------------------------
 
+
+
+def test_insert_division_matches_ieee_quotients():
+    # the insert divides each value x (|x| <= 448 s) by its token's scale s
+    # with a reciprocal and two correction steps (s >= 2^-100; the IEEE
+    # division below that). Every quotient an e4m3 code depends on (>= 2^-10
+    # in magnitude; smaller ones are code 0) must equal the IEEE one, over the
+    # insert's range of scales (bf16 tokens: s <= 2^128 / 448) and at the hard
+    # cases: quotients just below powers of two, all-ones significands, exact
+    # quotients and their neighbours, tiny scales and subnormal values.
+    g = torch.Generator(device=DEV).manual_seed(91)
+    n = 1 << 22
+    b = torch.exp2(torch.empty(n, device=DEV).uniform_(-126, 119, generator=g))
+    a = b * torch.empty(n, device=DEV).uniform_(-448, 448, generator=g)
+    ones = torch.tensor([1.9999999, 1.99999988, 1.5, 1.25, 1.0000001], device=DEV)
+    bb = (ones[None, :] * torch.exp2(torch.arange(-110, 110, device=DEV,
+                                                   dtype=torch.float32))[:, None]).reshape(-1)
+    k = torch.arange(1, 449, device=DEV, dtype=torch.float32)
+    a2 = (bb[:, None] * k[None, :]).reshape(-1)                        # exact quotients
+    b2 = bb[:, None].expand(-1, 448).reshape(-1)
+    below = torch.nextafter(torch.exp2(torch.arange(-9, 9, device=DEV, dtype=torch.float32)),
+                            torch.zeros(18, device=DEV))
+    a3 = (below[None, :] * bb[:, None]).reshape(-1)                    # just below 2^e
+    b3 = bb[:, None].expand(-1, 18).reshape(-1)
+    sub = torch.full((1 << 16,), 1e-39, device=DEV) * torch.empty(1 << 16, device=DEV).uniform_(
+        -1, 1, generator=g)                                            # subnormal values
+    bsub = torch.exp2(torch.empty(1 << 16, device=DEV).uniform_(-128, -90, generator=g))
+    cases = ((a, b), (a2, b2), (a3, b3), (torch.nextafter(a2, a2 * 2), b2), (sub, bsub))
+    for x, y in cases:
+        q, qi = saib.indexer_debug_divide(x.contiguous(), y.contiguous())
+        torch.cuda.synchronize()
+        matters = qi.abs() >= 2.0 ** -10
+        bad = ((q.view(torch.int32) != qi.view(torch.int32)) & matters).sum().item()
+        assert bad == 0, f"{bad} of {int(matters.sum())} quotients differ from the IEEE ones"
+        assert bool(((q.abs() < 2.0 ** -10) == ~matters).all())
+
+
 @pytest.mark.parametrize("n", [3, 4999])
 def test_insert_keys_bit_exact(n):
     pages = (n + 63) // 64 + 7
