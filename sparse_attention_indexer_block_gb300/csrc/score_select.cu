@@ -1144,30 +1144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int group = warp < 4 ? (warp >> 1) : epi_group();
   Smem s = carve<G>(base, group);
 
-  // Shared-memory setup needs nothing from earlier kernels; everything after
-  // pdl_wait() may read what they wrote.
+  // The shared-memory setup (barriers, tensor memory) needs nothing from
+  // earlier kernels and overlaps their tail; everything after pdl_wait() may
+  // read what they wrote.
   if (!kMx && warp == 0 && lane == 0) prefetch_tensormap(&map);  // (MXFP4 pages: bulk copies)
-  pdl_wait();
-
-  // With fewer tiles than virtual CTAs only the first T take part, so that
-  // every participating stream owns at least one tile (segment counts rely
-  // on it).
-  const int64_t T = p.wr_tile_start[p.num_wr];
-  const int64_t nV = min(static_cast<int64_t>(C::kStreams * gridDim.x), T);
-  Stream st[2];
-  bool part[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int v = C::kStreams * static_cast<int>(blockIdx.x) + j;
-    part[j] = j < C::kStreams && v < nV;
-    st[j].v = v;
-    st[j].t0 = part[j] ? p.cta_tile[v] : 0;
-    st[j].t1 = part[j] ? p.cta_tile[v + 1] : 0;
-  }
-  // stream of this thread's role (warps 2 and 3 have none when kStreams == 1)
-  const int js = warp < 4 ? (warp >> 1) : stream_of<G>(s);
-  if (!(p.trace && part[js] && token_of<G>(s) == 0)) s.trace = nullptr;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&s.full[i], 1);
@@ -1199,6 +1179,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   named_sync(kSetupBarrier, kThreads);
   tc_fence_after();
+  pdl_wait();
+
+  // With fewer tiles than virtual CTAs only the first T take part, so that
+  // every participating stream owns at least one tile (segment counts rely
+  // on it).
+  const int64_t T = p.wr_tile_start[p.num_wr];
+  const int64_t nV = min(static_cast<int64_t>(C::kStreams * gridDim.x), T);
+  Stream st[2];
+  bool part[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int v = C::kStreams * static_cast<int>(blockIdx.x) + j;
+    part[j] = j < C::kStreams && v < nV;
+    st[j].v = v;
+    st[j].t0 = part[j] ? p.cta_tile[v] : 0;
+    st[j].t1 = part[j] ? p.cta_tile[v + 1] : 0;
+  }
+  // stream of this thread's role (warps 2 and 3 have none when kStreams == 1)
+  const int js = warp < 4 ? (warp >> 1) : stream_of<G>(s);
+  if (!(p.trace && part[js] && token_of<G>(s) == 0)) s.trace = nullptr;
+
   pdl_trigger();
   const uint32_t tmem = s.cs->tmem_base;
   if (warp >= 4 && epi_tid() == 0 && s.trace) {
