@@ -95,6 +95,10 @@ def _load():
         lib.ora_dcp_global_index.argtypes = [i64, i32, i32, i32]
         lib.ora_index_key_count.restype = i64
         lib.ora_index_key_count.argtypes = [i64, i32, i32, i32, i32]
+        lib.ora_block_topk.restype = i32
+        lib.ora_block_topk.argtypes = [P, i64, i32, i32, i32, i32, P, i32]
+        lib.ora_expand_pools.restype = i32
+        lib.ora_expand_pools.argtypes = [P, i32, i64, i32, P, i32]
         lib.ora_merge_candidates.restype = None
         lib.ora_merge_candidates.argtypes = [P, P, i64, i32, P, P]
         _lib = lib
@@ -474,6 +478,31 @@ def dcp_prefill_topk(q_bf16_bits, w, shards, seq_lens, query_start_loc, k: int,
     Returns (idx [rows, k] by (logit desc, index asc), val [rows, k])."""
     req, ln = prefill_rows(seq_lens, query_start_loc)
     return dcp_decode_topk(q_bf16_bits, w, shards, ln, 1, k, interleave, ratio, bt_rows=req)
+
+
+# --------------------------------------------------------------------------
+# block / pool selection
+# --------------------------------------------------------------------------
+
+def block_topk(logits, length: int, block: int, k: int, n_init: int = 0, n_local: int = 0,
+               cap: int | None = None):
+    """Selected blocks of one row (ascending, -1 after) and their count: the
+    first n_init and last n_local blocks of `block` tokens plus the k best of
+    the others by their largest logit."""
+    lg = np.ascontiguousarray(logits, dtype=np.float64)
+    cap = k + n_init + n_local if cap is None else cap
+    out = np.empty(max(cap, 1), np.int32)
+    n = _load().ora_block_topk(_p(lg), length, block, k, n_init, n_local, _p(out), cap)
+    return out[:cap], int(n)
+
+
+def expand_pools(pools, length: int, pool: int, cap: int):
+    """Tokens of the selected complete pools, then the row's tail after its
+    last complete pool (-1 after them), and their count."""
+    pl = np.ascontiguousarray(pools, dtype=np.int32)
+    out = np.empty(max(cap, 1), np.int32)
+    n = _load().ora_expand_pools(_p(pl), pl.shape[0], length, pool, _p(out), cap)
+    return out[:cap], int(n)
 
 
 # --------------------------------------------------------------------------

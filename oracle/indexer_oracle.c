@@ -67,6 +67,12 @@
  *    in global token positions, are merged by the same rule as one row's
  *    top k. The merged set equals the unsharded row's top k, since every
  *    key of the global top k is in its own rank's top k.
+ *  - Block / pool selection (the MiniMax runner's topk_blocks, init_blocks,
+ *    local_blocks; GLM5's pool_topk and expand_pools_and_append_tail, named
+ *    on the pages without their rules): blocks of B tokens scored by their
+ *    largest logit; the first init and last local blocks always kept plus
+ *    the k best of the others; pools expanded to their tokens and the row's
+ *    incomplete last pool appended as its tail.
  *  - Rows with len <= k output [0, 1, ..., len-1, -1, ...]; rows with len > k
  *    output the k indices of the largest logits; ties are broken here by the
  *    smaller index (any k-subset that agrees within the tolerance is accepted
@@ -530,6 +536,65 @@ void ora_merge_candidates(const double* val, const int32_t* idx, int64_t n, int3
     out_val[i] = i < m ? p[i].v : -INFINITY;
   }
   free(p);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block / pool selection                                                    */
+/* ------------------------------------------------------------------------ */
+/* MiniMax runner (topk_blocks, init_blocks, local_blocks) and GLM5
+ * (pool_topk, expand_pools_and_append_tail) select whole blocks of tokens;
+ * the pages give the names only. Reading: a row of L tokens is cut into
+ * nb = ceil(L / B) blocks of B tokens (the last may be partial); a block's
+ * score is the largest logit of its tokens; the selection is the first
+ * n_init blocks, the last n_local blocks and the k highest-scoring of the
+ * others (ties: the smaller block index), out = the selected blocks in
+ * ascending order, -1 after them; returns how many. */
+int32_t ora_block_topk(const double* logits, int64_t L, int32_t B, int32_t k, int32_t n_init,
+                       int32_t n_local, int32_t* out, int32_t out_cap) {
+  const int64_t nb = (L + B - 1) / B;
+  char* sel = (char*)calloc((size_t)(nb > 0 ? nb : 1), 1);
+  ora_pair* p = (ora_pair*)malloc(sizeof(ora_pair) * (size_t)(nb > 0 ? nb : 1));
+  int64_t m = 0;
+  for (int64_t b = 0; b < nb; ++b) {
+    if (b < n_init || b >= nb - n_local) {
+      sel[b] = 1;
+      continue;
+    }
+    double best = -INFINITY;
+    for (int64_t t = b * B; t < L && t < (b + 1) * B; ++t)
+      if (logits[t] > best) best = logits[t];
+    p[m].v = best;
+    p[m].i = (int32_t)b;
+    ++m;
+  }
+  qsort(p, (size_t)m, sizeof(ora_pair), cmp_pair);
+  for (int64_t i = 0; i < m && i < k; ++i) sel[p[i].i] = 1;
+  int32_t n = 0;
+  for (int64_t b = 0; b < nb; ++b)
+    if (sel[b] && n < out_cap) out[n++] = (int32_t)b;
+  for (int32_t i = n; i < out_cap; ++i) out[i] = -1;
+  free(sel);
+  free(p);
+  return n;
+}
+
+/* GLM5 expand_pools_and_append_tail (reading): the tokens of the selected
+ * complete pools (pool b covers [b P, b P + P)), in the order given, then the
+ * row's tail [floor(L / P) P, L) (the tokens after its last complete pool);
+ * a selected pool that is not complete contributes nothing (its tokens are
+ * the tail). -1 after them; returns how many. */
+int32_t ora_expand_pools(const int32_t* pools, int32_t npools, int64_t L, int32_t P,
+                         int32_t* out, int32_t out_cap) {
+  int32_t n = 0;
+  const int64_t full = L / P;
+  for (int32_t i = 0; i < npools; ++i) {
+    const int64_t b = pools[i];
+    if (b < 0 || b >= full) continue;
+    for (int64_t t = b * P; t < (b + 1) * P && n < out_cap; ++t) out[n++] = (int32_t)t;
+  }
+  for (int64_t t = full * P; t < L && n < out_cap; ++t) out[n++] = (int32_t)t;
+  for (int32_t i = n; i < out_cap; ++i) out[i] = -1;
+  return n;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -787,3 +787,49 @@ def test_sharded_prefill_equals_the_unsharded_prefill(world, inter, ratio):
         order = np.lexsort((np.arange(L), -lg))[:n]
         assert np.array_equal(got[i, :n], order) and np.all(got[i, n:] == -1)
         assert np.array_equal(gv[i, :n], lg[order])
+
+
+# --------------------------------------------------------------------------
+# block / pool selection
+# --------------------------------------------------------------------------
+
+def _block_topk_brute(lg, L, B, k, n_init, n_local):
+    nb = -(-L // B)
+    forced = {b for b in range(nb) if b < n_init or b >= nb - n_local}
+    rest = sorted((b for b in range(nb) if b not in forced),
+                  key=lambda b: (-max(lg[b * B:min(L, b * B + B)]), b))
+    return sorted(forced | set(rest[:k]))
+
+
+def test_block_topk_brute_force_and_invariants():
+    rng = np.random.default_rng(21)
+    for L, B, k, ni, nl in [(1, 64, 4, 1, 2), (64, 64, 4, 1, 1), (65, 64, 1, 0, 0), (1000, 64, 5, 1, 2),
+                            (1000, 16, 3, 2, 2), (5000, 64, 16, 1, 4), (300, 7, 100, 0, 0),
+                            (4096, 64, 64, 0, 0)]:
+        lg = np.round(rng.standard_normal(L), 1)           # ties inside and across blocks
+        got, n = oracle.block_topk(lg, L, B, k, ni, nl)
+        ref = _block_topk_brute(lg, L, B, k, ni, nl)
+        assert list(got[:n]) == ref and np.all(got[n:] == -1)
+        nb = -(-L // B)
+        forced = set(range(min(ni, nb))) | set(range(max(0, nb - nl), nb))
+        assert n == len(forced) + min(k, nb - len(forced))   # count
+        assert forced <= set(ref)                             # init and local blocks kept
+
+
+def test_block_topk_hand_case():
+    # blocks of 4: [0 1 2 3] [9 0 0 0] [1 1 1 1] [0 0 5 0] [2]: scores 3, 9, 1, 5, 2
+    lg = np.array([0, 1, 2, 3, 9, 0, 0, 0, 1, 1, 1, 1, 0, 0, 5, 0, 2], np.float64)
+    got, n = oracle.block_topk(lg, 17, 4, 2, 0, 0)
+    assert list(got[:n]) == [1, 3]
+    got, n = oracle.block_topk(lg, 17, 4, 1, 1, 1)         # block 0 and block 4 forced, then 1
+    assert list(got[:n]) == [0, 1, 4]
+
+
+def test_expand_pools_and_tail():
+    # pools of 4 over 10 tokens: complete pools 0, 1; tail 8, 9; pool 2 is the tail
+    out, n = oracle.expand_pools(np.array([1, 0]), 10, 4, 16)
+    assert list(out[:n]) == [4, 5, 6, 7, 0, 1, 2, 3, 8, 9] and np.all(out[n:] == -1)
+    out, n = oracle.expand_pools(np.array([2, -1]), 10, 4, 16)
+    assert list(out[:n]) == [8, 9]
+    out, n = oracle.expand_pools(np.array([0]), 8, 4, 16)   # no tail
+    assert list(out[:n]) == [0, 1, 2, 3]
