@@ -103,6 +103,9 @@ WORKLOAD_DESCS = {
                      "top-2048"),
     "long_mxfp4": ("long context with MXFP4 index keys: 128 requests, next_n 1, seq_len 131072, "
                    "64 index heads x 128, 68-byte e2m1 + ue8m0 keys, top-2048"),
+    "long_blocks": ("long context (128 x 131072 keys, 1% heavy-tail), block selection: the "
+                    "decode logits, then per row the 32 best 64-token blocks by their largest "
+                    "logit plus the first and the last 4 blocks"),
     "dcp_long": ("long context (128 x 131072 keys, 1% heavy-tail) key-sharded over 2 decode-"
                  "context-parallel ranks in runs of 1 token, the ranks run one after the other "
                  "on one GPU: per rank top-2048 with logits over its 65536 keys per row, then "
@@ -608,6 +611,74 @@ def measure_dcp(workload, dcp_world, interleave, seed, dev, steps, world):
             "clocks": clk.summary(), "gpu_launches": (4 * dcp_world + 1) * steps}
 
 
+def measure_blocks(workload, seed, dev, steps, world):
+    """Device-timed block-selection steps (the decode logits, then the block
+    top-k), through the C ABI, in a CUDA graph; the index cache is well above
+    L2."""
+    import torch
+
+    import synth
+    import sparse_attention_indexer_block_gb300 as saib
+
+    d = synth.make_decode(workload, seed=seed, device=dev)
+    R, G, k = d.num_reqs, d.next_n, d.topk
+    assert G == 1
+    seq_h = d.seq_lens.cpu().numpy().astype(np.int64)
+    keys_per_step = int(seq_h.sum())
+    ld = int(d.block_table.shape[1]) * 64
+    logits = torch.empty((R, ld), dtype=torch.float32, device=dev)
+    ws = saib.decode_workspace(R, G, k, dev)
+    B, K, NI, NL = 64, 32, 1, 4
+    out = torch.empty((R, K + NI + NL), dtype=torch.int32, device=dev)
+    cnt = torch.empty(R, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        saib.indexer_decode_logits(d.q, d.w, d.cache, d.block_table, d.seq_lens, 1, k,
+                                   out_logits=logits, workspace=ws, dev_error=err, stream=stream)
+        saib.indexer_block_topk(logits, d.seq_lens, B, K, NI, NL, out=out, cnt=cnt, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} during warm-up (blocks)")
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                step()
+    torch.cuda.synchronize()
+    t_soak = time.time()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        with torch.cuda.stream(stream):
+            while time.time() - t_soak < 1.0:
+                g.replay()
+                stream.synchronize()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks([e0.elapsed_time(e1)], world, dev)[0]
+    peak, peak_kind = measured_peak_gbs()
+    algo = keys_per_step * (PAGE_KEY_BYTES + 8)  # keys, logits written and read back
+    gbs = algo * steps / (ms / 1e3) / 1e9
+    return {"workload": WORKLOAD_DESCS["long_blocks"],
+            "metric_value": whole_job_rate(keys_per_step, steps, world, ms), "unit": "keys/s",
+            "ms_per_step": ms / steps, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None, "peak_source": peak_kind,
+                         "kernel": "the whole step (prep, score/select in logits mode, block "
+                                   "top-k), CUDA events around graph replays",
+                         "algorithmic_bytes_per_step": algo},
+            "clocks": clk.summary(), "gpu_launches": 3 * steps}
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -693,6 +764,8 @@ def run_ours(args, rank, world, local):
             del r
             torch.cuda.empty_cache()
         extra["dcp_long"] = measure_dcp("long", 2, 1, seed, dev, 50, world)
+        torch.cuda.empty_cache()
+        extra["long_blocks"] = measure_blocks("long", seed, dev, 50, world)
         torch.cuda.empty_cache()
         for wl, steps in (("decode", 400), ("long", 100)):
             r = measure_decode(wl, seed, dev, steps, min(steps, 100), world, local, mx=True)

@@ -386,6 +386,42 @@ idx_status indexer_dcp_merge(const float* cand_val, const int32_t* cand_idx, int
                              void* stream);
 
 /*
+ * Block / pool selection over rows of logits ([RUNNER] the indexer's
+ * topk_blocks, init_blocks, local_blocks; [GLM5] pool_topk and
+ * expand_pools_and_append_tail: the pages give the names, the rules here are
+ * this library's reading). Typically the logits are indexer_decode_logits's.
+ *
+ * indexer_block_topk: row r's len = row_lens[r] logits (logits[r * ld_logits
+ * + s], s < len; len is clamped to [0, ld_logits]) are cut into
+ * ceil(len / block_size) blocks (the last may be partial); a block's score is
+ * its largest logit. The selection is the first init_blocks blocks, the last
+ * local_blocks blocks and the topk_blocks highest-scoring others (any of
+ * several equal to the last one taken); out_blocks [num_rows, out_cap] gets
+ * them in ascending order (at most out_cap, -1 after them), out_counts
+ * (nullable) [num_rows] how many. ceil(ld_logits / block_size) <= 16384,
+ * else IDX_ERR_UNSUPPORTED. One 512-thread CTA per row.
+ */
+idx_status indexer_block_topk(const float* logits, int64_t ld_logits, const int32_t* row_lens,
+                              int64_t num_rows, int32_t block_size, int32_t topk_blocks,
+                              int32_t init_blocks, int32_t local_blocks, int32_t* out_blocks,
+                              int32_t out_cap, int32_t* out_counts, void* stream);
+
+/*
+ * indexer_expand_pools: for row r, the token indices of the pools listed in
+ * pools [num_rows, pools_cap] (the first pool_counts[r] entries, or all when
+ * pool_counts is NULL), pool b being tokens [b * pool_size, (b + 1) *
+ * pool_size), in list order, then the row's tail: tokens [floor(L / P) * P,
+ * L) after its last complete pool (L = row_lens[r], P = pool_size). Entries
+ * < 0 and pools that are not complete add nothing. out_idx [num_rows,
+ * out_cap] (-1 after the tokens, which are cut at out_cap), out_counts
+ * (nullable) their number.
+ */
+idx_status indexer_expand_pools(const int32_t* pools, int32_t pools_cap, const int32_t* pool_counts,
+                                const int32_t* row_lens, int64_t num_rows, int32_t pool_size,
+                                int32_t* out_idx, int32_t out_cap, int32_t* out_counts,
+                                void* stream);
+
+/*
  * Host-only prefill chunk plan ([INDEXER] split_indexer_prefill_chunks): pack
  * requests greedily while the summed key count N <= workspace_tokens and
  * (summed query count M) * N <= logits_budget_bytes / 4; a request that fits

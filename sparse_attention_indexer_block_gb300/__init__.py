@@ -8,6 +8,7 @@ first call does, and raises if it has not been built.
 from .binding import (  # noqa: F401
     IndexerError,
     decode_workspace,
+    indexer_block_topk,
     indexer_dcp_merge,
     indexer_index_key_counts,
     indexer_decode_logits,
@@ -19,6 +20,7 @@ from .binding import (  # noqa: F401
     indexer_decode_topk_values,
     indexer_decode_workspace_bytes,
     indexer_expand_decode_rows,
+    indexer_expand_pools,
     indexer_insert_keys,
     indexer_plan_prefill_chunks,
     indexer_prefill_topk,

@@ -62,6 +62,9 @@ SIGNATURES = {
                                               _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32,
                                               _I64, _I64, _P, _P, _P, _SZ, _P, _P]),
     "indexer_dcp_merge": (C.c_int, [_P, _P, _I32, _I64, _I32, _P, _P, _P]),
+    "indexer_block_topk": (C.c_int, [_P, _I64, _P, _I64, _I32, _I32, _I32, _I32, _P, _I32, _P,
+                                     _P]),
+    "indexer_expand_pools": (C.c_int, [_P, _I32, _P, _P, _I64, _I32, _P, _I32, _P, _P]),
     "indexer_decode_topk_mxfp4": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
                                             _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "indexer_decode_logits_mxfp4": (C.c_int, [_P, _P, _P, _I64, _P, _I64, _I32, _P, _I32, _I32,
@@ -316,6 +319,35 @@ def indexer_decode_logits_mxfp4(q, weights, index_cache, block_table, row_seq_le
         int(workspace.numel() * workspace.element_size()), _ptr(dev_error), _stream(stream))
     _check("indexer_decode_logits_mxfp4", st)
     return out_logits
+
+
+def indexer_block_topk(logits, row_lens, block_size: int, topk_blocks: int, init_blocks: int = 0,
+                       local_blocks: int = 0, out_cap: int | None = None, out=None, cnt=None,
+                       stream=None):
+    """Selected blocks per row (ascending, -1 after) and their counts."""
+    rows = int(logits.shape[0])
+    cap = out_cap or (topk_blocks + init_blocks + local_blocks)
+    if out is None:
+        out = torch.empty((rows, cap), dtype=torch.int32, device=logits.device)
+    if cnt is None:
+        cnt = torch.empty(rows, dtype=torch.int32, device=logits.device)
+    st = load().indexer_block_topk(_ptr(logits), int(logits.stride(0)), _ptr(row_lens), rows,
+                                   block_size, topk_blocks, init_blocks, local_blocks, _ptr(out),
+                                   cap, _ptr(cnt), _stream(stream))
+    _check("indexer_block_topk", st)
+    return out, cnt
+
+
+def indexer_expand_pools(pools, row_lens, pool_size: int, out_cap: int, pool_counts=None,
+                         stream=None):
+    """Token indices of the listed pools then each row's tail, and counts."""
+    rows, pcap = int(pools.shape[0]), int(pools.shape[1])
+    out = torch.empty((rows, out_cap), dtype=torch.int32, device=pools.device)
+    cnt = torch.empty(rows, dtype=torch.int32, device=pools.device)
+    st = load().indexer_expand_pools(_ptr(pools), pcap, _ptr(pool_counts), _ptr(row_lens), rows,
+                                     pool_size, _ptr(out), out_cap, _ptr(cnt), _stream(stream))
+    _check("indexer_expand_pools", st)
+    return out, cnt
 
 
 def indexer_decode_logits(q, weights, index_cache, block_table, row_seq_lens, next_n: int,

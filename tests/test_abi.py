@@ -229,3 +229,17 @@ def test_mxfp4_argument_validation(lib):
     assert f(*args, 2, *tail) == 2                    # next_n must be 1
     assert f(*args, 1, *tail) == 3                    # valid up to the workspace size
     assert f(FAKE, FAKE, FAKE + 8, 10, FAKE, 4, 4, FAKE, 2, 1, *tail) == 1   # cache alignment
+
+
+def test_block_selection_argument_validation(lib):
+    f = lib.indexer_block_topk
+    assert f(FAKE, 4096, FAKE, 2, 0, 4, 0, 0, FAKE, 4, None, None) == 1       # block size 0
+    assert f(FAKE, 4096, FAKE, 2, 64, -1, 0, 0, FAKE, 4, None, None) == 1     # negative k
+    assert f(FAKE, 4096, FAKE, 2, 64, 4, 0, 0, FAKE, 0, None, None) == 1      # no output room
+    assert f(FAKE, 1 << 21, FAKE, 2, 64, 4, 0, 0, FAKE, 4, None, None) == 2   # > 16384 blocks
+    assert f(None, 4096, FAKE, 2, 64, 4, 0, 0, FAKE, 4, None, None) == 1
+    assert f(FAKE, 4096, FAKE, 0, 64, 4, 0, 0, FAKE, 4, None, None) == 0      # nothing to do
+    g = lib.indexer_expand_pools
+    assert g(FAKE, 4, None, FAKE, 2, 0, FAKE, 16, None, None) == 1            # pool size 0
+    assert g(FAKE, 4, None, None, 2, 64, FAKE, 16, None, None) == 1
+    assert g(FAKE, 4, None, FAKE, 0, 64, FAKE, 16, None, None) == 0
