@@ -306,3 +306,20 @@ def test_prefill_values_sharded_and_compressed_match_oracle(world, inter, ratio)
         tb.append(c)
     worst = _check_values_rows(out[sample], ov[sample], n_ent[sample], lg, ta, tb, k)
     print(f"prefill world {world} ratio {ratio}: max open keys per row {worst}")
+
+
+def test_dcp_long_context_sampled():
+    # the long-context workload (1% heavy-tail keys) over 2 ranks dealt in
+    # runs of 1 token, as the bench times it; 8 rows against the unsharded
+    # oracle
+    k = 2048
+    d = synth.make_decode("long", device=DEV)
+    lens = d.seq_lens.cpu().numpy().astype(np.int32)
+    _, _, _, out, ov = _sharded(d, lens, 1, k, 2, 1)
+    rows = np.array([0, 21, 42, 63, 64, 85, 106, 127])
+    _, lg, ta, tb, _ = oracle.decode_topk(synth.bf16_bits(d.q), d.w.cpu().numpy(),
+                                          d.cache.cpu().numpy(), d.block_table.cpu().numpy(),
+                                          lens.astype(np.int64), 1, k, rows=rows,
+                                          want_logits=True)
+    worst = _check_values_rows(out[rows], ov[rows], lens[rows], lg, ta, tb, k)
+    print(f"long context over 2 ranks: max open keys per row {worst}")

@@ -89,3 +89,17 @@ def test_mxfp4_decode_batch_shape_every_row():
         worst = max(worst, check_topk_row(out[r], o, a, b, k, int(seq[r])))
     print(f"max open keys per row {worst}")
     assert worst <= 4 + (3 * k) // 20
+
+
+def test_mxfp4_long_context_sampled():
+    # the long-context shape the bench times (128 requests x 131072 keys, the
+    # launch splitting every row over several CTAs), 8 rows checked
+    k = 2048
+    seq = synth.draw_seq_lens(synth.WORKLOADS["long"], synth.MASTER_SEED)
+    d = _inputs(seq, 131)
+    out = saib.indexer_decode_topk_mxfp4(d.q, d.w, d.cache, d.block_table, d.seq_lens, k)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy()
+    rows = [0, 17, 38, 63, 64, 90, 111, 127]
+    for r, (o, a, b) in zip(rows, _oracle(d, seq, rows)):
+        check_topk_row(out[r], o, a, b, k, int(seq[r]))
