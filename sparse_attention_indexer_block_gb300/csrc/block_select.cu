@@ -63,7 +63,8 @@ __device__ __forceinline__ int blk_scan(int v, int* total, BlkShared* sh) {
   return before + x - v;
 }
 
-// One CTA per row: block maxima (a warp per block, coalesced), the forced
+// One CTA per row: block maxima (coalesced float4 reads folded into block
+// keys when blocks are whole float4s, else a warp per block), the forced
 // first n_init and last n_local blocks, the k best of the others by an 8-bit
 // radix select over order-preserving keys (equal keys at the cut: any of
 // them), then the selected blocks in ascending order.
@@ -82,14 +83,44 @@ __global__ void __launch_bounds__(kBlkThreads) block_topk_kernel(
   const int64_t L = min(max(static_cast<int64_t>(row_lens[row]), int64_t{0}), ld);
   const int nb = static_cast<int>((L + B - 1) / B);  // <= nb_max <= kBlkCap (L <= ld)
   const float* lg = logits + row * ld;
-  for (int b = warp; b < nb; b += kBlkWarps) {
-    float m = -INFINITY;
-    const int64_t end = min(L, static_cast<int64_t>(b) * B + B);
-    for (int64_t i = static_cast<int64_t>(b) * B + lane; i < end; i += 32) m = fmaxf(m, lg[i]);
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) {
-      key[b] = float_key(m);
-      sel[b] = (b < n_init || b >= nb - n_local) ? 2 : 0;
+  if ((B & 3) == 0 && (ld & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+    // blocks of whole float4s: coalesced 16-byte reads, four per thread in
+    // flight, each folded into its block's key (keys start at the minimum)
+    for (int b = t; b < nb; b += kBlkThreads) key[b] = 0u;
+    __syncthreads();
+    const float4* lg4 = reinterpret_cast<const float4*>(lg);
+    const int64_t n4 = (L + 3) / 4;
+    for (int64_t i0 = t; i0 < n4; i0 += 4 * kBlkThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + u * kBlkThreads;
+        if (i < n4) v[u] = lg4[i];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + u * kBlkThreads;
+        if (i >= n4) continue;
+        const int64_t x = 4 * i;  // tokens x .. x + 3 (those < L count)
+        float m = v[u].x;
+        if (x + 1 < L) m = fmaxf(m, v[u].y);
+        if (x + 2 < L) m = fmaxf(m, v[u].z);
+        if (x + 3 < L) m = fmaxf(m, v[u].w);
+        atomicMax(&key[x / B], float_key(m));
+      }
+    }
+    __syncthreads();
+    for (int b = t; b < nb; b += kBlkThreads) sel[b] = (b < n_init || b >= nb - n_local) ? 2 : 0;
+  } else {
+    for (int b = warp; b < nb; b += kBlkWarps) {
+      float m = -INFINITY;
+      const int64_t end = min(L, static_cast<int64_t>(b) * B + B);
+      for (int64_t i = static_cast<int64_t>(b) * B + lane; i < end; i += 32) m = fmaxf(m, lg[i]);
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) {
+        key[b] = float_key(m);
+        sel[b] = (b < n_init || b >= nb - n_local) ? 2 : 0;
+      }
     }
   }
   __syncthreads();
