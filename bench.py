@@ -679,6 +679,40 @@ def measure_blocks(workload, seed, dev, steps, world):
             "clocks": clk.summary(), "gpu_launches": 3 * steps}
 
 
+def run_step_only(args, rank, world, local):
+    """The block-selection or key-sharded long-context step alone (as in the
+    default run's `configs`), one JSON line."""
+    import torch
+
+    import sparse_attention_indexer_block_gb300 as saib
+    from sparse_attention_indexer_block_gb300 import build as libbuild
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    libbuild.build()
+    saib.load()
+    seed = rank_seed(args.seed, rank)
+    if args.workload == "long_blocks":
+        r = measure_blocks("long", seed, dev, args.steps, world)
+    else:
+        r = measure_dcp("long", 2, 1, seed, dev, args.steps, world)
+    if rank == 0:
+        print(json.dumps({"metric": METRIC, "value": r["metric_value"], "unit": "keys/s",
+                          "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None,
+                          "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+                          "config": {"workload": r["workload"]}, "roofline": r["roofline"],
+                          "clocks": r["clocks"], "gpu_launches": r["gpu_launches"]}),
+              flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -963,6 +997,8 @@ def main():
         run_prefill(args, rank, world, local)
     elif args.workload == "insert":
         run_insert(args, rank, world, local)
+    elif args.workload in ("long_blocks", "dcp_long"):
+        run_step_only(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
 
