@@ -15,7 +15,8 @@
  *  [RUNNER]  "vllm.models.minimax_m3.amd.mono.runner" — token_rows: a request
  *            of q query tokens becomes q rows, token j seeing
  *            seq_len - (q - 1 - j) keys; StepTables: block table int32
- *            [rows, width], seq_lens int32 [rows].
+ *            [rows, width], seq_lens int32 [rows]; the indexer's
+ *            topk_blocks / init_blocks / local_blocks (names only).
  *  [INDEXER] "recipes/docker-images/glm52-nf3-hybrid/overlay/vllm/v1/attention/
  *            backends/mla/indexer.py" — DeepseekV32IndexerBackend
  *            (64-token blocks, cache shape (num_blocks, block_size, head_size),
@@ -26,11 +27,15 @@
  *            seq_lens [10, 7, 12, 0], decode_lens [3, 1, 4, 0]),
  *            split_indexer_prefill_chunks (M*N logits-budget chunking),
  *            _build_prefill_chunk_metadata_kernel (query i of a request sees
- *            keys [0, seq_len - query_len + 1 + i)).
+ *            keys [0, seq_len - query_len + 1 + i); with COMPRESS_RATIO and
+ *            its DCP branch, the compressed and key-sharded counts);
+ *            use_fp4_indexer_cache (the MXFP4 index cache).
  *  [GLM5]    "vllm.models.glm5next.common.sparse_indexer" — _decode_topk_seq_lens
  *            (padded grid rows get seq_len 0), _fill_short_decode_causal_indices
  *            (exact causal rows when every key would be selected),
- *            _gather_workspace_shapes (fp8 values + 4-byte fp32 scale per token).
+ *            _gather_workspace_shapes (fp8 values + 4-byte fp32 scale per token;
+ *            its MXFP4 branch), kv_cache_as_quant_view (the MXFP4 token
+ *            stride), pool_topk / expand_pools_and_append_tail (names only).
  *  The scoring formula and k = 2048 are the method's statement; the pages only
  *  name the kernels (fp8_fp4_paged_mqa_logits and "the topk kernels").
  *
