@@ -95,3 +95,24 @@ def test_shard_decode_places_each_token_once():
             j = (t // 128) * 64 + t % 64
             sc, sbt = shards[r]
             assert entry(c, bt, b, t) == entry(sc.numpy(), sbt.numpy(), b, j)
+
+
+def test_mxfp4_cache_draws_are_seeded_and_laid_out_as_stated():
+    seq = np.array([130, 64, 1], np.int32)
+    a = synth.make_decode_mxfp4_from_lens(seq, np.ones(3, np.int32), 1, seed=4)
+    b = synth.make_decode_mxfp4_from_lens(seq, np.ones(3, np.int32), 1, seed=4)
+    c = synth.make_decode_mxfp4_from_lens(seq, np.ones(3, np.int32), 1, seed=5)
+    assert torch.equal(a.cache, b.cache) and torch.equal(a.q, b.q)
+    assert not torch.equal(a.cache, c.cache)
+    P = a.cache.shape[0]
+    assert a.cache.shape == (P, 64 * 68) and P == 3 + 1 + 1      # ceil(L / 64) pages each
+    ent = a.cache.numpy().reshape(P, 64, 68)
+    scales = ent[..., 64:]
+    assert scales.min() >= 124 and scales.max() <= 127             # stated exponent range
+    codes = np.concatenate([ent[..., :64] & 15, ent[..., :64] >> 4]).ravel()
+    counts = np.bincount(codes, minlength=16)
+    assert counts.min() > 0.8 * counts.mean()                      # every e2m1 code drawn
+    # a key read through the oracle's MXFP4 decoding is finite and scaled by
+    # its blocks' exponents
+    vals = oracle.mxfp4_values(ent[0, :2])
+    assert np.all(np.isfinite(vals)) and np.abs(vals).max() <= 6 * 2.0 ** 0
